@@ -1,0 +1,280 @@
+"""Plain fp64 CPU oracle of the Mixture-of-Experts FFN layer.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports this module: the
+CUDA library and its Python binding share no code, table or helper with it.
+Only the tests, the smoke check and the benchmark's CPU-baseline / reference
+arm call it.
+
+What the layer computes, and where each step comes from:
+
+* Router.  A light learned gating network scores every expert for each token
+  and sends the token to its top-K experts ('PagedAttention, speculative
+  decoding, MoE and Blackwell', section 2, "How MoE layers work"; 'Chapter 9.
+  Distributed inference', section 9.3.4, the four steps around Fig. 9-16: "the
+  router picks eight experts for each token").  Gates are the softmax of the
+  logits, restricted to the chosen k and renormalised to sum to one; ties go to
+  the lower expert index.  The pages do not spell out the gate function; this
+  is the layer's specification and the plainest reading of "weighted by the
+  routing weights" in section 9.3.4.
+* Grouping.  Each token's row is laid out once per chosen expert, the rows of
+  one expert contiguous (section 9.3.4, step three: "permute the input rows by
+  expert and run the expert matrix multiplications"; 'Hosting Qwen on
+  Blackwell', "Expert parallelism": the dispatch kernel gathers the routing
+  information and prepares the MoE GEMM input buffers).  The per-expert row
+  counts m_j sum to n*k (section 9.4.1, the definition of m_j).
+* Expert FFN.  An expert is three matrices of d x I (section 9.3.2: Qwen3-235B-
+  A22B's expert has 3 x 4096 x 1536 parameters) used as a SwiGLU block:
+  h = silu(x W_gate^T) * (x W_up^T), y = h W_down^T.  Matrix work is 2 m P_e
+  FLOPs for m rows (section 9.3.2, F_e(m)).
+* Combine.  A token's output is the routing-weighted sum of its k expert
+  outputs (section 9.3.4, step four; 'Hosting Qwen on Blackwell', "MoE
+  Dispatch - Combine": weighted accumulation in combine).  An always-on shared
+  expert adds its output with weight one ('PagedAttention, speculative
+  decoding, MoE and Blackwell', section 2, shared experts).
+
+Precision: every product and sum is fp64 over the exact values of the bf16
+inputs.  The one deliberate rounding is h -> bf16 (round to nearest, ties to
+even): the down projection's input is a bf16 activation in the layer being
+modelled, so the oracle rounds h exactly once, like any bf16 implementation
+must.  The final output is left unrounded.
+
+Inputs are raw bf16 bit patterns (numpy uint16) so that the oracle decodes them
+itself.  Weight arguments only need ``w[e]`` indexing, so a caller may pass a
+lazy per-expert accessor instead of a whole [E, ...] array.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "bf16_bits_to_f64",
+    "round_to_bf16",
+    "f64_to_bf16_bits",
+    "router_logits",
+    "select_top_k",
+    "route",
+    "permute",
+    "swiglu_ffn",
+    "expert_ffn",
+    "combine",
+    "forward",
+    "forward_tokens",
+]
+
+
+# --------------------------------------------------------------------------
+# bf16 encoding (IEEE binary32 with the low 16 mantissa bits dropped)
+# --------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of each bf16 bit pattern, as fp64."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def round_to_bf16(x) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value, ties to even (one rounding).
+
+    bf16 keeps 8 significant bits.  For |x| in [2^(e-1), 2^e) the spacing of
+    bf16 values is 2^(e-8); below the smallest normal (2^-126) it stays 2^-133.
+    Dividing by a power of two is exact, and numpy's round() breaks ties to
+    even, so this is round-to-nearest-even straight from fp64.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    e = np.maximum(e, -125)
+    spacing = np.ldexp(1.0, e - 8)
+    r = np.round(x / spacing) * spacing
+    if np.any(np.abs(r) > 3.3895313892515355e38):  # largest finite bf16
+        raise OverflowError("value outside the bf16 range")
+    return r
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """Bit patterns of round_to_bf16(x)."""
+    r = round_to_bf16(x).astype(np.float32)  # exact: bf16 values are fp32 values
+    return (r.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# Router: logits, top-k selection, renormalised gates
+# --------------------------------------------------------------------------
+
+def router_logits(x_bits, w_router_bits, router_bias=None) -> np.ndarray:
+    """L[t, e] = x[t] . W_r[e] (+ b[e]) in fp64."""
+    x = bf16_bits_to_f64(x_bits)
+    w = bf16_bits_to_f64(w_router_bits)
+    logits = x @ w.T
+    if router_bias is not None:
+        logits = logits + np.asarray(router_bias, dtype=np.float64)[None, :]
+    return logits
+
+
+def select_top_k(logits_row, top_k: int) -> list:
+    """Indices of the k largest logits; an equal logit loses to a lower index.
+
+    Returned in ascending expert-id order: the chosen set is what the method
+    defines, and a canonical slot order makes the combine order well defined.
+    """
+    E = len(logits_row)
+    ranked = sorted(range(E), key=lambda e: (-logits_row[e], e))
+    return sorted(ranked[:top_k])
+
+
+def route(x_bits, w_router_bits, top_k: int, router_bias=None):
+    """Top-k routing with softmax gates renormalised over the chosen experts.
+
+    Returns (ids [T,k] int32, gates [T,k] fp64, logits [T,E] fp64).
+    """
+    logits = router_logits(x_bits, w_router_bits, router_bias)
+    T, E = logits.shape
+    if not 1 <= top_k <= E:
+        raise ValueError("top_k must be in [1, E]")
+    ids = np.empty((T, top_k), dtype=np.int32)
+    gates = np.empty((T, top_k), dtype=np.float64)
+    for t in range(T):
+        row = logits[t]
+        chosen = select_top_k(row, top_k)
+        # softmax over all E experts ...
+        p = np.exp(row - row.max())
+        p = p / p.sum()
+        # ... keep the chosen k and renormalise them to sum to one
+        kept = p[chosen]
+        ids[t] = chosen
+        gates[t] = kept / kept.sum()
+    return ids, gates, logits
+
+
+# --------------------------------------------------------------------------
+# Grouping rows by expert: counts, offsets, stable permutation
+# --------------------------------------------------------------------------
+
+def permute(ids, E: int):
+    """Counting sort of the T*k assignments by expert, stable in t*k+j order.
+
+    Returns (counts [E], offsets [E+1], perm [T*k], slot_pos [T,k]) where
+    perm[p] is the flat assignment index t*k+j stored at row p of the grouped
+    layout and slot_pos[t, j] is the row that holds assignment (t, j).
+    """
+    ids = np.asarray(ids)
+    T, k = ids.shape
+    flat = ids.reshape(-1)
+    counts = np.zeros(E, dtype=np.int64)
+    for e in flat:
+        if not 0 <= e < E:
+            raise ValueError("expert id out of range")
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    next_row = offsets[:-1].copy()
+    perm = np.empty(T * k, dtype=np.int64)
+    slot_pos = np.empty(T * k, dtype=np.int64)
+    for f in range(T * k):  # ascending flat index: equal keys keep their order
+        e = flat[f]
+        p = next_row[e]
+        next_row[e] += 1
+        perm[p] = f
+        slot_pos[f] = p
+    return counts, offsets, perm, slot_pos.reshape(T, k)
+
+
+# --------------------------------------------------------------------------
+# Expert FFN (SwiGLU, three matrices)
+# --------------------------------------------------------------------------
+
+def swiglu_ffn(x_rows, w_gate_up_bits, w_down_bits) -> np.ndarray:
+    """One expert on a block of rows: fp64, with h rounded once to bf16.
+
+    x_rows: [m, d] fp64.  w_gate_up: [2I, d] bf16 bits, rows [0, I) = gate and
+    rows [I, 2I) = up.  w_down: [d, I] bf16 bits.  Returns y [m, d] fp64.
+    """
+    w_gu = bf16_bits_to_f64(w_gate_up_bits)
+    w_d = bf16_bits_to_f64(w_down_bits)
+    I = w_gu.shape[0] // 2
+    gate = x_rows @ w_gu[:I].T
+    up = x_rows @ w_gu[I:].T
+    with np.errstate(over="ignore"):
+        silu = gate / (1.0 + np.exp(-gate))
+    h = round_to_bf16(silu * up)
+    return h @ w_d.T
+
+
+def expert_ffn(x_perm, offsets, w_gate_up, w_down) -> np.ndarray:
+    """Grouped expert FFN: rows [offsets[e], offsets[e+1]) go through expert e.
+
+    x_perm: [rows, d] fp64 (exact bf16 values).  Returns y [rows, d] fp64.
+    """
+    x_perm = np.asarray(x_perm, dtype=np.float64)
+    rows, d = x_perm.shape
+    E = len(offsets) - 1
+    y = np.zeros((rows, d), dtype=np.float64)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            y[r0:r1] = swiglu_ffn(x_perm[r0:r1], w_gate_up[e], w_down[e])
+    return y
+
+
+# --------------------------------------------------------------------------
+# Combine
+# --------------------------------------------------------------------------
+
+def combine(y, slot_pos, gates, y_shared=None) -> np.ndarray:
+    """out[t] = sum_j gates[t,j] * y[slot_pos[t,j]] (+ y_shared[t]), fp64."""
+    slot_pos = np.asarray(slot_pos)
+    T, k = slot_pos.shape
+    out = np.zeros((T, y.shape[1]), dtype=np.float64)
+    for j in range(k):
+        out += np.asarray(gates)[:, j:j + 1] * y[slot_pos[:, j]]
+    if y_shared is not None:
+        out += y_shared
+    return out
+
+
+# --------------------------------------------------------------------------
+# The whole layer
+# --------------------------------------------------------------------------
+
+def forward(x_bits, w_router, w_gate_up, w_down, top_k: int, router_bias=None,
+            w_gate_up_shared=None, w_down_shared=None) -> dict:
+    """Route -> group -> expert FFN -> combine, every intermediate returned."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    T = x_bits.shape[0]
+    E = np.asarray(w_router).shape[0]
+    ids, gates, logits = route(x_bits, w_router, top_k, router_bias)
+    counts, offsets, perm, slot_pos = permute(ids, E)
+    x = bf16_bits_to_f64(x_bits)
+    x_perm = x[perm // top_k]
+    y = expert_ffn(x_perm, offsets, w_gate_up, w_down)
+    y_shared = None
+    if w_gate_up_shared is not None:
+        y_shared = swiglu_ffn(x, w_gate_up_shared, w_down_shared)
+    out = combine(y, slot_pos, gates, y_shared)
+    return dict(ids=ids, gates=gates, logits=logits, counts=counts,
+                offsets=offsets, perm=perm, slot_pos=slot_pos, y=y,
+                y_shared=y_shared, out=out, T=T)
+
+
+def forward_tokens(x_bits, tokens, ids, gates, w_gate_up, w_down,
+                   w_gate_up_shared=None, w_down_shared=None) -> np.ndarray:
+    """Layer output for selected tokens only, given their routing.
+
+    The same per-expert arithmetic as forward(), applied to the selected rows:
+    out[t] = sum_j gates[t,j] * FFN_{ids[t,j]}(x[t]) (+ FFN_shared(x[t])).
+    Used for sampled checks at sizes where the full layer is too slow here.
+    ids/gates are [T,k] routing tables (from route()); tokens index into them.
+    """
+    tokens = np.asarray(tokens, dtype=np.int64)
+    x = bf16_bits_to_f64(np.asarray(x_bits)[tokens])
+    ids = np.asarray(ids)[tokens]
+    gates = np.asarray(gates)[tokens]
+    out = np.zeros_like(x)
+    for e in np.unique(ids):
+        rows, slots = np.nonzero(ids == e)
+        y = swiglu_ffn(x[rows], w_gate_up[e], w_down[e])
+        out[rows] += gates[rows, slots][:, None] * y
+    if w_gate_up_shared is not None:
+        out += swiglu_ffn(x, w_gate_up_shared, w_down_shared)
+    return out

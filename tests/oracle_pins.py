@@ -1,0 +1,289 @@
+"""Checks that pin the CPU oracle to facts other than itself.
+
+Each check takes the oracle module as an argument and raises AssertionError on
+a mismatch, so the same checks run against the real oracle (test_oracle_pins)
+and against copies with a planted mistake (test_oracle_mutations), where at
+least one of them must fail.
+
+What pins what:
+  bf16 decode / rounding ....... torch's own bf16 conversions (library routine)
+  router logits ................ one-hot tokens: logits are columns of W_r (closed form)
+  top-k set .................... brute force over all k-subsets (max logit sum)
+  tie-break .................... duplicated router rows give exact ties
+  gates ........................ k = E: scipy softmax; k = 1: exactly 1; subset-softmax identity
+  grouping ..................... numpy's stable argsort / bincount (library routines)
+  SwiGLU expert ................ a hand-computed one-element example; torch silu dense FFN
+  whole layer .................. brute-force dense form: every expert on every token,
+                                 masked by the routing (no grouping, no permutation)
+  shared expert, linearity ..... identical experts, exact power-of-two scaling
+"""
+
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+import scipy.special
+import torch
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_bits_from_f32(v):
+    t = torch.from_numpy(np.asarray(v, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _random_layer(seed, T, d, E, I, scale_x=1.0):
+    r = _rng(seed)
+    x = _bf16_bits_from_f32(r.standard_normal((T, d)) * scale_x)
+    wr = _bf16_bits_from_f32(r.standard_normal((E, d)) / math.sqrt(d))
+    wgu = _bf16_bits_from_f32(r.standard_normal((E, 2 * I, d)) / math.sqrt(d))
+    wd = _bf16_bits_from_f32(r.standard_normal((E, d, I)) / math.sqrt(I))
+    return x, wr, wgu, wd
+
+
+def _dec(bits):
+    """bf16 bits -> float64 through torch (independent of the oracle)."""
+    t = torch.from_numpy(np.asarray(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def _dense_ffn_torch(o, x64, wgu_bits, wd_bits):
+    """Textbook SwiGLU with torch's silu; h rounded by the (separately pinned)
+    oracle bf16 rounding."""
+    wgu = torch.from_numpy(_dec(wgu_bits))
+    wd = torch.from_numpy(_dec(wd_bits))
+    I = wgu.shape[0] // 2
+    x = torch.from_numpy(x64)
+    h = torch.nn.functional.silu(x @ wgu[:I].T) * (x @ wgu[I:].T)
+    h = torch.from_numpy(o.round_to_bf16(h.numpy()))
+    return (h @ wd.T).numpy()
+
+
+def _rel(a, b):
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-300))
+
+
+# ---------------------------------------------------------------- bf16
+
+def check_bf16_decode(o):
+    r = _rng(1)
+    bits = r.integers(0, 1 << 16, size=20000, dtype=np.uint32).astype(np.uint16)
+    exp = (bits >> 7) & 0xFF
+    bits = bits[exp != 0xFF]  # finite values only
+    assert np.array_equal(o.bf16_bits_to_f64(bits), _dec(bits))
+
+
+def check_bf16_round(o):
+    r = _rng(2)
+    v = np.concatenate([
+        r.standard_normal(20000),
+        r.standard_normal(2000) * 1e-39,   # bf16 subnormal range
+        r.standard_normal(2000) * 1e30,
+        [0.0, -0.0, 1.0, -1.5],
+    ]).astype(np.float32)
+    # exact midpoints between adjacent bf16 values: ties must go to even
+    base = _bf16_bits_from_f32(r.standard_normal(4000))
+    lo = (base.astype(np.uint32) << 16).view(np.float32)
+    hi = ((base.astype(np.uint32) + 1) << 16).view(np.float32)
+    mid = ((lo.astype(np.float64) + hi.astype(np.float64)) / 2).astype(np.float32)
+    v = np.concatenate([v, mid[np.isfinite(mid)]])
+    want = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    got = o.round_to_bf16(v.astype(np.float64))
+    assert np.array_equal(got, want)
+    assert np.array_equal(o.f64_to_bf16_bits(v.astype(np.float64)), _bf16_bits_from_f32(v))
+
+
+# ---------------------------------------------------------------- router
+
+def check_logits_one_hot(o):
+    r = _rng(3)
+    T, d, E = 12, 64, 8
+    hot = r.integers(0, d, size=T)
+    x = np.zeros((T, d), dtype=np.float32)
+    x[np.arange(T), hot] = 1.0
+    wr = _bf16_bits_from_f32(r.standard_normal((E, d)))
+    bias = r.standard_normal(E).astype(np.float32)
+    L = o.router_logits(_bf16_bits_from_f32(x), wr, bias)
+    want = _dec(wr)[:, hot].T + bias.astype(np.float64)[None, :]
+    assert np.array_equal(L, want)
+
+
+def check_topk_brute_force(o):
+    for (E, k, seed) in [(8, 1, 4), (8, 2, 5), (8, 3, 6), (6, 6, 7), (9, 4, 8)]:
+        x, wr, _, _ = _random_layer(seed, 24, 64, E, 8)
+        ids, gates, L = o.route(x, wr, k)
+        for t in range(24):
+            best = max(itertools.combinations(range(E), k),
+                       key=lambda s: sum(L[t, list(s)]))
+            assert list(ids[t]) == list(best), (E, k, t)
+
+
+def check_tie_break(o):
+    r = _rng(9)
+    d, E, k = 64, 6, 2
+    x = _bf16_bits_from_f32(np.abs(r.standard_normal((5, d))))
+    w = np.zeros((E, d), dtype=np.float32)
+    w[0] = 1.0            # largest logit
+    w[2] = 0.5            # tied for second place with expert 5
+    w[5] = 0.5
+    w[1] = w[3] = w[4] = -1.0
+    ids, gates, _ = o.route(x, _bf16_bits_from_f32(w), k)
+    assert (ids == np.array([0, 2])).all()
+    # all logits equal: the k lowest indices win, equal gates
+    ids, gates, _ = o.route(x, _bf16_bits_from_f32(np.zeros((E, d), np.float32)), 3)
+    assert (ids == np.array([0, 1, 2])).all()
+    assert np.allclose(gates, 1.0 / 3.0, rtol=0, atol=1e-15)
+
+
+def check_gates(o):
+    x, wr, _, _ = _random_layer(10, 32, 64, 8, 8)
+    ids, gates, L = o.route(x, wr, 8)          # k = E: the full softmax
+    assert (ids == np.arange(8)).all()
+    assert np.allclose(gates, scipy.special.softmax(L, axis=1), rtol=1e-13, atol=0)
+    ids, gates, L = o.route(x, wr, 1)          # k = 1: gate is exactly one
+    assert (gates == 1.0).all()
+    assert (ids[:, 0] == np.argmax(L, axis=1)).all()
+    bias = _rng(11).standard_normal(8).astype(np.float32) * 3
+    ids, gates, L = o.route(x, wr, 3, bias)
+    assert np.allclose(gates.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    sel = np.take_along_axis(L, ids.astype(np.int64), axis=1)
+    assert np.allclose(gates, scipy.special.softmax(sel, axis=1), rtol=1e-13, atol=0)
+    # the chosen k beat every other expert
+    for t in range(L.shape[0]):
+        rest = np.setdiff1d(np.arange(8), ids[t])
+        assert L[t, ids[t]].min() >= L[t, rest].max()
+
+
+# ---------------------------------------------------------------- grouping
+
+def check_permute(o):
+    r = _rng(12)
+    for (T, E, k) in [(50, 8, 2), (37, 16, 4), (1, 5, 5), (200, 64, 8)]:
+        ids = np.stack([np.sort(r.choice(E, size=k, replace=False)) for _ in range(T)])
+        ids[: T // 3] = np.sort(r.choice(max(k, E // 2), size=k, replace=False))  # skew
+        counts, offsets, perm, slot_pos = o.permute(ids, E)
+        flat = ids.reshape(-1)
+        assert np.array_equal(counts, np.bincount(flat, minlength=E))
+        assert counts.sum() == T * k
+        assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+        assert np.array_equal(perm, np.argsort(flat, kind="stable"))
+        inv = np.empty(T * k, dtype=np.int64)
+        inv[perm] = np.arange(T * k)
+        assert np.array_equal(slot_pos.reshape(-1), inv)
+
+
+# ---------------------------------------------------------------- expert FFN
+
+SWIGLU_HAND = [
+    # (gate pre-activation G, up U, expected bf16 h)
+    # h = G / (1 + exp(-G)) * U rounded to bf16 by hand:
+    # G=2, U=3: 5.28478...; bf16 spacing in [4,8) is 2^-5 -> 169 * 2^-5 = 5.28125
+    (2.0, 3.0, 5.28125),
+    # G=-2, U=3: -0.715217...; spacing in [0.5,1) is 2^-8 -> -183 * 2^-8 = -0.71484375
+    (-2.0, 3.0, -0.71484375),
+    # G=0: silu(0) = 0 whatever U is
+    (0.0, 7.0, 0.0),
+]
+
+
+def check_swiglu_hand_example(o):
+    d = 64
+    for (G, U, h) in SWIGLU_HAND:
+        wgu = np.zeros((2, d), dtype=np.float32)
+        wgu[0, 0] = G
+        wgu[1, 0] = U
+        wd = np.zeros((d, 1), dtype=np.float32)
+        wd[0, 0] = 1.0
+        wd[5, 0] = -2.0
+        x = np.zeros((1, d))
+        x[0, 0] = 1.0
+        y = o.swiglu_ffn(x, _bf16_bits_from_f32(wgu), _bf16_bits_from_f32(wd))
+        want = np.zeros((1, d))
+        want[0, 0] = h
+        want[0, 5] = -2.0 * h
+        assert np.array_equal(y, want), (G, U, y[0, :6])
+
+
+def check_single_expert_is_dense_ffn(o):
+    T, d, E, I = 24, 64, 6, 32
+    x, wr, wgu, wd = _random_layer(13, T, d, E, I)
+    bias = np.zeros(E, dtype=np.float32)
+    bias[2] = 1e4                                  # every token picks expert 2
+    res = o.forward(x, wr, wgu, wd, 1, router_bias=bias)
+    assert (res["ids"] == 2).all() and (res["gates"] == 1.0).all()
+    want = _dense_ffn_torch(o, _dec(x), wgu[2], wd[2])
+    assert _rel(res["out"], want) < 1e-12
+
+
+def check_identical_experts(o):
+    T, d, E, I = 20, 64, 8, 32
+    x, wr, wgu, wd = _random_layer(14, T, d, E, I)
+    wgu = np.broadcast_to(wgu[3], wgu.shape).copy()
+    wd = np.broadcast_to(wd[3], wd.shape).copy()
+    res = o.forward(x, wr, wgu, wd, 3)
+    want = _dense_ffn_torch(o, _dec(x), wgu[0], wd[0])
+    assert _rel(res["out"], want) < 1e-12
+    # an always-on shared expert equal to them doubles the output
+    res = o.forward(x, wr, wgu, wd, 3, w_gate_up_shared=wgu[0], w_down_shared=wd[0])
+    assert _rel(res["out"], 2 * want) < 1e-12
+
+
+def _brute_force_layer(o, x, wr, wgu, wd, k, bias=None):
+    """Every expert on every token, masked by the routing: no grouping step."""
+    xd = torch.from_numpy(_dec(x))
+    L = (xd @ torch.from_numpy(_dec(wr)).T).numpy()
+    if bias is not None:
+        L = L + np.asarray(bias, np.float64)[None, :]
+    T, E = L.shape
+    order = np.lexsort((np.tile(np.arange(E), (T, 1)), -L), axis=1)[:, :k]
+    mask = np.zeros((T, E))
+    np.put_along_axis(mask, order, 1.0, axis=1)
+    g = np.where(mask > 0, scipy.special.softmax(np.where(mask > 0, L, -np.inf), axis=1), 0.0)
+    out = np.zeros((T, x.shape[1]))
+    for e in range(E):
+        out += g[:, e:e + 1] * _dense_ffn_torch(o, xd.numpy(), wgu[e], wd[e])
+    return out
+
+
+def check_brute_force_layer(o):
+    for (T, d, E, I, k, seed) in [(40, 64, 8, 32, 2, 15), (33, 128, 16, 64, 4, 16)]:
+        x, wr, wgu, wd = _random_layer(seed, T, d, E, I)
+        bias = _rng(seed).standard_normal(E).astype(np.float32)
+        res = o.forward(x, wr, wgu, wd, k, router_bias=bias)
+        want = _brute_force_layer(o, x, wr, wgu, wd, k, bias)
+        assert _rel(res["out"], want) < 1e-12
+
+
+def check_down_scaling(o):
+    T, d, E, I = 16, 64, 8, 32
+    x, wr, wgu, wd = _random_layer(17, T, d, E, I)
+    a = o.forward(x, wr, wgu, wd, 2)["out"]
+    wd2 = _bf16_bits_from_f32(_dec(wd) * 2.0)
+    b = o.forward(x, wr, wgu, wd2, 2)["out"]
+    assert np.array_equal(b, 2.0 * a)
+
+
+def check_forward_tokens(o):
+    T, d, E, I, k = 30, 64, 8, 32, 3
+    x, wr, wgu, wd = _random_layer(18, T, d, E, I)
+    r = _rng(18)
+    wgus = _bf16_bits_from_f32(r.standard_normal((2 * I, d)) / 8)
+    wds = _bf16_bits_from_f32(r.standard_normal((d, I)) / 6)
+    res = o.forward(x, wr, wgu, wd, k, w_gate_up_shared=wgus, w_down_shared=wds)
+    toks = [0, 7, 29, 13]
+    part = o.forward_tokens(x, toks, res["ids"], res["gates"], wgu, wd, wgus, wds)
+    assert _rel(part, res["out"][toks]) < 1e-13
+
+
+ALL_CHECKS = [
+    check_bf16_decode, check_bf16_round, check_logits_one_hot,
+    check_topk_brute_force, check_tie_break, check_gates, check_permute,
+    check_swiglu_hand_example, check_single_expert_is_dense_ffn,
+    check_identical_experts, check_brute_force_layer, check_down_scaling,
+    check_forward_tokens,
+]
