@@ -1,0 +1,189 @@
+/*
+ * moe.h -- C ABI of the Mixture-of-Experts FFN layer on NVIDIA GB300 (sm_103a).
+ *
+ * The layer (sources: 'Chapter 9. Distributed inference', section 9.3.4, the
+ * four steps around Fig. 9-16; 'Hosting Qwen on Blackwell', "MoE Dispatch -
+ * Combine" and "Expert parallelism"; 'PagedAttention, speculative decoding,
+ * MoE and Blackwell', section 2):
+ *
+ *   1. route    : logits L = x W_r^T (+ b); per token the k largest logits
+ *                 (an equal logit loses to a lower expert index); gates =
+ *                 softmax of the chosen logits (= full softmax renormalised
+ *                 over the chosen k).  Slots are stored in ascending expert id.
+ *   2. permute  : per-expert row counts (they sum to T*k), exclusive offsets,
+ *                 and a stable grouping of the T*k assignments by expert.
+ *   3. expert   : each expert e is a SwiGLU FFN of three d x I matrices:
+ *                 h = silu(x W_gate^T) * (x W_up^T), rounded to bf16;
+ *                 y = h W_down^T, kept in fp32.
+ *   4. combine  : out[t] = sum_j gates[t,j] * y[slot_pos[t,j]] (+ shared
+ *                 expert output), summed in fp32 in slot order, rounded once
+ *                 to bf16.
+ *
+ * Conventions for every call
+ *   - All tensors are dense, row-major, on the current CUDA device, and owned
+ *     by the caller.  The library never allocates, frees or synchronises on
+ *     these calls; all work is queued on `stream` and is asynchronous.
+ *   - moe_bf16 is the raw bit pattern of an IEEE bfloat16 value.
+ *   - Every device pointer must be 16-byte aligned.  Shapes: d % 64 == 0,
+ *     I % 64 == 0, 1 <= E <= 256, 1 <= top_k <= min(E, 8), T >= 0.
+ *     T == 0 is a no-op that returns MOE_OK.
+ *   - Argument errors are found on the host before anything is queued and
+ *     return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE.
+ *     A failed launch returns MOE_ERR_CUDA (details: moe_last_error()).
+ *   - `ws` is a device workspace of at least moe_workspace_size() bytes for
+ *     the shapes in use; its first 256 bytes hold a sticky device status word
+ *     that must start at zero (moe_workspace_init).  Kernels record there what
+ *     they find on the device: an expert id out of range, inconsistent
+ *     offsets or slot positions (MOE_ERR_DEVICE_CHECK), a wait that gave up
+ *     (MOE_ERR_TIMEOUT).  Such a kernel skips the bad work instead of faulting;
+ *     read the word with moe_get_device_status().
+ *   - Calls that share a workspace must be ordered on one stream.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* a null/unaligned pointer or a bad shape */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but unsupported shape or device */
+  MOE_ERR_WORKSPACE = 3,     /* workspace too small */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  MOE_ERR_TIMEOUT = 5,       /* a device-side wait gave up (bounded) */
+  MOE_ERR_DEVICE_CHECK = 6   /* device-side validation found bad indices */
+} moe_status_t;
+
+typedef uint16_t moe_bf16;
+typedef struct CUstream_st* moe_stream_t;  /* same type as cudaStream_t */
+
+/* Workspace bytes that moe_forward / moe_forward_ex need for these shapes;
+ * it also covers every single-step call below on the same shapes
+ * (rows = T * top_k).  I_shared = 0 when there is no shared expert. */
+size_t moe_workspace_size(int T, int d, int E, int I, int top_k, int I_shared);
+
+/* Zero the workspace's status word (queued on `stream`). */
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 1, route.  x [T,d] bf16, w_router [E,d] bf16, router_bias [E] fp32 or
+ * NULL (added to the logits before selection and gating).  Writes
+ * topk_ids [T,top_k] int32 (ascending within a token) and topk_gates
+ * [T,top_k] fp32 (sum to 1 per token).  Logits are fp32 sums of bf16
+ * products on the tensor cores.
+ * Cite: 'PagedAttention, speculative decoding, MoE and Blackwell', section 2
+ * (gating network, top-K); 'Chapter 9. Distributed inference', section 9.3.4. */
+moe_status_t moe_route(const moe_bf16* x, const moe_bf16* w_router,
+                       const float* router_bias, int T, int d, int E, int top_k,
+                       int32_t* topk_ids, float* topk_gates,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 2, group by expert.  topk_ids [T,top_k] int32 in [0,E).  Writes
+ * expert_counts [E], expert_offsets [E+1] (offsets[E] = T*top_k),
+ * perm [T*top_k] (row p of the grouped layout holds assignment perm[p] =
+ * t*top_k+j; within an expert, ascending t*top_k+j) and slot_pos
+ * [T*top_k] (its inverse).  If x is not NULL, also gathers
+ * x_perm [T*top_k, d] bf16 with x_perm[p] = x[perm[p] / top_k].
+ * Ids out of range are skipped and flagged MOE_ERR_DEVICE_CHECK.
+ * Cite: 'Chapter 9. Distributed inference', section 9.3.4 (permute the input
+ * rows by expert) and section 9.4.1 (m_j sum to n k); 'Hosting Qwen on
+ * Blackwell', "Expert parallelism" (GEMM input buffers). */
+moe_status_t moe_permute(const int32_t* topk_ids, const moe_bf16* x,
+                         int T, int d, int E, int top_k,
+                         int32_t* expert_counts, int32_t* expert_offsets,
+                         int32_t* perm, int32_t* slot_pos, moe_bf16* x_perm,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 3, grouped expert FFN.  Rows [expert_offsets[e], expert_offsets[e+1])
+ * of x_perm [rows,d] go through expert e: w_gate_up [E,2I,d] (per expert,
+ * rows [0,I) gate, [I,2I) up), w_down [E,d,I].  Writes y [rows,d] fp32.
+ * h is kept in the workspace as bf16.  Offsets that do not start at 0, go
+ * down, or do not end at `rows` make the kernels skip all work and flag
+ * MOE_ERR_DEVICE_CHECK.
+ * Cite: 'Chapter 9. Distributed inference', section 9.3.2 (three matrices per
+ * expert, F_e(m) = 2 m P_e) and section 9.4.3 (grouped GEMM). */
+moe_status_t moe_expert_ffn(const moe_bf16* x_perm, const int32_t* expert_offsets,
+                            const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                            int rows, int d, int E, int I, float* y,
+                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 4, combine.  out[t] = bf16( sum_{j<top_k} topk_gates[t,j] *
+ * y[slot_pos[t,j]] (+ y_shared[t]) ), fp32 sums in j order (deterministic).
+ * y [rows,d] fp32 with rows = T*top_k, y_shared [T,d] fp32 or NULL.
+ * A slot position outside [0,rows) is skipped and flagged.
+ * Cite: 'Chapter 9. Distributed inference', section 9.3.4, step four;
+ * 'Hosting Qwen on Blackwell', "MoE Dispatch - Combine". */
+moe_status_t moe_combine(const float* y, const int32_t* slot_pos,
+                         const float* topk_gates, const float* y_shared,
+                         int T, int d, int top_k, moe_bf16* out,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole layer: steps 1-4 on one stream, intermediates in `ws`.
+ * x [T,d], w_router [E,d], w_gate_up [E,2I,d], w_down [E,d,I] -> out [T,d]. */
+moe_status_t moe_forward(const moe_bf16* x, const moe_bf16* w_router,
+                         const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                         int T, int d, int E, int I, int top_k, moe_bf16* out,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Optional parts of the layer.  router_bias: [E] fp32 added to the logits.
+ * Shared expert ('PagedAttention, speculative decoding, MoE and Blackwell',
+ * section 2: experts that process every token): w_gate_up_shared [2*I_shared,d],
+ * w_down_shared [d,I_shared]; its output is added with weight 1. */
+typedef struct {
+  const float* router_bias;
+  const moe_bf16* w_gate_up_shared;
+  const moe_bf16* w_down_shared;
+  int I_shared;
+} moe_forward_ext_t;
+
+moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
+                            const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                            int T, int d, int E, int I, int top_k, moe_bf16* out,
+                            void* ws, size_t ws_bytes, moe_stream_t stream,
+                            const moe_forward_ext_t* ext);
+
+/* Where moe_forward(_ex) keeps its intermediates: byte offsets into `ws`
+ * (each 256-byte aligned) for the same shapes. */
+typedef struct {
+  size_t status, topk_ids, topk_gates, expert_counts, expert_offsets, perm,
+         slot_pos, chunk_table, x_perm, h, h_shared, y, y_shared, total;
+} moe_workspace_layout_t;
+
+moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,
+                                  moe_workspace_layout_t* layout);
+
+/* Synchronise `stream`, read and clear the workspace's device status word. */
+moe_status_t moe_get_device_status(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+const char* moe_status_string(moe_status_t status);
+/* Message of the last failing call on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Bound on every device-side wait, in nanoseconds (default 2e9; 0 restores
+ * the default).  After it a kernel records MOE_ERR_TIMEOUT, drains its own
+ * copies and tensor-core work in flight, frees its tensor memory and
+ * returns; the context stays usable.  A bound of 1 makes every wait that is
+ * not already satisfied give up at once (used to test this path). */
+moe_status_t moe_set_wait_timeout_ns(unsigned long long ns);
+
+/* Kernel launches made by this library since it was loaded. */
+unsigned long long moe_launch_count(void);
+
+/* Tracing.  While enabled, every kernel launch is bracketed by CUDA events on
+ * its stream.  moe_profiler_collect() synchronises those events and returns,
+ * per kernel name (in first-launch order), the launch count and total
+ * milliseconds; it then clears the records.  names: n_max entries of 64 bytes.
+ * Returns the number of kernel names written in *n_out. */
+moe_status_t moe_profiler_enable(int enable);
+moe_status_t moe_profiler_collect(char* names, int* launches, double* total_ms,
+                                  int n_max, int* n_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,269 @@
+"""Thin Python binding of libmoe.so (the C ABI in include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  torch supplies device memory and the current stream.  Importing this
+module fails loudly when the library has not been built (run
+``python -m mixture_experts_layer_20_gb300.build`` or
+``__graft_entry__.build()``); there is no fallback of any kind.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                      "(python -m mixture_experts_layer_20_gb300.build)")
+_lib = ctypes.CDLL(LIB_PATH)
+
+_vp, _i, _sz, _st = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "status", "topk_ids", "topk_gates", "expert_counts", "expert_offsets", "perm",
+        "slot_pos", "chunk_table", "x_perm", "h", "h_shared", "y", "y_shared", "total")]
+
+
+class ForwardExt(ctypes.Structure):
+    _fields_ = [("router_bias", _vp), ("w_gate_up_shared", _vp), ("w_down_shared", _vp),
+                ("I_shared", _i)]
+
+
+_SIGS = {
+    "moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "moe_workspace_init": (_st, [_vp, _sz, _vp]),
+    "moe_route": (_st, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "moe_permute": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_expert_ffn": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "moe_combine": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "moe_forward": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "moe_forward_ex": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp,
+                             ctypes.POINTER(ForwardExt)]),
+    "moe_workspace_layout": (_st, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(WorkspaceLayout)]),
+    "moe_get_device_status": (_st, [_vp, _sz, _vp]),
+    "moe_status_string": (ctypes.c_char_p, [_st]),
+    "moe_last_error": (ctypes.c_char_p, []),
+    "moe_set_wait_timeout_ns": (_st, [ctypes.c_ulonglong]),
+    "moe_launch_count": (ctypes.c_ulonglong, []),
+    "moe_profiler_enable": (_st, [_i]),
+    "moe_profiler_collect": (_st, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int),
+                                   ctypes.POINTER(ctypes.c_double), _i, ctypes.POINTER(ctypes.c_int)]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype, _f.argtypes = _res, _args
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, \
+    MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK = range(7)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = _lib.moe_status_string(status).decode()
+        detail = _lib.moe_last_error().decode()
+        super().__init__(f"{what}: {name}: {detail}")
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _want(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+
+
+# ---------------------------------------------------------------- workspace
+
+def moe_workspace_size(T, d, E, I, top_k, I_shared=0) -> int:
+    return int(_lib.moe_workspace_size(T, d, E, I, top_k, I_shared))
+
+
+def moe_workspace_layout(T, d, E, I, top_k, I_shared=0) -> dict:
+    lay = WorkspaceLayout()
+    _check(_lib.moe_workspace_layout(T, d, E, I, top_k, I_shared, ctypes.byref(lay)),
+           "moe_workspace_layout")
+    return {n: getattr(lay, n) for n, _ in WorkspaceLayout._fields_}
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None):
+    _check(_lib.moe_workspace_init(_p(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
+
+
+def new_workspace(T, d, E, I, top_k, I_shared=0, device="cuda") -> torch.Tensor:
+    """A zeroed uint8 device workspace for these shapes."""
+    n = max(moe_workspace_size(T, d, E, I, top_k, I_shared), 256)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def moe_get_device_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise, read and clear the workspace's device status (MOE_OK,
+    MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK)."""
+    return int(_lib.moe_get_device_status(_p(ws), ws.numel(), _stream(stream)))
+
+
+def moe_set_wait_timeout_ns(ns: int):
+    _check(_lib.moe_set_wait_timeout_ns(ns), "moe_set_wait_timeout_ns")
+
+
+def moe_launch_count() -> int:
+    return int(_lib.moe_launch_count())
+
+
+def moe_profiler_enable(on: bool):
+    _check(_lib.moe_profiler_enable(1 if on else 0), "moe_profiler_enable")
+
+
+def moe_profiler_collect(n_max: int = 64) -> dict:
+    """{kernel name: (launches, total ms)} since the last collect."""
+    names = ctypes.create_string_buffer(64 * n_max)
+    launches = (ctypes.c_int * n_max)()
+    total = (ctypes.c_double * n_max)()
+    n = ctypes.c_int(0)
+    _check(_lib.moe_profiler_collect(names, launches, total, n_max, ctypes.byref(n)),
+           "moe_profiler_collect")
+    out = {}
+    for i in range(n.value):
+        nm = names.raw[64 * i:64 * (i + 1)].split(b"\0", 1)[0].decode()
+        out[nm] = (launches[i], total[i])
+    return out
+
+
+# ---------------------------------------------------------------- the four steps
+
+def moe_route(x, w_router, top_k, router_bias=None, topk_ids=None, topk_gates=None, ws=None,
+              stream=None):
+    _want(x, torch.bfloat16, "x"); _want(w_router, torch.bfloat16, "w_router")
+    _want(router_bias, torch.float32, "router_bias")
+    T, d = x.shape
+    E = w_router.shape[0]
+    if topk_ids is None:
+        topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    if topk_gates is None:
+        topk_gates = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    _want(topk_ids, torch.int32, "topk_ids"); _want(topk_gates, torch.float32, "topk_gates")
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=x.device)
+    _check(_lib.moe_route(_p(x), _p(w_router), _p(router_bias), T, d, E, top_k, _p(topk_ids),
+                          _p(topk_gates), _p(ws), ws.numel(), _stream(stream)), "moe_route")
+    return topk_ids, topk_gates
+
+
+def moe_permute(topk_ids, E, x=None, ws=None, stream=None):
+    """Returns (counts [E], offsets [E+1], perm [T*k], slot_pos [T,k], x_perm or None)."""
+    _want(topk_ids, torch.int32, "topk_ids"); _want(x, torch.bfloat16, "x")
+    T, k = topk_ids.shape
+    d = x.shape[1] if x is not None else 64
+    dev = topk_ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    slot_pos = torch.empty((T, k), dtype=torch.int32, device=dev)
+    x_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device=dev) if x is not None else None
+    if ws is None:
+        ws = new_workspace(T, d, E, 64, k, device=dev)
+    _check(_lib.moe_permute(_p(topk_ids), _p(x), T, d, E, k, _p(counts), _p(offsets), _p(perm),
+                            _p(slot_pos), _p(x_perm), _p(ws), ws.numel(), _stream(stream)),
+           "moe_permute")
+    return counts, offsets, perm, slot_pos, x_perm
+
+
+def moe_expert_ffn(x_perm, expert_offsets, w_gate_up, w_down, y=None, ws=None, stream=None):
+    _want(x_perm, torch.bfloat16, "x_perm"); _want(expert_offsets, torch.int32, "expert_offsets")
+    _want(w_gate_up, torch.bfloat16, "w_gate_up"); _want(w_down, torch.bfloat16, "w_down")
+    rows, d = x_perm.shape
+    E, I2, _ = w_gate_up.shape
+    I = I2 // 2
+    if y is None:
+        y = torch.empty((rows, d), dtype=torch.float32, device=x_perm.device)
+    _want(y, torch.float32, "y")
+    if ws is None:
+        ws = new_workspace(rows, d, E, I, 1, device=x_perm.device)
+    _check(_lib.moe_expert_ffn(_p(x_perm), _p(expert_offsets), _p(w_gate_up), _p(w_down), rows, d,
+                               E, I, _p(y), _p(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
+    return y
+
+
+def moe_combine(y, slot_pos, topk_gates, y_shared=None, out=None, ws=None, stream=None):
+    _want(y, torch.float32, "y"); _want(slot_pos, torch.int32, "slot_pos")
+    _want(topk_gates, torch.float32, "topk_gates"); _want(y_shared, torch.float32, "y_shared")
+    T, k = slot_pos.shape
+    d = y.shape[1]
+    if out is None:
+        out = torch.empty((T, d), dtype=torch.bfloat16, device=y.device)
+    _want(out, torch.bfloat16, "out")
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=y.device)
+    _check(_lib.moe_combine(_p(y), _p(slot_pos), _p(topk_gates), _p(y_shared), T, d, k, _p(out),
+                            _p(ws), ws.numel(), _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router_bias=None,
+                w_gate_up_shared=None, w_down_shared=None, stream=None):
+    """The whole layer.  Returns out [T, d] bf16."""
+    for t, n in ((x, "x"), (w_router, "w_router"), (w_gate_up, "w_gate_up"), (w_down, "w_down"),
+                 (w_gate_up_shared, "w_gate_up_shared"), (w_down_shared, "w_down_shared")):
+        _want(t, torch.bfloat16, n)
+    _want(router_bias, torch.float32, "router_bias")
+    T, d = x.shape
+    E, I2, _ = w_gate_up.shape
+    I = I2 // 2
+    I_s = w_down_shared.shape[1] if w_down_shared is not None else 0
+    if out is None:
+        out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
+    _want(out, torch.bfloat16, "out")
+    if ws is None:
+        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device)
+    s = _stream(stream)
+    if router_bias is None and I_s == 0:
+        st = _lib.moe_forward(_p(x), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E, I, top_k,
+                              _p(out), _p(ws), ws.numel(), s)
+    else:
+        ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
+                         w_gate_up_shared.data_ptr() if I_s else None,
+                         w_down_shared.data_ptr() if I_s else None, I_s)
+        st = _lib.moe_forward_ex(_p(x), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E, I,
+                                 top_k, _p(out), _p(ws), ws.numel(), s, ctypes.byref(ext))
+    _check(st, "moe_forward")
+    return out
+
+
+def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0) -> dict:
+    """Typed views of moe_forward's intermediates inside its workspace."""
+    L = moe_workspace_layout(T, d, E, I, top_k, I_shared)
+    n = T * top_k
+
+    def view(off, count, dtype, shape):
+        b = torch.empty((), dtype=dtype).element_size()
+        return ws[off:off + count * b].view(dtype).view(shape)
+
+    return {
+        "topk_ids": view(L["topk_ids"], n, torch.int32, (T, top_k)),
+        "topk_gates": view(L["topk_gates"], n, torch.float32, (T, top_k)),
+        "expert_counts": view(L["expert_counts"], E, torch.int32, (E,)),
+        "expert_offsets": view(L["expert_offsets"], E + 1, torch.int32, (E + 1,)),
+        "perm": view(L["perm"], n, torch.int32, (n,)),
+        "slot_pos": view(L["slot_pos"], n, torch.int32, (T, top_k)),
+        "x_perm": view(L["x_perm"], n * d, torch.bfloat16, (n, d)),
+        "h": view(L["h"], n * I, torch.bfloat16, (n, I)),
+        "y": view(L["y"], n * d, torch.float32, (n, d)),
+    }

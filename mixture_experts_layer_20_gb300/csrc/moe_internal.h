@@ -1,0 +1,62 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kPermuteChunk = 4096;  // assignments per permute CTA
+
+// Bits of the workspace's device status word.
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusDeviceCheck = 2u;
+
+// Records the kernel name, counts the launch and, while tracing is on,
+// brackets it with CUDA events on `stream`.  Defined in moe_api.cu.
+class KernelScope {
+ public:
+  KernelScope(cudaStream_t stream, const char* name);
+  ~KernelScope();
+  KernelScope(const KernelScope&) = delete;
+  KernelScope& operator=(const KernelScope&) = delete;
+
+ private:
+  cudaStream_t stream_;
+  int slot_;
+};
+
+int device_sm_count();
+
+// ---- tcgen05 GEMM launchers (moe_gemm.cu).  Return a CUDA error code.
+
+// Router: logits of x [T,d] against w_router [E,d] (+bias) on the tensor
+// cores, then per-token top-k and renormalised gates.
+cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, const float* bias,
+                          int T, int d, int E, int top_k, int32_t* ids, float* gates,
+                          unsigned* status, unsigned long long timeout_ns);
+
+// Grouped SwiGLU FFN.  Rows [offsets[e], offsets[e+1]) of a [rows, d] go
+// through expert e (weights per expert: w_gate_up [2I, d], w_down [d, I]).
+// offsets == nullptr: a single expert on all `rows` rows (dense).
+// Writes h [rows, I] bf16 (scratch) and y [rows, d] fp32.
+cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
+                               int d, int E, int I, const void* w_gate_up, const void* w_down,
+                               void* h, float* y, unsigned* status,
+                               unsigned long long timeout_ns);
+
+// ---- grouping and combine (moe_permute.cu)
+
+cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, int T, int d, int E,
+                           int top_k, int32_t* counts, int32_t* offsets, int32_t* perm,
+                           int32_t* slot_pos, void* x_perm, int32_t* chunk_table,
+                           unsigned* status);
+
+cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_pos,
+                           const float* gates, const float* y_shared, int T, int d, int top_k,
+                           void* out, unsigned* status);
+
+}  // namespace moe

@@ -1,0 +1,268 @@
+// Grouping of the T*k token-expert assignments by expert, and the combine.
+//
+// Grouping ('Chapter 9. Distributed inference', section 9.3.4: permute the
+// input rows by expert; section 9.4.1: the per-expert row counts m_j sum to
+// n k).  The flat assignment index f = t*k + j is cut into chunks of 4096:
+//   count   : one CTA per chunk, shared-memory histogram -> chunk_table[c][e]
+//   scan    : one CTA, one thread per expert, runs down the chunks (exclusive
+//             per-expert chunk bases, counts[e]) then scans the experts
+//             (offsets[e]) and adds offsets[e] to every chunk base
+//   scatter : one CTA per chunk; each warp owns 256 consecutive assignments;
+//             warp histograms (match.any) -> per-warp bases -> each lane's
+//             rank among earlier equal ids in its warp.  Positions are thus
+//             offsets[e] + (number of earlier f with the same e): a stable
+//             counting sort, deterministic with no global atomics.
+//   gather  : x_perm[p] = x[perm[p] / k], one warp per row, 16-byte copies.
+//
+// Combine ('Chapter 9. Distributed inference', section 9.3.4, step four;
+// 'Hosting Qwen on Blackwell', "MoE Dispatch - Combine": weighted
+// accumulation): one CTA per token, each thread 8 columns; the k weighted
+// rows are summed in fp32 in slot order, then rounded once to bf16.
+
+#include <cuda_bf16.h>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kScatterWarps = 16;
+constexpr int kPerWarp = kPermuteChunk / kScatterWarps;  // 256
+
+__global__ void __launch_bounds__(512) permute_count_kernel(const int32_t* __restrict__ ids, int n,
+                                                            int E, int32_t* __restrict__ table,
+                                                            unsigned* status) {
+  __shared__ int hist[kMaxExperts];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int beg = blockIdx.x * kPermuteChunk;
+  const int end = min(n, beg + kPermuteChunk);
+  bool bad = false;
+  for (int f = beg + threadIdx.x; f < end; f += blockDim.x) {
+    const int e = __ldg(ids + f);
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&hist[e], 1);
+    else bad = true;
+  }
+  if (bad) atomicOr(status, kStatusDeviceCheck);
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) table[(size_t)blockIdx.x * E + i] = hist[i];
+}
+
+__global__ void __launch_bounds__(kMaxExperts) permute_scan_kernel(int32_t* __restrict__ table,
+                                                                   int nchunks, int E,
+                                                                   int32_t* __restrict__ counts,
+                                                                   int32_t* __restrict__ offsets) {
+  __shared__ int s_scan[kMaxExperts];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = table[(size_t)c * E + e];
+      table[(size_t)c * E + e] = run;
+      run += v;
+    }
+    counts[e] = run;
+  }
+  s_scan[e] = e < E ? run : 0;
+  __syncthreads();
+  // inclusive Hillis-Steele scan over the (at most 256) experts
+  for (int o = 1; o < kMaxExperts; o <<= 1) {
+    const int v = e >= o ? s_scan[e - o] : 0;
+    __syncthreads();
+    s_scan[e] += v;
+    __syncthreads();
+  }
+  const int excl = s_scan[e] - (e < E ? run : 0);
+  if (e < E) {
+    offsets[e] = excl;
+    for (int c = 0; c < nchunks; ++c) table[(size_t)c * E + e] += excl;
+  }
+  if (e == E - 1) offsets[E] = s_scan[e];
+}
+
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    permute_scatter_kernel(const int32_t* __restrict__ ids, int n, int E,
+                           const int32_t* __restrict__ table, int32_t* __restrict__ perm,
+                           int32_t* __restrict__ slot_pos) {
+  __shared__ int wbase[kScatterWarps][kMaxExperts];
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kScatterWarps * kMaxExperts; i += blockDim.x)
+    (&wbase[0][0])[i] = 0;
+  __syncthreads();
+  const int wbeg = blockIdx.x * kPermuteChunk + w * kPerWarp;
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  // per-warp histogram
+  for (int r = 0; r < kPerWarp / 32; ++r) {
+    const int f = wbeg + r * 32 + lane;
+    const int e = f < n ? __ldg(ids + f) : -1;
+    const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // per-expert exclusive scan across the warps, on top of the chunk's base
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = table[(size_t)blockIdx.x * E + e];
+    for (int ww = 0; ww < kScatterWarps; ++ww) {
+      const int v = wbase[ww][e];
+      wbase[ww][e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // positions
+  for (int r = 0; r < kPerWarp / 32; ++r) {
+    const int f = wbeg + r * 32 + lane;
+    const int e = f < n ? __ldg(ids + f) : -1;
+    const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (valid) {
+      const int pos = wbase[w][e] + __popc(peers & lt_mask);
+      perm[pos] = f;
+      slot_pos[f] = pos;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __restrict__ perm,
+                                                             const uint4* __restrict__ x, int n,
+                                                             int k, int vec_per_row,
+                                                             uint4* __restrict__ x_perm,
+                                                             unsigned* status) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n; pos += warps) {
+    const int f = __ldg(perm + pos);
+    if (static_cast<unsigned>(f) >= static_cast<unsigned>(n)) {
+      if (lane == 0) atomicOr(status, kStatusDeviceCheck);
+      continue;
+    }
+    const uint4* src = x + (size_t)(f / k) * vec_per_row;
+    uint4* dst = x_perm + (size_t)pos * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
+                  d = __ldg(src + v + 96);
+      dst[v] = a; dst[v + 32] = b; dst[v + 64] = c; dst[v + 96] = d;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+__global__ void __launch_bounds__(1024) combine_kernel(const float* __restrict__ y,
+                                                       const int32_t* __restrict__ slot_pos,
+                                                       const float* __restrict__ gates,
+                                                       const float* __restrict__ y_shared, int T,
+                                                       int d, int k, int rows,
+                                                       __nv_bfloat16* __restrict__ out,
+                                                       unsigned* status) {
+  __shared__ int s_pos[kMaxTopK];
+  __shared__ float s_g[kMaxTopK];
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    if (threadIdx.x < kMaxTopK) {
+      int p = -1;
+      float g = 0.0f;
+      if (threadIdx.x < k) {
+        p = __ldg(slot_pos + (size_t)t * k + threadIdx.x);
+        g = __ldg(gates + (size_t)t * k + threadIdx.x);
+        if (static_cast<unsigned>(p) >= static_cast<unsigned>(rows)) {
+          atomicOr(status, kStatusDeviceCheck);
+          p = -1;
+        }
+      }
+      s_pos[threadIdx.x] = p;
+      s_g[threadIdx.x] = g;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        const int p = s_pos[j];
+        if (p >= 0) {
+          const float4* src = reinterpret_cast<const float4*>(y + (size_t)p * d + c);
+          const float4 lo = __ldg(src), hi = __ldg(src + 1);
+          const float g = s_g[j];
+          acc[0] = fmaf(g, lo.x, acc[0]); acc[1] = fmaf(g, lo.y, acc[1]);
+          acc[2] = fmaf(g, lo.z, acc[2]); acc[3] = fmaf(g, lo.w, acc[3]);
+          acc[4] = fmaf(g, hi.x, acc[4]); acc[5] = fmaf(g, hi.y, acc[5]);
+          acc[6] = fmaf(g, hi.z, acc[6]); acc[7] = fmaf(g, hi.w, acc[7]);
+        }
+      }
+      if (y_shared) {
+        const float4* src = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(out + (size_t)t * d + c) = o;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, int T, int d, int E,
+                           int top_k, int32_t* counts, int32_t* offsets, int32_t* perm,
+                           int32_t* slot_pos, void* x_perm, int32_t* chunk_table,
+                           unsigned* status) {
+  const int n = T * top_k;
+  const int nchunks = (n + kPermuteChunk - 1) / kPermuteChunk;
+  {
+    KernelScope scope(s, "moe_permute_count");
+    permute_count_kernel<<<nchunks, 512, 0, s>>>(ids, n, E, chunk_table, status);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    KernelScope scope(s, "moe_permute_scan");
+    permute_scan_kernel<<<1, kMaxExperts, 0, s>>>(chunk_table, nchunks, E, counts, offsets);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    KernelScope scope(s, "moe_permute_scatter");
+    permute_scatter_kernel<<<nchunks, kScatterWarps * 32, 0, s>>>(ids, n, E, chunk_table, perm,
+                                                                   slot_pos);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || x == nullptr) return e;
+  const int warps_per_cta = 8;
+  const int grid = std::min((n + warps_per_cta - 1) / warps_per_cta, device_sm_count() * 8);
+  {
+    KernelScope scope(s, "moe_permute_gather");
+    permute_gather_kernel<<<grid, warps_per_cta * 32, 0, s>>>(
+        perm, static_cast<const uint4*>(x), n, top_k, d / 8, static_cast<uint4*>(x_perm), status);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_pos,
+                           const float* gates, const float* y_shared, int T, int d, int top_k,
+                           void* out, unsigned* status) {
+  int threads = d / 8;
+  if (threads > 1024) threads = 1024;
+  threads = ((threads + 31) / 32) * 32;
+  const int grid = std::min(T, 65535 * 4);
+  {
+    KernelScope scope(s, "moe_combine");
+    combine_kernel<<<grid, threads, 0, s>>>(y, slot_pos, gates, y_shared, T, d, top_k,
+                                            T * top_k, static_cast<__nv_bfloat16*>(out), status);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,70 @@
+"""Full-size workloads, run exactly as the benchmark runs them (one
+moe_forward call on the default workspace), checked against the oracle:
+routing for every token, counts / offsets / permutation bit for bit, and the
+layer output on a seeded sample of tokens that the oracle computes one by one."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_20_gb300 import counters
+from mixture_experts_layer_20_gb300 import workloads as W
+from tests.gpu_util import ExpertsOnHost, assert_layer_close, compare_routing, f64
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE = 16
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_layer_20_gb300 import binding
+    return binding
+
+
+@pytest.mark.parametrize("name", [W.DECODE, W.PREFILL, W.SKEWED, W.DEEPSEEK])
+def test_full_size_sampled(moe, name):
+    w = W.WORKLOADS[name]
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k, w.I_shared)
+    out = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], w.top_k, ws=ws,
+                          router_bias=p["router_bias"], w_gate_up_shared=p["w_gate_up_shared"],
+                          w_down_shared=p["w_down_shared"])
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, w.T, w.d, w.E, w.I, w.top_k, w.I_shared)
+    bias = None if p["router_bias"] is None else p["router_bias"].cpu().numpy()
+    ids_ref, gates_ref, logits = oracle.route(W.to_bits(x), W.to_bits(p["w_router"]), w.top_k, bias)
+    ids = v["topk_ids"].cpu().numpy()
+    differ = compare_routing(ids, v["topk_gates"].cpu().numpy(), ids_ref, gates_ref, logits, w.top_k)
+    print(f"{name}: {differ.size} near-tie tokens routed differently: {differ.tolist()}")
+
+    counts = v["expert_counts"].cpu().numpy()
+    assert counts.sum() == w.T * w.top_k
+    if differ.size == 0:
+        c_ref, o_ref, p_ref, s_ref = oracle.permute(ids_ref, w.E)
+        assert np.array_equal(counts, c_ref)
+        assert np.array_equal(v["expert_offsets"].cpu().numpy(), o_ref)
+        assert np.array_equal(v["perm"].cpu().numpy(), p_ref)
+        assert np.array_equal(v["slot_pos"].cpu().numpy(), s_ref)
+    else:  # the grouping is still the exact stable grouping of the GPU's own ids
+        c_ref, o_ref, p_ref, s_ref = oracle.permute(ids, w.E)
+        assert np.array_equal(v["perm"].cpu().numpy(), p_ref)
+    if name == W.DECODE:
+        active = int((counts > 0).sum())
+        expect = counters.expected_active_experts(w.E, w.top_k, w.T)
+        assert 120 <= active <= 128, (active, expect)
+
+    rng = np.random.default_rng(7)
+    cand = np.setdiff1d(np.arange(w.T), differ)
+    tokens = np.unique(np.concatenate([[cand[0], cand[-1]],
+                                       rng.choice(cand, SAMPLE - 2, replace=False)]))
+    ref = oracle.forward_tokens(
+        W.to_bits(x), tokens, ids_ref, gates_ref, ExpertsOnHost(p["w_gate_up"]),
+        ExpertsOnHost(p["w_down"]),
+        None if p["w_gate_up_shared"] is None else W.to_bits(p["w_gate_up_shared"]),
+        None if p["w_down_shared"] is None else W.to_bits(p["w_down_shared"]))
+    got = f64(out[torch.as_tensor(tokens, device="cuda")])
+    max_rel, mean_rel = assert_layer_close(got, ref, name)
+    print(f"{name}: sampled {tokens.size} tokens max_rel={max_rel:.3e} mean_rel={mean_rel:.3e}")

@@ -1,0 +1,79 @@
+"""Device-side status reporting: bad indices are skipped and flagged (no
+fault), and a device wait that runs out of time gives up with
+MOE_ERR_TIMEOUT and leaves the context usable.
+
+The timeout is provoked by shortening the bound on every wait to 1 ns, so the
+first wait that is not already satisfied gives up.  The kernel then records
+the timeout, drains its own copies and tensor-core work in flight, frees its
+tensor memory and returns; the next call with the normal bound must succeed
+and match a run made before."""
+
+import pytest
+import torch
+
+from mixture_experts_layer_20_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_layer_20_gb300 import binding
+    return binding
+
+
+def _layer(T=300, d=512, E=16, k=4, I=256):
+    w = W.Workload("s", T, d, E, k, I, seed=1)
+    return w, W.make_x(w, device="cuda"), W.make_weights(w, device="cuda")
+
+
+def test_bad_expert_ids_are_flagged(moe):
+    ids, _ = W.random_routing(100, 8, 2, seed=2)
+    ids[17, 1] = 8          # out of range
+    ids[50, 0] = -3
+    ws = moe.new_workspace(100, 64, 8, 64, 2)
+    moe.moe_permute(ids.cuda(), 8, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_CHECK
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK   # reading clears it
+
+
+def test_bad_offsets_are_flagged(moe):
+    w, x, p = _layer()
+    x_perm = torch.zeros((40, w.d), dtype=torch.bfloat16, device="cuda")
+    offsets = torch.zeros(w.E + 1, dtype=torch.int32, device="cuda")
+    offsets[5:] = 50        # ends past the 40 rows
+    ws = moe.new_workspace(40, w.d, w.E, w.I, 1)
+    moe.moe_expert_ffn(x_perm, offsets, p["w_gate_up"], p["w_down"], ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_CHECK
+    offsets[5:] = 40
+    offsets[3] = 45         # goes down
+    moe.moe_expert_ffn(x_perm, offsets, p["w_gate_up"], p["w_down"], ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_CHECK
+
+
+def test_bad_slot_positions_are_flagged(moe):
+    y = torch.ones((20, 64), device="cuda")
+    slot_pos = torch.arange(20, dtype=torch.int32, device="cuda").view(10, 2).contiguous()
+    slot_pos[3, 1] = 20
+    gates = torch.full((10, 2), 0.5, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    out = moe.moe_combine(y, slot_pos, gates, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_CHECK
+    assert out[0].float().eq(1.0).all()
+
+
+def test_wait_timeout_is_reported_and_recoverable(moe):
+    w, x, p = _layer()
+    ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k)
+    ref = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], w.top_k, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    try:
+        moe.moe_set_wait_timeout_ns(1)
+        moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], w.top_k, ws=ws)
+        st = moe.moe_get_device_status(ws)
+    finally:
+        moe.moe_set_wait_timeout_ns(0)
+    assert st == moe.MOE_ERR_TIMEOUT
+    again = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], w.top_k, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    assert torch.equal(again, ref)
