@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the MoE FFN layer on GB300.
+
+One step = one moe_forward over one batch of T tokens: route -> group ->
+grouped SwiGLU experts -> combine, inputs resident in HBM.  Prints ONE JSON
+line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--also NAME,...]
+
+Default workload: the Qwen3-235B-A22B MoE layer on a 64-token decode batch
+(d=4096, E=128, top-8, I=1536).  Its 4.8 GB of expert weights exceed the
+129 MB L2, so every step streams them from HBM (no flush needed).
+--impl reference times the fp64 CPU oracle on the host cores instead.
+Multi-GPU (torchrun): independent replicas, one per GPU, no collective on
+the data path; value = all tokens processed / max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (prefill, decode) + % of bf16 TC peak / HBM GB/s, 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    from mixture_experts_layer_20_gb300 import workloads as W
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=W.DECODE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--also", default=W.PREFILL,
+                    help="comma-separated extra workloads measured at N=1 (empty for none)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T (smaller cases for profiler captures)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override E (smaller cases for profiler captures)")
+    return ap.parse_args()
+
+
+def pick_workload(W, args):
+    import dataclasses
+    w = W.WORKLOADS[args.workload]
+    changes = {}
+    if args.tokens:
+        changes["T"] = args.tokens
+    if args.experts:
+        changes["E"] = args.experts
+    if changes:
+        tag = ",".join(f"{k}={v}" for k, v in changes.items())
+        w = dataclasses.replace(w, name=f"{w.name}[{tag}]", **changes)
+    return w
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as f:
+            lines = [l.strip() for l in f if l.strip()]
+        os.unlink(self.file.name)
+        rows = []
+        for l in lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+        sample = inside or rows[-3:]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sample for i, v in enumerate(r[3]) if v == "Active"})
+        return {
+            "sm_mhz": statistics.median(r[1] for r in sample) if sample else None,
+            "sm_max_mhz": max(r[2] for r in sample) if sample else None,
+            "reasons": reasons,
+            "samples": len(inside),
+        }
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["mixture_experts_layer_20_gb300/csrc/moe_gemm.cu",
+                "mixture_experts_layer_20_gb300/csrc/moe_device.cuh"]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it still
+    describes the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[kernel][workload]
+        if e.get("source_sha") != source_sha(GEMM_SOURCES):
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def kernel_work(name, w, counts):
+    """Algorithmic (flops, bytes) of one launch of a kernel: each operand and
+    result counted once, weights only for experts that received rows."""
+    from mixture_experts_layer_20_gb300 import counters as C
+    T, d, E, k, I, Is = w.T, w.d, w.E, w.top_k, w.I, w.I_shared
+    rows = T * k
+    touched = sum(1 for c in counts if c > 0)
+    if name == "moe_gate_up_swiglu":
+        return 4 * rows * d * I, touched * 2 * I * d * 2 + rows * d * 2 + rows * I * 2
+    if name == "moe_down":
+        return 2 * rows * d * I, touched * d * I * 2 + rows * I * 2 + rows * d * 4
+    if name == "moe_shared_gate_up_swiglu":
+        return 4 * T * d * Is, 2 * Is * d * 2 + T * d * 2 + T * Is * 2
+    if name == "moe_shared_down":
+        return 2 * T * d * Is, d * Is * 2 + T * Is * 2 + T * d * 4
+    if name == "moe_router_topk":
+        return C.router_flops(T, d, E), T * d * 2 + E * d * 2 + rows * 8
+    if name == "moe_combine":
+        return 2 * rows * d, rows * d * 4 + T * d * 2 + rows * 8 + (T * d * 4 if Is else 0)
+    if name == "moe_permute_gather":
+        return 0, rows * d * 2 + T * d * 2 + rows * 4
+    return 0, rows * 4 * 4
+
+
+# ------------------------------------------------------------------ our arm
+
+def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, peaks):
+    import torch
+    from mixture_experts_layer_20_gb300 import counters as C
+    x = W.make_x(w, device="cuda")
+    ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k, w.I_shared)
+    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    kw = dict(out=out, ws=ws, router_bias=params["router_bias"],
+              w_gate_up_shared=params["w_gate_up_shared"], w_down_shared=params["w_down_shared"])
+
+    def step():
+        moe.moe_forward(x, params["w_router"], params["w_gate_up"], params["w_down"], w.top_k, **kw)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after warm-up")
+    views = moe.workspace_views(ws, w.T, w.d, w.E, w.I, w.top_k, w.I_shared)
+    counts = views["expert_counts"].cpu().tolist()
+
+    sampler = ClockSampler(sampler_index) if sampler_index is not None else None
+    time.sleep(0.3 if sampler else 0)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    moe.moe_profiler_collect()
+    moe.moe_profiler_enable(True)
+    l0 = moe.moe_launch_count()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record()
+    for _ in range(steps):
+        step()
+    stop.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    launches = moe.moe_launch_count() - l0
+    moe.moe_profiler_enable(False)
+    prof = moe.moe_profiler_collect()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    ms = start.elapsed_time(stop) / steps
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    if moe.moe_get_device_status(ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    # per-kernel breakdown and the dominant kernel's roofline
+    kernels = {}
+    for name, (n, tot) in prof.items():
+        fl, by = kernel_work(name, w, counts)
+        avg = tot / n
+        kernels[name] = {"launches": n, "avg_ms": round(avg, 5), "share": None,
+                         "tflops": round(fl / (avg * 1e-3) / 1e12, 2),
+                         "gbs": round(by / (avg * 1e-3) / 1e9, 1)}
+    total_k = sum(v[1] for v in prof.values()) or 1.0
+    for name, (n, tot) in prof.items():
+        kernels[name]["share"] = round(tot / total_k, 4)
+    dom = max(prof, key=lambda n: prof[n][1])
+    fl, by = kernel_work(dom, w, counts)
+    avg_s = prof[dom][1] / prof[dom][0] * 1e-3
+    region_s = ms * steps * 1e-3
+    tensor_peak = peaks["bf16_tflops_sustained"] if region_s > 1.0 else peaks["bf16_tflops"]
+    t_tensor = fl / (tensor_peak * 1e12)
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": round(fl / avg_s / 1e12, 1), "peak": tensor_peak,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(by / avg_s / 1e9, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    tr = ncu_traffic(dom, w.name)
+    roof.update({"traffic": tr, "kernel": dom, "algorithmic_bytes": by, "algorithmic_flops": fl,
+                 "avg_launch_ms": round(avg_s * 1e3, 5)})
+
+    flops = C.expert_flops(w.T, w.top_k, w.d, w.I, w.I_shared)
+    abytes = C.algorithmic_bytes(counts, w.T, w.d, w.E, w.I, w.I_shared)
+    layer = {
+        "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+        "tc_peak_frac": round(flops / (ms * 1e-3) / 1e12 / tensor_peak, 4),
+        "gbs": round(abytes / (ms * 1e-3) / 1e9, 1),
+        "hbm_frac": round(abytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "active_experts": sum(1 for c in counts if c > 0),
+        "padded_rows_128": C.padded_rows(counts, 128),
+    }
+    return {"ms": ms, "tokens_per_s": w.T * world / (ms * 1e-3), "launches": launches,
+            "clocks": clocks, "roofline": roof, "kernels": kernels, "layer": layer,
+            "x": x, "ws": ws, "counts": counts}
+
+
+def measure_e2e(moe, w, params, ws, x, steps):
+    """Tokens/s through moe_forward_host: H2D of x from pinned memory, the
+    layer, D2H of out, and a stream synchronisation every step."""
+    import torch
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    kw = dict(router_bias=params["router_bias"], w_gate_up_shared=params["w_gate_up_shared"],
+              w_down_shared=params["w_down_shared"])
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        moe.moe_forward_host(x_host, params["w_router"], params["w_gate_up"], params["w_down"],
+                             w.top_k, out_host, ws, **kw)
+        s.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        moe.moe_forward_host(x_host, params["w_router"], params["w_gate_up"], params["w_down"],
+                             w.top_k, out_host, ws, **kw)
+        s.synchronize()
+    el = time.perf_counter() - t0
+    nbytes = w.T * w.d * 2
+    return {"value": round(w.T * steps / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": nbytes}
+
+
+def cpu_baseline(W, w, params, x, target_s=15.0):
+    """The oracle, as it stands, on the first S tokens of the same batch."""
+    import numpy as np
+    import oracle
+    xb = W.to_bits(x)
+    wr = W.to_bits(params["w_router"])
+    bias = None if params["router_bias"] is None else params["router_bias"].cpu().numpy()
+    shared = (W.to_bits(params["w_gate_up_shared"]), W.to_bits(params["w_down_shared"])) \
+        if params["w_gate_up_shared"] is not None else (None, None)
+
+    class Host:
+        def __init__(self, t): self.t, self.c = t, {}
+        def __getitem__(self, e):
+            e = int(e)
+            if e not in self.c:
+                self.c[e] = W.to_bits(self.t[e])
+            return self.c[e]
+
+    gu, dn = Host(params["w_gate_up"]), Host(params["w_down"])
+
+    def run(S):
+        ids, _, _ = oracle.route(xb[:S], wr, w.top_k, bias)
+        for e in np.unique(ids):       # host copies of the weights are not timed
+            gu[e]; dn[e]
+        c0, t0 = time.process_time(), time.perf_counter()
+        oracle.forward(xb[:S], wr, gu, dn, w.top_k, router_bias=bias,
+                       w_gate_up_shared=shared[0], w_down_shared=shared[1])
+        return time.perf_counter() - t0, time.process_time() - c0
+
+    el1, _ = run(1)
+    S = int(max(1, min(w.T, target_s / max(el1, 1e-3) * 0.5)))
+    el, cpu = run(S)
+    return {"value": round(S / el, 3), "unit": "tokens/s", "cores": round(cpu / el, 1),
+            "host_cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {S} of {w.T} tokens of {w.name}, {el:.1f} s wall"}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def reference_arm(args):
+    import numpy as np
+    import torch
+    import oracle
+    from mixture_experts_layer_20_gb300 import workloads as W
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = pick_workload(W, args)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    params = W.make_weights(w, device=dev)
+    x = W.make_x(w, device=dev)
+    xb = W.to_bits(x)
+    wr = W.to_bits(params["w_router"])
+    bias = None if params["router_bias"] is None else params["router_bias"].cpu().numpy()
+    shared = (W.to_bits(params["w_gate_up_shared"]), W.to_bits(params["w_down_shared"])) \
+        if params["w_gate_up_shared"] is not None else (None, None)
+    cache_gu, cache_d = {}, {}
+
+    class Host:
+        def __init__(self, t, c): self.t, self.c = t, c
+        def __getitem__(self, e):
+            e = int(e)
+            if e not in self.c:
+                self.c[e] = W.to_bits(self.t[e])
+            return self.c[e]
+
+    gu, dn = Host(params["w_gate_up"], cache_gu), Host(params["w_down"], cache_d)
+
+    def tokens(i, S):
+        return [(i * S + j) % w.T for j in range(S)]
+
+    def one(i, S):
+        idx = tokens(i, S)
+        ids, _, _ = oracle.route(xb[idx], wr, w.top_k, bias)
+        for e in np.unique(ids):
+            gu[e]; dn[e]
+        t0 = time.perf_counter()
+        oracle.forward(xb[idx], wr, gu, dn, w.top_k, router_bias=bias,
+                       w_gate_up_shared=shared[0], w_down_shared=shared[1])
+        return time.perf_counter() - t0
+
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    S = max(1, min(w.T, int(budget / max(one(0, 1), 1e-3) * 0.7)))
+    for i in range(args.warmup):
+        one(i, S)
+    c0 = time.process_time()
+    times = [one(args.warmup + i, S) for i in range(args.steps)]
+    cpu = time.process_time() - c0
+    el = sum(times)
+    value = S * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "top_k": w.top_k, "I": w.I,
+                   "I_shared": w.I_shared, "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle",
+                         "cores": round(cpu / el, 1), "host_cores": os.cpu_count(),
+                         "sample": f"{S} tokens of {w.name} per step (rotating through the batch)"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    from mixture_experts_layer_20_gb300 import binding as moe
+    from mixture_experts_layer_20_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = vis.split(",")[local] if vis else local
+    peaks, peak_src = load_peaks()
+
+    w = pick_workload(W, args)
+    params = W.make_weights(w, device="cuda")
+    r = measure(moe, W, w, params, args.steps, args.warmup, rank, world, dist, smi_index, peaks)
+    e2e = measure_e2e(moe, w, params, r["ws"], r["x"], max(10, min(args.steps, 100)))
+    if dist:
+        t = torch.tensor([e2e["value"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MIN)
+        e2e["value"] = round(t.item() * world, 1)
+
+    also = []
+    if world == 1 and args.also:
+        for name in [n for n in args.also.split(",") if n]:
+            wa = W.WORKLOADS[name]
+            same = (wa.d, wa.E, wa.I, wa.I_shared, wa.zipf_bias, wa.seed) == \
+                (w.d, w.E, w.I, w.I_shared, w.zipf_bias, w.seed)
+            pa = params if same else W.make_weights(wa, device="cuda")
+            ra = measure(moe, W, wa, pa, max(3, args.steps // 10), 3, 0, 1, None, None, peaks)
+            also.append({"workload": name, "value": round(ra["tokens_per_s"], 1),
+                         "unit": "tokens/s", "ms_per_step": round(ra["ms"], 4),
+                         "layer": ra["layer"], "roofline": ra["roofline"],
+                         "kernels": ra["kernels"]})
+            del ra
+            if not same:
+                del pa
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(W, w, params, r["x"])
+
+    if rank == 0:
+        r["roofline"]["peak_source"] = peak_src
+        line = {
+            "metric": METRIC, "value": round(r["tokens_per_s"], 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(r["ms"], 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Gaussian x and weights)",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "top_k": w.top_k,
+                       "I": w.I, "I_shared": w.I_shared, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: every step streams the touched expert "
+                             "weights (up to 4.8 GB) from HBM"},
+            "clocks": r["clocks"], "e2e": e2e, "gpu_launches": r["launches"],
+            "roofline": r["roofline"], "cpu_baseline": cpu, "layer": r["layer"],
+            "kernels": r["kernels"], "also": also,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -146,11 +146,24 @@ moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
                             void* ws, size_t ws_bytes, moe_stream_t stream,
                             const moe_forward_ext_t* ext);
 
+/* The whole layer on host buffers: x_host [T,d] and out_host [T,d] are in host
+ * memory (pinned for asynchronous copies); weights stay on the device.  The
+ * copies go through the workspace (regions x_stage / out_stage) and are
+ * queued on `stream` with the layer between them; the call returns without
+ * synchronising, so out_host is ready once the stream reaches this point.
+ * ext may be NULL. */
+moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
+                              const moe_bf16* w_gate_up, const moe_bf16* w_down,
+                              int T, int d, int E, int I, int top_k, moe_bf16* out_host,
+                              void* ws, size_t ws_bytes, moe_stream_t stream,
+                              const moe_forward_ext_t* ext);
+
 /* Where moe_forward(_ex) keeps its intermediates: byte offsets into `ws`
  * (each 256-byte aligned) for the same shapes. */
 typedef struct {
   size_t status, topk_ids, topk_gates, expert_counts, expert_offsets, perm,
-         slot_pos, chunk_table, x_perm, h, h_shared, y, y_shared, total;
+         slot_pos, chunk_table, x_perm, h, h_shared, y, y_shared, x_stage, out_stage,
+         total;
 } moe_workspace_layout_t;
 
 moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,

@@ -26,7 +26,8 @@ _vp, _i, _sz, _st = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "topk_ids", "topk_gates", "expert_counts", "expert_offsets", "perm",
-        "slot_pos", "chunk_table", "x_perm", "h", "h_shared", "y", "y_shared", "total")]
+        "slot_pos", "chunk_table", "x_perm", "h", "h_shared", "y", "y_shared", "x_stage",
+        "out_stage", "total")]
 
 
 class ForwardExt(ctypes.Structure):
@@ -44,6 +45,8 @@ _SIGS = {
     "moe_forward": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "moe_forward_ex": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp,
                              ctypes.POINTER(ForwardExt)]),
+    "moe_forward_host": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp,
+                               ctypes.POINTER(ForwardExt)]),
     "moe_workspace_layout": (_st, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(WorkspaceLayout)]),
     "moe_get_device_status": (_st, [_vp, _sz, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_st]),
@@ -245,6 +248,28 @@ def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router
                                  top_k, _p(out), _p(ws), ws.numel(), s, ctypes.byref(ext))
     _check(st, "moe_forward")
     return out
+
+
+def moe_forward_host(x_host, w_router, w_gate_up, w_down, top_k, out_host, ws,
+                     router_bias=None, w_gate_up_shared=None, w_down_shared=None, stream=None):
+    """The whole layer on host tensors (pinned for async copies); queued on
+    the stream, not synchronised."""
+    if x_host.is_cuda or out_host.is_cuda or x_host.dtype != torch.bfloat16 \
+            or out_host.dtype != torch.bfloat16:
+        raise ValueError("x_host and out_host must be bf16 host tensors")
+    for t, n in ((w_router, "w_router"), (w_gate_up, "w_gate_up"), (w_down, "w_down"),
+                 (w_gate_up_shared, "w_gate_up_shared"), (w_down_shared, "w_down_shared")):
+        _want(t, torch.bfloat16, n)
+    T, d = x_host.shape
+    E, I2, _ = w_gate_up.shape
+    I_s = w_down_shared.shape[1] if w_down_shared is not None else 0
+    ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
+                     w_gate_up_shared.data_ptr() if I_s else None,
+                     w_down_shared.data_ptr() if I_s else None, I_s)
+    _check(_lib.moe_forward_host(_p(x_host), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E,
+                                 I2 // 2, top_k, _p(out_host), _p(ws), ws.numel(), _stream(stream),
+                                 ctypes.byref(ext)), "moe_forward_host")
+    return out_host
 
 
 def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0) -> dict:

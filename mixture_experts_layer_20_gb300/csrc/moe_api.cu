@@ -75,7 +75,7 @@ moe_status_t check_shapes(int T, int d, int E, int I, int top_k) {
 
 struct Layout {
   size_t status, ids, gates, counts, offsets, perm, slot_pos, chunk, x_perm, h, h_shared, y,
-      y_shared, total;
+      y_shared, x_stage, out_stage, total;
 };
 
 Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
@@ -97,6 +97,8 @@ Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
   L.h_shared = take(static_cast<size_t>(T) * I_shared * 2);
   L.y = take(n * d * 4);
   L.y_shared = take(I_shared ? static_cast<size_t>(T) * d * 4 : 0);
+  L.x_stage = take(static_cast<size_t>(T) * d * 2);
+  L.out_stage = take(static_cast<size_t>(T) * d * 2);
   L.total = off;
   return L;
 }
@@ -202,6 +204,8 @@ moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_s
   out->h_shared = L.h_shared;
   out->y = L.y;
   out->y_shared = L.y_shared;
+  out->x_stage = L.x_stage;
+  out->out_stage = L.out_stage;
   out->total = L.total;
   return MOE_OK;
 }
@@ -350,6 +354,32 @@ moe_status_t moe_forward(const moe_bf16* x, const moe_bf16* w_router, const moe_
                          moe_bf16* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
   return moe_forward_ex(x, w_router, w_gate_up, w_down, T, d, E, I, top_k, out, ws, ws_bytes,
                         stream, nullptr);
+}
+
+moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
+                              const moe_bf16* w_gate_up, const moe_bf16* w_down, int T, int d,
+                              int E, int I, int top_k, moe_bf16* out_host, void* ws,
+                              size_t ws_bytes, moe_stream_t stream, const moe_forward_ext_t* ext) {
+  moe_status_t st = check_shapes(T, d, E, I, top_k);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host || !ws) return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: null pointer");
+  const int I_shared = ext ? ext->I_shared : 0;
+  const Layout L = forward_layout(T, d, E, I, top_k, I_shared);
+  if (ws_bytes < L.total || !aligned16(ws))
+    return fail(MOE_ERR_WORKSPACE, "moe_forward_host: workspace too small");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  moe_bf16* x_dev = reinterpret_cast<moe_bf16*>(w + L.x_stage);
+  moe_bf16* out_dev = reinterpret_cast<moe_bf16*>(w + L.out_stage);
+  const size_t bytes = static_cast<size_t>(T) * d * 2;
+  cudaError_t e = cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync x");
+  st = moe_forward_ex(x_dev, w_router, w_gate_up, w_down, T, d, E, I, top_k, out_dev, ws,
+                      ws_bytes, stream, ext);
+  if (st != MOE_OK) return st;
+  e = cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaMemcpyAsync out");
 }
 
 moe_status_t moe_get_device_status(void* ws, size_t ws_bytes, moe_stream_t stream) {

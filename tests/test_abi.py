@@ -78,7 +78,8 @@ def test_workspace_layout():
     assert lay["x_perm"] + n * d * 2 <= lay["h"]
     assert lay["y"] + n * d * 4 <= lay["total"]
     lay5 = b.moe_workspace_layout(8192, 7168, 256, 2048, 8, 2048)
-    assert lay5["y_shared"] + 8192 * 7168 * 4 == lay5["total"]
+    assert lay5["y_shared"] + 8192 * 7168 * 4 <= lay5["x_stage"]
+    assert lay5["out_stage"] + 8192 * 7168 * 2 == lay5["total"]
 
 
 def test_status_strings():
