@@ -98,6 +98,37 @@ moe_status_t moe_permute(const int32_t* topk_ids, const moe_bf16* x,
                          int32_t* perm, int32_t* slot_pos, moe_bf16* x_perm,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Step 2 for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call: it is a convenience of this library.
+ *
+ * Same arguments and results as moe_permute, without the workspace.  Some
+ * callers have no device memory to give: a serving process that reserved
+ * the GPU's memory for its own pool at start-up (a cudaMalloc here would fail
+ * or fragment that pool), or a host framework whose plugin interface hands a
+ * kernel only its inputs and outputs.  For them the grouping's one scratch
+ * buffer (the per-chunk, per-expert count table) lives in a fixed device
+ * array inside this library: 256 KB plus a 256-byte status word, held on
+ * every GPU that loads the library until the process exits.  This call
+ * allocates and frees nothing.
+ *
+ * Limit: ceil(T*top_k / 4096) * E <= 65536, e.g. T*top_k <= 1,048,576 with
+ * E = 256; larger sizes return MOE_ERR_UNSUPPORTED with a message naming the
+ * limit (use moe_permute for them).
+ * device_status: a device uint32 into which the kernels OR their status bits
+ * (1 = a wait gave up, 2 = an expert id out of range was skipped); the caller
+ * zeroes it.  If NULL, the bits go to the library's own status word, which
+ * each call clears first and which cannot be read back.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the array: calls whose work
+ * can overlap on the GPU (unordered streams) race and may give wrong
+ * results, so order them on one stream. */
+moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, const moe_bf16* x,
+                                        int T, int d, int E, int top_k,
+                                        int32_t* expert_counts, int32_t* expert_offsets,
+                                        int32_t* perm, int32_t* slot_pos, moe_bf16* x_perm,
+                                        uint32_t* device_status, moe_stream_t stream);
+
 /* Step 3, grouped expert FFN.  Rows [expert_offsets[e], expert_offsets[e+1])
  * of x_perm [rows,d] go through expert e: w_gate_up [E,2I,d] (per expert,
  * rows [0,I) gate, [I,2I) up), w_down [E,d,I].  Writes y [rows,d] fp32.

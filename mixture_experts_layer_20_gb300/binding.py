@@ -40,6 +40,8 @@ _SIGS = {
     "moe_workspace_init": (_st, [_vp, _sz, _vp]),
     "moe_route": (_st, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_permute_static_scratch": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _vp]),
     "moe_expert_ffn": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "moe_combine": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "moe_forward": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
@@ -186,6 +188,26 @@ def moe_permute(topk_ids, E, x=None, ws=None, stream=None):
     _check(_lib.moe_permute(_p(topk_ids), _p(x), T, d, E, k, _p(counts), _p(offsets), _p(perm),
                             _p(slot_pos), _p(x_perm), _p(ws), ws.numel(), _stream(stream)),
            "moe_permute")
+    return counts, offsets, perm, slot_pos, x_perm
+
+
+def moe_permute_static_scratch(topk_ids, E, x=None, device_status=None, stream=None):
+    """moe_permute without a workspace: the scratch table lives in the
+    library's own fixed device array (for callers that cannot allocate)."""
+    _want(topk_ids, torch.int32, "topk_ids"); _want(x, torch.bfloat16, "x")
+    _want(device_status, torch.int32, "device_status")
+    T, k = topk_ids.shape
+    d = x.shape[1] if x is not None else 64
+    dev = topk_ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    slot_pos = torch.empty((T, k), dtype=torch.int32, device=dev)
+    x_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device=dev) if x is not None else None
+    _check(_lib.moe_permute_static_scratch(_p(topk_ids), _p(x), T, d, E, k, _p(counts),
+                                           _p(offsets), _p(perm), _p(slot_pos), _p(x_perm),
+                                           _p(device_status), _stream(stream)),
+           "moe_permute_static_scratch")
     return counts, offsets, perm, slot_pos, x_perm
 
 

@@ -131,6 +131,8 @@ KernelScope::~KernelScope() {
   cudaEventRecord(g_records[slot_].stop, stream_);
 }
 
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+
 int device_sm_count() {
   static int cached[64] = {0};
   int dev = 0;

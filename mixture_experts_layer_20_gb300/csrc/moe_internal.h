@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <string>
 
 namespace moe {
 
@@ -30,6 +31,9 @@ class KernelScope {
 };
 
 int device_sm_count();
+
+// Message returned by moe_last_error() on this thread.  Defined in moe_api.cu.
+void set_last_error(const std::string& msg);
 
 // ---- tcgen05 GEMM launchers (moe_gemm.cu).  Return a CUDA error code.
 
