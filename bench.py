@@ -40,7 +40,7 @@ def parse_args():
     from mixture_experts_layer_20_gb300 import workloads as W
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=W.DECODE, choices=sorted(W.WORKLOADS))
@@ -172,8 +172,11 @@ def kernel_work(name, w, counts):
         return 4 * T * d * Is, 2 * Is * d * 2 + T * d * 2 + T * Is * 2
     if name == "moe_shared_down":
         return 2 * T * d * Is, d * Is * 2 + T * Is * 2 + T * d * 4
+    partial = ((d + 511) // 512) * T * ((E + 15) // 16 * 16) * 4
+    if name == "moe_router_logits":
+        return C.router_flops(T, d, E), T * d * 2 + E * d * 2 + partial
     if name == "moe_router_topk":
-        return C.router_flops(T, d, E), T * d * 2 + E * d * 2 + rows * 8
+        return 0, partial + rows * 8
     if name == "moe_combine":
         return 2 * rows * d, rows * d * 4 + T * d * 2 + rows * 8 + (T * d * 4 if Is else 0)
     if name == "moe_permute_gather":

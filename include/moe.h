@@ -74,7 +74,10 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
  * NULL (added to the logits before selection and gating).  Writes
  * topk_ids [T,top_k] int32 (ascending within a token) and topk_gates
  * [T,top_k] fp32 (sum to 1 per token).  Logits are fp32 sums of bf16
- * products on the tensor cores.
+ * products on the tensor cores, accumulated over 512-wide ranges of d and
+ * then added in range order, so a token's result does not depend on the
+ * other tokens of the batch.  ws: at least moe_workspace_size(T, d, E, 64,
+ * top_k, 0) bytes (it holds the partial sums).
  * Cite: 'PagedAttention, speculative decoding, MoE and Blackwell', section 2
  * (gating network, top-K); 'Chapter 9. Distributed inference', section 9.3.4. */
 moe_status_t moe_route(const moe_bf16* x, const moe_bf16* w_router,
@@ -192,7 +195,7 @@ moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
 /* Where moe_forward(_ex) keeps its intermediates: byte offsets into `ws`
  * (each 256-byte aligned) for the same shapes. */
 typedef struct {
-  size_t status, topk_ids, topk_gates, expert_counts, expert_offsets, perm,
+  size_t status, router_logits, topk_ids, topk_gates, expert_counts, expert_offsets, perm,
          slot_pos, chunk_table, x_perm, h, h_shared, y, y_shared, x_stage, out_stage,
          total;
 } moe_workspace_layout_t;

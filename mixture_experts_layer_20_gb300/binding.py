@@ -25,7 +25,7 @@ _vp, _i, _sz, _st = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int
 
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "status", "topk_ids", "topk_gates", "expert_counts", "expert_offsets", "perm",
+        "status", "router_logits", "topk_ids", "topk_gates", "expert_counts", "expert_offsets", "perm",
         "slot_pos", "chunk_table", "x_perm", "h", "h_shared", "y", "y_shared", "x_stage",
         "out_stage", "total")]
 
@@ -166,7 +166,7 @@ def moe_route(x, w_router, top_k, router_bias=None, topk_ids=None, topk_gates=No
         topk_gates = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
     _want(topk_ids, torch.int32, "topk_ids"); _want(topk_gates, torch.float32, "topk_gates")
     if ws is None:
-        ws = torch.zeros(256, dtype=torch.uint8, device=x.device)
+        ws = new_workspace(T, d, E, 64, top_k, device=x.device)
     _check(_lib.moe_route(_p(x), _p(w_router), _p(router_bias), T, d, E, top_k, _p(topk_ids),
                           _p(topk_gates), _p(ws), ws.numel(), _stream(stream)), "moe_route")
     return topk_ids, topk_gates

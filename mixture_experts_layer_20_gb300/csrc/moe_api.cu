@@ -74,8 +74,8 @@ moe_status_t check_shapes(int T, int d, int E, int I, int top_k) {
 }
 
 struct Layout {
-  size_t status, ids, gates, counts, offsets, perm, slot_pos, chunk, x_perm, h, h_shared, y,
-      y_shared, x_stage, out_stage, total;
+  size_t status, logits, ids, gates, counts, offsets, perm, slot_pos, chunk, x_perm, h, h_shared,
+      y, y_shared, x_stage, out_stage, total;
 };
 
 Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
@@ -85,6 +85,7 @@ Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t at = off; off += align_up(bytes); return at; };
   L.status = take(kAlign);
+  L.logits = take(router_partial_bytes(T, d, E));
   L.ids = take(n * 4);
   L.gates = take(n * 4);
   L.counts = take(static_cast<size_t>(E) * 4);
@@ -169,9 +170,9 @@ moe_status_t check_device() {
 }
 
 moe_status_t route_impl(const moe_bf16* x, const moe_bf16* w_router, const float* bias, int T,
-                        int d, int E, int top_k, int32_t* ids, float* gates, unsigned* status,
-                        cudaStream_t s) {
-  cudaError_t e = launch_router(s, x, w_router, bias, T, d, E, top_k, ids, gates, status,
+                        int d, int E, int top_k, int32_t* ids, float* gates, float* partial,
+                        unsigned* status, cudaStream_t s) {
+  cudaError_t e = launch_router(s, x, w_router, bias, T, d, E, top_k, ids, gates, partial, status,
                                 g_timeout_ns.load());
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router launch");
 }
@@ -194,6 +195,7 @@ moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_s
     return fail(MOE_ERR_INVALID_ARG, "bad arguments to moe_workspace_layout");
   const Layout L = forward_layout(T, d, E, I, top_k, I_shared);
   out->status = L.status;
+  out->router_logits = L.logits;
   out->topk_ids = L.ids;
   out->topk_gates = L.gates;
   out->expert_counts = L.counts;
@@ -229,9 +231,11 @@ moe_status_t moe_route(const moe_bf16* x, const moe_bf16* w_router, const float*
     return fail(MOE_ERR_INVALID_ARG, "moe_route: null pointer");
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(ws))
     return fail(MOE_ERR_INVALID_ARG, "moe_route: pointers must be 16-byte aligned");
-  if (ws_bytes < kAlign) return fail(MOE_ERR_WORKSPACE, "moe_route: workspace too small");
+  if (ws_bytes < kAlign + router_partial_bytes(T, d, E))
+    return fail(MOE_ERR_WORKSPACE, "moe_route: workspace too small");
   if ((st = check_device()) != MOE_OK) return st;
-  return route_impl(x, w_router, router_bias, T, d, E, top_k, topk_ids, topk_gates,
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kAlign);
+  return route_impl(x, w_router, router_bias, T, d, E, top_k, topk_ids, topk_gates, partial,
                     status_word(ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -333,7 +337,9 @@ moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
   const unsigned long long tmo = g_timeout_ns.load();
   const int rows = T * top_k;
 
-  if ((st = route_impl(x, w_router, bias, T, d, E, top_k, ids, gates, status, s)) != MOE_OK)
+  float* partial = reinterpret_cast<float*>(w + L.logits);
+  if ((st = route_impl(x, w_router, bias, T, d, E, top_k, ids, gates, partial, status, s)) !=
+      MOE_OK)
     return st;
   cudaError_t e = launch_permute(s, ids, x, T, d, E, top_k, counts, offsets, perm, slot_pos,
                                  x_perm, table, status);

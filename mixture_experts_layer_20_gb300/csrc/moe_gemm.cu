@@ -1,9 +1,8 @@
 // Tensor-core kernels of the MoE layer on sm_103a: one warp-specialised,
 // persistent tcgen05 GEMM used three ways.
 //
-//   router  : logits = x W_r^T (+ b) for 128 tokens per tile, then each
-//             epilogue thread owns one token row and picks its top-k with the
-//             lowest-index tie-break and renormalised softmax gates.
+//   router  : partial logits x W_r^T over one 512-wide K range per tile
+//             (fp32); the top-k kernel sums the ranges in a fixed order.
 //   gate_up : per expert, [G | U] = x_perm W_gu^T with the gate and up rows of
 //             the same 128 output columns loaded side by side into one N=256
 //             operand; the epilogue computes h = silu(G) * U and rounds it to
@@ -44,7 +43,11 @@ constexpr int kStages = 4;
 constexpr int kMaxN = 256;
 constexpr int kABytes = kBM * kBK * 2;    // 16 KB
 constexpr int kBBytes = kMaxN * kBK * 2;  // 32 KB
-constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024;
+// Epilogue staging: per epilogue warp a 32 x 32 block of fp32 (rows padded
+// to 36 words) used to turn row-per-lane registers into row-contiguous stores.
+constexpr int kEpiStride = 36;
+constexpr int kEpiWarpBytes = 32 * kEpiStride * 4;
+constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 4 * kEpiWarpBytes + 1024;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;
@@ -71,6 +74,8 @@ struct GemmParams {
   long long ld_out;      // output row stride in elements
   unsigned* status;
   unsigned long long timeout_ns;
+  int k_splits;          // K ranges per output tile (router: d / 512; else 1)
+  int kb_per_split;      // 64-wide K blocks per range
 };
 
 __device__ __forceinline__ void decode_tile(int tau, int n_tiles, int groups, const int* s_mt,
@@ -89,116 +94,95 @@ __device__ __forceinline__ void decode_tile(int tau, int n_tiles, int groups, co
   row_end = s_off[g + 1];
 }
 
-// Keeps the 8 best (logit, expert) pairs: larger logit first, and for equal
-// logits the lower expert index first.
-__device__ __forceinline__ void topk_insert(float v, int e, float (&bv)[kMaxTopK],
-                                            int (&bi)[kMaxTopK]) {
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    const bool better = (v > bv[s]) || (v == bv[s] && e < bi[s]);
-    if (better) {
-      const float tv = bv[s]; bv[s] = v; v = tv;
-      const int ti = bi[s]; bi[s] = e; e = ti;
-    }
-  }
-}
-
+// The epilogue of one tile for one warp.  Thread `lane` owns accumulator row
+// row_base + lane (TMEM lane q*32 + lane).  Results go through `stage`, the
+// warp's padded shared-memory block, so that global stores run along rows:
+// each store instruction writes whole 64- or 128-byte row segments instead of
+// 32 separate 16-byte pieces.  Rows at or past row_end are not stored.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_row, int row,
-                                              bool valid, int n) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t t_row, int row_base,
+                                              int row_end, int n, int split, uint32_t* stage) {
+  const int lane = threadIdx.x & 31;
   if constexpr (KIND == kGateUp) {
     const int col0 = n * 128;
-    __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ld_out + col0;
+    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 1
     for (int c = 0; c < 128; c += 32) {
       uint32_t g[32], u[32];
       tmem_ld_32x32b_x32(t_row + c, g);
       tmem_ld_32x32b_x32(t_row + 128 + c, u);
       tmem_ld_wait();
-      if (valid && col0 + c < p.n_out) {
-        uint32_t packed[16];
+      if (col0 + c >= p.n_out) continue;  // uniform across the warp
+      uint32_t packed[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-          const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-          const float h0 = g0 / (1.0f + expf(-g0)) * u0;
-          const float h1 = g1 / (1.0f + expf(-g1)) * u1;
-          packed[j] = pack_bf16x2(h0, h1);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(hrow + c);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+      for (int j = 0; j < 16; ++j) {
+        const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+        const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+        const float h0 = g0 / (1.0f + expf(-g0)) * u0;
+        const float h1 = g1 / (1.0f + expf(-g1)) * u1;
+        packed[j] = pack_bf16x2(h0, h1);
       }
+      // 32 rows x 64 bytes, row pitch 20 words (80 bytes)
+      uint4* w = reinterpret_cast<uint4*>(stage + lane * 20);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < 32; r += 8) {
+        const int rr = r + (lane >> 2);
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 20 + (lane & 3) * 4);
+        const int row = row_base + rr;
+        if (row < row_end)
+          *reinterpret_cast<uint4*>(h + (size_t)row * p.ld_out + col0 + c + (lane & 3) * 8) = v;
+      }
+      __syncwarp();
     }
   } else if constexpr (KIND == kDown) {
     const int col0 = n * 256;
-    float* yrow = static_cast<float*>(p.out) + (size_t)row * p.ld_out + col0;
+    float* y = static_cast<float*>(p.out);
 #pragma unroll 1
     for (int c = 0; c < 256; c += 32) {
       uint32_t v[32];
       tmem_ld_32x32b_x32(t_row + c, v);
       tmem_ld_wait();
-      if (valid && col0 + c < p.n_out) {
-        uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+      if (col0 + c >= p.n_out) continue;  // uniform across the warp
+      // 32 rows x 128 bytes, row pitch 36 words (144 bytes)
+      uint4* w = reinterpret_cast<uint4*>(stage + lane * kEpiStride);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      for (int i = 0; i < 8; ++i) w[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < 32; r += 4) {
+        const int rr = r + (lane >> 3);
+        const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * kEpiStride + (lane & 7) * 4);
+        const int row = row_base + rr;
+        if (row < row_end)
+          *reinterpret_cast<uint4*>(y + (size_t)row * p.ld_out + col0 + c + (lane & 7) * 4) = val;
       }
+      __syncwarp();
     }
-  } else {  // router
-    float bv[kMaxTopK];
-    int bi[kMaxTopK];
-#pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) { bv[s] = -INFINITY; bi[s] = INT_MAX; }
+  } else {  // router: this K range's partial logits, fp32 [split][row][mma_n]
+    const int row = row_base + lane;
+    const bool valid = row < row_end;
+    float* dst = static_cast<float*>(p.out) + ((size_t)split * p.total_rows + row) * p.ld_out;
 #pragma unroll 1
     for (int c = 0; c < p.mma_n; c += 16) {
       uint32_t v[16];
       tmem_ld_32x32b_x16(t_row + c, v);
       tmem_ld_wait();
+      if (valid) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int e = c + j;
-        if (e < p.n_out) {
-          const float L = __uint_as_float(v[j]) + (p.bias ? __ldg(p.bias + e) : 0.0f);
-          topk_insert(L, e, bv, bi);
-        }
-      }
-    }
-    const int k = p.top_k;
-    float w[kMaxTopK];
-    float sum = 0.0f;
-#pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
-      w[s] = (s < k) ? expf(bv[s] - bv[0]) : 0.0f;
-      sum += w[s];
-      if (s >= k) bi[s] = INT_MAX;
-    }
-    // slots in ascending expert id
-#pragma unroll
-    for (int i = 0; i < kMaxTopK - 1; ++i) {
-#pragma unroll
-      for (int j = 0; j < kMaxTopK - 1 - i; ++j) {
-        if (bi[j] > bi[j + 1]) {
-          const int ti = bi[j]; bi[j] = bi[j + 1]; bi[j + 1] = ti;
-          const float tw = w[j]; w[j] = w[j + 1]; w[j + 1] = tw;
-        }
-      }
-    }
-    if (valid) {
-      int32_t* ids = static_cast<int32_t*>(p.out) + (size_t)row * k;
-      float* gates = p.out_gates + (size_t)row * k;
-#pragma unroll
-      for (int s = 0; s < kMaxTopK; ++s) {
-        if (s < k) { ids[s] = bi[s]; gates[s] = w[s] / sum; }
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       }
     }
   }
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
-    moe_tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                       const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                          const GemmParams& p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_mt[kMaxExperts + 1];
@@ -280,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
 
   const uint32_t tmem_base = s_tmem_base;
-  const int total_tiles = s_mt[G] * p.n_tiles;
+  const int total_tiles = s_mt[G] * p.n_tiles * p.k_splits;
   const int num_kb = p.K / kBK;
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
 
@@ -294,9 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
         int g, n, row0, row_end;
-        decode_tile(tau, p.n_tiles, G, s_mt, s_off, g, n, row0, row_end);
+        decode_tile(tau / p.k_splits, p.n_tiles, G, s_mt, s_off, g, n, row0, row_end);
         const int brow = g * p.b_rows_per_group + n * p.n_step;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int kb0 = (tau % p.k_splits) * p.kb_per_split;
+        const int kb1 = min(num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb = full_bar + 8 * stage;
           mbar_arrive_expect_tx(fb, tx_bytes);
@@ -327,7 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int kb0 = (tau % p.k_splits) * p.kb_per_split;
+        const int kb1 = min(num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
           tc_fence_after_sync();
           const uint32_t a_addr = a_base + stage * kABytes;
@@ -335,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             mma_bf16_ss(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
-                        idesc, (kb | k) != 0 ? 1u : 0u);
+                        idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           mma_commit(empty_bar + 8 * stage);  // frees the stage once these MMAs finish
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -351,17 +339,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue: warps 2..5 cover TMEM lanes by (warp % 4)
     const int q = warp & 3;
+    uint32_t* epi_stage = reinterpret_cast<uint32_t*>(
+        smem_raw + (base - smem_u32(smem_raw)) + kStages * (kABytes + kBBytes) + q * kEpiWarpBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tau = blockIdx.x; tau < total_tiles; tau += gridDim.x) {
       int g, n, row0, row_end;
-      decode_tile(tau, p.n_tiles, G, s_mt, s_off, g, n, row0, row_end);
+      decode_tile(tau / p.k_splits, p.n_tiles, G, s_mt, s_off, g, n, row0, row_end);
       const bool ok = mbar_wait(tfull_bar + 8 * acc, acc_phase, wc);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after_sync();
-      const int row = row0 + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
-      epilogue_tile<KIND>(p, t_row, row, row < row_end, n);
+      epilogue_tile<KIND>(p, t_row, row0 + q * 32, row_end, n, tau % p.k_splits, epi_stage);
       tc_fence_before_sync();
       mbar_arrive(tempty_bar + 8 * acc);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
@@ -375,6 +364,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_router_logits_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                           const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  gemm_body<kRouter>(tmap_a, tmap_b, p);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gate_up_swiglu_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                              const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  gemm_body<kGateUp>(tmap_a, tmap_b, p);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_down_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  gemm_body<kDown>(tmap_a, tmap_b, p);
+}
+
+typedef void (*GemmKernel)(const CUtensorMap, const CUtensorMap, const GemmParams);
+
+template <int KIND>
+constexpr GemmKernel kernel_of() {
+  return KIND == kRouter ? moe_router_logits_kernel
+                         : (KIND == kGateUp ? moe_gate_up_swiglu_kernel : moe_down_kernel);
 }
 
 // ------------------------------------------------------------------ host
@@ -424,7 +439,7 @@ cudaError_t ensure_smem_attr() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 32 && (done_mask >> dev) & 1u) return cudaSuccess;
-  e = cudaFuncSetAttribute(moe_tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(kernel_of<KIND>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
   if (e == cudaSuccess && dev < 32) done_mask |= 1u << dev;
   return e;
@@ -437,16 +452,16 @@ cudaError_t launch(cudaStream_t s, const char* name, const CUtensorMap& ma, cons
   if (e != cudaSuccess) return e;
   const long long grid = std::max(1LL, std::min<long long>(device_sm_count(), tiles_bound));
   KernelScope scope(s, name);
-  moe_tc_gemm_kernel<KIND><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(ma, mb, p);
+  kernel_of<KIND>()<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, const float* bias,
-                          int T, int d, int E, int top_k, int32_t* ids, float* gates,
-                          unsigned* status, unsigned long long timeout_ns) {
-  const int mma_n = ((E + 15) / 16) * 16;
+cudaError_t launch_router_logits(cudaStream_t s, const void* x, const void* w_router, int T,
+                                 int d, int E, float* partial, unsigned* status,
+                                 unsigned long long timeout_ns) {
+  const int mma_n = router_npad(E);
   CUtensorMap ma, mb;
   cudaError_t e = make_map(&ma, x, T, d, kBM);
   if (e == cudaSuccess) e = make_map(&mb, w_router, E, d, mma_n);
@@ -462,14 +477,14 @@ cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, c
   p.groups = 1;
   p.offsets = nullptr;
   p.total_rows = T;
-  p.out = ids;
-  p.out_gates = gates;
-  p.bias = bias;
-  p.top_k = top_k;
-  p.ld_out = top_k;
+  p.out = partial;
+  p.ld_out = mma_n;
   p.status = status;
   p.timeout_ns = timeout_ns;
-  return launch<kRouter>(s, "moe_router_topk", ma, mb, p, (T + kBM - 1) / kBM);
+  p.k_splits = router_splits(d);
+  p.kb_per_split = kRouterSplitK / kBK;
+  return launch<kRouter>(s, "moe_router_logits", ma, mb, p,
+                         static_cast<long long>((T + kBM - 1) / kBM) * p.k_splits);
 }
 
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
@@ -500,6 +515,8 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   p.ld_out = I;
   p.status = status;
   p.timeout_ns = timeout_ns;
+  p.k_splits = 1;
+  p.kb_per_split = d / kBK;
   e = launch<kGateUp>(s, offsets ? "moe_gate_up_swiglu" : "moe_shared_gate_up_swiglu", ma, mb, p,
                       mtiles_bound * p.n_tiles);
   if (e != cudaSuccess) return e;
@@ -523,6 +540,8 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   q.ld_out = d;
   q.status = status;
   q.timeout_ns = timeout_ns;
+  q.k_splits = 1;
+  q.kb_per_split = I / kBK;
   return launch<kDown>(s, offsets ? "moe_down" : "moe_shared_down", ma2, mb2, q,
                        mtiles_bound * q.n_tiles);
 }

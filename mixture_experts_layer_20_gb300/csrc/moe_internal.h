@@ -12,6 +12,16 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int kPermuteChunk = 4096;  // assignments per permute CTA
 
+// The router's logits are computed in K ranges of 512 on the tensor cores
+// and summed in range order by the top-k kernel.  The number of ranges
+// depends on d only, so a token's logits do not depend on the batch.
+constexpr int kRouterSplitK = 512;
+inline int router_splits(int d) { return (d + kRouterSplitK - 1) / kRouterSplitK; }
+inline int router_npad(int E) { return (E + 15) / 16 * 16; }
+inline size_t router_partial_bytes(int T, int d, int E) {
+  return static_cast<size_t>(router_splits(d)) * T * router_npad(E) * sizeof(float);
+}
+
 // Bits of the workspace's device status word.
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusDeviceCheck = 2u;
@@ -37,11 +47,17 @@ void set_last_error(const std::string& msg);
 
 // ---- tcgen05 GEMM launchers (moe_gemm.cu).  Return a CUDA error code.
 
-// Router: logits of x [T,d] against w_router [E,d] (+bias) on the tensor
-// cores, then per-token top-k and renormalised gates.
+// Router logits of x [T,d] against w_router [E,d] on the tensor cores:
+// partial sums over each 512-wide K range, partial [splits][T][npad] fp32.
+cudaError_t launch_router_logits(cudaStream_t s, const void* x, const void* w_router, int T,
+                                 int d, int E, float* partial, unsigned* status,
+                                 unsigned long long timeout_ns);
+
+// Router: logits (via the partials in `partial`), bias, top-k with the
+// lowest-index tie-break, renormalised gates (moe_router.cu).
 cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, const float* bias,
                           int T, int d, int E, int top_k, int32_t* ids, float* gates,
-                          unsigned* status, unsigned long long timeout_ns);
+                          float* partial, unsigned* status, unsigned long long timeout_ns);
 
 // Grouped SwiGLU FFN.  Rows [offsets[e], offsets[e+1]) of a [rows, d] go
 // through expert e (weights per expert: w_gate_up [2I, d], w_down [d, I]).

@@ -13,6 +13,7 @@
 //             offsets[e] + (number of earlier f with the same e): a stable
 //             counting sort, deterministic with no global atomics.
 //   gather  : x_perm[p] = x[perm[p] / k], one warp per row, 16-byte copies.
+// When all assignments fit one chunk, one CTA does count, scan and scatter.
 //
 // Combine ('Chapter 9. Distributed inference', section 9.3.4, step four;
 // 'Hosting Qwen on Blackwell', "MoE Dispatch - Combine": weighted
@@ -30,7 +31,7 @@ namespace {
 constexpr int kScatterWarps = 16;
 constexpr int kPerWarp = kPermuteChunk / kScatterWarps;  // 256
 
-__global__ void __launch_bounds__(512) permute_count_kernel(const int32_t* __restrict__ ids, int n,
+__global__ void __launch_bounds__(512) moe_permute_count_kernel(const int32_t* __restrict__ ids, int n,
                                                             int E, int32_t* __restrict__ table,
                                                             unsigned* status) {
   __shared__ int hist[kMaxExperts];
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(512) permute_count_kernel(const int32_t* __res
   for (int i = threadIdx.x; i < E; i += blockDim.x) table[(size_t)blockIdx.x * E + i] = hist[i];
 }
 
-__global__ void __launch_bounds__(kMaxExperts) permute_scan_kernel(int32_t* __restrict__ table,
+__global__ void __launch_bounds__(kMaxExperts) moe_permute_scan_kernel(int32_t* __restrict__ table,
                                                                    int nchunks, int E,
                                                                    int32_t* __restrict__ counts,
                                                                    int32_t* __restrict__ offsets) {
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kMaxExperts) permute_scan_kernel(int32_t* __re
 }
 
 __global__ void __launch_bounds__(kScatterWarps * 32)
-    permute_scatter_kernel(const int32_t* __restrict__ ids, int n, int E,
+    moe_permute_scatter_kernel(const int32_t* __restrict__ ids, int n, int E,
                            const int32_t* __restrict__ table, int32_t* __restrict__ perm,
                            int32_t* __restrict__ slot_pos) {
   __shared__ int wbase[kScatterWarps][kMaxExperts];
@@ -131,7 +132,78 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   }
 }
 
-__global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __restrict__ perm,
+// All of count, scan and scatter in one CTA when the T*k assignments fit one
+// chunk (decode batches): the same stable positions, two launches fewer.
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    moe_permute_small_kernel(const int32_t* __restrict__ ids, int n, int E,
+                             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                             int32_t* __restrict__ perm, int32_t* __restrict__ slot_pos,
+                             unsigned* status) {
+  __shared__ int wbase[kScatterWarps][kMaxExperts];
+  __shared__ int s_scan[kMaxExperts];
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kScatterWarps * kMaxExperts; i += blockDim.x)
+    (&wbase[0][0])[i] = 0;
+  __syncthreads();
+  const int wbeg = w * kPerWarp;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  bool bad = false;
+  for (int r = 0; r < kPerWarp / 32; ++r) {
+    const int f = wbeg + r * 32 + lane;
+    const int e = f < n ? __ldg(ids + f) : -1;
+    const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    bad |= f < n && !valid;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
+    __syncwarp();
+  }
+  if (bad) atomicOr(status, kStatusDeviceCheck);
+  __syncthreads();
+  // per-expert totals and the exclusive scan over experts
+  for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) {
+    int total = 0;
+    if (e < E)
+      for (int ww = 0; ww < kScatterWarps; ++ww) total += wbase[ww][e];
+    s_scan[e] = total;
+  }
+  __syncthreads();
+  for (int o = 1; o < kMaxExperts; o <<= 1) {
+    int v = 0;
+    if (threadIdx.x < kMaxExperts && threadIdx.x >= o) v = s_scan[threadIdx.x - o];
+    __syncthreads();
+    if (threadIdx.x < kMaxExperts) s_scan[threadIdx.x] += v;
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = e > 0 ? s_scan[e - 1] : 0;
+    offsets[e] = run;
+    counts[e] = s_scan[e] - run;
+    for (int ww = 0; ww < kScatterWarps; ++ww) {
+      const int v = wbase[ww][e];
+      wbase[ww][e] = run;
+      run += v;
+    }
+  }
+  if (threadIdx.x == 0) offsets[E] = s_scan[E - 1];
+  __syncthreads();
+  for (int r = 0; r < kPerWarp / 32; ++r) {
+    const int f = wbeg + r * 32 + lane;
+    const int e = f < n ? __ldg(ids + f) : -1;
+    const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (valid) {
+      const int pos = wbase[w][e] + __popc(peers & lt_mask);
+      perm[pos] = f;
+      slot_pos[f] = pos;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* __restrict__ perm,
                                                              const uint4* __restrict__ x, int n,
                                                              int k, int vec_per_row,
                                                              uint4* __restrict__ x_perm,
@@ -156,7 +228,7 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __re
   }
 }
 
-__global__ void __launch_bounds__(1024) combine_kernel(const float* __restrict__ y,
+__global__ void __launch_bounds__(1024) moe_combine_kernel(const float* __restrict__ y,
                                                        const int32_t* __restrict__ slot_pos,
                                                        const float* __restrict__ gates,
                                                        const float* __restrict__ y_shared, int T,
@@ -221,30 +293,36 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
                            unsigned* status) {
   const int n = T * top_k;
   const int nchunks = (n + kPermuteChunk - 1) / kPermuteChunk;
-  {
-    KernelScope scope(s, "moe_permute_count");
-    permute_count_kernel<<<nchunks, 512, 0, s>>>(ids, n, E, chunk_table, status);
+  cudaError_t e = cudaSuccess;
+  if (nchunks == 1) {
+    KernelScope scope(s, "moe_permute_small");
+    moe_permute_small_kernel<<<1, kScatterWarps * 32, 0, s>>>(ids, n, E, counts, offsets, perm,
+                                                              slot_pos, status);
+    e = cudaGetLastError();
+  } else {
+    {
+      KernelScope scope(s, "moe_permute_count");
+      moe_permute_count_kernel<<<nchunks, 512, 0, s>>>(ids, n, E, chunk_table, status);
+    }
+    e = cudaGetLastError();
+    if (e == cudaSuccess) {
+      KernelScope scope(s, "moe_permute_scan");
+      moe_permute_scan_kernel<<<1, kMaxExperts, 0, s>>>(chunk_table, nchunks, E, counts, offsets);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+      KernelScope scope(s, "moe_permute_scatter");
+      moe_permute_scatter_kernel<<<nchunks, kScatterWarps * 32, 0, s>>>(ids, n, E, chunk_table,
+                                                                         perm, slot_pos);
+      e = cudaGetLastError();
+    }
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  {
-    KernelScope scope(s, "moe_permute_scan");
-    permute_scan_kernel<<<1, kMaxExperts, 0, s>>>(chunk_table, nchunks, E, counts, offsets);
-  }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  {
-    KernelScope scope(s, "moe_permute_scatter");
-    permute_scatter_kernel<<<nchunks, kScatterWarps * 32, 0, s>>>(ids, n, E, chunk_table, perm,
-                                                                   slot_pos);
-  }
-  e = cudaGetLastError();
   if (e != cudaSuccess || x == nullptr) return e;
   const int warps_per_cta = 8;
   const int grid = std::min((n + warps_per_cta - 1) / warps_per_cta, device_sm_count() * 8);
   {
     KernelScope scope(s, "moe_permute_gather");
-    permute_gather_kernel<<<grid, warps_per_cta * 32, 0, s>>>(
+    moe_permute_gather_kernel<<<grid, warps_per_cta * 32, 0, s>>>(
         perm, static_cast<const uint4*>(x), n, top_k, d / 8, static_cast<uint4*>(x_perm), status);
   }
   return cudaGetLastError();
@@ -259,7 +337,7 @@ cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_p
   const int grid = std::min(T, 65535 * 4);
   {
     KernelScope scope(s, "moe_combine");
-    combine_kernel<<<grid, threads, 0, s>>>(y, slot_pos, gates, y_shared, T, d, top_k,
+    moe_combine_kernel<<<grid, threads, 0, s>>>(y, slot_pos, gates, y_shared, T, d, top_k,
                                             T * top_k, static_cast<__nv_bfloat16*>(out), status);
   }
   return cudaGetLastError();
