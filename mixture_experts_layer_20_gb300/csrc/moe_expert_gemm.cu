@@ -1,0 +1,485 @@
+// Grouped expert GEMMs of the MoE layer on sm_103a: 2-SM tcgen05 MMAs with the
+// expert weights on the M side.
+//
+//   gate_up : h[t, c] = silu(x[t] . W_gate[c]) * (x[t] . W_up[c]), bf16
+//   down    : y[t, c] = h[t] . W_down[c], fp32
+//
+// for every token row t of an expert's contiguous range of the grouped
+// activations ('Chapter 9. Distributed inference', section 9.3.2: three
+// d x I matrices per expert; section 9.4.3: one grouped GEMM for all experts).
+//
+// Work unit (a "tile") = one expert, one slab of 256 weight rows, one chunk
+// of that expert's tokens.  Weights are the MMA's M side, so M is always
+// full; tokens are the N side, chunked so that no expert is padded by more
+// than 31 rows per chunk (an expert with m rows gets ceil(m/256) chunks of
+// equal size rounded up to 32).  A cluster of two CTAs (a pair) computes a
+// tile with tcgen05.mma.cta_group::2 (M = 256): each CTA holds 128 weight
+// rows and half of the token rows of every K block, so each SM moves at most
+// 32 KB per 64-wide K block and the pair's shared memory holds 6 stages.
+// Tiles are ordered (expert, slab, chunk): pairs running at the same time
+// read the same weight slab, which is then read from HBM once.
+//
+// gate_up: rank r of the pair holds gate rows [128 s + 64 r, +64) of slab s
+// in A rows 0-63 and the matching up rows in A rows 64-127, so the gate and up
+// accumulators of the same h column sit in TMEM lanes l and l + 64 of one CTA;
+// the epilogue warps that read the up lanes pass them through shared memory
+// to the warps that read the gate lanes.  With the weights on M, a warp's 32
+// lanes are 32 consecutive output columns, so every store of one token row is
+// contiguous.
+//
+// Roles, per CTA (192 threads): warp 0 loads both operands with TMA into its
+// own shared memory, counting the bytes of both CTAs on the leader's full
+// barrier; warp 1 owns the tensor memory (512 columns: two accumulators of up
+// to 256 fp32 columns) and, in the leader, one of its threads issues the MMAs
+// and commits to both CTAs' barriers; warps 2-5 read the accumulator with
+// tcgen05.ld and store the tile while the next one accumulates.  Every wait
+// is bounded; on timeout a CTA records it, drains its copies in flight (and,
+// in the leader, its MMAs), and both CTAs still meet at the final cluster
+// barrier before freeing tensor memory.
+
+#include <algorithm>
+#include <mutex>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBK = 64;
+constexpr int kStages = 6;
+constexpr int kWRows = 128;                        // weight rows per CTA
+constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
+constexpr int kTokBox = 32;                        // token rows per TMA box
+constexpr int kABytes = kWRows * kBK * 2;          // 16 KB
+constexpr int kBBytes = (kTokMax / 2) * kBK * 2;   // 16 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kExchStride = 20;                    // words per lane in the exchange buffer
+constexpr int kExchBytes = 2 * 32 * kExchStride * 4;
+constexpr int kSmemBytes = kStages * kStageBytes + kExchBytes + 1024;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;
+constexpr uint32_t kEpiArrivals = 8;               // 4 epilogue warps x 2 CTAs
+
+enum Kind : int { kGateUp = 1, kDown = 2 };
+
+struct Params {
+  int K;                  // reduction length (d or I), a multiple of 64
+  int n_out;              // output columns: I (h) or d (y)
+  int slabs;              // 256-row weight slabs per expert
+  int groups;             // experts, or 1 when offsets == nullptr
+  const int32_t* offsets;  // [groups + 1] token row offsets, or nullptr
+  int total_rows;         // token rows of the B operand
+  int w_rows_per_group;   // weight rows per expert in the A tensor map
+  int up_offset;          // gate_up: I
+  void* out;              // gate_up: h bf16 [rows, I]; down: y fp32 [rows, d]
+  long long ld_out;
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+struct Tile {
+  int e, slab, tok0, tok_end, n;
+};
+
+__device__ __forceinline__ Tile decode_tile(int tau, int slabs, int groups, const int* s_off,
+                                            const int* s_ct) {
+  int lo = 0, hi = groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_ct[mid] * slabs <= tau) lo = mid; else hi = mid - 1;
+  }
+  Tile t;
+  t.e = lo;
+  const int ch = s_ct[lo + 1] - s_ct[lo];
+  const int local = tau - s_ct[lo] * slabs;
+  t.slab = local / ch;
+  const int c = local - t.slab * ch;
+  const int m = s_off[lo + 1] - s_off[lo];
+  const int per = (((m + ch - 1) / ch) + 31) / 32 * 32;
+  t.tok0 = s_off[lo] + c * per;
+  t.tok_end = min(t.tok0 + per, s_off[lo + 1]);
+  t.n = per;
+  return t;
+}
+
+__device__ __forceinline__ int token_boxes(int n) { return (n / 2 + kTokBox - 1) / kTokBox; }
+
+template <int KIND>
+__device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w,
+                                                 const CUtensorMap& tmap_x, const Params& p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_ct[kMaxExperts + 1];
+  __shared__ alignas(8) uint64_t s_bar[2 * kStages + 5];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t full_bar = smem_u32(&s_bar[0]);
+  const uint32_t empty_bar = smem_u32(&s_bar[kStages]);
+  const uint32_t tfull_bar = smem_u32(&s_bar[2 * kStages]);
+  const uint32_t tempty_bar = smem_u32(&s_bar[2 * kStages + 2]);
+  const uint32_t drain_bar = smem_u32(&s_bar[2 * kStages + 4]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar + 8 * s, 1);  // leader: counts both CTAs' bytes; unused in the follower
+      mbar_init(empty_bar + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar + 8 * a, 1);
+      mbar_init(tempty_bar + 8 * a, kEpiArrivals);
+    }
+    mbar_init(drain_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_w);
+    tma_prefetch_desc(&tmap_x);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&s_tmem_base), kTmemCols);
+    tmem_relinquish_pair();
+  }
+
+  // Schedule: token chunks per expert and their exclusive prefix.
+  const int G = p.groups;
+  for (int i = threadIdx.x; i <= G; i += blockDim.x)
+    s_off[i] = p.offsets ? __ldg(p.offsets + i) : (i == 0 ? 0 : p.total_rows);
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (G + 31) / 32;
+    int local = 0;
+    bool bad = false;
+    for (int j = 0; j < per; ++j) {
+      const int g = lane * per + j;
+      if (g < G) {
+        const int m = s_off[g + 1] - s_off[g];
+        bad |= m < 0;
+        local += m > 0 ? (m + kTokMax - 1) / kTokMax : 0;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per; ++j) {
+      const int g = lane * per + j;
+      if (g < G) {
+        s_ct[g] = run;
+        const int m = s_off[g + 1] - s_off[g];
+        run += m > 0 ? (m + kTokMax - 1) / kTokMax : 0;
+      }
+    }
+    bad |= (s_off[0] != 0) || (s_off[G] != p.total_rows);
+    bad = __any_sync(0xffffffffu, bad);
+    __syncwarp();
+    if (lane == 31) s_ct[G] = bad ? 0 : incl;
+    if (bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusDeviceCheck);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = s_tmem_base;
+  const int total_tiles = s_ct[G] * p.slabs;
+  const int num_kb = p.K / kBK;
+  const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs, own shared memory; the bytes
+      // of both are counted on the leader's full barrier, which the leader
+      // arms with the pair's total)
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      const uint32_t full_leader = mapa_shared(full_bar, 0);
+      for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+        const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+        const int nb = token_boxes(t.n);
+        const uint32_t tx = kABytes + nb * kTokBox * kBK * 2;  // per CTA
+        const int wrow = t.e * p.w_rows_per_group +
+                         (KIND == kGateUp ? t.slab * 128 + rank * 64 : t.slab * 256 + rank * 128);
+        const int trow = t.tok0 + rank * (t.n / 2);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
+          if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * tx);
+          const uint32_t fb = full_leader + 8 * stage;
+          const uint32_t a_dst = base + stage * kStageBytes;
+          const uint32_t b_dst = a_dst + kABytes;
+          const int kx = kb * kBK;
+          tma_load_2d_pair(a_dst, &tmap_w, fb, kx, wrow);
+          tma_load_2d_pair(a_dst + 64 * 128, &tmap_w, fb, kx,
+                           KIND == kGateUp ? wrow + p.up_offset : wrow + 64);
+          for (int i = 0; i < nb; ++i)
+            tma_load_2d_pair(b_dst + i * kTokBox * 128, &tmap_x, fb, kx, trow + i * kTokBox);
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (leader) {
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+          mbar_wait_drain(full_bar + 8 * (i % kStages), (i / kStages) & 1, p.status);
+      } else if (!ok) {
+        // The follower cannot see its copies complete (they count on the
+        // leader's barrier); after a give-up it leaves them time to land.
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 50000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (leader)
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+        const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+        const uint32_t idesc = idesc_bf16_f32(256, t.n);
+        if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * kAccCols;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a_addr = base + stage * kStageBytes;
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
+                          idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair(empty_bar + 8 * stage);  // frees this stage in both CTAs
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull_bar + 8 * acc);     // accumulator ready in both CTAs
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      mma_commit_pair(drain_bar);
+      mbar_wait_drain(drain_bar, 0, p.status);
+    } else if (lane == 0) {
+      // follower: the leader's last commit also arrives here once its MMAs are done
+      mbar_wait_drain(drain_bar, 0, p.status);
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5, TMEM lanes 32 (warp % 4) + lane
+    const int q = warp & 3;
+    float* exch = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)) +
+                                           kStages * kStageBytes) +
+                  (q & 1) * 32 * kExchStride;
+    const uint32_t tempty_leader = mapa_shared(tempty_bar, 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    // After a wait gives up, the loop still runs to the end (later waits fail
+    // at once) with its stores switched off: the two warps that exchange up
+    // values must pass the same named barriers.
+    for (int tau = pair; tau < total_tiles; tau += num_pairs) {
+      const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+      const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+      if constexpr (KIND == kDown) {
+        const int col = t.slab * 256 + rank * 128 + q * 32 + lane;
+        float* y = static_cast<float*>(p.out) + col;
+        const bool col_ok = live && col < p.n_out;
+#pragma unroll 1
+        for (int c = 0; c < t.n; c += 16) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(t_row + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = t.tok0 + c + j;
+            if (tok < t.tok_end && col_ok) y[(size_t)tok * p.ld_out] = __uint_as_float(v[j]);
+          }
+        }
+      } else {
+        const bool is_gate = q < 2;
+        const int col = t.slab * 128 + rank * 64 + (q & 1) * 32 + lane;
+        __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + col;
+        const bool col_ok = live && col < p.n_out;
+#pragma unroll 1
+        for (int c = 0; c < t.n; c += 16) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(t_row + c, v);
+          tmem_ld_wait();
+          float* mine = exch + lane * kExchStride;
+          if (!is_gate) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              reinterpret_cast<uint4*>(mine)[i] =
+                  make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+          if (q & 1) named_barrier_sync<2>(64); else named_barrier_sync<1>(64);
+          if (is_gate) {
+            float u[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 f = reinterpret_cast<const float4*>(mine)[i];
+              u[4 * i] = f.x; u[4 * i + 1] = f.y; u[4 * i + 2] = f.z; u[4 * i + 3] = f.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int tok = t.tok0 + c + j;
+              if (tok < t.tok_end && col_ok) {
+                const float g = __uint_as_float(v[j]);
+                h[(size_t)tok * p.ld_out] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u[j]);
+              }
+            }
+          }
+          if (q & 1) named_barrier_sync<2>(64); else named_barrier_sync<1>(64);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar + 8 * acc);
+        else mbar_arrive_cluster(tempty_leader + 8 * acc);
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    moe_gate_up_swiglu_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                              const __grid_constant__ CUtensorMap tmap_x, const Params p) {
+  expert_gemm_body<kGateUp>(tmap_w, tmap_x, p);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    moe_down_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                    const __grid_constant__ CUtensorMap tmap_x, const Params p) {
+  expert_gemm_body<kDown>(tmap_w, tmap_x, p);
+}
+
+typedef void (*ExpertKernel)(const CUtensorMap, const CUtensorMap, const Params);
+
+cudaError_t ensure_smem_attr(ExpertKernel k, int which) {
+  static std::mutex mu;
+  static unsigned done[2] = {0, 0};  // one bit per device, per kernel
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 32 && (done[which] >> dev) & 1u) return cudaSuccess;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && dev < 32) done[which] |= 1u << dev;
+  return e;
+}
+
+// Pairs that can be resident at once.  A pair needs two SMs of one GPC, so
+// this can be fewer than half the SMs; a persistent grid larger than it would
+// run its surplus pairs' whole tile lists as a second wave.
+int resident_pairs(ExpertKernel k, int which) {
+  static std::mutex mu;
+  static int cached[2][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[which][dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = device_sm_count() / 2;
+    }
+    cached[which][dev] = std::min(n, device_sm_count() / 2);
+  }
+  return cached[which][dev];
+}
+
+cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int which,
+                          const CUtensorMap& mw, const CUtensorMap& mx, const Params& p,
+                          long long tiles_bound) {
+  cudaError_t e = ensure_smem_attr(k, which);
+  if (e != cudaSuccess) return e;
+  const long long pairs =
+      std::max(1LL, std::min<long long>(resident_pairs(k, which), tiles_bound));
+  KernelScope scope(s, name);
+  k<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, s>>>(mw, mx, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
+                               int d, int E, int I, const void* w_gate_up, const void* w_down,
+                               void* h, float* y, unsigned* status,
+                               unsigned long long timeout_ns) {
+  const int groups = offsets ? E : 1;
+  const long long chunks_bound =
+      offsets ? rows / kTokMax + std::min(E, rows) : (rows + kTokMax - 1) / kTokMax;
+
+  CUtensorMap mw, mx;
+  cudaError_t e = make_bf16_map(&mw, w_gate_up, static_cast<uint64_t>(groups) * 2 * I, d, 64);
+  if (e == cudaSuccess) e = make_bf16_map(&mx, a, rows, d, kTokBox);
+  if (e != cudaSuccess) return e;
+  Params p{};
+  p.K = d;
+  p.n_out = I;
+  p.slabs = (I + 127) / 128;
+  p.groups = groups;
+  p.offsets = offsets;
+  p.total_rows = rows;
+  p.w_rows_per_group = 2 * I;
+  p.up_offset = I;
+  p.out = h;
+  p.ld_out = I;
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+  e = launch_expert(s, offsets ? "moe_gate_up_swiglu" : "moe_shared_gate_up_swiglu",
+                    moe_gate_up_swiglu_kernel, 0, mw, mx, p, chunks_bound * p.slabs);
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap mw2, mx2;
+  e = make_bf16_map(&mw2, w_down, static_cast<uint64_t>(groups) * d, I, 64);
+  if (e == cudaSuccess) e = make_bf16_map(&mx2, h, rows, I, kTokBox);
+  if (e != cudaSuccess) return e;
+  Params q{};
+  q.K = I;
+  q.n_out = d;
+  q.slabs = (d + 255) / 256;
+  q.groups = groups;
+  q.offsets = offsets;
+  q.total_rows = rows;
+  q.w_rows_per_group = d;
+  q.up_offset = 0;
+  q.out = y;
+  q.ld_out = d;
+  q.status = status;
+  q.timeout_ns = timeout_ns;
+  return launch_expert(s, offsets ? "moe_down" : "moe_shared_down", moe_down_kernel, 1, mw2, mx2,
+                       q, chunks_bound * q.slabs);
+}
+
+}  // namespace moe

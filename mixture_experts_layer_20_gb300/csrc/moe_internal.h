@@ -1,6 +1,7 @@
 // Host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -45,7 +46,12 @@ int device_sm_count();
 // Message returned by moe_last_error() on this thread.  Defined in moe_api.cu.
 void set_last_error(const std::string& msg);
 
-// ---- tcgen05 GEMM launchers (moe_gemm.cu).  Return a CUDA error code.
+// Row-major bf16 matrix [rows, cols] as a 2-D TMA tensor map with a box of
+// 64 columns x box_rows rows and 128-byte swizzling (moe_gemm.cu).
+cudaError_t make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows);
+
+// ---- tcgen05 GEMM launchers.  Return a CUDA error code.
 
 // Router logits of x [T,d] against w_router [E,d] on the tensor cores:
 // partial sums over each 512-wide K range, partial [splits][T][npad] fp32.
@@ -59,9 +65,9 @@ cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, c
                           int T, int d, int E, int top_k, int32_t* ids, float* gates,
                           float* partial, unsigned* status, unsigned long long timeout_ns);
 
-// Grouped SwiGLU FFN.  Rows [offsets[e], offsets[e+1]) of a [rows, d] go
-// through expert e (weights per expert: w_gate_up [2I, d], w_down [d, I]).
-// offsets == nullptr: a single expert on all `rows` rows (dense).
+// Grouped SwiGLU FFN (moe_expert_gemm.cu).  Rows [offsets[e], offsets[e+1])
+// of a [rows, d] go through expert e (weights per expert: w_gate_up [2I, d],
+// w_down [d, I]).  offsets == nullptr: a single expert on all `rows` rows.
 // Writes h [rows, I] bf16 (scratch) and y [rows, d] fp32.
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
