@@ -11,8 +11,11 @@
 // Work unit (a "tile") = one expert, one slab of 256 weight rows, one chunk
 // of that expert's tokens.  Weights are the MMA's M side, so M is always
 // full; tokens are the N side, chunked so that no expert is padded by more
-// than 31 rows per chunk (an expert with m rows gets ceil(m/256) chunks of
-// equal size rounded up to 32).  A cluster of two CTAs (a pair) computes a
+// than 63 rows per chunk (an expert with m rows gets ceil(m/256) chunks of
+// equal size rounded up to 64, so a CTA's half is 32, 64, 96 or 128 rows and
+// one TMA instruction fetches it; each TMA or MMA instruction costs its
+// single issuing thread tens of cycles, so few large ones keep the tensor
+// pipe fed).  A cluster of two CTAs (a pair) computes a
 // tile with tcgen05.mma.cta_group::2 (M = 256): each CTA holds 128 weight
 // rows and half of the token rows of every K block, so each SM moves at most
 // 32 KB per 64-wide K block and the pair's shared memory holds 6 stages.
@@ -50,7 +53,6 @@ constexpr int kBK = 64;
 constexpr int kStages = 6;
 constexpr int kWRows = 128;                        // weight rows per CTA
 constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
-constexpr int kTokBox = 32;                        // token rows per TMA box
 constexpr int kABytes = kWRows * kBK * 2;          // 16 KB
 constexpr int kBBytes = (kTokMax / 2) * kBK * 2;   // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -97,18 +99,22 @@ __device__ __forceinline__ Tile decode_tile(int tau, int slabs, int groups, cons
   t.slab = local / ch;
   const int c = local - t.slab * ch;
   const int m = s_off[lo + 1] - s_off[lo];
-  const int per = (((m + ch - 1) / ch) + 31) / 32 * 32;
+  const int per = (((m + ch - 1) / ch) + 63) / 64 * 64;
   t.tok0 = s_off[lo] + c * per;
   t.tok_end = min(t.tok0 + per, s_off[lo + 1]);
   t.n = per;
   return t;
 }
 
-__device__ __forceinline__ int token_boxes(int n) { return (n / 2 + kTokBox - 1) / kTokBox; }
+// The token operand comes through one of four tensor maps whose boxes are
+// 32, 64, 96 and 128 rows: one TMA instruction loads a CTA's n/2 token rows.
+struct TokenMaps {
+  const CUtensorMap* m[4];
+};
 
 template <int KIND>
-__device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w,
-                                                 const CUtensorMap& tmap_x, const Params& p) {
+__device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, const TokenMaps& tx,
+                                                 const Params& p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_ct[kMaxExperts + 1];
@@ -143,7 +149,10 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w,
     s_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap_w);
-    tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(tx.m[0]);
+    tma_prefetch_desc(tx.m[1]);
+    tma_prefetch_desc(tx.m[2]);
+    tma_prefetch_desc(tx.m[3]);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&s_tmem_base), kTmemCols);
@@ -210,23 +219,23 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w,
       const uint32_t full_leader = mapa_shared(full_bar, 0);
       for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
         const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-        const int nb = token_boxes(t.n);
-        const uint32_t tx = kABytes + nb * kTokBox * kBK * 2;  // per CTA
-        const int wrow = t.e * p.w_rows_per_group +
-                         (KIND == kGateUp ? t.slab * 128 + rank * 64 : t.slab * 256 + rank * 128);
-        const int trow = t.tok0 + rank * (t.n / 2);
+        const int half = t.n / 2;  // 32, 64, 96 or 128 token rows per CTA
+        const CUtensorMap* tmap_x =
+            half <= 32 ? tx.m[0] : (half <= 64 ? tx.m[1] : (half <= 96 ? tx.m[2] : tx.m[3]));
+        const uint32_t tx_bytes = kABytes + half * 128;  // per CTA
+        const int trow = t.tok0 + rank * half;
+        const int wrow = KIND == kGateUp ? t.slab * 128 + rank * 64
+                                         : t.e * p.w_rows_per_group + t.slab * 256 + rank * 128;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
-          if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * tx);
+          if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * tx_bytes);
           const uint32_t fb = full_leader + 8 * stage;
           const uint32_t a_dst = base + stage * kStageBytes;
-          const uint32_t b_dst = a_dst + kABytes;
           const int kx = kb * kBK;
-          tma_load_2d_pair(a_dst, &tmap_w, fb, kx, wrow);
-          tma_load_2d_pair(a_dst + 64 * 128, &tmap_w, fb, kx,
-                           KIND == kGateUp ? wrow + p.up_offset : wrow + 64);
-          for (int i = 0; i < nb; ++i)
-            tma_load_2d_pair(b_dst + i * kTokBox * 128, &tmap_x, fb, kx, trow + i * kTokBox);
+          // gate_up: one box holds 64 gate rows then the 64 matching up rows
+          if (KIND == kGateUp) tma_load_4d_pair(a_dst, &tmap_w, fb, kx, wrow, 0, t.e);
+          else tma_load_2d_pair(a_dst, &tmap_w, fb, kx, wrow);
+          tma_load_2d_pair(a_dst + kABytes, tmap_x, fb, kx, trow);
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -258,7 +267,6 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w,
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
-          tc_fence_after_sync();
           const uint32_t a_addr = base + stage * kStageBytes;
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
@@ -369,17 +377,23 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w,
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     moe_gate_up_swiglu_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                              const __grid_constant__ CUtensorMap tmap_x, const Params p) {
-  expert_gemm_body<kGateUp>(tmap_w, tmap_x, p);
+                              const __grid_constant__ CUtensorMap tx32,
+                              const __grid_constant__ CUtensorMap tx64,
+                              const __grid_constant__ CUtensorMap tx96,
+                              const __grid_constant__ CUtensorMap tx128, const Params p) {
+  expert_gemm_body<kGateUp>(tmap_w, TokenMaps{{&tx32, &tx64, &tx96, &tx128}}, p);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     moe_down_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                    const __grid_constant__ CUtensorMap tmap_x, const Params p) {
-  expert_gemm_body<kDown>(tmap_w, tmap_x, p);
+                    const __grid_constant__ CUtensorMap tx32, const __grid_constant__ CUtensorMap tx64,
+                    const __grid_constant__ CUtensorMap tx96,
+                    const __grid_constant__ CUtensorMap tx128, const Params p) {
+  expert_gemm_body<kDown>(tmap_w, TokenMaps{{&tx32, &tx64, &tx96, &tx128}}, p);
 }
 
-typedef void (*ExpertKernel)(const CUtensorMap, const CUtensorMap, const Params);
+typedef void (*ExpertKernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                             const CUtensorMap, const CUtensorMap, const Params);
 
 cudaError_t ensure_smem_attr(ExpertKernel k, int which) {
   static std::mutex mu;
@@ -418,15 +432,25 @@ int resident_pairs(ExpertKernel k, int which) {
   return cached[which][dev];
 }
 
+// Token-operand maps over a [rows, K] bf16 matrix, boxes of 32..128 rows.
+cudaError_t make_token_maps(CUtensorMap (&mx)[4], const void* a, int rows, int K) {
+  for (int i = 0; i < 4; ++i) {
+    cudaError_t e = make_bf16_map(&mx[i], a, rows, K, 32 * (i + 1));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int which,
-                          const CUtensorMap& mw, const CUtensorMap& mx, const Params& p,
+                          const CUtensorMap& mw, const CUtensorMap (&mx)[4], const Params& p,
                           long long tiles_bound) {
   cudaError_t e = ensure_smem_attr(k, which);
   if (e != cudaSuccess) return e;
   const long long pairs =
       std::max(1LL, std::min<long long>(resident_pairs(k, which), tiles_bound));
   KernelScope scope(s, name);
-  k<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, s>>>(mw, mx, p);
+  k<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, s>>>(mw, mx[0], mx[1], mx[2], mx[3],
+                                                                   p);
   return cudaGetLastError();
 }
 
@@ -440,9 +464,15 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   const long long chunks_bound =
       offsets ? rows / kTokMax + std::min(E, rows) : (rows + kTokMax - 1) / kTokMax;
 
-  CUtensorMap mw, mx;
-  cudaError_t e = make_bf16_map(&mw, w_gate_up, static_cast<uint64_t>(groups) * 2 * I, d, 64);
-  if (e == cudaSuccess) e = make_bf16_map(&mx, a, rows, d, kTokBox);
+  // W_gate_up viewed as [groups][2][I][d]: one box = 64 gate rows + the 64 matching up rows
+  CUtensorMap mw, mx[4];
+  const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(I), 2,
+                            static_cast<uint64_t>(groups)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(I) * d * 2,
+                               2ull * I * d * 2};
+  const uint32_t box[4] = {64, 64, 2, 1};
+  cudaError_t e = make_bf16_map_nd(&mw, w_gate_up, 4, dims, strides, box);
+  if (e == cudaSuccess) e = make_token_maps(mx, a, rows, d);
   if (e != cudaSuccess) return e;
   Params p{};
   p.K = d;
@@ -461,9 +491,9 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
                     moe_gate_up_swiglu_kernel, 0, mw, mx, p, chunks_bound * p.slabs);
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mw2, mx2;
-  e = make_bf16_map(&mw2, w_down, static_cast<uint64_t>(groups) * d, I, 64);
-  if (e == cudaSuccess) e = make_bf16_map(&mx2, h, rows, I, kTokBox);
+  CUtensorMap mw2, mx2[4];
+  e = make_bf16_map(&mw2, w_down, static_cast<uint64_t>(groups) * d, I, 128);
+  if (e == cudaSuccess) e = make_token_maps(mx2, h, rows, I);
   if (e != cudaSuccess) return e;
   Params q{};
   q.K = I;

@@ -51,6 +51,12 @@ void set_last_error(const std::string& msg);
 cudaError_t make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                           uint32_t box_rows);
 
+// bf16 tensor of rank 2..5 (dims innermost first, in elements; strides of
+// dims 1.. in bytes) as a TMA tensor map with 128-byte swizzling; box[0] must
+// be 64 (one 128-byte row).
+cudaError_t make_bf16_map_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                             const uint64_t* strides_bytes, const uint32_t* box);
+
 // ---- tcgen05 GEMM launchers.  Return a CUDA error code.
 
 // Router logits of x [T,d] against w_router [E,d] on the tensor cores:
