@@ -18,15 +18,18 @@
 // pipe fed).  A cluster of two CTAs (a pair) computes a
 // tile with tcgen05.mma.cta_group::2 (M = 256): each CTA holds 128 weight
 // rows and half of the token rows of every K block, so each SM moves at most
-// 32 KB per 64-wide K block and the pair's shared memory holds 6 stages.
+// 32 KB per 64-wide K block.  A pipeline stage holds two such K blocks: the
+// thread that issues the MMAs pays tens of cycles per instruction and per
+// barrier round, so 8 MMAs per wait / commit keep it ahead of a 256 x 256
+// tile's tensor work; 3 stages fill the shared memory.
 // Tiles are ordered (expert, slab, chunk): pairs running at the same time
 // read the same weight slab, which is then read from HBM once.
 //
 // gate_up: rank r of the pair holds gate rows [128 s + 64 r, +64) of slab s
 // in A rows 0-63 and the matching up rows in A rows 64-127, so the gate and up
 // accumulators of the same h column sit in TMEM lanes l and l + 64 of one CTA;
-// the epilogue warps that read the up lanes pass them through shared memory
-// to the warps that read the gate lanes.  With the weights on M, a warp's 32
+// the epilogue warps that read the gate lanes pass them through shared memory
+// to the warps that read the up lanes, which compute h.  With the weights on M, a warp's 32
 // lanes are 32 consecutive output columns, so every store of one token row is
 // contiguous.
 //
@@ -49,13 +52,14 @@
 namespace moe {
 namespace {
 
-constexpr int kBK = 64;
-constexpr int kStages = 6;
+constexpr int kBK = 64;     // one 128-byte swizzle row of bf16: the K of one TMA box
+constexpr int kSub = 2;     // K boxes per pipeline stage: 8 MMAs per barrier round
+constexpr int kStages = 3;
 constexpr int kWRows = 128;                        // weight rows per CTA
 constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
-constexpr int kABytes = kWRows * kBK * 2;          // 16 KB
-constexpr int kBBytes = (kTokMax / 2) * kBK * 2;   // 16 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kABytes = kWRows * kBK * 2;          // 16 KB per K box
+constexpr int kBBytes = (kTokMax / 2) * kBK * 2;   // 16 KB per K box (capacity)
+constexpr int kStageBytes = kSub * (kABytes + kBBytes);
 constexpr int kExchStride = 20;                    // words per lane in the exchange buffer
 constexpr int kExchBytes = 2 * 32 * kExchStride * 4;
 constexpr int kSmemBytes = kStages * kStageBytes + kExchBytes + 1024;
@@ -204,7 +208,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 
   const uint32_t tmem_base = s_tmem_base;
   const int total_tiles = s_ct[G] * p.slabs;
-  const int num_kb = p.K / kBK;
+  const int num_kb = p.K / kBK;                   // 64-wide K boxes
+  const int num_ks = (num_kb + kSub - 1) / kSub;  // pipeline stages per tile
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
 
   if (warp == 0) {
@@ -226,16 +231,22 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
         const int trow = t.tok0 + rank * half;
         const int wrow = KIND == kGateUp ? t.slab * 128 + rank * 64
                                          : t.e * p.w_rows_per_group + t.slab * 256 + rank * 128;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int ks = 0; ks < num_ks; ++ks) {
+          const int nsub = min(kSub, num_kb - ks * kSub);
           if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
-          if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * tx_bytes);
+          if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * nsub * tx_bytes);
           const uint32_t fb = full_leader + 8 * stage;
           const uint32_t a_dst = base + stage * kStageBytes;
-          const int kx = kb * kBK;
-          // gate_up: one box holds 64 gate rows then the 64 matching up rows
-          if (KIND == kGateUp) tma_load_4d_pair(a_dst, &tmap_w, fb, kx, wrow, 0, t.e);
-          else tma_load_2d_pair(a_dst, &tmap_w, fb, kx, wrow);
-          tma_load_2d_pair(a_dst + kABytes, tmap_x, fb, kx, trow);
+          const uint32_t b_dst = a_dst + kSub * kABytes;
+          for (int sub = 0; sub < nsub; ++sub) {
+            const int kx = (ks * kSub + sub) * kBK;
+            // gate_up: one box holds 64 gate rows then the 64 matching up rows
+            if (KIND == kGateUp)
+              tma_load_4d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow, 0, t.e);
+            else
+              tma_load_2d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow);
+            tma_load_2d_pair(b_dst + sub * kBBytes, tmap_x, fb, kx, trow);
+          }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -265,14 +276,18 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
         if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int ks = 0; ks < num_ks; ++ks) {
+          const int nsub = min(kSub, num_kb - ks * kSub);
           if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
           const uint32_t a_addr = base + stage * kStageBytes;
-          const uint32_t b_addr = a_addr + kABytes;
+          const uint32_t b_addr = a_addr + kSub * kABytes;
+          for (int sub = 0; sub < nsub; ++sub) {
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
-                          idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + sub * kABytes + k * 32),
+                            smem_desc_sw128(b_addr + sub * kBBytes + k * 32), idesc,
+                            (ks | sub | k) != 0 ? 1u : 0u);
+          }
           mma_commit_pair(empty_bar + 8 * stage);  // frees this stage in both CTAs
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -305,20 +320,30 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
       if constexpr (KIND == kDown) {
         const int col = t.slab * 256 + rank * 128 + q * 32 + lane;
-        float* y = static_cast<float*>(p.out) + col;
         const bool col_ok = live && col < p.n_out;
 #pragma unroll 1
         for (int c = 0; c < t.n; c += 16) {
           uint32_t v[16];
           tmem_ld_32x32b_x16(t_row + c, v);
           tmem_ld_wait();
+          const int nvalid = min(16, t.tok_end - t.tok0 - c);  // uniform across the warp
+          float* yp = static_cast<float*>(p.out) + (size_t)(t.tok0 + c) * p.ld_out + col;
+          if (col_ok) {
+            if (nvalid == 16) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int tok = t.tok0 + c + j;
-            if (tok < t.tok_end && col_ok) y[(size_t)tok * p.ld_out] = __uint_as_float(v[j]);
+              for (int j = 0; j < 16; ++j) yp[(size_t)j * p.ld_out] = __uint_as_float(v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < nvalid) yp[(size_t)j * p.ld_out] = __uint_as_float(v[j]);
+            }
           }
         }
       } else {
+        // Warps 4 and 5 (TMEM lanes 0-63, the gate rows) share their schedulers
+        // with the producer (warp 0) and the MMA issuer (warp 1), so they only
+        // pass the gate values through shared memory; warps 2 and 3 (lanes
+        // 64-127, the up rows) compute h = silu(gate) * up and store it.
         const bool is_gate = q < 2;
         const int col = t.slab * 128 + rank * 64 + (q & 1) * 32 + lane;
         __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + col;
@@ -329,26 +354,29 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
           tmem_ld_32x32b_x16(t_row + c, v);
           tmem_ld_wait();
           float* mine = exch + lane * kExchStride;
-          if (!is_gate) {
+          if (is_gate) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               reinterpret_cast<uint4*>(mine)[i] =
                   make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
           if (q & 1) named_barrier_sync<2>(64); else named_barrier_sync<1>(64);
-          if (is_gate) {
-            float u[16];
+          if (!is_gate) {
+            float g[16];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const float4 f = reinterpret_cast<const float4*>(mine)[i];
-              u[4 * i] = f.x; u[4 * i + 1] = f.y; u[4 * i + 2] = f.z; u[4 * i + 3] = f.w;
+              g[4 * i] = f.x; g[4 * i + 1] = f.y; g[4 * i + 2] = f.z; g[4 * i + 3] = f.w;
             }
+            const int nvalid = min(16, t.tok_end - t.tok0 - c);  // uniform across the warp
+            __nv_bfloat16* hp = h + (size_t)(t.tok0 + c) * p.ld_out;
+            if (col_ok) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int tok = t.tok0 + c + j;
-              if (tok < t.tok_end && col_ok) {
-                const float g = __uint_as_float(v[j]);
-                h[(size_t)tok * p.ld_out] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u[j]);
+              for (int j = 0; j < 16; ++j) {
+                if (j < nvalid) {
+                  const float silu = __fdividef(g[j], 1.0f + __expf(-g[j]));
+                  hp[(size_t)j * p.ld_out] = __float2bfloat16_rn(silu * __uint_as_float(v[j]));
+                }
               }
             }
           }
