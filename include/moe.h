@@ -226,6 +226,12 @@ unsigned long long moe_launch_count(void);
  * milliseconds; it then clears the records.  names: n_max entries of 64 bytes.
  * Returns the number of kernel names written in *n_out. */
 moe_status_t moe_profiler_enable(int enable);
+/* Restrict tracing to launches of one kernel name (as reported by
+ * moe_profiler_collect, at most 63 bytes); NULL or "" traces every launch.
+ * Each traced launch costs two event records on its stream, which also
+ * delay the next launch, so a timed region traces only the kernel whose
+ * duration it needs. */
+moe_status_t moe_profiler_only(const char* kernel_name);
 moe_status_t moe_profiler_collect(char* names, int* launches, double* total_ms,
                                   int n_max, int* n_out);
 

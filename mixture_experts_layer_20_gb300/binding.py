@@ -56,6 +56,7 @@ _SIGS = {
     "moe_set_wait_timeout_ns": (_st, [ctypes.c_ulonglong]),
     "moe_launch_count": (ctypes.c_ulonglong, []),
     "moe_profiler_enable": (_st, [_i]),
+    "moe_profiler_only": (_st, [ctypes.c_char_p]),
     "moe_profiler_collect": (_st, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_double), _i, ctypes.POINTER(ctypes.c_int)]),
 }
@@ -135,6 +136,11 @@ def moe_launch_count() -> int:
 
 def moe_profiler_enable(on: bool):
     _check(_lib.moe_profiler_enable(1 if on else 0), "moe_profiler_enable")
+
+
+def moe_profiler_only(name):
+    """Trace only launches of kernel `name` (None: every launch)."""
+    _check(_lib.moe_profiler_only(name.encode() if name else None), "moe_profiler_only")
 
 
 def moe_profiler_collect(n_max: int = 64) -> dict:

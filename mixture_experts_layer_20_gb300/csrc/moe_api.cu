@@ -45,6 +45,7 @@ struct Record {
 
 std::mutex g_prof_mu;
 bool g_prof_on = false;
+std::string g_prof_only;  // trace only launches of this kernel name (empty: all)
 std::vector<Record> g_records;
 std::vector<cudaEvent_t> g_event_pool;
 constexpr size_t kMaxRecords = 1 << 16;
@@ -119,6 +120,7 @@ KernelScope::KernelScope(cudaStream_t stream, const char* name) : stream_(stream
   g_launches.fetch_add(1, std::memory_order_relaxed);
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (!g_prof_on || g_records.size() >= kMaxRecords) return;
+  if (!g_prof_only.empty() && g_prof_only != name) return;
   Record r{name, take_event(), take_event()};
   if (!r.start || !r.stop) return;
   cudaEventRecord(r.start, stream_);
@@ -433,6 +435,12 @@ unsigned long long moe_launch_count(void) { return g_launches.load(); }
 moe_status_t moe_profiler_enable(int enable) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   g_prof_on = enable != 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_profiler_only(const char* kernel_name) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_only = kernel_name ? std::string(kernel_name, strnlen(kernel_name, 63)) : std::string();
   return MOE_OK;
 }
 
