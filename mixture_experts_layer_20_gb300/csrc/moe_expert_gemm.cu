@@ -25,13 +25,14 @@
 // Tiles are ordered (expert, slab, chunk): pairs running at the same time
 // read the same weight slab, which is then read from HBM once.
 //
-// gate_up: rank r of the pair holds gate rows [128 s + 64 r, +64) of slab s
-// in A rows 0-63 and the matching up rows in A rows 64-127, so the gate and up
-// accumulators of the same h column sit in TMEM lanes l and l + 64 of one CTA;
-// the epilogue warps that read the gate lanes pass them through shared memory
-// to the warps that read the up lanes, which compute h.  With the weights on M, a warp's 32
-// lanes are 32 consecutive output columns, so every store of one token row is
-// contiguous.
+// gate_up: rank r of the pair holds the gate rows [128 s + 64 r, +64) of slab
+// s and the matching up rows, interleaved in groups of 16 (A rows 32 j .. 32 j
+// + 15: gate rows 16 j .. 16 j + 15 of the CTA's 64, A rows 32 j + 16 .. 32 j
+// + 31: the matching up rows), so the gate and up accumulators of one h column
+// sit in TMEM lanes l and l + 16 of the same 32-lane quarter, which one
+// epilogue warp reads: a register shuffle pairs them.  With the weights on M,
+// a warp's lanes are consecutive output columns, so every store of one token
+// row is contiguous.
 //
 // Roles, per CTA (192 threads): warp 0 loads both operands with TMA into its
 // own shared memory, counting the bytes of both CTAs on the leader's full
@@ -60,9 +61,7 @@ constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
 constexpr int kABytes = kWRows * kBK * 2;          // 16 KB per K box
 constexpr int kBBytes = (kTokMax / 2) * kBK * 2;   // 16 KB per K box (capacity)
 constexpr int kStageBytes = kSub * (kABytes + kBBytes);
-constexpr int kExchStride = 20;                    // words per lane in the exchange buffer
-constexpr int kExchBytes = 2 * 32 * kExchStride * 4;
-constexpr int kSmemBytes = kStages * kStageBytes + kExchBytes + 1024;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
@@ -163,6 +162,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     tmem_relinquish_pair();
   }
 
+  pdl_wait_and_release();
+
   // Schedule: token chunks per expert and their exclusive prefix.
   const int G = p.groups;
   for (int i = threadIdx.x; i <= G; i += blockDim.x)
@@ -240,9 +241,9 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
           const uint32_t b_dst = a_dst + kSub * kABytes;
           for (int sub = 0; sub < nsub; ++sub) {
             const int kx = (ks * kSub + sub) * kBK;
-            // gate_up: one box holds 64 gate rows then the 64 matching up rows
+            // gate_up: one box holds 4 groups of {16 gate rows, the 16 matching up rows}
             if (KIND == kGateUp)
-              tma_load_4d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow, 0, t.e);
+              tma_load_5d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, 0, 0, wrow / 16, t.e);
             else
               tma_load_2d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow);
             tma_load_2d_pair(b_dst + sub * kBBytes, tmap_x, fb, kx, trow);
@@ -304,15 +305,11 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   } else {
     // ---------------- epilogue: warps 2..5, TMEM lanes 32 (warp % 4) + lane
     const int q = warp & 3;
-    float* exch = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)) +
-                                           kStages * kStageBytes) +
-                  (q & 1) * 32 * kExchStride;
     const uint32_t tempty_leader = mapa_shared(tempty_bar, 0);
     int acc = 0;
     uint32_t acc_phase = 0;
     // After a wait gives up, the loop still runs to the end (later waits fail
-    // at once) with its stores switched off: the two warps that exchange up
-    // values must pass the same named barriers.
+    // at once) with its stores switched off.
     for (int tau = pair; tau < total_tiles; tau += num_pairs) {
       const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
       const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
@@ -340,47 +337,34 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
           }
         }
       } else {
-        // Warps 4 and 5 (TMEM lanes 0-63, the gate rows) share their schedulers
-        // with the producer (warp 0) and the MMA issuer (warp 1), so they only
-        // pass the gate values through shared memory; warps 2 and 3 (lanes
-        // 64-127, the up rows) compute h = silu(gate) * up and store it.
-        const bool is_gate = q < 2;
-        const int col = t.slab * 128 + rank * 64 + (q & 1) * 32 + lane;
-        __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + col;
+        // In each warp's quarter of the TMEM lanes, lanes 0-15 hold 16 gate
+        // rows and lanes 16-31 the matching up rows (the weight map
+        // interleaves them in groups of 16), so one shuffle pairs them: lane
+        // l < 16 computes tokens c..c+7 and lane l + 16 tokens c+8..c+15 of
+        // h column l, and all four warps share the SwiGLU and the stores.
+        const bool lo = lane < 16;
+        const int col = t.slab * 128 + rank * 64 + q * 16 + (lane & 15);
         const bool col_ok = live && col < p.n_out;
+        __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + col;
 #pragma unroll 1
         for (int c = 0; c < t.n; c += 16) {
           uint32_t v[16];
           tmem_ld_32x32b_x16(t_row + c, v);
           tmem_ld_wait();
-          float* mine = exch + lane * kExchStride;
-          if (is_gate) {
+          const int row0 = t.tok0 + c + (lo ? 0 : 8);
+          const int nvalid = min(8, t.tok_end - row0);  // <= 0: rows past the expert's end
+          __nv_bfloat16* hp = h + (size_t)row0 * p.ld_out;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              reinterpret_cast<uint4*>(mine)[i] =
-                  make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) {
+            const float mine = __uint_as_float(lo ? v[i] : v[8 + i]);
+            const float other =
+                __shfl_xor_sync(0xffffffffu, __uint_as_float(lo ? v[8 + i] : v[i]), 16);
+            const float g = lo ? mine : other;
+            const float u = lo ? other : mine;
+            if (col_ok && i < nvalid)
+              hp[(size_t)i * p.ld_out] =
+                  __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
           }
-          if (q & 1) named_barrier_sync<2>(64); else named_barrier_sync<1>(64);
-          if (!is_gate) {
-            float g[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 f = reinterpret_cast<const float4*>(mine)[i];
-              g[4 * i] = f.x; g[4 * i + 1] = f.y; g[4 * i + 2] = f.z; g[4 * i + 3] = f.w;
-            }
-            const int nvalid = min(16, t.tok_end - t.tok0 - c);  // uniform across the warp
-            __nv_bfloat16* hp = h + (size_t)(t.tok0 + c) * p.ld_out;
-            if (col_ok) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                if (j < nvalid) {
-                  const float silu = __fdividef(g[j], 1.0f + __expf(-g[j]));
-                  hp[(size_t)j * p.ld_out] = __float2bfloat16_rn(silu * __uint_as_float(v[j]));
-                }
-              }
-            }
-          }
-          if (q & 1) named_barrier_sync<2>(64); else named_barrier_sync<1>(64);
         }
       }
       tc_fence_before_sync();
@@ -477,9 +461,8 @@ cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int 
   const long long pairs =
       std::max(1LL, std::min<long long>(resident_pairs(k, which), tiles_bound));
   KernelScope scope(s, name);
-  k<<<static_cast<unsigned>(2 * pairs), kThreads, kSmemBytes, s>>>(mw, mx[0], mx[1], mx[2], mx[3],
-                                                                   p);
-  return cudaGetLastError();
+  return launch_kernel(k, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads), kSmemBytes, s, mw,
+                       mx[0], mx[1], mx[2], mx[3], p);
 }
 
 }  // namespace
@@ -492,14 +475,15 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   const long long chunks_bound =
       offsets ? rows / kTokMax + std::min(E, rows) : (rows + kTokMax - 1) / kTokMax;
 
-  // W_gate_up viewed as [groups][2][I][d]: one box = 64 gate rows + the 64 matching up rows
+  // W_gate_up [groups][2][I][d] viewed as (d, 16 rows, gate|up, I/16 row groups, groups): one
+  // box = 4 row groups, each 16 gate rows followed by the 16 matching up rows
   CUtensorMap mw, mx[4];
-  const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(I), 2,
+  const uint64_t dims[5] = {static_cast<uint64_t>(d), 16, 2, static_cast<uint64_t>(I / 16),
                             static_cast<uint64_t>(groups)};
-  const uint64_t strides[3] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(I) * d * 2,
-                               2ull * I * d * 2};
-  const uint32_t box[4] = {64, 64, 2, 1};
-  cudaError_t e = make_bf16_map_nd(&mw, w_gate_up, 4, dims, strides, box);
+  const uint64_t strides[4] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(I) * d * 2,
+                               16ull * d * 2, 2ull * I * d * 2};
+  const uint32_t box[5] = {64, 16, 2, 4, 1};
+  cudaError_t e = make_bf16_map_nd(&mw, w_gate_up, 5, dims, strides, box);
   if (e == cudaSuccess) e = make_token_maps(mx, a, rows, d);
   if (e != cudaSuccess) return e;
   Params p{};

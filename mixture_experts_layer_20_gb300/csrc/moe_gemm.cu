@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  pdl_wait_and_release();
 
   const uint32_t tmem_base = s_tmem_base;
   const int m_tiles = (p.T + kBM - 1) / kBM;
@@ -282,7 +283,9 @@ cudaError_t launch_router_logits(cudaStream_t s, const void* x, const void* w_ro
   const long long tiles = static_cast<long long>((T + kBM - 1) / kBM) * p.k_splits;
   const long long grid = std::max(1LL, std::min<long long>(device_sm_count(), tiles));
   KernelScope scope(s, "moe_router_logits");
-  moe_router_logits_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(mx, mw, p);
+  cudaError_t le = launch_kernel(moe_router_logits_kernel, dim3(static_cast<unsigned>(grid)),
+                                 dim3(kThreads), kSmemBytes, s, mx, mw, p);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

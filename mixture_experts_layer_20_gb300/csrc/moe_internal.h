@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <string>
+#include <utility>
 
 namespace moe {
 
@@ -26,6 +27,41 @@ inline size_t router_partial_bytes(int T, int d, int E) {
 // Bits of the workspace's device status word.
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusDeviceCheck = 2u;
+
+// Programmatic dependent launch.  Every kernel of the layer is launched with
+// programmatic stream serialisation, so it may be scheduled while the kernel
+// before it in the stream is still finishing.  Before its first global-memory
+// access each kernel waits for that kernel to complete (griddepcontrol.wait;
+// a no-op for a normal launch) and then lets the next kernel be scheduled:
+// its launch latency and prologue (barrier init, tensor-memory allocation)
+// overlap the tail of this one, and at most one kernel waits at a time.
+#ifndef MOE_PDL
+#define MOE_PDL 1
+#endif
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait_and_release() {
+#if MOE_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#endif
 
 // Records the kernel name, counts the launch and, while tracing is on,
 // brackets it with CUDA events on `stream`.  Defined in moe_api.cu.

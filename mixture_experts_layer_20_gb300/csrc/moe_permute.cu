@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(512) moe_permute_count_kernel(const int32_t* _
                                                             int E, int32_t* __restrict__ table,
                                                             unsigned* status) {
   __shared__ int hist[kMaxExperts];
+  pdl_wait_and_release();
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int beg = blockIdx.x * kPermuteChunk;
@@ -55,6 +56,7 @@ __global__ void __launch_bounds__(kMaxExperts) moe_permute_scan_kernel(int32_t* 
                                                                    int32_t* __restrict__ counts,
                                                                    int32_t* __restrict__ offsets) {
   __shared__ int s_scan[kMaxExperts];
+  pdl_wait_and_release();
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
                            const int32_t* __restrict__ table, int32_t* __restrict__ perm,
                            int32_t* __restrict__ slot_pos) {
   __shared__ int wbase[kScatterWarps][kMaxExperts];
+  pdl_wait_and_release();
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kScatterWarps * kMaxExperts; i += blockDim.x)
@@ -146,6 +149,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   for (int i = threadIdx.x; i < kScatterWarps * kMaxExperts; i += blockDim.x)
     (&wbase[0][0])[i] = 0;
   __syncthreads();
+  pdl_wait_and_release();
   const int wbeg = w * kPerWarp;
   const unsigned lt_mask = (1u << lane) - 1u;
   bool bad = false;
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* 
                                                              int k, int vec_per_row,
                                                              uint4* __restrict__ x_perm,
                                                              unsigned* status) {
+  pdl_wait_and_release();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n; pos += warps) {
@@ -237,6 +242,7 @@ __global__ void __launch_bounds__(1024) moe_combine_kernel(const float* __restri
                                                        unsigned* status) {
   __shared__ int s_pos[kMaxTopK];
   __shared__ float s_g[kMaxTopK];
+  pdl_wait_and_release();
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     if (threadIdx.x < kMaxTopK) {
       int p = -1;
@@ -296,36 +302,32 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
   cudaError_t e = cudaSuccess;
   if (nchunks == 1) {
     KernelScope scope(s, "moe_permute_small");
-    moe_permute_small_kernel<<<1, kScatterWarps * 32, 0, s>>>(ids, n, E, counts, offsets, perm,
-                                                              slot_pos, status);
-    e = cudaGetLastError();
+    e = launch_kernel(moe_permute_small_kernel, dim3(1), dim3(kScatterWarps * 32), 0, s, ids, n, E,
+                      counts, offsets, perm, slot_pos, status);
   } else {
     {
       KernelScope scope(s, "moe_permute_count");
-      moe_permute_count_kernel<<<nchunks, 512, 0, s>>>(ids, n, E, chunk_table, status);
+      e = launch_kernel(moe_permute_count_kernel, dim3(nchunks), dim3(512), 0, s, ids, n, E,
+                        chunk_table, status);
     }
-    e = cudaGetLastError();
     if (e == cudaSuccess) {
       KernelScope scope(s, "moe_permute_scan");
-      moe_permute_scan_kernel<<<1, kMaxExperts, 0, s>>>(chunk_table, nchunks, E, counts, offsets);
-      e = cudaGetLastError();
+      e = launch_kernel(moe_permute_scan_kernel, dim3(1), dim3(kMaxExperts), 0, s, chunk_table,
+                        nchunks, E, counts, offsets);
     }
     if (e == cudaSuccess) {
       KernelScope scope(s, "moe_permute_scatter");
-      moe_permute_scatter_kernel<<<nchunks, kScatterWarps * 32, 0, s>>>(ids, n, E, chunk_table,
-                                                                         perm, slot_pos);
-      e = cudaGetLastError();
+      e = launch_kernel(moe_permute_scatter_kernel, dim3(nchunks), dim3(kScatterWarps * 32), 0, s,
+                        ids, n, E, chunk_table, perm, slot_pos);
     }
   }
   if (e != cudaSuccess || x == nullptr) return e;
   const int warps_per_cta = 8;
   const int grid = std::min((n + warps_per_cta - 1) / warps_per_cta, device_sm_count() * 8);
-  {
-    KernelScope scope(s, "moe_permute_gather");
-    moe_permute_gather_kernel<<<grid, warps_per_cta * 32, 0, s>>>(
-        perm, static_cast<const uint4*>(x), n, top_k, d / 8, static_cast<uint4*>(x_perm), status);
-  }
-  return cudaGetLastError();
+  KernelScope scope(s, "moe_permute_gather");
+  return launch_kernel(moe_permute_gather_kernel, dim3(grid), dim3(warps_per_cta * 32), 0, s, perm,
+                       static_cast<const uint4*>(x), n, top_k, d / 8, static_cast<uint4*>(x_perm),
+                       status);
 }
 
 cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_pos,
@@ -335,12 +337,9 @@ cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_p
   if (threads > 1024) threads = 1024;
   threads = ((threads + 31) / 32) * 32;
   const int grid = std::min(T, 65535 * 4);
-  {
-    KernelScope scope(s, "moe_combine");
-    moe_combine_kernel<<<grid, threads, 0, s>>>(y, slot_pos, gates, y_shared, T, d, top_k,
-                                            T * top_k, static_cast<__nv_bfloat16*>(out), status);
-  }
-  return cudaGetLastError();
+  KernelScope scope(s, "moe_combine");
+  return launch_kernel(moe_combine_kernel, dim3(grid), dim3(threads), 0, s, y, slot_pos, gates,
+                       y_shared, T, d, top_k, T * top_k, static_cast<__nv_bfloat16*>(out), status);
 }
 
 }  // namespace moe

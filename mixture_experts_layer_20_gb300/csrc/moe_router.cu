@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(kTokensPerCta * 32)
     moe_router_topk_kernel(const float* __restrict__ partial, int splits, int T, int npad, int E,
                            int k, const float* __restrict__ bias, int32_t* __restrict__ ids,
                            float* __restrict__ gates) {
+  pdl_wait_and_release();
   const int t = blockIdx.x * kTokensPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;  // whole warps only
@@ -112,12 +113,10 @@ cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, c
                           float* partial, unsigned* status, unsigned long long timeout_ns) {
   cudaError_t e = launch_router_logits(s, x, w_router, T, d, E, partial, status, timeout_ns);
   if (e != cudaSuccess) return e;
-  {
-    KernelScope scope(s, "moe_router_topk");
-    moe_router_topk_kernel<<<(T + kTokensPerCta - 1) / kTokensPerCta, kTokensPerCta * 32, 0, s>>>(
-        partial, router_splits(d), T, router_npad(E), E, top_k, bias, ids, gates);
-  }
-  return cudaGetLastError();
+  KernelScope scope(s, "moe_router_topk");
+  return launch_kernel(moe_router_topk_kernel, dim3((T + kTokensPerCta - 1) / kTokensPerCta),
+                       dim3(kTokensPerCta * 32), 0, s, partial, router_splits(d), T,
+                       router_npad(E), E, top_k, bias, ids, gates);
 }
 
 }  // namespace moe
