@@ -11,17 +11,18 @@
 // Work unit (a "tile") = one expert, one slab of 256 weight rows, one chunk
 // of that expert's tokens.  Weights are the MMA's M side, so M is always
 // full; tokens are the N side, chunked so that no expert is padded by more
-// than 63 rows per chunk (an expert with m rows gets ceil(m/256) chunks of
-// equal size rounded up to 64, so a CTA's half is 32, 64, 96 or 128 rows and
-// one TMA instruction fetches it; each TMA or MMA instruction costs its
-// single issuing thread tens of cycles, so few large ones keep the tensor
-// pipe fed).  A cluster of two CTAs (a pair) computes a
+// than 63 rows (an expert with m rows gets ceil(m/256) chunks that share its
+// ceil(m/64) 64-row units as evenly as possible, so a CTA's half of a chunk
+// is 32, 64, 96 or 128 rows and one TMA instruction fetches it; each TMA or
+// MMA instruction costs its single issuing thread tens of cycles, so few
+// large ones keep the tensor pipe fed).  A cluster of two CTAs (a pair) computes a
 // tile with tcgen05.mma.cta_group::2 (M = 256): each CTA holds 128 weight
 // rows and half of the token rows of every K block, so each SM moves at most
 // 32 KB per 64-wide K block.  A pipeline stage holds two such K blocks: the
 // thread that issues the MMAs pays tens of cycles per instruction and per
 // barrier round, so 8 MMAs per wait / commit keep it ahead of a 256 x 256
-// tile's tensor work; 3 stages fill the shared memory.
+// tile's tensor work.  The stages are sized for the launch's largest chunk:
+// 3 fit in shared memory for 256-token chunks, 4 when no chunk exceeds 192.
 // Tiles are ordered (expert, slab, chunk): pairs running at the same time
 // read the same weight slab, which is then read from HBM once.
 //
@@ -55,13 +56,11 @@ namespace {
 
 constexpr int kBK = 64;     // one 128-byte swizzle row of bf16: the K of one TMA box
 constexpr int kSub = 2;     // K boxes per pipeline stage: 8 MMAs per barrier round
-constexpr int kStages = 3;
+constexpr int kMaxStages = 4;                      // pipeline stages that fit when chunks are <= 192 tokens
 constexpr int kWRows = 128;                        // weight rows per CTA
 constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
 constexpr int kABytes = kWRows * kBK * 2;          // 16 KB per K box
-constexpr int kBBytes = (kTokMax / 2) * kBK * 2;   // 16 KB per K box (capacity)
-constexpr int kStageBytes = kSub * (kABytes + kBBytes);
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+constexpr int kMinStages = 3;                      // 3 stages of the largest (256-token) chunks
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
@@ -80,6 +79,7 @@ struct Params {
   int up_offset;          // gate_up: I
   void* out;              // gate_up: h bf16 [rows, I]; down: y fp32 [rows, d]
   long long ld_out;
+  int smem_bytes;         // dynamic shared memory of the launch
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -101,11 +101,14 @@ __device__ __forceinline__ Tile decode_tile(int tau, int slabs, int groups, cons
   const int local = tau - s_ct[lo] * slabs;
   t.slab = local / ch;
   const int c = local - t.slab * ch;
+  // the expert's ceil(m / 64) row units, spread over its ch chunks as evenly as
+  // possible (the first `rem` chunks take one unit more)
   const int m = s_off[lo + 1] - s_off[lo];
-  const int per = (((m + ch - 1) / ch) + 63) / 64 * 64;
-  t.tok0 = s_off[lo] + c * per;
-  t.tok_end = min(t.tok0 + per, s_off[lo + 1]);
-  t.n = per;
+  const int u = (m + 63) / 64;
+  const int base_u = u / ch, rem = u - base_u * ch;
+  t.tok0 = s_off[lo] + 64 * (c * base_u + min(c, rem));
+  t.n = 64 * (base_u + (c < rem ? 1 : 0));
+  t.tok_end = min(t.tok0 + t.n, s_off[lo + 1]);
   return t;
 }
 
@@ -121,7 +124,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_ct[kMaxExperts + 1];
-  __shared__ alignas(8) uint64_t s_bar[2 * kStages + 5];
+  __shared__ alignas(8) uint64_t s_bar[2 * kMaxStages + 5];
+  __shared__ int s_half_max;
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
@@ -134,13 +138,13 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t full_bar = smem_u32(&s_bar[0]);
-  const uint32_t empty_bar = smem_u32(&s_bar[kStages]);
-  const uint32_t tfull_bar = smem_u32(&s_bar[2 * kStages]);
-  const uint32_t tempty_bar = smem_u32(&s_bar[2 * kStages + 2]);
-  const uint32_t drain_bar = smem_u32(&s_bar[2 * kStages + 4]);
+  const uint32_t empty_bar = smem_u32(&s_bar[kMaxStages]);
+  const uint32_t tfull_bar = smem_u32(&s_bar[2 * kMaxStages]);
+  const uint32_t tempty_bar = smem_u32(&s_bar[2 * kMaxStages + 2]);
+  const uint32_t drain_bar = smem_u32(&s_bar[2 * kMaxStages + 4]);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(full_bar + 8 * s, 1);  // leader: counts both CTAs' bytes; unused in the follower
       mbar_init(empty_bar + 8 * s, 1);
     }
@@ -172,15 +176,22 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   if (warp == 0) {
     const int per = (G + 31) / 32;
     int local = 0;
+    int half_max = 32;
     bool bad = false;
     for (int j = 0; j < per; ++j) {
       const int g = lane * per + j;
       if (g < G) {
         const int m = s_off[g + 1] - s_off[g];
         bad |= m < 0;
-        local += m > 0 ? (m + kTokMax - 1) / kTokMax : 0;
+        if (m > 0) {
+          const int ch = (m + kTokMax - 1) / kTokMax;
+          local += ch;
+          half_max = max(half_max, (((m + 63) / 64 + ch - 1) / ch) * 32);
+        }
       }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) half_max = max(half_max, __shfl_xor_sync(0xffffffffu, half_max, o));
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -200,6 +211,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     bad = __any_sync(0xffffffffu, bad);
     __syncwarp();
     if (lane == 31) s_ct[G] = bad ? 0 : incl;
+    if (lane == 0) s_half_max = bad ? kTokMax / 2 : min(half_max, kTokMax / 2);
     if (bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusDeviceCheck);
   }
   tc_fence_before_sync();
@@ -212,6 +224,13 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   const int num_kb = p.K / kBK;                   // 64-wide K boxes
   const int num_ks = (num_kb + kSub - 1) / kSub;  // pipeline stages per tile
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
+  // Stage geometry: a stage holds kSub K boxes of the weights and of the
+  // largest token-chunk half of this launch, so smaller chunks leave room for
+  // a fourth stage.  Both CTAs of a pair derive the same layout.
+  const uint32_t b_sub_bytes = static_cast<uint32_t>(s_half_max) * kBK * 2;
+  const uint32_t stage_bytes = kSub * (kABytes + b_sub_bytes);
+  const uint32_t avail = static_cast<uint32_t>(p.smem_bytes) - (base - smem_u32(smem_raw));
+  const int nst = min(kMaxStages, static_cast<int>(avail / stage_bytes));
 
   if (warp == 0) {
     if (lane == 0) {
@@ -237,7 +256,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
           if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * nsub * tx_bytes);
           const uint32_t fb = full_leader + 8 * stage;
-          const uint32_t a_dst = base + stage * kStageBytes;
+          const uint32_t a_dst = base + stage * stage_bytes;
           const uint32_t b_dst = a_dst + kSub * kABytes;
           for (int sub = 0; sub < nsub; ++sub) {
             const int kx = (ks * kSub + sub) * kBK;
@@ -246,15 +265,15 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
               tma_load_5d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, 0, 0, wrow / 16, t.e);
             else
               tma_load_2d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow);
-            tma_load_2d_pair(b_dst + sub * kBBytes, tmap_x, fb, kx, trow);
+            tma_load_2d_pair(b_dst + sub * b_sub_bytes, tmap_x, fb, kx, trow);
           }
           ++issued;
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
       }
       if (leader) {
-        for (int i = max(0, issued - kStages); i < issued; ++i)
-          mbar_wait_drain(full_bar + 8 * (i % kStages), (i / kStages) & 1, p.status);
+        for (int i = max(0, issued - nst); i < issued; ++i)
+          mbar_wait_drain(full_bar + 8 * (i % nst), (i / nst) & 1, p.status);
       } else if (!ok) {
         // The follower cannot see its copies complete (they count on the
         // leader's barrier); after a give-up it leaves them time to land.
@@ -280,17 +299,17 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
         for (int ks = 0; ks < num_ks; ++ks) {
           const int nsub = min(kSub, num_kb - ks * kSub);
           if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
-          const uint32_t a_addr = base + stage * kStageBytes;
+          const uint32_t a_addr = base + stage * stage_bytes;
           const uint32_t b_addr = a_addr + kSub * kABytes;
           for (int sub = 0; sub < nsub; ++sub) {
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
               mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + sub * kABytes + k * 32),
-                            smem_desc_sw128(b_addr + sub * kBBytes + k * 32), idesc,
+                            smem_desc_sw128(b_addr + sub * b_sub_bytes + k * 32), idesc,
                             (ks | sub | k) != 0 ? 1u : 0u);
           }
           mma_commit_pair(empty_bar + 8 * stage);  // frees this stage in both CTAs
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit_pair(tfull_bar + 8 * acc);     // accumulator ready in both CTAs
@@ -407,23 +426,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 typedef void (*ExpertKernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
                              const CUtensorMap, const CUtensorMap, const Params);
 
-cudaError_t ensure_smem_attr(ExpertKernel k, int which) {
+// Dynamic shared memory of a launch: all that a block may use beyond the
+// kernel's static shared memory (the pipeline takes as many stages as fit).
+// Set as the kernel's limit on first use per device; 0 on failure.
+int ensure_smem_attr(ExpertKernel k, int which) {
   static std::mutex mu;
-  static unsigned done[2] = {0, 0};  // one bit per device, per kernel
+  static int bytes[2][64] = {};
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (dev < 32 && (done[which] >> dev) & 1u) return cudaSuccess;
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess && dev < 32) done[which] |= 1u << dev;
-  return e;
+  if (bytes[which][dev]) return bytes[which][dev];
+  int optin = 0;
+  cudaFuncAttributes fa{};
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, k) != cudaSuccess)
+    return 0;
+  const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
+  if (dyn < kMinStages * kSub * (kABytes + (kTokMax / 2) * kBK * 2) + 1024) return 0;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
+    return 0;
+  bytes[which][dev] = dyn;
+  return dyn;
 }
 
 // Pairs that can be resident at once.  A pair needs two SMs of one GPC, so
 // this can be fewer than half the SMs; a persistent grid larger than it would
 // run its surplus pairs' whole tile lists as a second wave.
-int resident_pairs(ExpertKernel k, int which) {
+int resident_pairs(ExpertKernel k, int which, int smem_bytes) {
   static std::mutex mu;
   static int cached[2][64] = {};
   int dev = 0;
@@ -433,7 +462,7 @@ int resident_pairs(ExpertKernel k, int which) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
@@ -454,15 +483,19 @@ cudaError_t make_token_maps(CUtensorMap (&mx)[4], const void* a, int rows, int K
 }
 
 cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int which,
-                          const CUtensorMap& mw, const CUtensorMap (&mx)[4], const Params& p,
+                          const CUtensorMap& mw, const CUtensorMap (&mx)[4], Params p,
                           long long tiles_bound) {
-  cudaError_t e = ensure_smem_attr(k, which);
-  if (e != cudaSuccess) return e;
+  const int smem = ensure_smem_attr(k, which);
+  if (smem <= 0) {
+    cudaGetLastError();
+    return cudaErrorInvalidConfiguration;
+  }
+  p.smem_bytes = smem;
   const long long pairs =
-      std::max(1LL, std::min<long long>(resident_pairs(k, which), tiles_bound));
+      std::max(1LL, std::min<long long>(resident_pairs(k, which, smem), tiles_bound));
   KernelScope scope(s, name);
-  return launch_kernel(k, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads), kSmemBytes, s, mw,
-                       mx[0], mx[1], mx[2], mx[3], p);
+  return launch_kernel(k, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads),
+                       static_cast<size_t>(smem), s, mw, mx[0], mx[1], mx[2], mx[3], p);
 }
 
 }  // namespace
