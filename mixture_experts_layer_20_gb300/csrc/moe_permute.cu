@@ -207,6 +207,10 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   }
 }
 
+// One warp copies one row: each lane issues all of its 16-byte loads of the
+// row (up to kGatherVec) before the stores, so a row is one round trip.
+constexpr int kGatherVec = 16;  // uint4 per lane: rows of up to 32 * 16 * 8 = 4096 bf16
+
 __global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* __restrict__ perm,
                                                              const uint4* __restrict__ x, int n,
                                                              int k, int vec_per_row,
@@ -223,72 +227,76 @@ __global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* 
     }
     const uint4* src = x + (size_t)(f / k) * vec_per_row;
     uint4* dst = x_perm + (size_t)pos * vec_per_row;
-    int v = lane;
-    for (; v + 96 < vec_per_row; v += 128) {
-      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
-                  d = __ldg(src + v + 96);
-      dst[v] = a; dst[v + 32] = b; dst[v + 64] = c; dst[v + 96] = d;
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * kGatherVec) {
+      uint4 r[kGatherVec];
+#pragma unroll
+      for (int i = 0; i < kGatherVec; ++i) {
+        const int v = v0 + lane + 32 * i;
+        if (v < vec_per_row) r[i] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int i = 0; i < kGatherVec; ++i) {
+        const int v = v0 + lane + 32 * i;
+        if (v < vec_per_row) dst[v] = r[i];
+      }
     }
-    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
   }
 }
 
-__global__ void __launch_bounds__(1024) moe_combine_kernel(const float* __restrict__ y,
-                                                       const int32_t* __restrict__ slot_pos,
-                                                       const float* __restrict__ gates,
-                                                       const float* __restrict__ y_shared, int T,
-                                                       int d, int k, int rows,
-                                                       __nv_bfloat16* __restrict__ out,
-                                                       unsigned* status) {
-  __shared__ int s_pos[kMaxTopK];
-  __shared__ float s_g[kMaxTopK];
+// One thread: 4 columns of one token, all k slot rows loaded before the sum
+// (k independent 16-byte loads in flight per thread), then the fp32 sum in
+// slot order and one bf16 rounding.  A block covers 1024 columns of a token.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineCols = kCombineThreads * 4;
+
+__global__ void __launch_bounds__(kCombineThreads) moe_combine_kernel(
+    const float* __restrict__ y, const int32_t* __restrict__ slot_pos,
+    const float* __restrict__ gates, const float* __restrict__ y_shared, int T, int d, int k,
+    int rows, int blocks_per_token, __nv_bfloat16* __restrict__ out, unsigned* status) {
   pdl_wait_and_release();
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    if (threadIdx.x < kMaxTopK) {
-      int p = -1;
-      float g = 0.0f;
-      if (threadIdx.x < k) {
-        p = __ldg(slot_pos + (size_t)t * k + threadIdx.x);
-        g = __ldg(gates + (size_t)t * k + threadIdx.x);
-        if (static_cast<unsigned>(p) >= static_cast<unsigned>(rows)) {
-          atomicOr(status, kStatusDeviceCheck);
-          p = -1;
-        }
-      }
-      s_pos[threadIdx.x] = p;
-      s_g[threadIdx.x] = g;
-    }
-    __syncthreads();
-    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int t = blockIdx.x / blocks_per_token;
+  const int c = (blockIdx.x - t * blocks_per_token) * kCombineCols + threadIdx.x * 4;
+  if (t >= T || c >= d) return;
+  int pos[kMaxTopK];
+  float g[kMaxTopK];
+  bool bad = false;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        const int p = s_pos[j];
-        if (p >= 0) {
-          const float4* src = reinterpret_cast<const float4*>(y + (size_t)p * d + c);
-          const float4 lo = __ldg(src), hi = __ldg(src + 1);
-          const float g = s_g[j];
-          acc[0] = fmaf(g, lo.x, acc[0]); acc[1] = fmaf(g, lo.y, acc[1]);
-          acc[2] = fmaf(g, lo.z, acc[2]); acc[3] = fmaf(g, lo.w, acc[3]);
-          acc[4] = fmaf(g, hi.x, acc[4]); acc[5] = fmaf(g, hi.y, acc[5]);
-          acc[6] = fmaf(g, hi.z, acc[6]); acc[7] = fmaf(g, hi.w, acc[7]);
-        }
+  for (int j = 0; j < kMaxTopK; ++j) {
+    pos[j] = 0;
+    g[j] = 0.0f;
+    if (j < k) {
+      const int p = __ldg(slot_pos + (size_t)t * k + j);
+      if (static_cast<unsigned>(p) < static_cast<unsigned>(rows)) {
+        pos[j] = p;
+        g[j] = __ldg(gates + (size_t)t * k + j);
+      } else {
+        bad = true;
       }
-      if (y_shared) {
-        const float4* src = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
-        const float4 a = __ldg(src), b = __ldg(src + 1);
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-      }
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(out + (size_t)t * d + c) = o;
     }
-    __syncthreads();
   }
+  if (bad && c == 0) atomicOr(status, kStatusDeviceCheck);
+  float4 v[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) v[j] = __ldg(reinterpret_cast<const float4*>(y + (size_t)pos[j] * d + c));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) {
+      acc.x = fmaf(g[j], v[j].x, acc.x);
+      acc.y = fmaf(g[j], v[j].y, acc.y);
+      acc.z = fmaf(g[j], v[j].z, acc.z);
+      acc.w = fmaf(g[j], v[j].w, acc.w);
+    }
+  }
+  if (y_shared) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c));
+    acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+  }
+  uint2 o;
+  o.x = pack_bf16x2(acc.x, acc.y);
+  o.y = pack_bf16x2(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(out + (size_t)t * d + c) = o;
 }
 
 }  // namespace
@@ -333,13 +341,13 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
 cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_pos,
                            const float* gates, const float* y_shared, int T, int d, int top_k,
                            void* out, unsigned* status) {
-  int threads = d / 8;
-  if (threads > 1024) threads = 1024;
-  threads = ((threads + 31) / 32) * 32;
-  const int grid = std::min(T, 65535 * 4);
+  const int blocks_per_token = (d + kCombineCols - 1) / kCombineCols;
+  const long long grid = static_cast<long long>(T) * blocks_per_token;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   KernelScope scope(s, "moe_combine");
-  return launch_kernel(moe_combine_kernel, dim3(grid), dim3(threads), 0, s, y, slot_pos, gates,
-                       y_shared, T, d, top_k, T * top_k, static_cast<__nv_bfloat16*>(out), status);
+  return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(grid)),
+                       dim3(kCombineThreads), 0, s, y, slot_pos, gates, y_shared, T, d, top_k,
+                       T * top_k, blocks_per_token, static_cast<__nv_bfloat16*>(out), status);
 }
 
 }  // namespace moe
