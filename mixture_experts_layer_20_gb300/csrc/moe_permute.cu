@@ -4,10 +4,10 @@
 // input rows by expert; section 9.4.1: the per-expert row counts m_j sum to
 // n k).  The flat assignment index f = t*k + j is cut into chunks of 4096:
 //   count   : one CTA per chunk, shared-memory histogram -> chunk_table[c][e]
-//   scan    : one CTA, one thread per expert, runs down the chunks (exclusive
-//             per-expert chunk bases, counts[e]) then scans the experts
-//             (offsets[e]) and adds offsets[e] to every chunk base
-//   scatter : one CTA per chunk; each warp owns 256 consecutive assignments;
+//   scatter : one CTA per chunk.  Each CTA scans the chunk table itself:
+//             expert totals (counts[e]), their exclusive scan (offsets[e]),
+//             and its chunk's base per expert = offsets[e] + rows of expert e
+//             in earlier chunks.  Each warp owns 256 consecutive assignments;
 //             warp histograms (match.any) -> per-warp bases -> each lane's
 //             rank among earlier equal ids in its warp.  Positions are thus
 //             offsets[e] + (number of earlier f with the same e): a stable
@@ -17,8 +17,8 @@
 //
 // Combine ('Chapter 9. Distributed inference', section 9.3.4, step four;
 // 'Hosting Qwen on Blackwell', "MoE Dispatch - Combine": weighted
-// accumulation): one CTA per token, each thread 8 columns; the k weighted
-// rows are summed in fp32 in slot order, then rounded once to bf16.
+// accumulation): each thread sums 4 columns of one token's k weighted rows in
+// fp32 in slot order, then rounds once to bf16.
 
 #include <cuda_bf16.h>
 
@@ -51,44 +51,14 @@ __global__ void __launch_bounds__(512) moe_permute_count_kernel(const int32_t* _
   for (int i = threadIdx.x; i < E; i += blockDim.x) table[(size_t)blockIdx.x * E + i] = hist[i];
 }
 
-__global__ void __launch_bounds__(kMaxExperts) moe_permute_scan_kernel(int32_t* __restrict__ table,
-                                                                   int nchunks, int E,
-                                                                   int32_t* __restrict__ counts,
-                                                                   int32_t* __restrict__ offsets) {
-  __shared__ int s_scan[kMaxExperts];
-  pdl_wait_and_release();
-  const int e = threadIdx.x;
-  int run = 0;
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = table[(size_t)c * E + e];
-      table[(size_t)c * E + e] = run;
-      run += v;
-    }
-    counts[e] = run;
-  }
-  s_scan[e] = e < E ? run : 0;
-  __syncthreads();
-  // inclusive Hillis-Steele scan over the (at most 256) experts
-  for (int o = 1; o < kMaxExperts; o <<= 1) {
-    const int v = e >= o ? s_scan[e - o] : 0;
-    __syncthreads();
-    s_scan[e] += v;
-    __syncthreads();
-  }
-  const int excl = s_scan[e] - (e < E ? run : 0);
-  if (e < E) {
-    offsets[e] = excl;
-    for (int c = 0; c < nchunks; ++c) table[(size_t)c * E + e] += excl;
-  }
-  if (e == E - 1) offsets[E] = s_scan[e];
-}
-
 __global__ void __launch_bounds__(kScatterWarps * 32)
-    moe_permute_scatter_kernel(const int32_t* __restrict__ ids, int n, int E,
-                           const int32_t* __restrict__ table, int32_t* __restrict__ perm,
+    moe_permute_scatter_kernel(const int32_t* __restrict__ ids, int n, int E, int nchunks,
+                           const int32_t* __restrict__ table, int32_t* __restrict__ counts,
+                           int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                            int32_t* __restrict__ slot_pos) {
   __shared__ int wbase[kScatterWarps][kMaxExperts];
+  __shared__ int s_scan[kMaxExperts];
+  __shared__ int s_before[kMaxExperts];
   pdl_wait_and_release();
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -107,10 +77,39 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
     __syncwarp();
   }
+  // Every CTA scans the per-chunk counts itself: expert totals, the exclusive
+  // scan over experts (the offsets; CTA 0 stores them and the counts) and this
+  // chunk's base = offset + the expert's rows in earlier chunks.
+  for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) {
+    int total = 0, before = 0;
+    if (e < E)
+      for (int c = 0; c < nchunks; ++c) {
+        const int v = __ldg(table + (size_t)c * E + e);
+        if (c < static_cast<int>(blockIdx.x)) before += v;
+        total += v;
+      }
+    s_scan[e] = total;
+    s_before[e] = before;
+  }
   __syncthreads();
+  for (int o = 1; o < kMaxExperts; o <<= 1) {
+    int v = 0;
+    if (threadIdx.x < kMaxExperts && threadIdx.x >= o) v = s_scan[threadIdx.x - o];
+    __syncthreads();
+    if (threadIdx.x < kMaxExperts) s_scan[threadIdx.x] += v;
+    __syncthreads();
+  }
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const int excl = e > 0 ? s_scan[e - 1] : 0;
+      offsets[e] = excl;
+      counts[e] = s_scan[e] - excl;
+    }
+    if (threadIdx.x == 0) offsets[E] = s_scan[E - 1];
+  }
   // per-expert exclusive scan across the warps, on top of the chunk's base
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = table[(size_t)blockIdx.x * E + e];
+    int run = (e > 0 ? s_scan[e - 1] : 0) + s_before[e];
     for (int ww = 0; ww < kScatterWarps; ++ww) {
       const int v = wbase[ww][e];
       wbase[ww][e] = run;
@@ -136,31 +135,50 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
 }
 
 // All of count, scan and scatter in one CTA when the T*k assignments fit one
-// chunk (decode batches): the same stable positions, two launches fewer.
-__global__ void __launch_bounds__(kScatterWarps * 32)
+// chunk (decode batches): the same stable positions as the multi-CTA path, two
+// launches fewer.  Each warp owns a contiguous range of flat indices and walks
+// it 32 at a time in index order (loads issued kPrefetch groups ahead); a
+// per-warp, per-expert count then a scan over warps and experts give every
+// warp its start position per expert.  (One CTA for much larger batches is
+// slower than the three-kernel path: a single SM issues all the scattered
+// position stores.)
+constexpr int kPrefetch = 8;
+
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
     moe_permute_small_kernel(const int32_t* __restrict__ ids, int n, int E,
                              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                              int32_t* __restrict__ perm, int32_t* __restrict__ slot_pos,
                              unsigned* status) {
-  __shared__ int wbase[kScatterWarps][kMaxExperts];
+  __shared__ int wbase[WARPS][kMaxExperts];
   __shared__ int s_scan[kMaxExperts];
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kScatterWarps * kMaxExperts; i += blockDim.x)
-    (&wbase[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < WARPS * kMaxExperts; i += blockDim.x) (&wbase[0][0])[i] = 0;
   __syncthreads();
   pdl_wait_and_release();
-  const int wbeg = w * kPerWarp;
+  const int per_warp = ((n + WARPS * 32 - 1) / (WARPS * 32)) * 32;
+  const int wbeg = w * per_warp;
+  const int wend = min(n, wbeg + per_warp);
   const unsigned lt_mask = (1u << lane) - 1u;
   bool bad = false;
-  for (int r = 0; r < kPerWarp / 32; ++r) {
-    const int f = wbeg + r * 32 + lane;
-    const int e = f < n ? __ldg(ids + f) : -1;
-    const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
-    bad |= f < n && !valid;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
-    __syncwarp();
+  for (int g0 = wbeg; g0 < wend; g0 += 32 * kPrefetch) {
+    int ev[kPrefetch];
+#pragma unroll
+    for (int b = 0; b < kPrefetch; ++b) {
+      const int f = g0 + 32 * b + lane;
+      ev[b] = f < wend ? __ldg(ids + f) : -1;
+    }
+#pragma unroll
+    for (int b = 0; b < kPrefetch; ++b) {
+      const int f = g0 + 32 * b + lane;
+      const int e = ev[b];
+      const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+      bad |= f < wend && !valid;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
+      __syncwarp();
+    }
   }
   if (bad) atomicOr(status, kStatusDeviceCheck);
   __syncthreads();
@@ -168,7 +186,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) {
     int total = 0;
     if (e < E)
-      for (int ww = 0; ww < kScatterWarps; ++ww) total += wbase[ww][e];
+      for (int ww = 0; ww < WARPS; ++ww) total += wbase[ww][e];
     s_scan[e] = total;
   }
   __syncthreads();
@@ -183,7 +201,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     int run = e > 0 ? s_scan[e - 1] : 0;
     offsets[e] = run;
     counts[e] = s_scan[e] - run;
-    for (int ww = 0; ww < kScatterWarps; ++ww) {
+    for (int ww = 0; ww < WARPS; ++ww) {
       const int v = wbase[ww][e];
       wbase[ww][e] = run;
       run += v;
@@ -191,19 +209,28 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   }
   if (threadIdx.x == 0) offsets[E] = s_scan[E - 1];
   __syncthreads();
-  for (int r = 0; r < kPerWarp / 32; ++r) {
-    const int f = wbeg + r * 32 + lane;
-    const int e = f < n ? __ldg(ids + f) : -1;
-    const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (valid) {
-      const int pos = wbase[w][e] + __popc(peers & lt_mask);
-      perm[pos] = f;
-      slot_pos[f] = pos;
+  for (int g0 = wbeg; g0 < wend; g0 += 32 * kPrefetch) {
+    int ev[kPrefetch];
+#pragma unroll
+    for (int b = 0; b < kPrefetch; ++b) {
+      const int f = g0 + 32 * b + lane;
+      ev[b] = f < wend ? __ldg(ids + f) : -1;
     }
-    __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < kPrefetch; ++b) {
+      const int f = g0 + 32 * b + lane;
+      const int e = ev[b];
+      const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (valid) {
+        const int pos = wbase[w][e] + __popc(peers & lt_mask);
+        perm[pos] = f;
+        slot_pos[f] = pos;
+      }
+      __syncwarp();
+      if (valid && lane == __ffs(peers) - 1) wbase[w][e] += __popc(peers);
+      __syncwarp();
+    }
   }
 }
 
@@ -308,10 +335,10 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
   const int n = T * top_k;
   const int nchunks = (n + kPermuteChunk - 1) / kPermuteChunk;
   cudaError_t e = cudaSuccess;
-  if (nchunks == 1) {
+  if (n <= kPermuteChunk) {
     KernelScope scope(s, "moe_permute_small");
-    e = launch_kernel(moe_permute_small_kernel, dim3(1), dim3(kScatterWarps * 32), 0, s, ids, n, E,
-                      counts, offsets, perm, slot_pos, status);
+    e = launch_kernel(moe_permute_small_kernel<kScatterWarps>, dim3(1), dim3(kScatterWarps * 32),
+                      0, s, ids, n, E, counts, offsets, perm, slot_pos, status);
   } else {
     {
       KernelScope scope(s, "moe_permute_count");
@@ -319,14 +346,9 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
                         chunk_table, status);
     }
     if (e == cudaSuccess) {
-      KernelScope scope(s, "moe_permute_scan");
-      e = launch_kernel(moe_permute_scan_kernel, dim3(1), dim3(kMaxExperts), 0, s, chunk_table,
-                        nchunks, E, counts, offsets);
-    }
-    if (e == cudaSuccess) {
       KernelScope scope(s, "moe_permute_scatter");
       e = launch_kernel(moe_permute_scatter_kernel, dim3(nchunks), dim3(kScatterWarps * 32), 0, s,
-                        ids, n, E, chunk_table, perm, slot_pos);
+                        ids, n, E, nchunks, chunk_table, counts, offsets, perm, slot_pos);
     }
   }
   if (e != cudaSuccess || x == nullptr) return e;

@@ -20,6 +20,105 @@ namespace {
 
 constexpr int kTokensPerCta = 8;  // one warp each
 
+// A float's bits mapped to an unsigned key with the same order.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int SLOTS>  // experts per lane: lane, lane + 32, ... (SLOTS * 32 >= E)
+__device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int splits, int T,
+                                          int npad, int E, int k, const float* __restrict__ bias,
+                                          int t, int lane, int32_t* __restrict__ ids,
+                                          float* __restrict__ gates) {
+  // K ranges summed in range order (a token's logits do not depend on the
+  // batch); all loads of a range are issued before its adds
+  float L[SLOTS];
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) L[i] = 0.0f;
+#pragma unroll 4
+  for (int sp = 0; sp < splits; ++sp) {
+    const float* row = partial + ((size_t)sp * T + t) * npad;
+    float v[SLOTS];
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) v[i] = lane + 32 * i < E ? __ldg(row + lane + 32 * i) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) L[i] += v[i];
+  }
+  // 64-bit keys: logit order in the high word, lower expert index wins ties
+  unsigned long long key[SLOTS];
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    const int e = lane + 32 * i;
+    float l = e < E ? L[i] + (bias ? __ldg(bias + e) : 0.0f) : -INFINITY;
+    if (l == 0.0f) l = 0.0f;  // -0 and +0 compare equal: one key for both
+    key[i] = e < E ? (static_cast<unsigned long long>(order_key(l)) << 32) |
+                         static_cast<uint32_t>(kMaxExperts - 1 - e)
+                   : 0ull;
+  }
+  // each lane sorts its own keys, descending
+#pragma unroll
+  for (int a = 0; a < SLOTS - 1; ++a)
+#pragma unroll
+    for (int b = 0; b < SLOTS - 1 - a; ++b)
+      if (key[b] < key[b + 1]) { const unsigned long long x = key[b]; key[b] = key[b + 1]; key[b + 1] = x; }
+
+  // k rounds: the warp's largest head wins; its lane pops it
+  unsigned long long sel[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    sel[j] = 0ull;
+    if (j < k) {
+      unsigned long long best = key[0];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o > best ? o : best;
+      }
+      sel[j] = best;
+      if (key[0] == best) {
+#pragma unroll
+        for (int i = 0; i < SLOTS - 1; ++i) key[i] = key[i + 1];
+        key[SLOTS - 1] = 0ull;
+      }
+    }
+  }
+
+  if (lane == 0) {
+    int e_of[kMaxTopK];
+    float w[kMaxTopK];
+    float sum = 0.0f;
+    float top = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      const uint32_t hi = static_cast<uint32_t>(sel[j] >> 32);
+      const float l = __uint_as_float((hi & 0x80000000u) ? (hi & 0x7fffffffu) : ~hi);
+      if (j == 0) top = l;
+      e_of[j] = j < k ? kMaxExperts - 1 - static_cast<int>(sel[j] & 0xffffffffu) : INT_MAX;
+      w[j] = j < k ? expf(l - top) : 0.0f;
+      sum += w[j];
+    }
+    // ascending expert id (unused slots hold INT_MAX and sort last)
+#pragma unroll
+    for (int a = 0; a < kMaxTopK - 1; ++a) {
+#pragma unroll
+      for (int b = 0; b < kMaxTopK - 1 - a; ++b) {
+        if (e_of[b] > e_of[b + 1]) {
+          const int te = e_of[b]; e_of[b] = e_of[b + 1]; e_of[b + 1] = te;
+          const float tw = w[b]; w[b] = w[b + 1]; w[b + 1] = tw;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        ids[(size_t)t * k + j] = e_of[j];
+        gates[(size_t)t * k + j] = w[j] / sum;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kTokensPerCta * 32)
     moe_router_topk_kernel(const float* __restrict__ partial, int splits, int T, int npad, int E,
                            int k, const float* __restrict__ bias, int32_t* __restrict__ ids,
@@ -28,82 +127,9 @@ __global__ void __launch_bounds__(kTokensPerCta * 32)
   const int t = blockIdx.x * kTokensPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;  // whole warps only
-
-  // lane owns experts lane, lane+32, ... (at most 8 of them)
-  float L[kMaxExperts / 32];
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; ++i) L[i] = 0.0f;
-  // K ranges in order; the loads of one range are independent of each other
-#pragma unroll 2
-  for (int sp = 0; sp < splits; ++sp) {
-    const float* row = partial + ((size_t)sp * T + t) * npad;
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i)
-      if (lane + 32 * i < E) L[i] += __ldg(row + lane + 32 * i);
-  }
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; ++i) {
-    const int e = lane + 32 * i;
-    L[i] = e < E ? L[i] + (bias ? __ldg(bias + e) : 0.0f) : -INFINITY;
-  }
-
-  float sel_v[kMaxTopK];
-  int sel_e[kMaxTopK];
-  unsigned taken = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    sel_v[j] = -INFINITY;
-    sel_e[j] = INT_MAX;
-    if (j < k) {
-      float bv = -INFINITY;
-      int be = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = lane + 32 * i;
-        const bool free = e < E && !((taken >> i) & 1u);
-        if (free && (L[i] > bv || (L[i] == bv && e < be))) { bv = L[i]; be = e; }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      sel_v[j] = bv;
-      sel_e[j] = be;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i)
-        if (lane + 32 * i == be) taken |= 1u << i;
-    }
-  }
-
-  if (lane == 0) {
-    float w[kMaxTopK];
-    float sum = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      w[j] = (j < k) ? expf(sel_v[j] - sel_v[0]) : 0.0f;
-      sum += w[j];
-    }
-    // ascending expert id (unused slots hold INT_MAX and sort last)
-#pragma unroll
-    for (int a = 0; a < kMaxTopK - 1; ++a) {
-#pragma unroll
-      for (int b = 0; b < kMaxTopK - 1 - a; ++b) {
-        if (sel_e[b] > sel_e[b + 1]) {
-          const int te = sel_e[b]; sel_e[b] = sel_e[b + 1]; sel_e[b + 1] = te;
-          const float tw = w[b]; w[b] = w[b + 1]; w[b + 1] = tw;
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k) {
-        ids[(size_t)t * k + j] = sel_e[j];
-        gates[(size_t)t * k + j] = w[j] / sum;
-      }
-    }
-  }
+  if (E <= 64) topk_warp<2>(partial, splits, T, npad, E, k, bias, t, lane, ids, gates);
+  else if (E <= 128) topk_warp<4>(partial, splits, T, npad, E, k, bias, t, lane, ids, gates);
+  else topk_warp<8>(partial, splits, T, npad, E, k, bias, t, lane, ids, gates);
 }
 
 }  // namespace

@@ -79,6 +79,8 @@ def test_route_ties(moe):
 
 PERMUTE_CASES = [
     (64, 8, 2), (1, 8, 8), (1500, 128, 8), (4096, 256, 8), (777, 16, 4), (5000, 64, 1),
+    (512, 128, 8),    # 4096 assignments: the largest single-CTA grouping
+    (9000, 200, 8),   # 72000 assignments: 18 chunks of the multi-CTA path
 ]
 
 
