@@ -59,6 +59,7 @@ constexpr int kSub = 2;     // K boxes per pipeline stage: 8 MMAs per barrier ro
 constexpr int kMaxStages = 4;                      // pipeline stages that fit when chunks are <= 192 tokens
 constexpr int kWRows = 128;                        // weight rows per CTA
 constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
+constexpr int kUnit = 32;                          // token rows: chunks are multiples of this
 constexpr int kABytes = kWRows * kBK * 2;          // 16 KB per K box
 constexpr int kMinStages = 3;                      // 3 stages of the largest (256-token) chunks
 constexpr int kThreads = 192;
@@ -101,25 +102,26 @@ __device__ __forceinline__ Tile decode_tile(int tau, int slabs, int groups, cons
   const int local = tau - s_ct[lo] * slabs;
   t.slab = local / ch;
   const int c = local - t.slab * ch;
-  // the expert's ceil(m / 64) row units, spread over its ch chunks as evenly as
+  // the expert's ceil(m / 32) row units, spread over its ch chunks as evenly as
   // possible (the first `rem` chunks take one unit more)
   const int m = s_off[lo + 1] - s_off[lo];
-  const int u = (m + 63) / 64;
+  const int u = (m + kUnit - 1) / kUnit;
   const int base_u = u / ch, rem = u - base_u * ch;
-  t.tok0 = s_off[lo] + 64 * (c * base_u + min(c, rem));
-  t.n = 64 * (base_u + (c < rem ? 1 : 0));
+  t.tok0 = s_off[lo] + kUnit * (c * base_u + min(c, rem));
+  t.n = kUnit * (base_u + (c < rem ? 1 : 0));
   t.tok_end = min(t.tok0 + t.n, s_off[lo + 1]);
   return t;
 }
 
-// The token operand comes through one of four tensor maps whose boxes are
-// 32, 64, 96 and 128 rows: one TMA instruction loads a CTA's n/2 token rows.
-struct TokenMaps {
-  const CUtensorMap* m[4];
+// The token operand comes through one of eight tensor maps whose boxes are
+// 16, 32, ..., 128 rows: one TMA instruction loads a CTA's n/2 token rows.
+constexpr int kTokenMaps = 8;
+struct TokenMapSet {
+  CUtensorMap m[kTokenMaps];
 };
 
 template <int KIND>
-__device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, const TokenMaps& tx,
+__device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, const TokenMapSet& tx,
                                                  const Params& p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
@@ -156,10 +158,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     s_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap_w);
-    tma_prefetch_desc(tx.m[0]);
-    tma_prefetch_desc(tx.m[1]);
-    tma_prefetch_desc(tx.m[2]);
-    tma_prefetch_desc(tx.m[3]);
+#pragma unroll
+    for (int i = 0; i < kTokenMaps; ++i) tma_prefetch_desc(&tx.m[i]);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&s_tmem_base), kTmemCols);
@@ -176,7 +176,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   if (warp == 0) {
     const int per = (G + 31) / 32;
     int local = 0;
-    int half_max = 32;
+    int half_max = kUnit / 2;
     bool bad = false;
     for (int j = 0; j < per; ++j) {
       const int g = lane * per + j;
@@ -186,7 +186,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
         if (m > 0) {
           const int ch = (m + kTokMax - 1) / kTokMax;
           local += ch;
-          half_max = max(half_max, (((m + 63) / 64 + ch - 1) / ch) * 32);
+          half_max = max(half_max, (((m + kUnit - 1) / kUnit + ch - 1) / ch) * (kUnit / 2));
         }
       }
     }
@@ -244,9 +244,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       const uint32_t full_leader = mapa_shared(full_bar, 0);
       for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
         const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-        const int half = t.n / 2;  // 32, 64, 96 or 128 token rows per CTA
-        const CUtensorMap* tmap_x =
-            half <= 32 ? tx.m[0] : (half <= 64 ? tx.m[1] : (half <= 96 ? tx.m[2] : tx.m[3]));
+        const int half = t.n / 2;  // 16, 32, ..., 128 token rows per CTA
+        const CUtensorMap* tmap_x = &tx.m[half / 16 - 1];
         const uint32_t tx_bytes = kABytes + half * 128;  // per CTA
         const int trow = t.tok0 + rank * half;
         const int wrow = KIND == kGateUp ? t.slab * 128 + rank * 64
@@ -408,23 +407,17 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     moe_gate_up_swiglu_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                              const __grid_constant__ CUtensorMap tx32,
-                              const __grid_constant__ CUtensorMap tx64,
-                              const __grid_constant__ CUtensorMap tx96,
-                              const __grid_constant__ CUtensorMap tx128, const Params p) {
-  expert_gemm_body<kGateUp>(tmap_w, TokenMaps{{&tx32, &tx64, &tx96, &tx128}}, p);
+                              const __grid_constant__ TokenMapSet tx, const Params p) {
+  expert_gemm_body<kGateUp>(tmap_w, tx, p);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     moe_down_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                    const __grid_constant__ CUtensorMap tx32, const __grid_constant__ CUtensorMap tx64,
-                    const __grid_constant__ CUtensorMap tx96,
-                    const __grid_constant__ CUtensorMap tx128, const Params p) {
-  expert_gemm_body<kDown>(tmap_w, TokenMaps{{&tx32, &tx64, &tx96, &tx128}}, p);
+                    const __grid_constant__ TokenMapSet tx, const Params p) {
+  expert_gemm_body<kDown>(tmap_w, tx, p);
 }
 
-typedef void (*ExpertKernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                             const CUtensorMap, const CUtensorMap, const Params);
+typedef void (*ExpertKernel)(const CUtensorMap, const TokenMapSet, const Params);
 
 // Dynamic shared memory of a launch: all that a block may use beyond the
 // kernel's static shared memory (the pipeline takes as many stages as fit).
@@ -473,17 +466,17 @@ int resident_pairs(ExpertKernel k, int which, int smem_bytes) {
   return cached[which][dev];
 }
 
-// Token-operand maps over a [rows, K] bf16 matrix, boxes of 32..128 rows.
-cudaError_t make_token_maps(CUtensorMap (&mx)[4], const void* a, int rows, int K) {
-  for (int i = 0; i < 4; ++i) {
-    cudaError_t e = make_bf16_map(&mx[i], a, rows, K, 32 * (i + 1));
+// Token-operand maps over a [rows, K] bf16 matrix, boxes of 16, 32, ..., 128 rows.
+cudaError_t make_token_maps(TokenMapSet& mx, const void* a, int rows, int K) {
+  for (int i = 0; i < kTokenMaps; ++i) {
+    cudaError_t e = make_bf16_map(&mx.m[i], a, rows, K, 16 * (i + 1));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int which,
-                          const CUtensorMap& mw, const CUtensorMap (&mx)[4], Params p,
+                          const CUtensorMap& mw, const TokenMapSet& mx, Params p,
                           long long tiles_bound) {
   const int smem = ensure_smem_attr(k, which);
   if (smem <= 0) {
@@ -495,7 +488,7 @@ cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int 
       std::max(1LL, std::min<long long>(resident_pairs(k, which, smem), tiles_bound));
   KernelScope scope(s, name);
   return launch_kernel(k, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads),
-                       static_cast<size_t>(smem), s, mw, mx[0], mx[1], mx[2], mx[3], p);
+                       static_cast<size_t>(smem), s, mw, mx, p);
 }
 
 }  // namespace
@@ -510,7 +503,8 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
 
   // W_gate_up [groups][2][I][d] viewed as (d, 16 rows, gate|up, I/16 row groups, groups): one
   // box = 4 row groups, each 16 gate rows followed by the 16 matching up rows
-  CUtensorMap mw, mx[4];
+  CUtensorMap mw;
+  TokenMapSet mx;
   const uint64_t dims[5] = {static_cast<uint64_t>(d), 16, 2, static_cast<uint64_t>(I / 16),
                             static_cast<uint64_t>(groups)};
   const uint64_t strides[4] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(I) * d * 2,
@@ -536,7 +530,8 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
                     moe_gate_up_swiglu_kernel, 0, mw, mx, p, chunks_bound * p.slabs);
   if (e != cudaSuccess) return e;
 
-  CUtensorMap mw2, mx2[4];
+  CUtensorMap mw2;
+  TokenMapSet mx2;
   e = make_bf16_map(&mw2, w_down, static_cast<uint64_t>(groups) * d, I, 128);
   if (e == cudaSuccess) e = make_token_maps(mx2, h, rows, I);
   if (e != cudaSuccess) return e;
