@@ -11,9 +11,9 @@
 // Work unit (a "tile") = one expert, one slab of 256 weight rows, one chunk
 // of that expert's tokens.  Weights are the MMA's M side, so M is always
 // full; tokens are the N side, chunked so that no expert is padded by more
-// than 63 rows (an expert with m rows gets ceil(m/256) chunks that share its
-// ceil(m/64) 64-row units as evenly as possible, so a CTA's half of a chunk
-// is 32, 64, 96 or 128 rows and one TMA instruction fetches it; each TMA or
+// than 15 rows (an expert with m rows gets ceil(m/256) chunks that share its
+// ceil(m/16) 16-row units as evenly as possible, so a CTA's half of a chunk
+// is a multiple of 8 rows up to 128 and one TMA instruction fetches it; each TMA or
 // MMA instruction costs its single issuing thread tens of cycles, so few
 // large ones keep the tensor pipe fed).  A cluster of two CTAs (a pair) computes a
 // tile with tcgen05.mma.cta_group::2 (M = 256): each CTA holds 128 weight
@@ -59,7 +59,7 @@ constexpr int kSub = 2;     // K boxes per pipeline stage: 8 MMAs per barrier ro
 constexpr int kMaxStages = 4;                      // pipeline stages that fit when chunks are <= 192 tokens
 constexpr int kWRows = 128;                        // weight rows per CTA
 constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
-constexpr int kUnit = 32;                          // token rows: chunks are multiples of this
+constexpr int kUnit = 16;                          // token rows: chunks are multiples of this
 constexpr int kABytes = kWRows * kBK * 2;          // 16 KB per K box
 constexpr int kMinStages = 3;                      // 3 stages of the largest (256-token) chunks
 constexpr int kThreads = 192;
@@ -102,7 +102,7 @@ __device__ __forceinline__ Tile decode_tile(int tau, int slabs, int groups, cons
   const int local = tau - s_ct[lo] * slabs;
   t.slab = local / ch;
   const int c = local - t.slab * ch;
-  // the expert's ceil(m / 32) row units, spread over its ch chunks as evenly as
+  // the expert's ceil(m / 16) row units, spread over its ch chunks as evenly as
   // possible (the first `rem` chunks take one unit more)
   const int m = s_off[lo + 1] - s_off[lo];
   const int u = (m + kUnit - 1) / kUnit;
@@ -113,9 +113,9 @@ __device__ __forceinline__ Tile decode_tile(int tau, int slabs, int groups, cons
   return t;
 }
 
-// The token operand comes through one of eight tensor maps whose boxes are
-// 16, 32, ..., 128 rows: one TMA instruction loads a CTA's n/2 token rows.
-constexpr int kTokenMaps = 8;
+// The token operand comes through one of sixteen tensor maps whose boxes are
+// 8, 16, ..., 128 rows: one TMA instruction loads a CTA's n/2 token rows.
+constexpr int kTokenMaps = kTokMax / kUnit;
 struct TokenMapSet {
   CUtensorMap m[kTokenMaps];
 };
@@ -244,8 +244,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       const uint32_t full_leader = mapa_shared(full_bar, 0);
       for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
         const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-        const int half = t.n / 2;  // 16, 32, ..., 128 token rows per CTA
-        const CUtensorMap* tmap_x = &tx.m[half / 16 - 1];
+        const int half = t.n / 2;  // 8, 16, ..., 128 token rows per CTA
+        const CUtensorMap* tmap_x = &tx.m[half / (kUnit / 2) - 1];
         const uint32_t tx_bytes = kABytes + half * 128;  // per CTA
         const int trow = t.tok0 + rank * half;
         const int wrow = KIND == kGateUp ? t.slab * 128 + rank * 64
@@ -466,10 +466,10 @@ int resident_pairs(ExpertKernel k, int which, int smem_bytes) {
   return cached[which][dev];
 }
 
-// Token-operand maps over a [rows, K] bf16 matrix, boxes of 16, 32, ..., 128 rows.
+// Token-operand maps over a [rows, K] bf16 matrix, boxes of 8, 16, ..., 128 rows.
 cudaError_t make_token_maps(TokenMapSet& mx, const void* a, int rows, int K) {
   for (int i = 0; i < kTokenMaps; ++i) {
-    cudaError_t e = make_bf16_map(&mx.m[i], a, rows, K, 16 * (i + 1));
+    cudaError_t e = make_bf16_map(&mx.m[i], a, rows, K, (kUnit / 2) * (i + 1));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
