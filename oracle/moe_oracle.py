@@ -31,6 +31,11 @@ What the layer computes, and where each step comes from:
   Dispatch - Combine": weighted accumulation in combine).  An always-on shared
   expert adds its output with weight one ('PagedAttention, speculative
   decoding, MoE and Blackwell', section 2, shared experts).
+* Router bias.  A per-expert bias is added to the logits; by default it takes
+  part in both the selection and the gates.  The variant the same section
+  names for balancing (DeepSeek's bias adjustment) uses the bias only to pick
+  the experts: selection on logits + bias, gates from the unbiased logits of
+  the chosen experts (``bias_for_selection_only``).
 
 Precision: every product and sum is fp64 over the exact values of the bf16
 inputs.  The one deliberate rounding is h -> bf16 (round to nearest, ties to
@@ -122,21 +127,31 @@ def select_top_k(logits_row, top_k: int) -> list:
     return sorted(ranked[:top_k])
 
 
-def route(x_bits, w_router_bits, top_k: int, router_bias=None):
+def route(x_bits, w_router_bits, top_k: int, router_bias=None,
+          bias_for_selection_only: bool = False):
     """Top-k routing with softmax gates renormalised over the chosen experts.
 
-    Returns (ids [T,k] int32, gates [T,k] fp64, logits [T,E] fp64).
+    With bias_for_selection_only the bias decides which experts are chosen but
+    the gates are computed from the unbiased logits ('PagedAttention,
+    speculative decoding, MoE and Blackwell', section 2: bias adjustment steers
+    the load without changing the mixing weights).
+
+    Returns (ids [T,k] int32, gates [T,k] fp64, logits [T,E] fp64); logits are
+    the ones the selection used.
     """
     logits = router_logits(x_bits, w_router_bits, router_bias)
+    gate_logits = logits
+    if bias_for_selection_only and router_bias is not None:
+        gate_logits = router_logits(x_bits, w_router_bits, None)
     T, E = logits.shape
     if not 1 <= top_k <= E:
         raise ValueError("top_k must be in [1, E]")
     ids = np.empty((T, top_k), dtype=np.int32)
     gates = np.empty((T, top_k), dtype=np.float64)
     for t in range(T):
-        row = logits[t]
-        chosen = select_top_k(row, top_k)
+        chosen = select_top_k(logits[t], top_k)
         # softmax over all E experts ...
+        row = gate_logits[t]
         p = np.exp(row - row.max())
         p = p / p.sum()
         # ... keep the chosen k and renormalise them to sum to one
@@ -238,12 +253,13 @@ def combine(y, slot_pos, gates, y_shared=None) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def forward(x_bits, w_router, w_gate_up, w_down, top_k: int, router_bias=None,
-            w_gate_up_shared=None, w_down_shared=None) -> dict:
+            w_gate_up_shared=None, w_down_shared=None,
+            bias_for_selection_only: bool = False) -> dict:
     """Route -> group -> expert FFN -> combine, every intermediate returned."""
     x_bits = np.asarray(x_bits, dtype=np.uint16)
     T = x_bits.shape[0]
     E = np.asarray(w_router).shape[0]
-    ids, gates, logits = route(x_bits, w_router, top_k, router_bias)
+    ids, gates, logits = route(x_bits, w_router, top_k, router_bias, bias_for_selection_only)
     counts, offsets, perm, slot_pos = permute(ids, E)
     x = bf16_bits_to_f64(x_bits)
     x_perm = x[perm // top_k]

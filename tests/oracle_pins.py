@@ -11,6 +11,9 @@ What pins what:
   top-k set .................... brute force over all k-subsets (max logit sum)
   tie-break .................... duplicated router rows give exact ties
   gates ........................ k = E: scipy softmax; k = 1: exactly 1; subset-softmax identity
+  selection-only bias .......... k = E: scipy softmax of the unbiased logits; k = 2 with a
+                                 dominant bias: the forced expert plus the unbiased argmax,
+                                 gates = scipy expit of the unbiased logit difference
   grouping ..................... numpy's stable argsort / bincount (library routines)
   SwiGLU expert ................ a hand-computed one-element example; torch silu dense FFN
   whole layer .................. brute-force dense form: every expert on every token,
@@ -159,6 +162,34 @@ def check_gates(o):
         assert L[t, ids[t]].min() >= L[t, rest].max()
 
 
+def check_selection_only_bias(o):
+    x, wr, _, _ = _random_layer(13, 24, 64, 8, 8)
+    bias = _rng(14).standard_normal(8).astype(np.float32) * 3
+    L0 = _dec(x) @ _dec(wr).T                      # unbiased logits, computed here
+    # k = E: every expert chosen, gates = the softmax of the unbiased logits
+    ids, gates, _ = o.route(x, wr, 8, bias, True)
+    assert (ids == np.arange(8)).all()
+    assert np.allclose(gates, scipy.special.softmax(L0, axis=1), rtol=1e-12, atol=0)
+    # the biased variant differs (the bias is large), so the check discriminates
+    _, gates_b, _ = o.route(x, wr, 8, bias, False)
+    assert np.abs(gates_b - gates).max() > 1e-3
+    # k = 2 with a dominant bias on expert 5: expert 5 is always chosen with the
+    # unbiased argmax of the others; the gates are a logistic of the unbiased gap
+    big = np.zeros(8, dtype=np.float32)
+    big[5] = 1e4
+    ids, gates, _ = o.route(x, wr, 2, big, True)
+    for t in range(L0.shape[0]):
+        others = [e for e in range(8) if e != 5]
+        second = others[int(np.argmax(L0[t, others]))]
+        assert sorted(ids[t].tolist()) == sorted([5, second])
+        g5 = gates[t, list(ids[t]).index(5)]
+        assert abs(g5 - scipy.special.expit(L0[t, 5] - L0[t, second])) < 1e-12
+    # the selection itself is the biased one
+    ids_sel, _, _ = o.route(x, wr, 3, bias, True)
+    ids_b, _, _ = o.route(x, wr, 3, bias, False)
+    assert (ids_sel == ids_b).all()
+
+
 # ---------------------------------------------------------------- grouping
 
 def check_permute(o):
@@ -282,7 +313,7 @@ def check_forward_tokens(o):
 
 ALL_CHECKS = [
     check_bf16_decode, check_bf16_round, check_logits_one_hot,
-    check_topk_brute_force, check_tie_break, check_gates, check_permute,
+    check_topk_brute_force, check_tie_break, check_gates, check_selection_only_bias, check_permute,
     check_swiglu_hand_example, check_single_expert_is_dense_ffn,
     check_identical_experts, check_brute_force_layer, check_down_scaling,
     check_forward_tokens,

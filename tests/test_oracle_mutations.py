@@ -88,8 +88,8 @@ def _m_slots_by_logit(o):
 def _m_no_renormalise(o):
     orig = o.route
 
-    def route(x, wr, k, bias=None):
-        ids, gates, L = orig(x, wr, k, bias)
+    def route(x, wr, k, bias=None, sel_only=False):
+        ids, gates, L = orig(x, wr, k, bias, sel_only)
         p = np.exp(L - L.max(axis=1, keepdims=True))
         p = p / p.sum(axis=1, keepdims=True)
         return ids, np.take_along_axis(p, ids.astype(np.int64), axis=1), L
@@ -135,9 +135,10 @@ def _m_unstable_permute(o):
 def _m_gather_wrong_index(o):
     orig_forward = o.forward
 
-    def forward(x_bits, wr, wgu, wd, k, router_bias=None, w_gate_up_shared=None, w_down_shared=None):
+    def forward(x_bits, wr, wgu, wd, k, router_bias=None, w_gate_up_shared=None, w_down_shared=None,
+                bias_for_selection_only=False):
         x_bits = np.asarray(x_bits, dtype=np.uint16)
-        ids, gates, logits = o.route(x_bits, wr, k, router_bias)
+        ids, gates, logits = o.route(x_bits, wr, k, router_bias, bias_for_selection_only)
         counts, offsets, perm, slot_pos = o.permute(ids, np.asarray(wr).shape[0])
         x = o.bf16_bits_to_f64(x_bits)
         x_perm = x[(perm % k) % x.shape[0]]       # token index taken modulo k
@@ -191,12 +192,29 @@ def _m_forward_tokens_no_gate(o):
     o.forward_tokens = forward_tokens
 
 
+def _m_selection_only_ignored(o):
+    orig = o.route
+    o.route = lambda x, wr, k, bias=None, sel_only=False: orig(x, wr, k, bias, False)
+
+
+def _m_selection_only_unbiased_pick(o):
+    orig = o.route
+
+    def route(x, wr, k, bias=None, sel_only=False):
+        if not sel_only:
+            return orig(x, wr, k, bias, False)
+        ids, gates, L = orig(x, wr, k, None, False)   # picks on the unbiased logits too
+        return ids, gates, L
+    o.route = route
+
+
 MUTATIONS = [
     _m_silu_sign, _m_gate_up_swapped, _m_no_h_rounding, _m_down_transposed,
     _m_tie_high_index, _m_slots_by_logit, _m_no_renormalise, _m_bias_dropped,
     _m_bf16_round_truncates, _m_bf16_decode_shift, _m_unstable_permute,
     _m_gather_wrong_index, _m_combine_ignores_gates, _m_combine_drops_shared,
-    _m_expert_shift, _m_forward_tokens_no_gate,
+    _m_expert_shift, _m_forward_tokens_no_gate, _m_selection_only_ignored,
+    _m_selection_only_unbiased_pick,
 ]
 
 
