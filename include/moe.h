@@ -85,6 +85,17 @@ moe_status_t moe_route(const moe_bf16* x, const moe_bf16* w_router,
                        int32_t* topk_ids, float* topk_gates,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_route with a choice of what the bias does.  bias_selection_only = 0:
+ * as moe_route.  1: the experts are chosen on logits + router_bias, the gates
+ * are the softmax of the chosen experts' unbiased logits (the bias only
+ * steers the load; 'PagedAttention, speculative decoding, MoE and
+ * Blackwell', section 2, bias adjustment for balancing).  Same buffers,
+ * workspace and errors as moe_route. */
+moe_status_t moe_route_ex(const moe_bf16* x, const moe_bf16* w_router,
+                          const float* router_bias, int bias_selection_only, int T, int d,
+                          int E, int top_k, int32_t* topk_ids, float* topk_gates, void* ws,
+                          size_t ws_bytes, moe_stream_t stream);
+
 /* Step 2, group by expert.  topk_ids [T,top_k] int32 in [0,E).  Writes
  * expert_counts [E], expert_offsets [E+1] (offsets[E] = T*top_k),
  * perm [T*top_k] (row p of the grouped layout holds assignment perm[p] =
@@ -163,15 +174,18 @@ moe_status_t moe_forward(const moe_bf16* x, const moe_bf16* w_router,
                          int T, int d, int E, int I, int top_k, moe_bf16* out,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Optional parts of the layer.  router_bias: [E] fp32 added to the logits.
- * Shared expert ('PagedAttention, speculative decoding, MoE and Blackwell',
- * section 2: experts that process every token): w_gate_up_shared [2*I_shared,d],
- * w_down_shared [d,I_shared]; its output is added with weight 1. */
+/* Optional parts of the layer.  router_bias: [E] fp32 added to the logits;
+ * bias_selection_only: 0 = the bias enters selection and gates, 1 = selection
+ * only (see moe_route_ex).  Shared expert ('PagedAttention, speculative
+ * decoding, MoE and Blackwell', section 2: experts that process every token):
+ * w_gate_up_shared [2*I_shared,d], w_down_shared [d,I_shared]; its output is
+ * added with weight 1.  Zero-initialise the struct: later fields default to 0. */
 typedef struct {
   const float* router_bias;
   const moe_bf16* w_gate_up_shared;
   const moe_bf16* w_down_shared;
   int I_shared;
+  int bias_selection_only;
 } moe_forward_ext_t;
 
 moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,

@@ -32,13 +32,14 @@ class WorkspaceLayout(ctypes.Structure):
 
 class ForwardExt(ctypes.Structure):
     _fields_ = [("router_bias", _vp), ("w_gate_up_shared", _vp), ("w_down_shared", _vp),
-                ("I_shared", _i)]
+                ("I_shared", _i), ("bias_selection_only", _i)]
 
 
 _SIGS = {
     "moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_workspace_init": (_st, [_vp, _sz, _vp]),
     "moe_route": (_st, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "moe_route_ex": (_st, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute_static_scratch": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp]),
@@ -161,7 +162,7 @@ def moe_profiler_collect(n_max: int = 64) -> dict:
 # ---------------------------------------------------------------- the four steps
 
 def moe_route(x, w_router, top_k, router_bias=None, topk_ids=None, topk_gates=None, ws=None,
-              stream=None):
+              stream=None, bias_selection_only=False):
     _want(x, torch.bfloat16, "x"); _want(w_router, torch.bfloat16, "w_router")
     _want(router_bias, torch.float32, "router_bias")
     T, d = x.shape
@@ -173,8 +174,9 @@ def moe_route(x, w_router, top_k, router_bias=None, topk_ids=None, topk_gates=No
     _want(topk_ids, torch.int32, "topk_ids"); _want(topk_gates, torch.float32, "topk_gates")
     if ws is None:
         ws = new_workspace(T, d, E, 64, top_k, device=x.device)
-    _check(_lib.moe_route(_p(x), _p(w_router), _p(router_bias), T, d, E, top_k, _p(topk_ids),
-                          _p(topk_gates), _p(ws), ws.numel(), _stream(stream)), "moe_route")
+    _check(_lib.moe_route_ex(_p(x), _p(w_router), _p(router_bias), 1 if bias_selection_only else 0,
+                             T, d, E, top_k, _p(topk_ids), _p(topk_gates), _p(ws), ws.numel(),
+                             _stream(stream)), "moe_route")
     return topk_ids, topk_gates
 
 
@@ -249,7 +251,7 @@ def moe_combine(y, slot_pos, topk_gates, y_shared=None, out=None, ws=None, strea
 
 
 def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router_bias=None,
-                w_gate_up_shared=None, w_down_shared=None, stream=None):
+                w_gate_up_shared=None, w_down_shared=None, stream=None, bias_selection_only=False):
     """The whole layer.  Returns out [T, d] bf16."""
     for t, n in ((x, "x"), (w_router, "w_router"), (w_gate_up, "w_gate_up"), (w_down, "w_down"),
                  (w_gate_up_shared, "w_gate_up_shared"), (w_down_shared, "w_down_shared")):
@@ -271,7 +273,8 @@ def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router
     else:
         ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
                          w_gate_up_shared.data_ptr() if I_s else None,
-                         w_down_shared.data_ptr() if I_s else None, I_s)
+                         w_down_shared.data_ptr() if I_s else None, I_s,
+                         1 if bias_selection_only else 0)
         st = _lib.moe_forward_ex(_p(x), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E, I,
                                  top_k, _p(out), _p(ws), ws.numel(), s, ctypes.byref(ext))
     _check(st, "moe_forward")

@@ -171,11 +171,11 @@ moe_status_t check_device() {
   return MOE_OK;
 }
 
-moe_status_t route_impl(const moe_bf16* x, const moe_bf16* w_router, const float* bias, int T,
-                        int d, int E, int top_k, int32_t* ids, float* gates, float* partial,
-                        unsigned* status, cudaStream_t s) {
-  cudaError_t e = launch_router(s, x, w_router, bias, T, d, E, top_k, ids, gates, partial, status,
-                                g_timeout_ns.load());
+moe_status_t route_impl(const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                        int bias_selection_only, int T, int d, int E, int top_k, int32_t* ids,
+                        float* gates, float* partial, unsigned* status, cudaStream_t s) {
+  cudaError_t e = launch_router(s, x, w_router, bias, bias_selection_only, T, d, E, top_k, ids,
+                                gates, partial, status, g_timeout_ns.load());
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router launch");
 }
 
@@ -226,6 +226,14 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) 
 moe_status_t moe_route(const moe_bf16* x, const moe_bf16* w_router, const float* router_bias,
                        int T, int d, int E, int top_k, int32_t* topk_ids, float* topk_gates,
                        void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return moe_route_ex(x, w_router, router_bias, 0, T, d, E, top_k, topk_ids, topk_gates, ws,
+                      ws_bytes, stream);
+}
+
+moe_status_t moe_route_ex(const moe_bf16* x, const moe_bf16* w_router, const float* router_bias,
+                          int bias_selection_only, int T, int d, int E, int top_k,
+                          int32_t* topk_ids, float* topk_gates, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
   moe_status_t st = check_shapes(T, d, E, 64, top_k);
   if (st != MOE_OK) return st;
   if (T == 0) return MOE_OK;
@@ -237,8 +245,8 @@ moe_status_t moe_route(const moe_bf16* x, const moe_bf16* w_router, const float*
     return fail(MOE_ERR_WORKSPACE, "moe_route: workspace too small");
   if ((st = check_device()) != MOE_OK) return st;
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kAlign);
-  return route_impl(x, w_router, router_bias, T, d, E, top_k, topk_ids, topk_gates, partial,
-                    status_word(ws), reinterpret_cast<cudaStream_t>(stream));
+  return route_impl(x, w_router, router_bias, bias_selection_only, T, d, E, top_k, topk_ids,
+                    topk_gates, partial, status_word(ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_permute(const int32_t* topk_ids, const moe_bf16* x, int T, int d, int E,
@@ -308,6 +316,7 @@ moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
   moe_status_t st = check_shapes(T, d, E, I, top_k);
   if (st != MOE_OK) return st;
   const float* bias = ext ? ext->router_bias : nullptr;
+  const int bias_sel = ext ? ext->bias_selection_only : 0;
   const int I_shared = ext ? ext->I_shared : 0;
   const moe_bf16* wgu_s = ext ? ext->w_gate_up_shared : nullptr;
   const moe_bf16* wd_s = ext ? ext->w_down_shared : nullptr;
@@ -340,8 +349,8 @@ moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
   const int rows = T * top_k;
 
   float* partial = reinterpret_cast<float*>(w + L.logits);
-  if ((st = route_impl(x, w_router, bias, T, d, E, top_k, ids, gates, partial, status, s)) !=
-      MOE_OK)
+  if ((st = route_impl(x, w_router, bias, bias_sel, T, d, E, top_k, ids, gates, partial, status,
+                       s)) != MOE_OK)
     return st;
   cudaError_t e = launch_permute(s, ids, x, T, d, E, top_k, counts, offsets, perm, slot_pos,
                                  x_perm, table, status);

@@ -102,10 +102,13 @@ cudaError_t launch_router_logits(cudaStream_t s, const void* x, const void* w_ro
                                  unsigned long long timeout_ns);
 
 // Router: logits (via the partials in `partial`), bias, top-k with the
-// lowest-index tie-break, renormalised gates (moe_router.cu).
+// lowest-index tie-break, renormalised gates (moe_router.cu).  With
+// bias_selection_only the bias picks the experts and the gates come from the
+// unbiased logits.
 cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, const float* bias,
-                          int T, int d, int E, int top_k, int32_t* ids, float* gates,
-                          float* partial, unsigned* status, unsigned long long timeout_ns);
+                          int bias_selection_only, int T, int d, int E, int top_k, int32_t* ids,
+                          float* gates, float* partial, unsigned* status,
+                          unsigned long long timeout_ns);
 
 // Grouped SwiGLU FFN (moe_expert_gemm.cu).  Rows [offsets[e], offsets[e+1])
 // of a [rows, d] go through expert e (weights per expert: w_gate_up [2I, d],

@@ -29,8 +29,8 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 template <int SLOTS>  // experts per lane: lane, lane + 32, ... (SLOTS * 32 >= E)
 __device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int splits, int T,
                                           int npad, int E, int k, const float* __restrict__ bias,
-                                          int t, int lane, int32_t* __restrict__ ids,
-                                          float* __restrict__ gates) {
+                                          int sel_only, int t, int lane,
+                                          int32_t* __restrict__ ids, float* __restrict__ gates) {
   // K ranges summed in range order (a token's logits do not depend on the
   // batch); all loads of a range are issued before its adds
   float L[SLOTS];
@@ -45,12 +45,16 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int
 #pragma unroll
     for (int i = 0; i < SLOTS; ++i) L[i] += v[i];
   }
-  // 64-bit keys: logit order in the high word, lower expert index wins ties
+  // 64-bit keys: selection-logit order in the high word, lower expert index
+  // wins ties.  Each key carries the logit its gate is computed from: the
+  // same biased logit, or the unbiased one when the bias only selects.
   unsigned long long key[SLOTS];
+  float gl[SLOTS];
 #pragma unroll
   for (int i = 0; i < SLOTS; ++i) {
     const int e = lane + 32 * i;
     float l = e < E ? L[i] + (bias ? __ldg(bias + e) : 0.0f) : -INFINITY;
+    gl[i] = sel_only ? L[i] : l;
     if (l == 0.0f) l = 0.0f;  // -0 and +0 compare equal: one key for both
     key[i] = e < E ? (static_cast<unsigned long long>(order_key(l)) << 32) |
                          static_cast<uint32_t>(kMaxExperts - 1 - e)
@@ -61,13 +65,18 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int
   for (int a = 0; a < SLOTS - 1; ++a)
 #pragma unroll
     for (int b = 0; b < SLOTS - 1 - a; ++b)
-      if (key[b] < key[b + 1]) { const unsigned long long x = key[b]; key[b] = key[b + 1]; key[b + 1] = x; }
+      if (key[b] < key[b + 1]) {
+        const unsigned long long x = key[b]; key[b] = key[b + 1]; key[b + 1] = x;
+        const float y = gl[b]; gl[b] = gl[b + 1]; gl[b + 1] = y;
+      }
 
   // k rounds: the warp's largest head wins; its lane pops it
   unsigned long long sel[kMaxTopK];
+  float sel_g[kMaxTopK];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
     sel[j] = 0ull;
+    sel_g[j] = 0.0f;
     if (j < k) {
       unsigned long long best = key[0];
 #pragma unroll
@@ -75,10 +84,12 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int
         const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
         best = o > best ? o : best;
       }
+      const unsigned owner = __ballot_sync(0xffffffffu, key[0] == best);
       sel[j] = best;
+      sel_g[j] = __shfl_sync(0xffffffffu, gl[0], __ffs(owner) - 1);
       if (key[0] == best) {
 #pragma unroll
-        for (int i = 0; i < SLOTS - 1; ++i) key[i] = key[i + 1];
+        for (int i = 0; i < SLOTS - 1; ++i) { key[i] = key[i + 1]; gl[i] = gl[i + 1]; }
         key[SLOTS - 1] = 0ull;
       }
     }
@@ -88,14 +99,14 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int
     int e_of[kMaxTopK];
     float w[kMaxTopK];
     float sum = 0.0f;
-    float top = 0.0f;
+    float top = sel_g[0];
+#pragma unroll
+    for (int j = 1; j < kMaxTopK; ++j)
+      if (j < k) top = fmaxf(top, sel_g[j]);
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
-      const uint32_t hi = static_cast<uint32_t>(sel[j] >> 32);
-      const float l = __uint_as_float((hi & 0x80000000u) ? (hi & 0x7fffffffu) : ~hi);
-      if (j == 0) top = l;
       e_of[j] = j < k ? kMaxExperts - 1 - static_cast<int>(sel[j] & 0xffffffffu) : INT_MAX;
-      w[j] = j < k ? expf(l - top) : 0.0f;
+      w[j] = j < k ? expf(sel_g[j] - top) : 0.0f;
       sum += w[j];
     }
     // ascending expert id (unused slots hold INT_MAX and sort last)
@@ -121,28 +132,29 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int
 
 __global__ void __launch_bounds__(kTokensPerCta * 32)
     moe_router_topk_kernel(const float* __restrict__ partial, int splits, int T, int npad, int E,
-                           int k, const float* __restrict__ bias, int32_t* __restrict__ ids,
-                           float* __restrict__ gates) {
+                           int k, const float* __restrict__ bias, int sel_only,
+                           int32_t* __restrict__ ids, float* __restrict__ gates) {
   pdl_wait_and_release();
   const int t = blockIdx.x * kTokensPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;  // whole warps only
-  if (E <= 64) topk_warp<2>(partial, splits, T, npad, E, k, bias, t, lane, ids, gates);
-  else if (E <= 128) topk_warp<4>(partial, splits, T, npad, E, k, bias, t, lane, ids, gates);
-  else topk_warp<8>(partial, splits, T, npad, E, k, bias, t, lane, ids, gates);
+  if (E <= 64) topk_warp<2>(partial, splits, T, npad, E, k, bias, sel_only, t, lane, ids, gates);
+  else if (E <= 128) topk_warp<4>(partial, splits, T, npad, E, k, bias, sel_only, t, lane, ids, gates);
+  else topk_warp<8>(partial, splits, T, npad, E, k, bias, sel_only, t, lane, ids, gates);
 }
 
 }  // namespace
 
 cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, const float* bias,
-                          int T, int d, int E, int top_k, int32_t* ids, float* gates,
-                          float* partial, unsigned* status, unsigned long long timeout_ns) {
+                          int bias_selection_only, int T, int d, int E, int top_k, int32_t* ids,
+                          float* gates, float* partial, unsigned* status,
+                          unsigned long long timeout_ns) {
   cudaError_t e = launch_router_logits(s, x, w_router, T, d, E, partial, status, timeout_ns);
   if (e != cudaSuccess) return e;
   KernelScope scope(s, "moe_router_topk");
   return launch_kernel(moe_router_topk_kernel, dim3((T + kTokensPerCta - 1) / kTokensPerCta),
                        dim3(kTokensPerCta * 32), 0, s, partial, router_splits(d), T,
-                       router_npad(E), E, top_k, bias, ids, gates);
+                       router_npad(E), E, top_k, bias, bias_selection_only ? 1 : 0, ids, gates);
 }
 
 }  // namespace moe

@@ -75,6 +75,22 @@ def test_route_ties(moe):
     assert (ids.cpu() == torch.tensor([3, 9], dtype=torch.int32)).all()
 
 
+@pytest.mark.parametrize("T,d,E,k", [(300, 512, 20, 3), (129, 1024, 128, 8), (40, 256, 256, 8)])
+def test_route_bias_selection_only(moe, T, d, E, k):
+    """The bias picks the experts; the gates come from the unbiased logits."""
+    w, x, p = _layer(T, d, E, k, 64, zipf=True, seed=T + 1)
+    bias = p["router_bias"]
+    ids, gates = moe.moe_route(x, p["w_router"], k, router_bias=bias, bias_selection_only=True)
+    torch.cuda.synchronize()
+    ids_ref, gates_ref, logits = oracle.route(W.to_bits(x), W.to_bits(p["w_router"]), k,
+                                              bias.cpu().numpy(), bias_for_selection_only=True)
+    compare_routing(ids.cpu().numpy(), gates.cpu().numpy(), ids_ref, gates_ref, logits, k)
+    # the same selection as the biased router, other gates
+    ids_b, gates_b = moe.moe_route(x, p["w_router"], k, router_bias=bias)
+    assert torch.equal(ids, ids_b)
+    assert not torch.equal(gates, gates_b)
+
+
 # ------------------------------------------------------------------ permute
 
 PERMUTE_CASES = [
@@ -188,6 +204,23 @@ def test_forward(moe, T, d, E, k, I, Is, zipf):
     assert np.array_equal(v["perm"].cpu().numpy(), ref["perm"])
     assert np.array_equal(v["slot_pos"].cpu().numpy(), ref["slot_pos"])
     assert_layer_close(f64(v["y"]), ref["y"], "y")
+    assert_layer_close(f64(out), ref["out"], "out")
+
+
+def test_forward_bias_selection_only(moe):
+    T, d, E, k, I = 250, 512, 16, 4, 256
+    w, x, p = _layer(T, d, E, k, I, zipf=True, seed=21)
+    ws = moe.new_workspace(T, d, E, I, k)
+    out = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], k, ws=ws,
+                          router_bias=p["router_bias"], bias_selection_only=True)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, T, d, E, I, k)
+    ref = oracle.forward(W.to_bits(x), W.to_bits(p["w_router"]), ExpertsOnHost(p["w_gate_up"]),
+                         ExpertsOnHost(p["w_down"]), k, router_bias=p["router_bias"].cpu().numpy(),
+                         bias_for_selection_only=True)
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ref["ids"], ref["gates"], ref["logits"], k)
+    assert differ.size == 0
     assert_layer_close(f64(out), ref["out"], "out")
 
 
