@@ -206,6 +206,27 @@ moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
                               void* ws, size_t ws_bytes, moe_stream_t stream,
                               const moe_forward_ext_t* ext);
 
+/* The whole layer as a CUDA graph, for calls repeated with the same shapes and
+ * buffers (decode steps).  moe_forward_graph captures one moe_forward_ex
+ * (host_buffers = 0: x, out in device memory) or one moe_forward_host
+ * (host_buffers = 1: x, out pinned host buffers, the copies captured too) into
+ * an executable graph; nothing runs at capture.  moe_graph_launch replays it
+ * on `stream`, reading x and writing out (and the workspace) as the captured
+ * call would: change the contents of x between replays, not the pointers.
+ * All buffers must outlive the graph.  Errors as the captured call, plus
+ * MOE_ERR_CUDA when capture or instantiation fails.  The pages fuse the whole
+ * decode step into one launch ('Hosting Qwen on Blackwell', "Expert
+ * parallelism"); a graph replays the layer's kernels with one host call. */
+typedef struct moe_graph_s* moe_graph_t;
+
+moe_status_t moe_forward_graph(const moe_bf16* x, const moe_bf16* w_router,
+                               const moe_bf16* w_gate_up, const moe_bf16* w_down, int T, int d,
+                               int E, int I, int top_k, moe_bf16* out, void* ws, size_t ws_bytes,
+                               const moe_forward_ext_t* ext, int host_buffers,
+                               moe_graph_t* graph);
+moe_status_t moe_graph_launch(moe_graph_t graph, moe_stream_t stream);
+moe_status_t moe_graph_destroy(moe_graph_t graph);
+
 /* Where moe_forward(_ex) keeps its intermediates: byte offsets into `ws`
  * (each 256-byte aligned) for the same shapes. */
 typedef struct {

@@ -40,6 +40,10 @@ _SIGS = {
     "moe_workspace_init": (_st, [_vp, _sz, _vp]),
     "moe_route": (_st, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "moe_route_ex": (_st, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "moe_forward_graph": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _i,
+                                ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_graph_launch": (_st, [_vp, _vp]),
+    "moe_graph_destroy": (_st, [_vp]),
     "moe_permute": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute_static_scratch": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _vp]),
@@ -301,6 +305,51 @@ def moe_forward_host(x_host, w_router, w_gate_up, w_down, top_k, out_host, ws,
                                  I2 // 2, top_k, _p(out_host), _p(ws), ws.numel(), _stream(stream),
                                  ctypes.byref(ext)), "moe_forward_host")
     return out_host
+
+
+class ForwardGraph:
+    """The whole layer captured once as a CUDA graph (moe_forward_graph) and
+    replayed with launch(): x and out are device tensors, or bf16 host tensors
+    (pinned) whose copies are captured too.  Change x's contents between
+    replays, not the tensor; every buffer is kept alive by this object."""
+
+    def __init__(self, x, w_router, w_gate_up, w_down, top_k, out, ws, router_bias=None,
+                 w_gate_up_shared=None, w_down_shared=None, bias_selection_only=False):
+        host = not x.is_cuda
+        if x.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or out.is_cuda == host:
+            raise ValueError("x and out must be bf16 tensors on the same side (device or host)")
+        for t, n in ((w_router, "w_router"), (w_gate_up, "w_gate_up"), (w_down, "w_down"),
+                     (w_gate_up_shared, "w_gate_up_shared"), (w_down_shared, "w_down_shared")):
+            _want(t, torch.bfloat16, n)
+        _want(router_bias, torch.float32, "router_bias")
+        T, d = x.shape
+        E, I2, _ = w_gate_up.shape
+        I_s = w_down_shared.shape[1] if w_down_shared is not None else 0
+        self._ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
+                               w_gate_up_shared.data_ptr() if I_s else None,
+                               w_down_shared.data_ptr() if I_s else None, I_s,
+                               1 if bias_selection_only else 0)
+        self._keep = (x, w_router, w_gate_up, w_down, out, ws, router_bias, w_gate_up_shared,
+                      w_down_shared)
+        self._h = ctypes.c_void_p()
+        _check(_lib.moe_forward_graph(x.data_ptr(), _p(w_router), _p(w_gate_up), _p(w_down), T, d,
+                                      E, I2 // 2, top_k, out.data_ptr(), _p(ws), ws.numel(),
+                                      ctypes.byref(self._ext), 1 if host else 0,
+                                      ctypes.byref(self._h)), "moe_forward_graph")
+
+    def launch(self, stream=None):
+        _check(_lib.moe_graph_launch(self._h, _stream(stream)), "moe_graph_launch")
+
+    def close(self):
+        if self._h:
+            _lib.moe_graph_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0) -> dict:

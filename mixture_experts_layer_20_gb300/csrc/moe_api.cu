@@ -20,6 +20,10 @@ constexpr size_t kAlign = 256;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 std::atomic<unsigned long long> g_launches{0};
+// Launches made by this thread, and whether it is capturing a graph (then no
+// tracing events are recorded: they would become graph nodes).
+thread_local unsigned long long t_launches = 0;
+thread_local bool t_capturing = false;
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 thread_local std::string g_last_error;
 
@@ -118,6 +122,8 @@ unsigned* status_word(void* ws) { return static_cast<unsigned*>(ws); }
 
 KernelScope::KernelScope(cudaStream_t stream, const char* name) : stream_(stream), slot_(-1) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  ++t_launches;
+  if (t_capturing) return;
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (!g_prof_on || g_records.size() >= kMaxRecords) return;
   if (!g_prof_only.empty() && g_prof_only != name) return;
@@ -183,6 +189,11 @@ moe_status_t route_impl(const moe_bf16* x, const moe_bf16* w_router, const float
 }  // namespace moe
 
 using namespace moe;
+
+struct moe_graph_s {
+  cudaGraphExec_t exec;
+  unsigned long long kernels;  // kernels per replay
+};
 
 extern "C" {
 
@@ -399,6 +410,66 @@ moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
   if (st != MOE_OK) return st;
   e = cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaMemcpyAsync out");
+}
+
+moe_status_t moe_forward_graph(const moe_bf16* x, const moe_bf16* w_router,
+                               const moe_bf16* w_gate_up, const moe_bf16* w_down, int T, int d,
+                               int E, int I, int top_k, moe_bf16* out, void* ws, size_t ws_bytes,
+                               const moe_forward_ext_t* ext, int host_buffers,
+                               moe_graph_t* graph) {
+  if (!graph) return fail(MOE_ERR_INVALID_ARG, "moe_forward_graph: null graph pointer");
+  *graph = nullptr;
+  moe_status_t st = check_shapes(T, d, E, I, top_k);
+  if (st != MOE_OK) return st;
+  if (T == 0) return fail(MOE_ERR_INVALID_ARG, "moe_forward_graph: T must be positive");
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+  const unsigned long long k0 = t_launches;
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return cuda_fail(e, "cudaStreamBeginCapture");
+  }
+  t_capturing = true;
+  const moe_stream_t ms = reinterpret_cast<moe_stream_t>(cs);
+  st = host_buffers ? moe_forward_host(x, w_router, w_gate_up, w_down, T, d, E, I, top_k, out, ws,
+                                       ws_bytes, ms, ext)
+                    : moe_forward_ex(x, w_router, w_gate_up, w_down, T, d, E, I, top_k, out, ws,
+                                     ws_bytes, ms, ext);
+  t_capturing = false;
+  const unsigned long long kernels = t_launches - k0;
+  g_launches.fetch_sub(kernels, std::memory_order_relaxed);  // captured, not run
+  cudaGraph_t g = nullptr;
+  const cudaError_t ee = cudaStreamEndCapture(cs, &g);
+  cudaStreamDestroy(cs);
+  if (st != MOE_OK) {
+    if (g) cudaGraphDestroy(g);
+    return st;
+  }
+  if (ee != cudaSuccess) return cuda_fail(ee, "cudaStreamEndCapture");
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
+  *graph = new moe_graph_s{exec, kernels};
+  return MOE_OK;
+}
+
+moe_status_t moe_graph_launch(moe_graph_t graph, moe_stream_t stream) {
+  if (!graph) return fail(MOE_ERR_INVALID_ARG, "moe_graph_launch: null graph");
+  const cudaError_t e = cudaGraphLaunch(graph->exec, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
+  g_launches.fetch_add(graph->kernels, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status_t moe_graph_destroy(moe_graph_t graph) {
+  if (!graph) return MOE_OK;
+  const cudaError_t e = cudaGraphExecDestroy(graph->exec);
+  delete graph;
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaGraphExecDestroy");
 }
 
 moe_status_t moe_get_device_status(void* ws, size_t ws_bytes, moe_stream_t stream) {
