@@ -31,6 +31,15 @@ What the layer computes, and where each step comes from:
   Dispatch - Combine": weighted accumulation in combine).  An always-on shared
   expert adds its output with weight one ('PagedAttention, speculative
   decoding, MoE and Blackwell', section 2, shared experts).
+* MXFP8 expert weights ('Hosting Qwen on Blackwell', "Quantization": the
+  weights are converted to MXFP8 statically after training).  MXFP8 is the
+  OCP microscaling format with FP8 E4M3 elements: each run of 32 consecutive
+  values along the reduction dimension shares one power-of-two scale (an E8M0
+  exponent) chosen from the run's largest magnitude so that it maps into
+  E4M3's top binade; the elements are rounded to nearest, ties to even, and
+  clamped to E4M3's largest finite value.  A layer with MXFP8 weights is the
+  layer computed with the dequantised weights (codes times scales), which the
+  oracle obtains with mxfp8_quantize / mxfp8_dequantize.
 * Router bias.  A per-expert bias is added to the logits; by default it takes
   part in both the selection and the gates.  The variant the same section
   names for balancing (DeepSeek's bias adjustment) uses the bias only to pick
@@ -65,6 +74,10 @@ __all__ = [
     "combine",
     "forward",
     "forward_tokens",
+    "e4m3_values",
+    "round_to_e4m3",
+    "mxfp8_quantize",
+    "mxfp8_dequantize",
 ]
 
 
@@ -159,6 +172,78 @@ def route(x_bits, w_router_bits, top_k: int, router_bias=None,
         ids[t] = chosen
         gates[t] = kept / kept.sum()
     return ids, gates, logits
+
+
+# --------------------------------------------------------------------------
+# MXFP8: FP8 E4M3 elements with one E8M0 (power-of-two) scale per 32 values
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0        # 1.75 * 2^8, the largest finite E4M3 value
+E4M3_EMAX = 8           # exponent of E4M3's top binade
+MX_BLOCK = 32           # values that share one scale
+
+
+def e4m3_values() -> np.ndarray:
+    """fp64 value of each of the 256 E4M3 codes (bit 7 sign, bits 6-3 the
+    exponent with bias 7, bits 2-0 the mantissa; exponent 0 is subnormal,
+    codes 0x7f / 0xff are NaN, there are no infinities)."""
+    vals = np.empty(256, dtype=np.float64)
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e = (c >> 3) & 0xF
+        m = c & 0x7
+        if e == 0xF and m == 0x7:
+            vals[c] = np.nan
+        elif e == 0:
+            vals[c] = sign * m * 2.0 ** -9           # (m / 8) * 2^(1 - 7)
+        else:
+            vals[c] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+def round_to_e4m3(v) -> np.ndarray:
+    """Round fp64 values to the E4M3 grid: nearest, ties to even, magnitudes
+    above 448 clamped to 448.  Returns the rounded fp64 values."""
+    v = np.clip(np.asarray(v, dtype=np.float64), -E4M3_MAX, E4M3_MAX)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    quantum = np.where(a >= 2.0 ** -6, 2.0 ** (np.maximum(e, -6) - 3), 2.0 ** -9)
+    return np.minimum(np.rint(a / quantum) * quantum, E4M3_MAX) * np.sign(v)
+
+
+def mxfp8_quantize(w):
+    """Quantise along the last axis (a multiple of 32) to MXFP8.
+
+    Per block of 32: X = floor(log2(max |v|)) - 8, stored as the E8M0 byte
+    X + 127 (clamped to 0..254; an all-zero block stores 0); elements are
+    round_to_e4m3(v / 2^X) encoded as E4M3 codes.  Returns (codes uint8 with
+    w's shape, scales uint8 with the last axis divided by 32)."""
+    w = np.asarray(w, dtype=np.float64)
+    K = w.shape[-1]
+    if K % MX_BLOCK:
+        raise ValueError("the quantised axis must be a multiple of 32")
+    blocks = w.reshape(*w.shape[:-1], K // MX_BLOCK, MX_BLOCK)
+    amax = np.abs(blocks).max(axis=-1)
+    with np.errstate(divide="ignore"):
+        xexp = np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - E4M3_EMAX
+    scale_byte = np.where(amax > 0, np.clip(xexp + 127, 0, 254), 0).astype(np.uint8)
+    xexp = scale_byte.astype(np.float64) - 127
+    q = round_to_e4m3(blocks / 2.0 ** xexp[..., None])
+    # encode: codes 0x00..0x7e hold the non-negative values in increasing order
+    positive = e4m3_values()[:0x7F]
+    mag = np.searchsorted(positive, np.abs(q))
+    codes = np.where(q < 0, mag | 0x80, mag).astype(np.uint8)
+    return codes.reshape(w.shape), scale_byte
+
+
+def mxfp8_dequantize(codes, scales) -> np.ndarray:
+    """codes times 2^(scale byte - 127), in fp64."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    K = codes.shape[-1]
+    vals = e4m3_values()[codes].reshape(*codes.shape[:-1], K // MX_BLOCK, MX_BLOCK)
+    x = 2.0 ** (np.asarray(scales, dtype=np.float64) - 127)
+    return (vals * x[..., None]).reshape(codes.shape)
 
 
 # --------------------------------------------------------------------------

@@ -19,6 +19,9 @@ What pins what:
   whole layer .................. brute-force dense form: every expert on every token,
                                  masked by the routing (no grouping, no permutation)
   shared expert, linearity ..... identical experts, exact power-of-two scaling
+  MXFP8 ........................ E4M3 decode and rounding against torch.float8_e4m3fn; block
+                                 scales from numpy frexp; codes against torch's conversion of the
+                                 scaled, clamped block; exact round trip of representable values
 """
 
 from __future__ import annotations
@@ -190,6 +193,42 @@ def check_selection_only_bias(o):
     assert (ids_sel == ids_b).all()
 
 
+def check_mxfp8(o):
+    # decode of every code = torch's float8_e4m3fn decode
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    ref = ref.to(torch.float64).numpy()
+    mine = o.e4m3_values()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[~np.isnan(ref)], ref[~np.isnan(ref)])
+    # rounding = torch's conversion (nearest, ties to even) on [-448, 448], incl. subnormals and ties
+    r = _rng(15)
+    v = np.concatenate([r.uniform(-448, 448, 4000), r.uniform(-2**-5, 2**-5, 4000),
+                        np.arange(-64, 65) * 2.0 ** -10, np.arange(-14, 14) * 2.0 ** 5 + 2.0 ** 4])
+    v = v.astype(np.float32).astype(np.float64)
+    torch_r = torch.from_numpy(v).to(torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(o.round_to_e4m3(v), torch_r)
+    # quantisation of blocks with a spread of magnitudes
+    w = (r.standard_normal((6, 128)) * np.exp(r.uniform(-8, 4, (6, 1)))).astype(np.float32)
+    w[2, 32:64] = 0.0                                   # an all-zero block
+    w[3, :32] = 3.5 * 2.0 ** r.integers(-6, 5, 32)       # on the block's grid: exactly representable
+    codes, scales = o.mxfp8_quantize(w.astype(np.float64))
+    blocks = w.astype(np.float64).reshape(6, 4, 32)
+    amax = np.abs(blocks).max(axis=-1)
+    mant, expo = np.frexp(amax)                          # amax = mant * 2^expo, mant in [0.5, 1)
+    xexp = np.where(amax > 0, expo - 1 - 8, -127)
+    assert np.array_equal(scales.astype(np.int64), np.where(amax > 0, xexp + 127, 0))
+    scaled = np.clip(blocks / 2.0 ** xexp[..., None], -448, 448).astype(np.float32)
+    ref_codes = torch.from_numpy(scaled).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref_codes = np.where(ref_codes == 0x80, 0, ref_codes)   # -0 encodes as +0
+    assert np.array_equal(codes.reshape(6, 4, 32), ref_codes)
+    back = o.mxfp8_dequantize(codes, scales)
+    assert np.array_equal(back[3, :32], w[3, :32].astype(np.float64))   # exact round trip
+    assert (back[2, 32:64] == 0).all()
+    nz = amax > 0
+    top = np.abs(o.e4m3_values()[codes.reshape(6, 4, 32)]).max(axis=-1)
+    assert ((top[nz] >= 256) & (top[nz] <= 448)).all()   # the largest maps into the top binade
+
+
 # ---------------------------------------------------------------- grouping
 
 def check_permute(o):
@@ -313,7 +352,8 @@ def check_forward_tokens(o):
 
 ALL_CHECKS = [
     check_bf16_decode, check_bf16_round, check_logits_one_hot,
-    check_topk_brute_force, check_tie_break, check_gates, check_selection_only_bias, check_permute,
+    check_topk_brute_force, check_tie_break, check_gates, check_selection_only_bias, check_mxfp8,
+    check_permute,
     check_swiglu_hand_example, check_single_expert_is_dense_ffn,
     check_identical_experts, check_brute_force_layer, check_down_scaling,
     check_forward_tokens,

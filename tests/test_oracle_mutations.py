@@ -208,13 +208,35 @@ def _m_selection_only_unbiased_pick(o):
     o.route = route
 
 
+def _m_mx_scale_off_by_one(o):
+    o.E4M3_EMAX = 7
+
+
+def _m_mx_truncates(o):
+    orig = o.round_to_e4m3
+
+    def round_to_e4m3(v):
+        v = np.clip(np.asarray(v, dtype=np.float64), -448.0, 448.0)
+        a = np.abs(v)
+        with np.errstate(divide="ignore"):
+            e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+        q = np.where(a >= 2.0 ** -6, 2.0 ** (np.maximum(e, -6) - 3), 2.0 ** -9)
+        return np.floor(a / q) * q * np.sign(v)
+    assert orig
+    o.round_to_e4m3 = round_to_e4m3
+
+
+def _m_mx_no_clamp(o):
+    o.E4M3_MAX = 512.0
+
+
 MUTATIONS = [
     _m_silu_sign, _m_gate_up_swapped, _m_no_h_rounding, _m_down_transposed,
     _m_tie_high_index, _m_slots_by_logit, _m_no_renormalise, _m_bias_dropped,
     _m_bf16_round_truncates, _m_bf16_decode_shift, _m_unstable_permute,
     _m_gather_wrong_index, _m_combine_ignores_gates, _m_combine_drops_shared,
     _m_expert_shift, _m_forward_tokens_no_gate, _m_selection_only_ignored,
-    _m_selection_only_unbiased_pick,
+    _m_selection_only_unbiased_pick, _m_mx_scale_off_by_one, _m_mx_truncates, _m_mx_no_clamp,
 ]
 
 
