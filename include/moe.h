@@ -206,6 +206,19 @@ moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
                               void* ws, size_t ws_bytes, moe_stream_t stream,
                               const moe_forward_ext_t* ext);
 
+/* MXFP8 expert weights ('Hosting Qwen on Blackwell', "Quantization": the
+ * weights are converted statically after training).  Quantises w [rows, K]
+ * bf16 (K a multiple of 128) to E4M3 codes [rows, K] uint8 and E8M0 scales
+ * [K/128][rows][4] uint8 following the OCP microscaling definition: one scale
+ * per 32 values along K, X = floor(log2(max |v|)) - 8 stored as X + 127
+ * (clamped to 0..254; an all-zero run stores 0), elements v / 2^X rounded to
+ * nearest even and clamped to +-448.  The scale layout keeps the four scales
+ * of a 128-wide K block of a row in one 32-bit word, which is what
+ * moe_forward_mxfp8 reads.  Device pointers, 16-byte aligned; asynchronous on
+ * `stream`.  MOE_ERR_INVALID_ARG for bad pointers or shapes. */
+moe_status_t moe_mxfp8_quantize(const moe_bf16* w, long long rows, int K, uint8_t* codes,
+                                uint8_t* scales, moe_stream_t stream);
+
 /* The whole layer as a CUDA graph, for calls repeated with the same shapes and
  * buffers (decode steps).  moe_forward_graph captures one moe_forward_ex
  * (host_buffers = 0: x, out in device memory) or one moe_forward_host

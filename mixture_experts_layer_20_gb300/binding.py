@@ -43,6 +43,7 @@ _SIGS = {
     "moe_forward_graph": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp, _i,
                                 ctypes.POINTER(ctypes.c_void_p)]),
     "moe_graph_launch": (_st, [_vp, _vp]),
+    "moe_mxfp8_quantize": (_st, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
     "moe_graph_destroy": (_st, [_vp]),
     "moe_permute": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute_static_scratch": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -305,6 +306,19 @@ def moe_forward_host(x_host, w_router, w_gate_up, w_down, top_k, out_host, ws,
                                  I2 // 2, top_k, _p(out_host), _p(ws), ws.numel(), _stream(stream),
                                  ctypes.byref(ext)), "moe_forward_host")
     return out_host
+
+
+def moe_mxfp8_quantize(w, stream=None):
+    """bf16 [..., K] weights -> (codes uint8 [..., K], scales uint8 [K/128, rows, 4]) on the
+    device, rows = the product of the leading dimensions."""
+    _want(w, torch.bfloat16, "w")
+    K = w.shape[-1]
+    rows = w.numel() // K
+    codes = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    scales = torch.empty((K // 128, rows, 4), dtype=torch.uint8, device=w.device)
+    _check(_lib.moe_mxfp8_quantize(_p(w), rows, K, _p(codes), _p(scales), _stream(stream)),
+           "moe_mxfp8_quantize")
+    return codes, scales
 
 
 class ForwardGraph:

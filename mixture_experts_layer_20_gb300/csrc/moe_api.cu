@@ -412,6 +412,19 @@ moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaMemcpyAsync out");
 }
 
+moe_status_t moe_mxfp8_quantize(const moe_bf16* w, long long rows, int K, uint8_t* codes,
+                                uint8_t* scales, moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || K % 128) return fail(MOE_ERR_INVALID_ARG, "moe_mxfp8_quantize: K must be a positive multiple of 128");
+  if (rows == 0) return MOE_OK;
+  if (!w || !codes || !scales || !aligned16(w) || !aligned16(codes) || !aligned16(scales))
+    return fail(MOE_ERR_INVALID_ARG, "moe_mxfp8_quantize: null or unaligned pointer");
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  const cudaError_t e =
+      launch_mxfp8_quantize(reinterpret_cast<cudaStream_t>(stream), w, rows, K, codes, scales);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "mxfp8 quantize launch");
+}
+
 moe_status_t moe_forward_graph(const moe_bf16* x, const moe_bf16* w_router,
                                const moe_bf16* w_gate_up, const moe_bf16* w_down, int T, int d,
                                int E, int I, int top_k, moe_bf16* out, void* ws, size_t ws_bytes,

@@ -130,4 +130,11 @@ cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_p
                            const float* gates, const float* y_shared, int T, int d, int top_k,
                            void* out, unsigned* status);
 
+// ---- MXFP8 weights (moe_mxfp8.cu)
+
+// bf16 [rows, K] (K a multiple of 128) -> E4M3 codes [rows, K] and E8M0
+// scales [K / 128][rows][4].
+cudaError_t launch_mxfp8_quantize(cudaStream_t s, const void* w, long long rows, int K,
+                                  uint8_t* codes, uint8_t* scales);
+
 }  // namespace moe
