@@ -219,6 +219,22 @@ moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
 moe_status_t moe_mxfp8_quantize(const moe_bf16* w, long long rows, int K, uint8_t* codes,
                                 uint8_t* scales, moe_stream_t stream);
 
+/* The whole layer with MXFP8 expert weights (quantised by moe_mxfp8_quantize):
+ * codes_gate_up [E, 2I, d] and scales_gate_up [d/128][E*2I][4], codes_down
+ * [E, d, I] and scales_down [I/128][E*d][4].  Activations, router, shared
+ * expert (ext) and outputs are as in moe_forward_ex; the experts compute
+ * with the dequantised weights (codes x 2^(scale - 127), exact in bf16) on
+ * the bf16 tensor cores, half the weight bytes read from HBM.  d and I must
+ * be multiples of 128 (else MOE_ERR_UNSUPPORTED); token chunks are capped at
+ * 192 rows (tensor memory holds the dequantised weights too).  Same workspace
+ * as moe_forward. */
+moe_status_t moe_forward_mxfp8(const moe_bf16* x, const moe_bf16* w_router,
+                               const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
+                               const uint8_t* codes_down, const uint8_t* scales_down, int T,
+                               int d, int E, int I, int top_k, moe_bf16* out, void* ws,
+                               size_t ws_bytes, moe_stream_t stream,
+                               const moe_forward_ext_t* ext);
+
 /* The whole layer as a CUDA graph, for calls repeated with the same shapes and
  * buffers (decode steps).  moe_forward_graph captures one moe_forward_ex
  * (host_buffers = 0: x, out in device memory) or one moe_forward_host

@@ -44,6 +44,8 @@ _SIGS = {
                                 ctypes.POINTER(ctypes.c_void_p)]),
     "moe_graph_launch": (_st, [_vp, _vp]),
     "moe_mxfp8_quantize": (_st, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
+    "moe_forward_mxfp8": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
+                                _vp, _vp]),
     "moe_graph_destroy": (_st, [_vp]),
     "moe_permute": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute_static_scratch": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -319,6 +321,39 @@ def moe_mxfp8_quantize(w, stream=None):
     _check(_lib.moe_mxfp8_quantize(_p(w), rows, K, _p(codes), _p(scales), _stream(stream)),
            "moe_mxfp8_quantize")
     return codes, scales
+
+
+def moe_forward_mxfp8(x, w_router, mx_gate_up, mx_down, top_k, out=None, ws=None,
+                      router_bias=None, w_gate_up_shared=None, w_down_shared=None, stream=None,
+                      bias_selection_only=False):
+    """The whole layer with MXFP8 expert weights: mx_gate_up / mx_down are the
+    (codes, scales) pairs of moe_mxfp8_quantize for W_gate_up [E,2I,d] and
+    W_down [E,d,I].  Returns out [T, d] bf16."""
+    for t, n in ((x, "x"), (w_router, "w_router"), (w_gate_up_shared, "w_gate_up_shared"),
+                 (w_down_shared, "w_down_shared")):
+        _want(t, torch.bfloat16, n)
+    _want(router_bias, torch.float32, "router_bias")
+    cgu, sgu = mx_gate_up
+    cd, sd = mx_down
+    for t, n in ((cgu, "codes_gate_up"), (sgu, "scales_gate_up"), (cd, "codes_down"),
+                 (sd, "scales_down")):
+        _want(t, torch.uint8, n)
+    T, d = x.shape
+    E, I2, _ = cgu.shape
+    I = I2 // 2
+    I_s = w_down_shared.shape[1] if w_down_shared is not None else 0
+    if out is None:
+        out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device)
+    ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
+                     w_gate_up_shared.data_ptr() if I_s else None,
+                     w_down_shared.data_ptr() if I_s else None, I_s,
+                     1 if bias_selection_only else 0)
+    _check(_lib.moe_forward_mxfp8(_p(x), _p(w_router), _p(cgu), _p(sgu), _p(cd), _p(sd), T, d, E,
+                                  I, top_k, _p(out), _p(ws), ws.numel(), _stream(stream),
+                                  ctypes.byref(ext)), "moe_forward_mxfp8")
+    return out
 
 
 class ForwardGraph:

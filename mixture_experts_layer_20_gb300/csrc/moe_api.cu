@@ -320,12 +320,21 @@ moe_status_t moe_combine(const float* y, const int32_t* slot_pos, const float* t
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
 }
 
-moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
-                            const moe_bf16* w_gate_up, const moe_bf16* w_down, int T, int d,
-                            int E, int I, int top_k, moe_bf16* out, void* ws, size_t ws_bytes,
-                            moe_stream_t stream, const moe_forward_ext_t* ext) {
+namespace {
+
+// MXFP8 expert weights (codes and scales); null for bf16 weights.
+struct MxWeights {
+  const uint8_t *codes_gate_up, *scales_gate_up, *codes_down, *scales_down;
+};
+
+moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
+                          const moe_bf16* w_gate_up, const moe_bf16* w_down, const MxWeights* mx,
+                          int T, int d, int E, int I, int top_k, moe_bf16* out, void* ws,
+                          size_t ws_bytes, moe_stream_t stream, const moe_forward_ext_t* ext) {
   moe_status_t st = check_shapes(T, d, E, I, top_k);
   if (st != MOE_OK) return st;
+  if (mx && (d % 128 || I % 128))
+    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 weights need d and I multiples of 128");
   const float* bias = ext ? ext->router_bias : nullptr;
   const int bias_sel = ext ? ext->bias_selection_only : 0;
   const int I_shared = ext ? ext->I_shared : 0;
@@ -366,7 +375,11 @@ moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
   cudaError_t e = launch_permute(s, ids, x, T, d, E, top_k, counts, offsets, perm, slot_pos,
                                  x_perm, table, status);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
-  e = launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status, tmo);
+  e = mx ? launch_grouped_ffn_mxfp8(s, x_perm, offsets, rows, d, E, I, mx->codes_gate_up,
+                                    mx->scales_gate_up, mx->codes_down, mx->scales_down, h, y,
+                                    status, tmo)
+         : launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status,
+                              tmo);
   if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
   float* y_shared = nullptr;
   if (I_shared) {
@@ -377,6 +390,33 @@ moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
   }
   e = launch_combine(s, y, slot_pos, gates, y_shared, T, d, top_k, out, status);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
+}
+
+}  // namespace
+
+moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
+                            const moe_bf16* w_gate_up, const moe_bf16* w_down, int T, int d,
+                            int E, int I, int top_k, moe_bf16* out, void* ws, size_t ws_bytes,
+                            moe_stream_t stream, const moe_forward_ext_t* ext) {
+  return forward_impl(x, w_router, w_gate_up, w_down, nullptr, T, d, E, I, top_k, out, ws,
+                      ws_bytes, stream, ext);
+}
+
+moe_status_t moe_forward_mxfp8(const moe_bf16* x, const moe_bf16* w_router,
+                               const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
+                               const uint8_t* codes_down, const uint8_t* scales_down, int T,
+                               int d, int E, int I, int top_k, moe_bf16* out, void* ws,
+                               size_t ws_bytes, moe_stream_t stream,
+                               const moe_forward_ext_t* ext) {
+  if (T > 0 && (!codes_gate_up || !scales_gate_up || !codes_down || !scales_down ||
+                !aligned16(codes_gate_up) || !aligned16(scales_gate_up) ||
+                !aligned16(codes_down) || !aligned16(scales_down)))
+    return fail(MOE_ERR_INVALID_ARG, "moe_forward_mxfp8: null or unaligned weight pointer");
+  const MxWeights mx{codes_gate_up, scales_gate_up, codes_down, scales_down};
+  // the bf16 weight pointers are not read on this path; pass the codes to pass the null checks
+  return forward_impl(x, w_router, reinterpret_cast<const moe_bf16*>(codes_gate_up),
+                      reinterpret_cast<const moe_bf16*>(codes_down), &mx, T, d, E, I, top_k, out,
+                      ws, ws_bytes, stream, ext);
 }
 
 moe_status_t moe_forward(const moe_bf16* x, const moe_bf16* w_router, const moe_bf16* w_gate_up,

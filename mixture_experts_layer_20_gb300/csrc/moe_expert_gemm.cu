@@ -48,6 +48,9 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -80,6 +83,8 @@ struct Params {
   int up_offset;          // gate_up: I
   void* out;              // gate_up: h bf16 [rows, I]; down: y fp32 [rows, d]
   long long ld_out;
+  const uint8_t* scales;  // MXFP8 weights: E8M0 scales [K / 128][scale_rows][4]
+  long long scale_rows;   // MXFP8 weights: weight rows of the whole tensor
   int smem_bytes;         // dynamic shared memory of the launch
   unsigned* status;
   unsigned long long timeout_ns;
@@ -119,6 +124,121 @@ constexpr int kTokenMaps = kTokMax / kUnit;
 struct TokenMapSet {
   CUtensorMap m[kTokenMaps];
 };
+
+// Schedule (all threads of the CTA): token chunks per expert (at most TOKCAP
+// tokens each) and their exclusive prefix in s_ct, and the largest chunk half
+// of the launch in *s_half_max.  Inconsistent offsets give an empty schedule
+// and MOE_ERR_DEVICE_CHECK.
+template <int TOKCAP>
+__device__ __forceinline__ void build_schedule(const Params& p, int* s_off, int* s_ct,
+                                               int* s_half_max, int warp, int lane) {
+  const int G = p.groups;
+  for (int i = threadIdx.x; i <= G; i += blockDim.x)
+    s_off[i] = p.offsets ? __ldg(p.offsets + i) : (i == 0 ? 0 : p.total_rows);
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (G + 31) / 32;
+    int local = 0;
+    int half_max = kUnit / 2;
+    bool bad = false;
+    for (int j = 0; j < per; ++j) {
+      const int g = lane * per + j;
+      if (g < G) {
+        const int m = s_off[g + 1] - s_off[g];
+        bad |= m < 0;
+        if (m > 0) {
+          const int ch = (m + TOKCAP - 1) / TOKCAP;
+          local += ch;
+          half_max = max(half_max, (((m + kUnit - 1) / kUnit + ch - 1) / ch) * (kUnit / 2));
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) half_max = max(half_max, __shfl_xor_sync(0xffffffffu, half_max, o));
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per; ++j) {
+      const int g = lane * per + j;
+      if (g < G) {
+        s_ct[g] = run;
+        const int m = s_off[g + 1] - s_off[g];
+        run += m > 0 ? (m + TOKCAP - 1) / TOKCAP : 0;
+      }
+    }
+    bad |= (s_off[0] != 0) || (s_off[G] != p.total_rows);
+    bad = __any_sync(0xffffffffu, bad);
+    __syncwarp();
+    if (lane == 31) s_ct[G] = bad ? 0 : incl;
+    if (lane == 0) *s_half_max = bad ? TOKCAP / 2 : min(half_max, TOKCAP / 2);
+    if (bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusDeviceCheck);
+  }
+}
+
+// Epilogue of one tile (one of warps 2-5, q = warp % 4, reading TMEM lanes
+// 32 q .. 32 q + 31 from t_row): gate_up stores h = silu(gate) * up in bf16,
+// down stores y in fp32; `live` false (a wait gave up) stores nothing.
+template <int KIND, int SLAB = (KIND == kGateUp ? 128 : 256)>
+__device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, bool live,
+                                              const Params& p, int q, int lane, uint32_t rank) {
+  // SLAB: output columns of one tile (h columns for gate_up, y columns for down)
+  if constexpr (KIND == kDown) {
+    const int col = t.slab * SLAB + rank * 128 + q * 32 + lane;
+    const bool col_ok = live && col < p.n_out;
+#pragma unroll 1
+    for (int c = 0; c < t.n; c += 16) {
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(t_row + c, v);
+      tmem_ld_wait();
+      const int nvalid = min(16, t.tok_end - t.tok0 - c);  // uniform across the warp
+      float* yp = static_cast<float*>(p.out) + (size_t)(t.tok0 + c) * p.ld_out + col;
+      if (col_ok) {
+        if (nvalid == 16) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) yp[(size_t)j * p.ld_out] = __uint_as_float(v[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < nvalid) yp[(size_t)j * p.ld_out] = __uint_as_float(v[j]);
+        }
+      }
+    }
+  } else {
+    // In each warp's quarter of the TMEM lanes, lanes 0-15 hold 16 gate
+    // rows and lanes 16-31 the matching up rows (the weight map
+    // interleaves them in groups of 16), so one shuffle pairs them: lane
+    // l < 16 computes tokens c..c+7 and lane l + 16 tokens c+8..c+15 of
+    // h column l, and all four warps share the SwiGLU and the stores.
+    const bool lo = lane < 16;
+    const int col = t.slab * SLAB + rank * 64 + q * 16 + (lane & 15);
+    const bool col_ok = live && col < p.n_out;
+    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + col;
+#pragma unroll 1
+    for (int c = 0; c < t.n; c += 16) {
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(t_row + c, v);
+      tmem_ld_wait();
+      const int row0 = t.tok0 + c + (lo ? 0 : 8);
+      const int nvalid = min(8, t.tok_end - row0);  // <= 0: rows past the expert's end
+      __nv_bfloat16* hp = h + (size_t)row0 * p.ld_out;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float mine = __uint_as_float(lo ? v[i] : v[8 + i]);
+        const float other =
+            __shfl_xor_sync(0xffffffffu, __uint_as_float(lo ? v[8 + i] : v[i]), 16);
+        const float g = lo ? mine : other;
+        const float u = lo ? other : mine;
+        if (col_ok && i < nvalid)
+          hp[(size_t)i * p.ld_out] =
+              __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
+      }
+    }
+  }
+}
 
 template <int KIND>
 __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, const TokenMapSet& tx,
@@ -168,52 +288,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 
   pdl_wait_and_release();
 
-  // Schedule: token chunks per expert and their exclusive prefix.
   const int G = p.groups;
-  for (int i = threadIdx.x; i <= G; i += blockDim.x)
-    s_off[i] = p.offsets ? __ldg(p.offsets + i) : (i == 0 ? 0 : p.total_rows);
-  __syncthreads();
-  if (warp == 0) {
-    const int per = (G + 31) / 32;
-    int local = 0;
-    int half_max = kUnit / 2;
-    bool bad = false;
-    for (int j = 0; j < per; ++j) {
-      const int g = lane * per + j;
-      if (g < G) {
-        const int m = s_off[g + 1] - s_off[g];
-        bad |= m < 0;
-        if (m > 0) {
-          const int ch = (m + kTokMax - 1) / kTokMax;
-          local += ch;
-          half_max = max(half_max, (((m + kUnit - 1) / kUnit + ch - 1) / ch) * (kUnit / 2));
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) half_max = max(half_max, __shfl_xor_sync(0xffffffffu, half_max, o));
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - local;
-    for (int j = 0; j < per; ++j) {
-      const int g = lane * per + j;
-      if (g < G) {
-        s_ct[g] = run;
-        const int m = s_off[g + 1] - s_off[g];
-        run += m > 0 ? (m + kTokMax - 1) / kTokMax : 0;
-      }
-    }
-    bad |= (s_off[0] != 0) || (s_off[G] != p.total_rows);
-    bad = __any_sync(0xffffffffu, bad);
-    __syncwarp();
-    if (lane == 31) s_ct[G] = bad ? 0 : incl;
-    if (lane == 0) s_half_max = bad ? kTokMax / 2 : min(half_max, kTokMax / 2);
-    if (bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusDeviceCheck);
-  }
+  build_schedule<kTokMax>(p, s_off, s_ct, &s_half_max, warp, lane);
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised before any remote arrive
@@ -333,58 +409,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
-      if constexpr (KIND == kDown) {
-        const int col = t.slab * 256 + rank * 128 + q * 32 + lane;
-        const bool col_ok = live && col < p.n_out;
-#pragma unroll 1
-        for (int c = 0; c < t.n; c += 16) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(t_row + c, v);
-          tmem_ld_wait();
-          const int nvalid = min(16, t.tok_end - t.tok0 - c);  // uniform across the warp
-          float* yp = static_cast<float*>(p.out) + (size_t)(t.tok0 + c) * p.ld_out + col;
-          if (col_ok) {
-            if (nvalid == 16) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) yp[(size_t)j * p.ld_out] = __uint_as_float(v[j]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j < nvalid) yp[(size_t)j * p.ld_out] = __uint_as_float(v[j]);
-            }
-          }
-        }
-      } else {
-        // In each warp's quarter of the TMEM lanes, lanes 0-15 hold 16 gate
-        // rows and lanes 16-31 the matching up rows (the weight map
-        // interleaves them in groups of 16), so one shuffle pairs them: lane
-        // l < 16 computes tokens c..c+7 and lane l + 16 tokens c+8..c+15 of
-        // h column l, and all four warps share the SwiGLU and the stores.
-        const bool lo = lane < 16;
-        const int col = t.slab * 128 + rank * 64 + q * 16 + (lane & 15);
-        const bool col_ok = live && col < p.n_out;
-        __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + col;
-#pragma unroll 1
-        for (int c = 0; c < t.n; c += 16) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(t_row + c, v);
-          tmem_ld_wait();
-          const int row0 = t.tok0 + c + (lo ? 0 : 8);
-          const int nvalid = min(8, t.tok_end - row0);  // <= 0: rows past the expert's end
-          __nv_bfloat16* hp = h + (size_t)row0 * p.ld_out;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float mine = __uint_as_float(lo ? v[i] : v[8 + i]);
-            const float other =
-                __shfl_xor_sync(0xffffffffu, __uint_as_float(lo ? v[8 + i] : v[i]), 16);
-            const float g = lo ? mine : other;
-            const float u = lo ? other : mine;
-            if (col_ok && i < nvalid)
-              hp[(size_t)i * p.ld_out] =
-                  __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
-          }
-        }
-      }
+      epilogue_tile<KIND>(t, t_row, live, p, q, lane, rank);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -403,6 +428,441 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, kTmemCols);
   }
+}
+
+// ---------------------------------------------------------------- MXFP8 weights
+//
+// The same tiles with the weights stored as MXFP8 ('Hosting Qwen on
+// Blackwell', "Quantization"): E4M3 codes and one E8M0 scale per 32 values
+// along K (moe_mxfp8.cu).  Per 128-wide K stage each CTA's TMA brings its 128
+// weight rows of codes (16 KB, on the CTA's own barrier) and their scales
+// (512 B), and the pair's tokens as before (on the leader's barrier).
+// Sixteen converter warps (four per TMEM lane quarter, one 32-value scale
+// block each) turn each code into code x 2^(scale - 127) in bf16 -- exact, a
+// code has four significant bits.  In a CTA pair they store the rows into
+// tensor memory and the leader's MMAs read A from there (tcgen05.mma ...
+// [a_tmem]) and B (tokens) from shared memory.  Tensor memory holds two
+// accumulators sized for the launch's largest token chunk (at most 192
+// columns, so chunks are capped at 192 here) and as many A buffers of 64
+// columns (128 K of bf16) as fit beside them, up to 4: the converters run
+// that many stages ahead of the MMAs.  Half the weight bytes of the bf16
+// kernel cross HBM and shared memory.
+//
+// One-CTA variant (few tokens per expert): the converters write the bf16
+// weights into shared memory in the layout TMA would give (K-major, 128-byte
+// swizzle) and the MMAs read both operands from shared memory: an MMA that
+// reads A from tensor memory was measured at about twice the issue time of
+// one that reads it from shared memory, and with few tokens the MMA issue
+// rate is what bounds the stage.
+constexpr int kTokMax8 = 192;
+constexpr int kBK8 = 128;                            // K per stage: one 128-byte row of codes
+constexpr int kABufCols = kBK8 / 2;                  // TMEM columns of one A buffer (bf16 pairs)
+constexpr int kMaxABufs = 4;
+constexpr int kA8Bytes = kWRows * kBK8;              // codes per CTA per stage
+constexpr int kScaleBytes = kWRows * 4;              // four E8M0 scales per row per stage
+constexpr int kConvWarp0 = 6;
+constexpr int kConvWarps = 16;                       // four per lane quarter, one scale block each
+constexpr int kABufBytes = kWRows * kBK8 * 2;        // one converted A stage in shared memory
+constexpr int kThreads8 = (kConvWarp0 + kConvWarps) * 32;
+constexpr int kMaxStages8 = 8;
+
+// 2^(byte - 127) as a float (byte 0: 2^-127, a subnormal).
+__device__ __forceinline__ float e8m0_to_float(uint32_t byte) {
+  return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
+// 4 E4M3 codes (a 32-bit word, lowest byte first) times 2^(S - 127) as two
+// bf16x2, by bits: a code's seven magnitude bits placed at bf16 bit 4 and its
+// sign at bit 15 form the bf16 (normal, or subnormal for a subnormal code)
+// whose value is the code's times 2^-120; one exact bf16x2 multiply by
+// mul = 2^(S - 7) applies the scale.  Valid while 2^(S - 7) is a finite bf16
+// (S <= 134); larger scales take e4m3x8_to_bf16.
+__device__ __forceinline__ void e4m3x4_to_bf16_bits(uint32_t w, __nv_bfloat162 mul,
+                                                    uint32_t* out) {
+  uint32_t a = __byte_perm(w, 0u, 0x4140u);  // code 0 | code 1 << 16
+  uint32_t b = __byte_perm(w, 0u, 0x4342u);  // code 2 | code 3 << 16
+  a = ((a << 4) & 0x07F007F0u) | ((a << 8) & 0x80008000u);
+  b = ((b << 4) & 0x07F007F0u) | ((b << 8) & 0x80008000u);
+  const __nv_bfloat162 pa = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), mul);
+  const __nv_bfloat162 pb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), mul);
+  out[0] = *reinterpret_cast<const uint32_t*>(&pa);
+  out[1] = *reinterpret_cast<const uint32_t*>(&pb);
+}
+
+// 8 E4M3 codes (a 64-bit word, lowest byte first) times `scale` as 4 bf16x2,
+// through the hardware conversions (any scale).
+__device__ __forceinline__ void e4m3x8_to_bf16(uint32_t lo, uint32_t hi, float scale,
+                                               uint32_t* out) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w = i < 2 ? lo : hi;
+    const __nv_fp8x2_storage_t two =
+        static_cast<__nv_fp8x2_storage_t>((w >> (16 * (i & 1))) & 0xffffu);
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    out[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+}
+
+template <int KIND, bool PAIR>
+__device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
+                                                     const TokenMapSet& tx, const Params& p) {
+  // one CTA's tile: 128 weight rows; a pair's tile spans two CTAs' rows
+  constexpr int kSlabH = PAIR ? 128 : 64;     // gate_up: h columns per tile
+  constexpr int kSlabRows = PAIR ? 256 : 128;  // down: y columns per tile
+  constexpr int kTokCap = PAIR ? kTokMax8 : kTokMax / 2;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_ct[kMaxExperts + 1];
+  __shared__ alignas(8) uint64_t s_bar[3 * kMaxStages8 + 2 * kMaxABufs + 5];
+  __shared__ int s_half_max;
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int pair = PAIR ? blockIdx.x >> 1 : blockIdx.x;
+  const int num_pairs = PAIR ? gridDim.x >> 1 : gridDim.x;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t a_full = smem_u32(&s_bar[0]);                    // own codes + scales landed
+  const uint32_t b_full = smem_u32(&s_bar[kMaxStages8]);          // leader: both CTAs' tokens
+  const uint32_t st_empty = smem_u32(&s_bar[2 * kMaxStages8]);    // stage consumed
+  const uint32_t conv_full = smem_u32(&s_bar[3 * kMaxStages8]);   // leader: A buffer converted
+  const uint32_t conv_empty = conv_full + 8 * kMaxABufs;          // A buffer read by the MMAs
+  const uint32_t tfull_bar = conv_empty + 8 * kMaxABufs;
+  const uint32_t tempty_bar = tfull_bar + 16;
+  const uint32_t drain_bar = tempty_bar + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxStages8; ++s) {
+      mbar_init(a_full + 8 * s, 1);
+      mbar_init(b_full + 8 * s, 1);
+      mbar_init(st_empty + 8 * s, 1 + kConvWarps);  // the MMA commit + this CTA's converters
+    }
+    for (int b = 0; b < kMaxABufs; ++b) {
+      mbar_init(conv_full + 8 * b, (PAIR ? 2 : 1) * kConvWarps);  // the converters of the CTA(s)
+      mbar_init(conv_empty + 8 * b, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar + 8 * b, 1);
+      mbar_init(tempty_bar + 8 * b, PAIR ? kEpiArrivals : kEpiArrivals / 2);
+    }
+    mbar_init(drain_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_w);
+#pragma unroll
+    for (int i = 0; i < kTokenMaps; ++i) tma_prefetch_desc(&tx.m[i]);
+  }
+  if (warp == 1) {
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(&s_tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&s_tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
+  }
+
+  pdl_wait_and_release();
+
+  const int G = p.groups;
+  build_schedule<kTokCap>(p, s_off, s_ct, &s_half_max, warp, lane);
+  tc_fence_before_sync();
+  __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = s_tmem_base;
+  const int total_tiles = s_ct[G] * p.slabs;
+  const int num_ks = p.K / kBK8;  // K is a multiple of 128
+  const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
+  // token rows this CTA holds per K box: half the largest chunk in a pair, all of it alone
+  const uint32_t b_sub_bytes = static_cast<uint32_t>((PAIR ? 1 : 2) * s_half_max) * kBK * 2;
+  const uint32_t stage_bytes = (kA8Bytes + kSub * b_sub_bytes + kScaleBytes + 1023u) & ~1023u;
+  const uint32_t avail = static_cast<uint32_t>(p.smem_bytes) - (base - smem_u32(smem_raw));
+  // s_half_max: half the largest chunk (a pair CTA's share); accumulators hold the whole chunk
+  const uint32_t acc_cols = static_cast<uint32_t>(2 * s_half_max);
+  // converted A: in tensor memory after the two accumulators (pair), or two
+  // shared-memory buffers after the stages (one CTA)
+  const uint32_t abuf0 = PAIR ? (2 * acc_cols + kABufCols - 1) / kABufCols * kABufCols : 0u;
+  const int nbuf = PAIR ? min(kMaxABufs, static_cast<int>((kTmemCols - abuf0) / kABufCols)) : 2;
+  const uint32_t a_smem_bytes = PAIR ? 0u : 2u * kABufBytes;
+  const int nst = min(kMaxStages8, static_cast<int>((avail - a_smem_bytes) / stage_bytes));
+  const uint32_t abuf_smem = base + nst * stage_bytes;  // one CTA: converted A buffers
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      const uint32_t b_leader = PAIR ? mapa_shared(b_full, 0) : b_full;
+      for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+        const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+        const int half = PAIR ? t.n / 2 : t.n;  // token rows this CTA loads
+        const CUtensorMap* tmap_x = &tx.m[half / (kUnit / 2) - 1];
+        const int trow = t.tok0 + static_cast<int>(rank) * half;
+        // this CTA's weight rows, and how many of them exist (the last slab may be ragged)
+        int row0, row1 = 0, nrow;
+        if (KIND == kGateUp) {
+          const int g0 = t.slab * kSlabH + static_cast<int>(rank) * 64;
+          nrow = max(0, min(64, p.n_out - g0));
+          row0 = t.e * p.w_rows_per_group + g0;
+          row1 = row0 + p.up_offset;
+        } else {
+          const int r0 = t.slab * kSlabRows + static_cast<int>(rank) * 128;
+          nrow = max(0, min(128, p.n_out - r0));
+          row0 = t.e * p.w_rows_per_group + r0;
+        }
+        const uint32_t scale_tx = (KIND == kGateUp ? 2 : 1) * static_cast<uint32_t>(nrow) * 4;
+        for (int ks = 0; ks < num_ks; ++ks) {
+          if (!mbar_wait(st_empty + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
+          const uint32_t a_dst = base + stage * stage_bytes;
+          const uint32_t b_dst = a_dst + kA8Bytes;
+          const uint32_t s_dst = b_dst + kSub * b_sub_bytes;
+          const uint32_t af = a_full + 8 * stage;
+          mbar_arrive_expect_tx(af, kA8Bytes + scale_tx);
+          const int kx = ks * kBK8;
+          if (KIND == kGateUp)
+            tma_load_5d(a_dst, &tmap_w, af, kx, 0, 0, (row0 - t.e * p.w_rows_per_group) / 16, t.e);
+          else
+            tma_load_2d(a_dst, &tmap_w, af, kx, row0);
+          const uint8_t* sc = p.scales + (static_cast<size_t>(ks) * p.scale_rows) * 4;
+          if (nrow > 0) {
+            bulk_load(s_dst, sc + static_cast<size_t>(row0) * 4, nrow * 4, af);
+            if (KIND == kGateUp)
+              bulk_load(s_dst + 256, sc + static_cast<size_t>(row1) * 4, nrow * 4, af);
+          }
+          if (leader)
+            mbar_arrive_expect_tx(b_full + 8 * stage, (PAIR ? 2 : 1) * kSub * half * kBK * 2);
+          const uint32_t bf = b_leader + 8 * stage;
+          for (int sub = 0; sub < kSub; ++sub) {
+            if constexpr (PAIR)
+              tma_load_2d_pair(b_dst + sub * b_sub_bytes, tmap_x, bf, kx + sub * kBK, trow);
+            else
+              tma_load_2d(b_dst + sub * b_sub_bytes, tmap_x, b_full + 8 * stage, kx + sub * kBK,
+                          trow);
+          }
+          ++issued;
+          if (++stage == nst) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int i = max(0, issued - nst); i < issued; ++i) {
+        mbar_wait_drain(a_full + 8 * (i % nst), (i / nst) & 1, p.status);
+        if (leader) mbar_wait_drain(b_full + 8 * (i % nst), (i / nst) & 1, p.status);
+      }
+      if (PAIR && !leader && !ok) {
+        // the follower's token copies count on the leader's barrier
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 50000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (leader)
+      int stage = 0, cb = 0, acc = 0;
+      uint32_t phase = 0, cphase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+        const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+        const uint32_t idesc = idesc_bf16_f32(PAIR ? 256 : 128, t.n);
+        if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * acc_cols;
+        for (int ks = 0; ks < num_ks; ++ks) {
+          if (!mbar_wait(b_full + 8 * stage, phase, wc)) { ok = false; break; }
+          if (!mbar_wait(conv_full + 8 * cb, cphase, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t b_addr = base + stage * stage_bytes + kA8Bytes;
+          const uint32_t a_tmem = tmem_base + abuf0 + cb * kABufCols;
+#pragma unroll
+          for (int k = 0; k < kBK8 / 16; ++k) {
+            const uint64_t bd = smem_desc_sw128(b_addr + (k >> 2) * b_sub_bytes + (k & 3) * 32);
+            if constexpr (PAIR) {
+              mma_bf16_pair_tmem_a(d_tmem, a_tmem + k * 8, bd, idesc, (ks | k) != 0 ? 1u : 0u);
+            } else {
+              const uint32_t a_addr = abuf_smem + cb * kABufBytes + (k >> 2) * kABytes + (k & 3) * 32;
+              mma_bf16_ss(d_tmem, smem_desc_sw128(a_addr), bd, idesc, (ks | k) != 0 ? 1u : 0u);
+            }
+          }
+          if constexpr (PAIR) {
+            mma_commit_pair(st_empty + 8 * stage);  // the tokens of this stage, both CTAs
+            mma_commit_pair(conv_empty + 8 * cb);   // the A buffer, both CTAs
+          } else {
+            mma_commit(st_empty + 8 * stage);
+            mma_commit(conv_empty + 8 * cb);
+          }
+          if (++stage == nst) { stage = 0; phase ^= 1u; }
+          if (++cb == nbuf) { cb = 0; cphase ^= 1u; }
+        }
+        if (!ok) break;
+        if constexpr (PAIR) mma_commit_pair(tfull_bar + 8 * acc);
+        else mma_commit(tfull_bar + 8 * acc);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if constexpr (PAIR) mma_commit_pair(drain_bar);
+      else mma_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0, p.status);
+    } else if (PAIR && lane == 0) {
+      mbar_wait_drain(drain_bar, 0, p.status);
+    }
+  } else if (warp < kConvWarp0) {
+    // ---------------- epilogue: warps 2..5
+    const int q = warp & 3;
+    const uint32_t tempty_leader = mapa_shared(tempty_bar, 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tau = pair; tau < total_tiles; tau += num_pairs) {
+      const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+      const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
+      epilogue_tile<KIND, KIND == kGateUp ? kSlabH : kSlabRows>(t, t_row, live, p, q, lane, rank);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar + 8 * acc);
+        else mbar_arrive_cluster(tempty_leader + 8 * acc);
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  } else {
+    // ---------------- converters: warps 6..21, TMEM lanes 32 (warp % 4) + lane.
+    // Thread (q, lane) of converter kq converts K values 32 kq .. 32 kq + 31 (one
+    // scale block) of A row r = 32 q + lane: for gate_up the row of group q that
+    // is gate row 16 q + lane (lane < 16) or the matching up row.
+    const int q = warp & 3;
+    const int kq = (warp - kConvWarp0) >> 2;
+    const int r = q * 32 + lane;
+    const uint32_t conv_leader = mapa_shared(conv_full, 0);
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf0;
+    int stage = 0, cb = 0;
+    uint32_t phase = 0, cphase = 0;
+    bool ok = true;
+    for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+      const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+      int col, srow;
+      if (KIND == kGateUp) {
+        col = t.slab * kSlabH + static_cast<int>(rank) * 64 + q * 16 + (lane & 15);
+        srow = lane < 16 ? q * 16 + lane : 64 + q * 16 + (lane - 16);
+      } else {
+        col = t.slab * kSlabRows + static_cast<int>(rank) * 128 + r;
+        srow = r;
+      }
+      const bool row_ok = col < p.n_out;
+      for (int ks = 0; ks < num_ks; ++ks) {
+        if (!mbar_wait(a_full + 8 * stage, phase, wc)) { ok = false; break; }
+        if (!mbar_wait(conv_empty + 8 * cb, cphase ^ 1u, wc)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t a_src = base + stage * stage_bytes;
+        const uint32_t s_src = a_src + kA8Bytes + kSub * b_sub_bytes;
+        uint32_t sc = 0;
+        if (row_ok) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc) : "r"(s_src + srow * 4));
+        const uint32_t t_buf = t_lane + cb * kABufCols;
+        {
+          const int blk = kq;  // 32 K values: one scale, 16 TMEM columns / 64 bytes of the row
+          const uint32_t sbyte = (sc >> (8 * blk)) & 0xffu;
+          const bool fast = sbyte <= 134u;
+          // 2^(S - 7) as a bf16 pair (exponent field S + 120)
+          const uint32_t mbits = ((sbyte + 120u) << 7) * 0x00010001u;
+          const __nv_bfloat162 mul = *reinterpret_cast<const __nv_bfloat162*>(&mbits);
+          const float scale = e8m0_to_float(sbyte);
+          uint32_t out[16];
+#pragma unroll
+          for (int hch = 0; hch < 2; ++hch) {
+            const int chunk = blk * 2 + hch;  // 16-byte chunk of the 128-byte row
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(a_src + r * 128 + ((chunk ^ (r & 7)) << 4)));
+            if (fast) {
+              e4m3x4_to_bf16_bits(w0, mul, out + hch * 8);
+              e4m3x4_to_bf16_bits(w1, mul, out + hch * 8 + 2);
+              e4m3x4_to_bf16_bits(w2, mul, out + hch * 8 + 4);
+              e4m3x4_to_bf16_bits(w3, mul, out + hch * 8 + 6);
+            } else {
+              e4m3x8_to_bf16(w0, w1, scale, out + hch * 8);
+              e4m3x8_to_bf16(w2, w3, scale, out + hch * 8 + 4);
+            }
+          }
+          if (!row_ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) out[i] = 0u;
+          }
+          if constexpr (PAIR) {
+            tmem_st_32x32b_x16(t_buf + blk * 16, out);
+          } else {
+            // K box blk / 2 of the buffer, 16-byte chunks 4 (blk % 2) .. +3 of row r, swizzled
+            const uint32_t row_addr = abuf_smem + cb * kABufBytes + (blk >> 1) * kABytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int chunk = (blk & 1) * 4 + c;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               row_addr + ((chunk ^ (r & 7)) << 4)),
+                           "r"(out[4 * c]), "r"(out[4 * c + 1]), "r"(out[4 * c + 2]),
+                           "r"(out[4 * c + 3])
+                           : "memory");
+            }
+          }
+        }
+        if constexpr (PAIR) tmem_st_wait();
+        else asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the MMAs' reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(st_empty + 8 * stage);  // codes and scales of this stage read
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(conv_full + 8 * cb);
+          else mbar_arrive_cluster(conv_leader + 8 * cb);
+        }
+        if (++stage == nst) { stage = 0; phase ^= 1u; }
+        if (++cb == nbuf) { cb = 0; cphase ^= 1u; }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if constexpr (PAIR) cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1)
+    moe_gate_up_swiglu_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                                    const __grid_constant__ TokenMapSet tx, const Params p) {
+  expert_gemm_fp8_body<kGateUp, true>(tmap_w, tx, p);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1)
+    moe_down_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                          const __grid_constant__ TokenMapSet tx, const Params p) {
+  expert_gemm_fp8_body<kDown, true>(tmap_w, tx, p);
+}
+
+// One CTA per tile (M = 128 weight rows, the whole token chunk, chunks of at
+// most 128): no signal crosses SMs, which suits few tokens per expert.
+__global__ void __launch_bounds__(kThreads8, 1)
+    moe_gate_up_swiglu_mxfp8_1cta_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                                         const __grid_constant__ TokenMapSet tx, const Params p) {
+  expert_gemm_fp8_body<kGateUp, false>(tmap_w, tx, p);
+}
+
+__global__ void __launch_bounds__(kThreads8, 1)
+    moe_down_mxfp8_1cta_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                               const __grid_constant__ TokenMapSet tx, const Params p) {
+  expert_gemm_fp8_body<kDown, false>(tmap_w, tx, p);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -424,7 +884,7 @@ typedef void (*ExpertKernel)(const CUtensorMap, const TokenMapSet, const Params)
 // Set as the kernel's limit on first use per device; 0 on failure.
 int ensure_smem_attr(ExpertKernel k, int which) {
   static std::mutex mu;
-  static int bytes[2][64] = {};
+  static int bytes[6][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
@@ -445,16 +905,16 @@ int ensure_smem_attr(ExpertKernel k, int which) {
 // Pairs that can be resident at once.  A pair needs two SMs of one GPC, so
 // this can be fewer than half the SMs; a persistent grid larger than it would
 // run its surplus pairs' whole tile lists as a second wave.
-int resident_pairs(ExpertKernel k, int which, int smem_bytes) {
+int resident_pairs(ExpertKernel k, int which, int smem_bytes, int threads) {
   static std::mutex mu;
-  static int cached[2][64] = {};
+  static int cached[4][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   std::lock_guard<std::mutex> lock(mu);
   if (!cached[which][dev]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
@@ -477,7 +937,7 @@ cudaError_t make_token_maps(TokenMapSet& mx, const void* a, int rows, int K) {
 
 cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int which,
                           const CUtensorMap& mw, const TokenMapSet& mx, Params p,
-                          long long tiles_bound) {
+                          long long tiles_bound, int threads = kThreads) {
   const int smem = ensure_smem_attr(k, which);
   if (smem <= 0) {
     cudaGetLastError();
@@ -485,9 +945,25 @@ cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int 
   }
   p.smem_bytes = smem;
   const long long pairs =
-      std::max(1LL, std::min<long long>(resident_pairs(k, which, smem), tiles_bound));
+      std::max(1LL, std::min<long long>(resident_pairs(k, which, smem, threads), tiles_bound));
   KernelScope scope(s, name);
-  return launch_kernel(k, dim3(static_cast<unsigned>(2 * pairs)), dim3(kThreads),
+  return launch_kernel(k, dim3(static_cast<unsigned>(2 * pairs)), dim3(threads),
+                       static_cast<size_t>(smem), s, mw, mx, p);
+}
+
+// One CTA per SM (the kernels take all the shared memory), static stride over tiles.
+cudaError_t launch_expert_1cta(cudaStream_t s, const char* name, ExpertKernel k, int which,
+                               const CUtensorMap& mw, const TokenMapSet& mx, Params p,
+                               long long tiles_bound) {
+  const int smem = ensure_smem_attr(k, which);
+  if (smem <= 0) {
+    cudaGetLastError();
+    return cudaErrorInvalidConfiguration;
+  }
+  p.smem_bytes = smem;
+  const long long grid = std::max(1LL, std::min<long long>(device_sm_count(), tiles_bound));
+  KernelScope scope(s, name);
+  return launch_kernel(k, dim3(static_cast<unsigned>(grid)), dim3(kThreads8),
                        static_cast<size_t>(smem), s, mw, mx, p);
 }
 
@@ -550,6 +1026,78 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   q.timeout_ns = timeout_ns;
   return launch_expert(s, offsets ? "moe_down" : "moe_shared_down", moe_down_kernel, 1, mw2, mx2,
                        q, chunks_bound * q.slabs);
+}
+
+cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_t* offsets,
+                                     int rows, int d, int E, int I, const uint8_t* codes_gate_up,
+                                     const uint8_t* scales_gate_up, const uint8_t* codes_down,
+                                     const uint8_t* scales_down, void* h, float* y,
+                                     unsigned* status, unsigned long long timeout_ns) {
+  // Few rows per expert (decode): one CTA per tile, nothing signalled across SMs.
+  // Many: CTA pairs, which halve each SM's share of the tokens.
+  const bool one = rows <= 128LL * E;
+  const int cap = one ? kTokMax / 2 : kTokMax8;
+  const long long chunks_bound = rows / cap + std::min(E, rows);
+
+  // codes of W_gate_up [E][2][I][d] viewed as (d, 16 rows, gate|up, I/16 row groups, E): one
+  // box = 128 K of 4 row groups, each 16 gate rows followed by the 16 matching up rows
+  CUtensorMap mw;
+  TokenMapSet mx;
+  const uint64_t dims[5] = {static_cast<uint64_t>(d), 16, 2, static_cast<uint64_t>(I / 16),
+                            static_cast<uint64_t>(E)};
+  const uint64_t strides[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(I) * d,
+                               16ull * d, 2ull * I * d};
+  const uint32_t box[5] = {kBK8, 16, 2, 4, 1};
+  cudaError_t e = make_u8_map_nd(&mw, codes_gate_up, 5, dims, strides, box);
+  if (e == cudaSuccess) e = make_token_maps(mx, a, rows, d);
+  if (e != cudaSuccess) return e;
+  Params p{};
+  p.K = d;
+  p.n_out = I;
+  p.slabs = one ? I / 64 : I / 128;
+  p.groups = E;
+  p.offsets = offsets;
+  p.total_rows = rows;
+  p.w_rows_per_group = 2 * I;
+  p.up_offset = I;
+  p.out = h;
+  p.ld_out = I;
+  p.scales = scales_gate_up;
+  p.scale_rows = 2LL * I * E;
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+  e = one ? launch_expert_1cta(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_1cta_kernel,
+                               4, mw, mx, p, chunks_bound * p.slabs)
+          : launch_expert(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_kernel, 2, mw, mx,
+                          p, chunks_bound * p.slabs, kThreads8);
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap mw2;
+  TokenMapSet mx2;
+  const uint64_t dims2[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(E) * d};
+  const uint64_t strides2[1] = {static_cast<uint64_t>(I)};
+  const uint32_t box2[2] = {kBK8, 128};
+  e = make_u8_map_nd(&mw2, codes_down, 2, dims2, strides2, box2);
+  if (e == cudaSuccess) e = make_token_maps(mx2, h, rows, I);
+  if (e != cudaSuccess) return e;
+  Params q{};
+  q.K = I;
+  q.n_out = d;
+  q.slabs = one ? (d + 127) / 128 : (d + 255) / 256;
+  q.groups = E;
+  q.offsets = offsets;
+  q.total_rows = rows;
+  q.w_rows_per_group = d;
+  q.out = y;
+  q.ld_out = d;
+  q.scales = scales_down;
+  q.scale_rows = static_cast<long long>(E) * d;
+  q.status = status;
+  q.timeout_ns = timeout_ns;
+  return one ? launch_expert_1cta(s, "moe_down_mxfp8", moe_down_mxfp8_1cta_kernel, 5, mw2, mx2, q,
+                                  chunks_bound * q.slabs)
+             : launch_expert(s, "moe_down_mxfp8", moe_down_mxfp8_kernel, 3, mw2, mx2, q,
+                             chunks_bound * q.slabs, kThreads8);
 }
 
 }  // namespace moe

@@ -92,6 +92,9 @@ cudaError_t make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, uin
 // be 64 (one 128-byte row).
 cudaError_t make_bf16_map_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                              const uint64_t* strides_bytes, const uint32_t* box);
+// The same for a uint8 tensor (MXFP8 codes), 128-byte swizzle.
+cudaError_t make_u8_map_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box);
 
 // ---- tcgen05 GEMM launchers.  Return a CUDA error code.
 
@@ -118,6 +121,14 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
                                void* h, float* y, unsigned* status,
                                unsigned long long timeout_ns);
+
+// The same with MXFP8 expert weights: E4M3 codes [E, 2I, d] / [E, d, I] and
+// E8M0 scales [d/128][E*2I][4] / [I/128][E*d][4]; d and I multiples of 128.
+cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_t* offsets,
+                                     int rows, int d, int E, int I, const uint8_t* codes_gate_up,
+                                     const uint8_t* scales_gate_up, const uint8_t* codes_down,
+                                     const uint8_t* scales_down, void* h, float* y,
+                                     unsigned* status, unsigned long long timeout_ns);
 
 // ---- grouping and combine (moe_permute.cu)
 

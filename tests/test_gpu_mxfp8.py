@@ -1,5 +1,6 @@
 """MXFP8 weights on the GPU against the oracle: quantisation codes and scales
-bit for bit."""
+bit for bit, and the whole layer against the oracle's layer with the weights
+it quantised and dequantised itself."""
 
 import numpy as np
 import pytest
@@ -7,6 +8,7 @@ import torch
 
 import oracle
 from mixture_experts_layer_20_gb300 import workloads as W
+from tests.gpu_util import assert_layer_close, compare_routing, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -40,3 +42,72 @@ def test_quantize_matches_oracle(moe, shape):
     ref_codes, ref_scales = _oracle_layout(ref_codes, ref_scales)
     assert np.array_equal(codes.cpu().numpy().reshape(-1, K), ref_codes)
     assert np.array_equal(scales.cpu().numpy(), ref_scales)
+
+
+def _dequantised_bits(w):
+    """The oracle's own MXFP8 round trip of a bf16 [E, rows, K] weight tensor,
+    as bf16 bits (exact: codes times powers of two have four significant bits)."""
+    K = w.shape[-1]
+    codes, scales = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(W.to_bits(w)).reshape(-1, K))
+    deq = oracle.mxfp8_dequantize(codes, scales).reshape(w.shape)
+    bits = oracle.f64_to_bf16_bits(deq)
+    assert np.array_equal(oracle.bf16_bits_to_f64(bits), deq)
+    return bits
+
+
+FORWARD_CASES = [
+    # T, d, E, k, I, I_shared, zipf
+    (64, 512, 32, 8, 256, 0, False),     # decode-like: a few rows per expert, 16-row chunks
+    (600, 512, 8, 4, 384, 0, False),     # ~300 rows per expert: two chunks, three slabs
+    (200, 384, 16, 4, 128, 0, True),     # d = 384: the last down slab has one populated half
+    (130, 768, 64, 8, 256, 128, True),   # bias and a (bf16) shared expert
+]
+
+
+@pytest.mark.parametrize("T,d,E,k,I,Is,zipf", FORWARD_CASES)
+def test_forward_mxfp8(moe, T, d, E, k, I, Is, zipf):
+    w = W.Workload("mx", T, d, E, k, I, I_shared=Is, zipf_bias=zipf, seed=T + d)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    mx_gu = moe.moe_mxfp8_quantize(p["w_gate_up"])
+    mx_d = moe.moe_mxfp8_quantize(p["w_down"])
+    ws = moe.new_workspace(T, d, E, I, k, Is)
+    out = moe.moe_forward_mxfp8(x, p["w_router"], mx_gu, mx_d, k, ws=ws,
+                                router_bias=p["router_bias"],
+                                w_gate_up_shared=p["w_gate_up_shared"],
+                                w_down_shared=p["w_down_shared"])
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, T, d, E, I, k, Is)
+    ref = oracle.forward(
+        W.to_bits(x), W.to_bits(p["w_router"]), _dequantised_bits(p["w_gate_up"]),
+        _dequantised_bits(p["w_down"]), k,
+        router_bias=None if p["router_bias"] is None else p["router_bias"].cpu().numpy(),
+        w_gate_up_shared=None if p["w_gate_up_shared"] is None else W.to_bits(p["w_gate_up_shared"]),
+        w_down_shared=None if p["w_down_shared"] is None else W.to_bits(p["w_down_shared"]))
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ref["ids"], ref["gates"], ref["logits"], k)
+    assert differ.size == 0
+    assert_layer_close(f64(v["y"]), ref["y"], "y")
+    assert_layer_close(f64(out), ref["out"], "out")
+
+
+def test_forward_mxfp8_extreme_codes(moe):
+    """Subnormal E4M3 codes (tiny weights inside a block) and scales above
+    2^7 (the converter's general path) still match the oracle."""
+    T, d, E, k, I = 96, 512, 8, 2, 256
+    w = W.Workload("mx_extreme", T, d, E, k, I, seed=77)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    wgu = p["w_gate_up"].clone()
+    wgu[1, :, 0::32] *= 2.0 ** -14          # one value per run far below the run maximum
+    wd = p["w_down"].clone()
+    wd[2] *= 2.0 ** 20                      # run maxima near 2^19: scale bytes above 134
+    mx_gu = moe.moe_mxfp8_quantize(wgu)
+    mx_d = moe.moe_mxfp8_quantize(wd)
+    assert int(mx_d[1].max()) > 134
+    assert bool(((mx_gu[0][1] & 0x78) == 0).any())   # exponent field 0: subnormal codes
+    out = moe.moe_forward_mxfp8(x, p["w_router"], mx_gu, mx_d, k)
+    torch.cuda.synchronize()
+    ref = oracle.forward(W.to_bits(x), W.to_bits(p["w_router"]), _dequantised_bits(wgu),
+                         _dequantised_bits(wd), k)
+    assert_layer_close(f64(out), ref["out"], "out")
