@@ -437,23 +437,16 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 // along K (moe_mxfp8.cu).  Per 128-wide K stage each CTA's TMA brings its 128
 // weight rows of codes (16 KB, on the CTA's own barrier) and their scales
 // (512 B), and the pair's tokens as before (on the leader's barrier).
-// Sixteen converter warps (four per TMEM lane quarter, one 32-value scale
-// block each) turn each code into code x 2^(scale - 127) in bf16 -- exact, a
-// code has four significant bits.  In a CTA pair they store the rows into
-// tensor memory and the leader's MMAs read A from there (tcgen05.mma ...
-// [a_tmem]) and B (tokens) from shared memory.  Tensor memory holds two
+// Converter warps turn each code into code x 2^(scale - 127) in bf16 --
+// exact, a code has four significant bits -- and store the rows into tensor
+// memory; the leader's MMAs read A from there (tcgen05.mma ... [a_tmem]) and
+// B (tokens) from shared memory.  Tensor memory holds two
 // accumulators sized for the launch's largest token chunk (at most 192
 // columns, so chunks are capped at 192 here) and as many A buffers of 64
 // columns (128 K of bf16) as fit beside them, up to 4: the converters run
 // that many stages ahead of the MMAs.  Half the weight bytes of the bf16
 // kernel cross HBM and shared memory.
-//
-// One-CTA variant (few tokens per expert): the converters write the bf16
-// weights into shared memory in the layout TMA would give (K-major, 128-byte
-// swizzle) and the MMAs read both operands from shared memory: an MMA that
-// reads A from tensor memory was measured at about twice the issue time of
-// one that reads it from shared memory, and with few tokens the MMA issue
-// rate is what bounds the stage.
+
 constexpr int kTokMax8 = 192;
 constexpr int kBK8 = 128;                            // K per stage: one 128-byte row of codes
 constexpr int kABufCols = kBK8 / 2;                  // TMEM columns of one A buffer (bf16 pairs)
@@ -461,9 +454,13 @@ constexpr int kMaxABufs = 4;
 constexpr int kA8Bytes = kWRows * kBK8;              // codes per CTA per stage
 constexpr int kScaleBytes = kWRows * 4;              // four E8M0 scales per row per stage
 constexpr int kConvWarp0 = 6;
-constexpr int kConvWarps = 16;                       // four per lane quarter, one scale block each
-constexpr int kABufBytes = kWRows * kBK8 * 2;        // one converted A stage in shared memory
-constexpr int kThreads8 = (kConvWarp0 + kConvWarps) * 32;
+// Converter warps: 16 in a CTA pair (four per TMEM lane quarter, one scale
+// block each), 8 alone (two per quarter, two blocks each).  Measured: with few
+// tokens the one-CTA tile's MMAs share the issue slots of the converters'
+// sub-partitions and 8 warps leave them more; with a CTA pair's large chunks
+// conversion is the longer side and 16 warps shorten it.
+__host__ __device__ constexpr int conv_warps(bool pair) { return pair ? 16 : 8; }
+__host__ __device__ constexpr int threads8(bool pair) { return (kConvWarp0 + conv_warps(pair)) * 32; }
 constexpr int kMaxStages8 = 8;
 
 // 2^(byte - 127) as a float (byte 0: 2^-127, a subnormal).
@@ -476,13 +473,17 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t byte) {
 // sign at bit 15 form the bf16 (normal, or subnormal for a subnormal code)
 // whose value is the code's times 2^-120; one exact bf16x2 multiply by
 // mul = 2^(S - 7) applies the scale.  Valid while 2^(S - 7) is a finite bf16
-// (S <= 134); larger scales take e4m3x8_to_bf16.
+// (S <= 134); larger scales take e4m3x8_to_bf16.  The byte permute
+// sign-extends each code to 16 bits (prmt selector nibbles with bit 3 set
+// replicate the selected byte's sign), so one shift moves the magnitude to
+// bits 4-10 and a sign copy to bit 15, and one mask clears the rest.
 __device__ __forceinline__ void e4m3x4_to_bf16_bits(uint32_t w, __nv_bfloat162 mul,
                                                     uint32_t* out) {
-  uint32_t a = __byte_perm(w, 0u, 0x4140u);  // code 0 | code 1 << 16
-  uint32_t b = __byte_perm(w, 0u, 0x4342u);  // code 2 | code 3 << 16
-  a = ((a << 4) & 0x07F007F0u) | ((a << 8) & 0x80008000u);
-  b = ((b << 4) & 0x07F007F0u) | ((b << 8) & 0x80008000u);
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));  // sext16(code 0) | sext16(code 1) << 16
+  asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));  // codes 2 and 3
+  a = (a << 4) & 0x87F087F0u;
+  b = (b << 4) & 0x87F087F0u;
   const __nv_bfloat162 pa = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), mul);
   const __nv_bfloat162 pb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), mul);
   out[0] = *reinterpret_cast<const uint32_t*>(&pa);
@@ -512,6 +513,8 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
   constexpr int kSlabH = PAIR ? 128 : 64;     // gate_up: h columns per tile
   constexpr int kSlabRows = PAIR ? 256 : 128;  // down: y columns per tile
   constexpr int kTokCap = PAIR ? kTokMax8 : kTokMax / 2;
+  constexpr int kConvWarps = conv_warps(PAIR);
+  constexpr int kBlkPerWarp = 16 / kConvWarps;  // 32-value scale blocks per warp per stage
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_ct[kMaxExperts + 1];
@@ -587,13 +590,10 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
   const uint32_t avail = static_cast<uint32_t>(p.smem_bytes) - (base - smem_u32(smem_raw));
   // s_half_max: half the largest chunk (a pair CTA's share); accumulators hold the whole chunk
   const uint32_t acc_cols = static_cast<uint32_t>(2 * s_half_max);
-  // converted A: in tensor memory after the two accumulators (pair), or two
-  // shared-memory buffers after the stages (one CTA)
-  const uint32_t abuf0 = PAIR ? (2 * acc_cols + kABufCols - 1) / kABufCols * kABufCols : 0u;
-  const int nbuf = PAIR ? min(kMaxABufs, static_cast<int>((kTmemCols - abuf0) / kABufCols)) : 2;
-  const uint32_t a_smem_bytes = PAIR ? 0u : 2u * kABufBytes;
-  const int nst = min(kMaxStages8, static_cast<int>((avail - a_smem_bytes) / stage_bytes));
-  const uint32_t abuf_smem = base + nst * stage_bytes;  // one CTA: converted A buffers
+  const int nst = min(kMaxStages8, static_cast<int>(avail / stage_bytes));
+  // tensor memory: accumulators [0, acc_cols), [acc_cols, 2 acc_cols); A buffers after them
+  const uint32_t abuf0 = (2 * acc_cols + kABufCols - 1) / kABufCols * kABufCols;
+  const int nbuf = min(kMaxABufs, static_cast<int>((kTmemCols - abuf0) / kABufCols));
 
   if (warp == 0) {
     if (lane == 0) {
@@ -685,12 +685,10 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
 #pragma unroll
           for (int k = 0; k < kBK8 / 16; ++k) {
             const uint64_t bd = smem_desc_sw128(b_addr + (k >> 2) * b_sub_bytes + (k & 3) * 32);
-            if constexpr (PAIR) {
+            if constexpr (PAIR)
               mma_bf16_pair_tmem_a(d_tmem, a_tmem + k * 8, bd, idesc, (ks | k) != 0 ? 1u : 0u);
-            } else {
-              const uint32_t a_addr = abuf_smem + cb * kABufBytes + (k >> 2) * kABytes + (k & 3) * 32;
-              mma_bf16_ss(d_tmem, smem_desc_sw128(a_addr), bd, idesc, (ks | k) != 0 ? 1u : 0u);
-            }
+            else
+              mma_bf16_tmem_a(d_tmem, a_tmem + k * 8, bd, idesc, (ks | k) != 0 ? 1u : 0u);
           }
           if constexpr (PAIR) {
             mma_commit_pair(st_empty + 8 * stage);  // the tokens of this stage, both CTAs
@@ -734,10 +732,10 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   } else {
-    // ---------------- converters: warps 6..21, TMEM lanes 32 (warp % 4) + lane.
-    // Thread (q, lane) of converter kq converts K values 32 kq .. 32 kq + 31 (one
-    // scale block) of A row r = 32 q + lane: for gate_up the row of group q that
-    // is gate row 16 q + lane (lane < 16) or the matching up row.
+    // ---------------- converters: warps 6.., TMEM lanes 32 (warp % 4) + lane.
+    // Thread (q, lane) of converter kq converts scale blocks kq * kBlkPerWarp ..
+    // (32 K values each) of A row r = 32 q + lane: for gate_up the row of
+    // group q that is gate row 16 q + lane (lane < 16) or the matching up row.
     const int q = warp & 3;
     const int kq = (warp - kConvWarp0) >> 2;
     const int r = q * 32 + lane;
@@ -766,8 +764,9 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
         uint32_t sc = 0;
         if (row_ok) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc) : "r"(s_src + srow * 4));
         const uint32_t t_buf = t_lane + cb * kABufCols;
-        {
-          const int blk = kq;  // 32 K values: one scale, 16 TMEM columns / 64 bytes of the row
+#pragma unroll
+        for (int bi = 0; bi < kBlkPerWarp; ++bi) {
+          const int blk = kq * kBlkPerWarp + bi;  // 32 K values: one scale, 16 TMEM columns
           const uint32_t sbyte = (sc >> (8 * blk)) & 0xffu;
           const bool fast = sbyte <= 134u;
           // 2^(S - 7) as a bf16 pair (exponent field S + 120)
@@ -796,24 +795,9 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
 #pragma unroll
             for (int i = 0; i < 16; ++i) out[i] = 0u;
           }
-          if constexpr (PAIR) {
-            tmem_st_32x32b_x16(t_buf + blk * 16, out);
-          } else {
-            // K box blk / 2 of the buffer, 16-byte chunks 4 (blk % 2) .. +3 of row r, swizzled
-            const uint32_t row_addr = abuf_smem + cb * kABufBytes + (blk >> 1) * kABytes + r * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int chunk = (blk & 1) * 4 + c;
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                               row_addr + ((chunk ^ (r & 7)) << 4)),
-                           "r"(out[4 * c]), "r"(out[4 * c + 1]), "r"(out[4 * c + 2]),
-                           "r"(out[4 * c + 3])
-                           : "memory");
-            }
-          }
+          tmem_st_32x32b_x16(t_buf + blk * 16, out);
         }
-        if constexpr (PAIR) tmem_st_wait();
-        else asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the MMAs' reads
+        tmem_st_wait();
         __syncwarp();
         if (lane == 0) mbar_arrive(st_empty + 8 * stage);  // codes and scales of this stage read
         tc_fence_before_sync();
@@ -839,13 +823,13 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads8(true), 1)
     moe_gate_up_swiglu_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                     const __grid_constant__ TokenMapSet tx, const Params p) {
   expert_gemm_fp8_body<kGateUp, true>(tmap_w, tx, p);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads8(true), 1)
     moe_down_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
                           const __grid_constant__ TokenMapSet tx, const Params p) {
   expert_gemm_fp8_body<kDown, true>(tmap_w, tx, p);
@@ -853,13 +837,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads8, 1)
 
 // One CTA per tile (M = 128 weight rows, the whole token chunk, chunks of at
 // most 128): no signal crosses SMs, which suits few tokens per expert.
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(threads8(false), 1)
     moe_gate_up_swiglu_mxfp8_1cta_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                          const __grid_constant__ TokenMapSet tx, const Params p) {
   expert_gemm_fp8_body<kGateUp, false>(tmap_w, tx, p);
 }
 
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(threads8(false), 1)
     moe_down_mxfp8_1cta_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                const __grid_constant__ TokenMapSet tx, const Params p) {
   expert_gemm_fp8_body<kDown, false>(tmap_w, tx, p);
@@ -963,7 +947,7 @@ cudaError_t launch_expert_1cta(cudaStream_t s, const char* name, ExpertKernel k,
   p.smem_bytes = smem;
   const long long grid = std::max(1LL, std::min<long long>(device_sm_count(), tiles_bound));
   KernelScope scope(s, name);
-  return launch_kernel(k, dim3(static_cast<unsigned>(grid)), dim3(kThreads8),
+  return launch_kernel(k, dim3(static_cast<unsigned>(grid)), dim3(threads8(false)),
                        static_cast<size_t>(smem), s, mw, mx, p);
 }
 
@@ -1069,7 +1053,7 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   e = one ? launch_expert_1cta(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_1cta_kernel,
                                4, mw, mx, p, chunks_bound * p.slabs)
           : launch_expert(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_kernel, 2, mw, mx,
-                          p, chunks_bound * p.slabs, kThreads8);
+                          p, chunks_bound * p.slabs, threads8(true));
   if (e != cudaSuccess) return e;
 
   CUtensorMap mw2;
@@ -1097,7 +1081,7 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   return one ? launch_expert_1cta(s, "moe_down_mxfp8", moe_down_mxfp8_1cta_kernel, 5, mw2, mx2, q,
                                   chunks_bound * q.slabs)
              : launch_expert(s, "moe_down_mxfp8", moe_down_mxfp8_kernel, 3, mw2, mx2, q,
-                             chunks_bound * q.slabs, kThreads8);
+                             chunks_bound * q.slabs, threads8(true));
 }
 
 }  // namespace moe
