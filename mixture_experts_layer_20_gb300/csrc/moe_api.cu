@@ -362,7 +362,6 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
   int32_t* slot_pos = reinterpret_cast<int32_t*>(w + L.slot_pos);
   int32_t* table = reinterpret_cast<int32_t*>(w + L.chunk);
-  void* x_perm = w + L.x_perm;
   void* h = w + L.h;
   float* y = reinterpret_cast<float*>(w + L.y);
   const unsigned long long tmo = g_timeout_ns.load();
@@ -372,14 +371,21 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   if ((st = route_impl(x, w_router, bias, bias_sel, T, d, E, top_k, ids, gates, partial, status,
                        s)) != MOE_OK)
     return st;
-  cudaError_t e = launch_permute(s, ids, x, T, d, E, top_k, counts, offsets, perm, slot_pos,
-                                 x_perm, table, status);
+  // Few rows per expert (decode): the bf16 gate_up GEMM gathers its token
+  // rows from x through perm (four rows per TMA gather), so no permuted copy
+  // of x is written.  Many rows: one TMA box per K box of x_perm loads faster
+  // than that many gathers.
+  void* x_perm = w + L.x_perm;
+  const bool gather_rows = !mx && rows <= 128LL * E;
+  cudaError_t e = launch_permute(s, ids, gather_rows ? nullptr : x, T, d, E, top_k, counts,
+                                 offsets, perm, slot_pos, x_perm, table, status);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+  const TokenGather gather{x, perm, top_k, T};
   e = mx ? launch_grouped_ffn_mxfp8(s, x_perm, offsets, rows, d, E, I, mx->codes_gate_up,
                                     mx->scales_gate_up, mx->codes_down, mx->scales_down, h, y,
                                     status, tmo)
          : launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status,
-                              tmo);
+                              tmo, gather_rows ? &gather : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
   float* y_shared = nullptr;
   if (I_shared) {

@@ -315,6 +315,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Row gather for a CTA pair: four rows r0..r3 of a 2-D map whose box is one
+// row high (x = first column, a multiple of 8 for bf16) land as four
+// consecutive box rows at dst with the map's swizzle; completion counted in
+// bytes on `bar`, which may be the peer's barrier (mapa address).  A row
+// index past the tensor reads the fill value (zeros).
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int x, int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map,
                                                  uint32_t bar, int c0, int c1, int c2, int c3) {
   asm volatile(

@@ -60,6 +60,9 @@ namespace {
 constexpr int kBK = 64;     // one 128-byte swizzle row of bf16: the K of one TMA box
 constexpr int kSub = 2;     // K boxes per pipeline stage: 8 MMAs per barrier round
 constexpr int kMaxStages = 4;                      // pipeline stages that fit when chunks are <= 192 tokens
+constexpr int kMaxStagesWide = 6;                  // one K box per stage (wide chunks)
+constexpr int kTokMaxWide = 512;                   // wide chunks: two MMAs of up to 256 tokens
+constexpr int kWideRowsPerGroup = 256;             // launches with this many rows per expert go wide
 constexpr int kWRows = 128;                        // weight rows per CTA
 constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
 constexpr int kUnit = 16;                          // token rows: chunks are multiples of this
@@ -83,9 +86,16 @@ struct Params {
   int up_offset;          // gate_up: I
   void* out;              // gate_up: h bf16 [rows, I]; down: y fp32 [rows, d]
   long long ld_out;
+  // Token rows gathered on the fly (null: B is [total_rows, K] in row order):
+  // B row of slot pos is row gather_perm[pos] / gather_div of the map over
+  // the unpermuted tokens; slots past total_rows read row gather_oob (zeros).
+  const int32_t* gather_perm;
+  int gather_div;
+  int gather_oob;
   const uint8_t* scales;  // MXFP8 weights: E8M0 scales [K / 128][scale_rows][4]
   long long scale_rows;   // MXFP8 weights: weight rows of the whole tensor
   int smem_bytes;         // dynamic shared memory of the launch
+  int tok_cap;            // bf16 kernels: token rows per chunk, kTokMax or kTokMaxWide
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -93,6 +103,24 @@ struct Params {
 struct Tile {
   int e, slab, tok0, tok_end, n;
 };
+
+// Gathered B operand: lane l of the producer warp brings token rows
+// 4 l .. 4 l + 3 of the `cnt` rows from slot row0 on; their source rows.
+struct GatherRows {
+  int r[4];
+  bool on;  // this lane has rows to bring
+};
+
+__device__ __forceinline__ GatherRows gather_rows(const Params& p, int row0, int cnt, int lane) {
+  GatherRows g;
+  g.on = p.gather_perm != nullptr && 4 * lane < cnt;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pos = row0 + 4 * lane + i;
+    g.r[i] = g.on && pos < p.total_rows ? __ldg(p.gather_perm + pos) / p.gather_div : p.gather_oob;
+  }
+  return g;
+}
 
 __device__ __forceinline__ Tile decode_tile(int tau, int slabs, int groups, const int* s_off,
                                             const int* s_ct) {
@@ -129,9 +157,8 @@ struct TokenMapSet {
 // tokens each) and their exclusive prefix in s_ct, and the largest chunk half
 // of the launch in *s_half_max.  Inconsistent offsets give an empty schedule
 // and MOE_ERR_DEVICE_CHECK.
-template <int TOKCAP>
 __device__ __forceinline__ void build_schedule(const Params& p, int* s_off, int* s_ct,
-                                               int* s_half_max, int warp, int lane) {
+                                               int* s_half_max, int warp, int lane, int TOKCAP) {
   const int G = p.groups;
   for (int i = threadIdx.x; i <= G; i += blockDim.x)
     s_off[i] = p.offsets ? __ldg(p.offsets + i) : (i == 0 ? 0 : p.total_rows);
@@ -246,7 +273,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_ct[kMaxExperts + 1];
-  __shared__ alignas(8) uint64_t s_bar[2 * kMaxStages + 5];
+  __shared__ alignas(8) uint64_t s_bar[2 * kMaxStagesWide + 5];
   __shared__ int s_half_max;
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
@@ -260,13 +287,13 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t full_bar = smem_u32(&s_bar[0]);
-  const uint32_t empty_bar = smem_u32(&s_bar[kMaxStages]);
-  const uint32_t tfull_bar = smem_u32(&s_bar[2 * kMaxStages]);
-  const uint32_t tempty_bar = smem_u32(&s_bar[2 * kMaxStages + 2]);
-  const uint32_t drain_bar = smem_u32(&s_bar[2 * kMaxStages + 4]);
+  const uint32_t empty_bar = smem_u32(&s_bar[kMaxStagesWide]);
+  const uint32_t tfull_bar = smem_u32(&s_bar[2 * kMaxStagesWide]);
+  const uint32_t tempty_bar = smem_u32(&s_bar[2 * kMaxStagesWide + 2]);
+  const uint32_t drain_bar = smem_u32(&s_bar[2 * kMaxStagesWide + 4]);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kMaxStages; ++s) {
+    for (int s = 0; s < kMaxStagesWide; ++s) {
       mbar_init(full_bar + 8 * s, 1);  // leader: counts both CTAs' bytes; unused in the follower
       mbar_init(empty_bar + 8 * s, 1);
     }
@@ -289,7 +316,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   pdl_wait_and_release();
 
   const int G = p.groups;
-  build_schedule<kTokMax>(p, s_off, s_ct, &s_half_max, warp, lane);
+  build_schedule(p, s_off, s_ct, &s_half_max, warp, lane, p.tok_cap);
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised before any remote arrive
@@ -298,54 +325,83 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   const uint32_t tmem_base = s_tmem_base;
   const int total_tiles = s_ct[G] * p.slabs;
   const int num_kb = p.K / kBK;                   // 64-wide K boxes
-  const int num_ks = (num_kb + kSub - 1) / kSub;  // pipeline stages per tile
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
-  // Stage geometry: a stage holds kSub K boxes of the weights and of the
+  // Wide chunks (more than 256 tokens: launches with many rows per expert)
+  // hold twice the tokens per weight byte brought in: one accumulator set of
+  // up to 512 columns (no second one to overlap the epilogue), two MMAs per
+  // K step, one K box per stage so that enough stages fit.
+  const bool wide = s_half_max > kTokMax / 2;
+  const int nacc = wide ? 1 : 2;
+  const int ksub = wide ? 1 : kSub;
+  const int num_ks = (num_kb + ksub - 1) / ksub;  // pipeline stages per tile
+  // Stage geometry: a stage holds ksub K boxes of the weights and of the
   // largest token-chunk half of this launch, so smaller chunks leave room for
-  // a fourth stage.  Both CTAs of a pair derive the same layout.
+  // more stages.  Both CTAs of a pair derive the same layout.
   const uint32_t b_sub_bytes = static_cast<uint32_t>(s_half_max) * kBK * 2;
-  const uint32_t stage_bytes = kSub * (kABytes + b_sub_bytes);
+  const uint32_t stage_bytes = ksub * (kABytes + b_sub_bytes);
   const uint32_t avail = static_cast<uint32_t>(p.smem_bytes) - (base - smem_u32(smem_raw));
-  const int nst = min(kMaxStages, static_cast<int>(avail / stage_bytes));
+  const int nst = min(wide ? kMaxStagesWide : kMaxStages, static_cast<int>(avail / stage_bytes));
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer (both CTAs, own shared memory; the bytes
-      // of both are counted on the leader's full barrier, which the leader
-      // arms with the pair's total)
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      bool ok = true;
-      const uint32_t full_leader = mapa_shared(full_bar, 0);
-      for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
-        const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-        const int half = t.n / 2;  // 8, 16, ..., 128 token rows per CTA
-        const CUtensorMap* tmap_x = &tx.m[half / (kUnit / 2) - 1];
-        const uint32_t tx_bytes = kABytes + half * 128;  // per CTA
-        const int trow = t.tok0 + rank * half;
-        const int wrow = KIND == kGateUp ? t.slab * 128 + rank * 64
-                                         : t.e * p.w_rows_per_group + t.slab * 256 + rank * 128;
-        for (int ks = 0; ks < num_ks; ++ks) {
-          const int nsub = min(kSub, num_kb - ks * kSub);
-          if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
+    // ---------------- TMA producer (warp 0 of both CTAs, own shared memory;
+    // the bytes of both are counted on the leader's full barrier, which the
+    // leader arms with the pair's total).  Lane 0 waits, arms and loads the
+    // weights; the token rows come in one box per K box, or, gathered, four
+    // rows per lane.
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool ok = true;
+    const uint32_t full_leader = mapa_shared(full_bar, 0);
+    for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+      const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+      const int half = t.n / 2;  // token rows per CTA: 8, 16, ..., 256
+      // A chunk of n tokens is one MMA of n0 = min(n, 256) tokens and, wide,
+      // one of n1 = n - n0; each CTA holds its half of each: rows tok0 +
+      // rank n0/2 .. (n0/2 of them) and tok0 + n0 + rank n1/2 .. after them.
+      const int n0 = min(t.n, static_cast<int>(kAccCols)), n1 = t.n - n0;
+      const CUtensorMap* tmap_x0 = &tx.m[n0 / kUnit - 1];
+      const CUtensorMap* tmap_x1 = &tx.m[max(n1, kUnit) / kUnit - 1];
+      const uint32_t tx_bytes = kABytes + half * 128;  // per CTA
+      const int trow = t.tok0 + rank * half;  // gathered rows (never wide)
+      const int trow0 = t.tok0 + rank * (n0 / 2);
+      const int trow1 = t.tok0 + n0 + rank * (n1 / 2);
+      const int wrow = KIND == kGateUp ? t.slab * 128 + rank * 64
+                                       : t.e * p.w_rows_per_group + t.slab * 256 + rank * 128;
+      const GatherRows gr = gather_rows(p, trow, half, lane);
+      for (int ks = 0; ks < num_ks; ++ks) {
+        const int nsub = min(ksub, num_kb - ks * ksub);
+        const bool got = lane == 0 ? mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc) : true;
+        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        const uint32_t fb = full_leader + 8 * stage;
+        const uint32_t a_dst = base + stage * stage_bytes;
+        const uint32_t b_dst = a_dst + ksub * kABytes;
+        if (lane == 0) {
           if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * nsub * tx_bytes);
-          const uint32_t fb = full_leader + 8 * stage;
-          const uint32_t a_dst = base + stage * stage_bytes;
-          const uint32_t b_dst = a_dst + kSub * kABytes;
           for (int sub = 0; sub < nsub; ++sub) {
-            const int kx = (ks * kSub + sub) * kBK;
+            const int kx = (ks * ksub + sub) * kBK;
             // gate_up: one box holds 4 groups of {16 gate rows, the 16 matching up rows}
             if (KIND == kGateUp)
               tma_load_5d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, 0, 0, wrow / 16, t.e);
             else
               tma_load_2d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow);
-            tma_load_2d_pair(b_dst + sub * b_sub_bytes, tmap_x, fb, kx, trow);
+            if (p.gather_perm == nullptr) {
+              const uint32_t bs = b_dst + sub * b_sub_bytes;
+              tma_load_2d_pair(bs, tmap_x0, fb, kx, trow0);
+              if (n1 > 0) tma_load_2d_pair(bs + (n0 / 2) * 128, tmap_x1, fb, kx, trow1);
+            }
           }
-          ++issued;
-          if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
+        if (gr.on) {
+          for (int sub = 0; sub < nsub; ++sub)
+            tma_gather4_pair(b_dst + sub * b_sub_bytes + lane * 512, &tx.m[0], fb,
+                             (ks * ksub + sub) * kBK, gr.r[0], gr.r[1], gr.r[2], gr.r[3]);
+        }
+        ++issued;
+        if (++stage == nst) { stage = 0; phase ^= 1u; }
       }
+    }
+    if (lane == 0) {
       if (leader) {
         for (int i = max(0, issued - nst); i < issued; ++i)
           mbar_wait_drain(full_bar + 8 * (i % nst), (i / nst) & 1, p.status);
@@ -367,28 +423,43 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       bool ok = true;
       for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
         const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-        const uint32_t idesc = idesc_bf16_f32(256, t.n);
+        const int n0 = min(t.n, static_cast<int>(kAccCols)), n1 = t.n - n0;
+        const uint32_t idesc0 = idesc_bf16_f32(256, n0);
+        const uint32_t idesc1 = idesc_bf16_f32(256, max(n1, kUnit));
         if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * kAccCols;
+        const uint32_t d_tmem = tmem_base + acc * kAccCols;  // TMEM column c: chunk token c
         for (int ks = 0; ks < num_ks; ++ks) {
-          const int nsub = min(kSub, num_kb - ks * kSub);
+          const int nsub = min(ksub, num_kb - ks * ksub);
           if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
           const uint32_t a_addr = base + stage * stage_bytes;
-          const uint32_t b_addr = a_addr + kSub * kABytes;
-          for (int sub = 0; sub < nsub; ++sub) {
+          const uint32_t b_addr = a_addr + ksub * kABytes;
+          if (n1 == 0) {
+            for (int sub = 0; sub < nsub; ++sub) {
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + sub * kABytes + k * 32),
-                            smem_desc_sw128(b_addr + sub * b_sub_bytes + k * 32), idesc,
-                            (ks | sub | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < kBK / 16; ++k)
+                mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + sub * kABytes + k * 32),
+                              smem_desc_sw128(b_addr + sub * b_sub_bytes + k * 32), idesc0,
+                              (ks | sub | k) != 0 ? 1u : 0u);
+            }
+          } else {
+            for (int sub = 0; sub < nsub; ++sub) {
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k) {
+                const uint64_t ad = smem_desc_sw128(a_addr + sub * kABytes + k * 32);
+                const uint32_t bs = b_addr + sub * b_sub_bytes + k * 32;
+                const uint32_t accum = (ks | sub | k) != 0 ? 1u : 0u;
+                mma_bf16_pair(d_tmem, ad, smem_desc_sw128(bs), idesc0, accum);
+                mma_bf16_pair(d_tmem + n0, ad, smem_desc_sw128(bs + (n0 / 2) * 128), idesc1, accum);
+              }
+            }
           }
           mma_commit_pair(empty_bar + 8 * stage);  // frees this stage in both CTAs
           if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit_pair(tfull_bar + 8 * acc);     // accumulator ready in both CTAs
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
       }
       mma_commit_pair(drain_bar);
       mbar_wait_drain(drain_bar, 0, p.status);
@@ -416,7 +487,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
         if (leader) mbar_arrive(tempty_bar + 8 * acc);
         else mbar_arrive_cluster(tempty_leader + 8 * acc);
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -574,7 +645,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
   pdl_wait_and_release();
 
   const int G = p.groups;
-  build_schedule<kTokCap>(p, s_off, s_ct, &s_half_max, warp, lane);
+  build_schedule(p, s_off, s_ct, &s_half_max, warp, lane, kTokCap);
   tc_fence_before_sync();
   __syncthreads();
   if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
@@ -919,6 +990,21 @@ cudaError_t make_token_maps(TokenMapSet& mx, const void* a, int rows, int K) {
   return cudaSuccess;
 }
 
+// Gate_up's token operand: boxes over a [rows, K] matrix, or, gathering, a
+// one-row box over the unpermuted tokens in every slot; sets p's gather fields.
+cudaError_t make_gate_up_token_maps(TokenMapSet& mx, Params& p, const void* a, int rows, int K,
+                                    const TokenGather* g) {
+  p.gather_perm = nullptr;
+  if (!g) return make_token_maps(mx, a, rows, K);
+  const cudaError_t e = make_bf16_map(&mx.m[0], g->src, g->src_rows, K, 1);
+  if (e != cudaSuccess) return e;
+  for (int i = 1; i < kTokenMaps; ++i) mx.m[i] = mx.m[0];
+  p.gather_perm = g->perm;
+  p.gather_div = g->div;
+  p.gather_oob = g->src_rows;
+  return cudaSuccess;
+}
+
 cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int which,
                           const CUtensorMap& mw, const TokenMapSet& mx, Params p,
                           long long tiles_bound, int threads = kThreads) {
@@ -956,8 +1042,13 @@ cudaError_t launch_expert_1cta(cudaStream_t s, const char* name, ExpertKernel k,
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
                                void* h, float* y, unsigned* status,
-                               unsigned long long timeout_ns) {
+                               unsigned long long timeout_ns, const TokenGather* gather) {
   const int groups = offsets ? E : 1;
+  // Down launches with at least 256 rows per expert take wide chunks (up to
+  // 512 tokens).  Gate_up keeps chunks of at most 256 and its second
+  // accumulator: its SwiGLU epilogue is long enough that losing the overlap
+  // costs more than the wider tiles save (measured).
+  const int cap = rows < kWideRowsPerGroup * groups ? kTokMax : kTokMaxWide;
   const long long chunks_bound =
       offsets ? rows / kTokMax + std::min(E, rows) : (rows + kTokMax - 1) / kTokMax;
 
@@ -970,10 +1061,10 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   const uint64_t strides[4] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(I) * d * 2,
                                16ull * d * 2, 2ull * I * d * 2};
   const uint32_t box[5] = {64, 16, 2, 4, 1};
-  cudaError_t e = make_bf16_map_nd(&mw, w_gate_up, 5, dims, strides, box);
-  if (e == cudaSuccess) e = make_token_maps(mx, a, rows, d);
-  if (e != cudaSuccess) return e;
   Params p{};
+  cudaError_t e = make_bf16_map_nd(&mw, w_gate_up, 5, dims, strides, box);
+  if (e == cudaSuccess) e = make_gate_up_token_maps(mx, p, a, rows, d, gather);
+  if (e != cudaSuccess) return e;
   p.K = d;
   p.n_out = I;
   p.slabs = (I + 127) / 128;
@@ -986,6 +1077,7 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   p.ld_out = I;
   p.status = status;
   p.timeout_ns = timeout_ns;
+  p.tok_cap = kTokMax;
   e = launch_expert(s, offsets ? "moe_gate_up_swiglu" : "moe_shared_gate_up_swiglu",
                     moe_gate_up_swiglu_kernel, 0, mw, mx, p, chunks_bound * p.slabs);
   if (e != cudaSuccess) return e;
@@ -1008,6 +1100,7 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   q.ld_out = d;
   q.status = status;
   q.timeout_ns = timeout_ns;
+  q.tok_cap = cap;
   return launch_expert(s, offsets ? "moe_down" : "moe_shared_down", moe_down_kernel, 1, mw2, mx2,
                        q, chunks_bound * q.slabs);
 }
@@ -1032,10 +1125,10 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   const uint64_t strides[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(I) * d,
                                16ull * d, 2ull * I * d};
   const uint32_t box[5] = {kBK8, 16, 2, 4, 1};
+  Params p{};
   cudaError_t e = make_u8_map_nd(&mw, codes_gate_up, 5, dims, strides, box);
   if (e == cudaSuccess) e = make_token_maps(mx, a, rows, d);
   if (e != cudaSuccess) return e;
-  Params p{};
   p.K = d;
   p.n_out = I;
   p.slabs = one ? I / 64 : I / 128;

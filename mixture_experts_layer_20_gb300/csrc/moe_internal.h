@@ -113,14 +113,25 @@ cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, c
                           float* gates, float* partial, unsigned* status,
                           unsigned long long timeout_ns);
 
+// Gate_up's token rows taken straight from the unpermuted tokens: row pos of
+// the grouped operand is src[perm[pos] / div] (src: [src_rows, d] bf16).
+struct TokenGather {
+  const void* src;
+  const int32_t* perm;
+  int div;
+  int src_rows;
+};
+
 // Grouped SwiGLU FFN (moe_expert_gemm.cu).  Rows [offsets[e], offsets[e+1])
 // of a [rows, d] go through expert e (weights per expert: w_gate_up [2I, d],
 // w_down [d, I]).  offsets == nullptr: a single expert on all `rows` rows.
+// With `gather`, a is not read: gate_up gathers its rows (see TokenGather).
 // Writes h [rows, I] bf16 (scratch) and y [rows, d] fp32.
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
                                void* h, float* y, unsigned* status,
-                               unsigned long long timeout_ns);
+                               unsigned long long timeout_ns,
+                               const TokenGather* gather = nullptr);
 
 // The same with MXFP8 expert weights: E4M3 codes [E, 2I, d] / [E, d, I] and
 // E8M0 scales [d/128][E*2I][4] / [I/128][E*d][4]; d and I multiples of 128.
