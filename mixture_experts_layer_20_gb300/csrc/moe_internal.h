@@ -12,7 +12,8 @@ namespace moe {
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
-constexpr int kPermuteChunk = 4096;  // assignments per permute CTA
+constexpr int kPermuteChunk = 1024;     // assignments per count / scatter CTA
+constexpr int kPermuteSmallMax = 4096;  // up to this many, one CTA groups them all
 
 // The router's logits are computed in K ranges of 512 on the tensor cores
 // and summed in range order by the top-k kernel.  The number of ranges

@@ -2,18 +2,19 @@
 //
 // Grouping ('Chapter 9. Distributed inference', section 9.3.4: permute the
 // input rows by expert; section 9.4.1: the per-expert row counts m_j sum to
-// n k).  The flat assignment index f = t*k + j is cut into chunks of 4096:
+// n k).  The flat assignment index f = t*k + j is cut into chunks of 1024:
 //   count   : one CTA per chunk, shared-memory histogram -> chunk_table[c][e]
 //   scatter : one CTA per chunk.  Each CTA scans the chunk table itself:
 //             expert totals (counts[e]), their exclusive scan (offsets[e]),
 //             and its chunk's base per expert = offsets[e] + rows of expert e
 //             in earlier chunks.  Each warp owns 256 consecutive assignments;
 //             warp histograms (match.any) -> per-warp bases -> each lane's
-//             rank among earlier equal ids in its warp.  Positions are thus
+//             rank among earlier equal ids in its warp.  Small chunks give
+//             the grouping of a prefill batch (48k assignments) ~50 CTAs.  Positions are thus
 //             offsets[e] + (number of earlier f with the same e): a stable
 //             counting sort, deterministic with no global atomics.
 //   gather  : x_perm[p] = x[perm[p] / k], one warp per row, 16-byte copies.
-// When all assignments fit one chunk, one CTA does count, scan and scatter.
+// Up to 4096 assignments, one CTA does count, scan and scatter.
 //
 // Combine ('Chapter 9. Distributed inference', section 9.3.4, step four;
 // 'Hosting Qwen on Blackwell', "MoE Dispatch - Combine": weighted
@@ -29,7 +30,7 @@ namespace moe {
 namespace {
 
 constexpr int kScatterWarps = 16;
-constexpr int kPerWarp = kPermuteChunk / kScatterWarps;  // 256
+constexpr int kPerWarp = kPermuteChunk / kScatterWarps;  // 64
 
 __global__ void __launch_bounds__(512) moe_permute_count_kernel(const int32_t* __restrict__ ids, int n,
                                                             int E, int32_t* __restrict__ table,
@@ -335,7 +336,7 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
   const int n = T * top_k;
   const int nchunks = (n + kPermuteChunk - 1) / kPermuteChunk;
   cudaError_t e = cudaSuccess;
-  if (n <= kPermuteChunk) {
+  if (n <= kPermuteSmallMax) {
     KernelScope scope(s, "moe_permute_small");
     e = launch_kernel(moe_permute_small_kernel<kScatterWarps>, dim3(1), dim3(kScatterWarps * 32),
                       0, s, ids, n, E, counts, offsets, perm, slot_pos, status);

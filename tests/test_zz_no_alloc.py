@@ -68,8 +68,8 @@ def test_static_scratch_without_status_word(moe):
 
 
 def test_static_scratch_rejects_sizes_beyond_its_table(moe):
-    # ceil(T*k/4096) * E = 257 * 256 > 65536 table entries; nothing is launched
-    T, k, E = 4096 * 257 // 8, 8, 256
+    # ceil(T*k/1024) * E = 257 * 256 > 65536 table entries; nothing is launched
+    T, k, E = 1024 * 257 // 8, 8, 256
     ids = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
     st = moe._lib.moe_permute_static_scratch(
         ctypes.c_void_p(ids.data_ptr()), None, T, 64, E, k, ctypes.c_void_p(ids.data_ptr()),
