@@ -393,22 +393,6 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
 
 // Arrive once on the mbarrier at shared offset `bar` in both CTAs of the pair
 // when all tcgen05 operations issued so far by this thread have completed.
-// As mma_bf16_pair, with A read from tensor memory: each CTA's 128 A rows in
-// TMEM lanes 0..127, K along the columns (two bf16 per 32-bit column) from
-// a_tmem on, at the same address in both CTAs.
-__device__ __forceinline__ void mma_bf16_pair_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
-                                                     uint64_t b_desc, uint32_t idesc,
-                                                     uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"

@@ -503,35 +503,37 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 
 // ---------------------------------------------------------------- MXFP8 weights
 //
-// The same tiles with the weights stored as MXFP8 ('Hosting Qwen on
+// The expert GEMMs with the weights stored as MXFP8 ('Hosting Qwen on
 // Blackwell', "Quantization"): E4M3 codes and one E8M0 scale per 32 values
-// along K (moe_mxfp8.cu).  Per 128-wide K stage each CTA's TMA brings its 128
-// weight rows of codes (16 KB, on the CTA's own barrier) and their scales
-// (512 B), and the pair's tokens as before (on the leader's barrier).
+// along K (moe_mxfp8.cu).  One CTA per tile: 128 weight rows (gate_up: 64
+// gate rows interleaved with the 64 matching up rows) and a chunk of up to
+// 128 tokens.  Per 128-wide K stage the TMA brings the tile's codes (16 KB)
+// and a bulk copy their scales (512 B) on one barrier, the tokens on another.
 // Converter warps turn each code into code x 2^(scale - 127) in bf16 --
 // exact, a code has four significant bits -- and store the rows into tensor
-// memory; the leader's MMAs read A from there (tcgen05.mma ... [a_tmem]) and
-// B (tokens) from shared memory.  Tensor memory holds two
-// accumulators sized for the launch's largest token chunk (at most 192
-// columns, so chunks are capped at 192 here) and as many A buffers of 64
-// columns (128 K of bf16) as fit beside them, up to 4: the converters run
-// that many stages ahead of the MMAs.  Half the weight bytes of the bf16
-// kernel cross HBM and shared memory.
+// memory; the MMAs read A from there (tcgen05.mma ... [a_tmem]) and B
+// (tokens) from shared memory.  Tensor memory holds two accumulators sized
+// for the launch's largest chunk and as many A buffers of 64 columns (128 K
+// of bf16) as fit beside them, up to 4: the converters run that many stages
+// ahead of the MMAs.  Half the weight bytes of the bf16 kernel cross HBM and
+// shared memory.
+//
+// Measured (Qwen3 layer): CTA pairs, whose converters in both CTAs must
+// arrive on the leader's barrier before each stage's MMAs, ran prefill at
+// 2.92 ms against 2.47 ms for one-CTA tiles; and the converters share the
+// sub-partitions' issue slots with the MMA issuer, so four converter warps
+// (one per TMEM lane quarter, all four scale blocks of a row each) beat 8 and
+// 16 (decode 0.654 / 0.668 / 0.709 ms).
 
-constexpr int kTokMax8 = 192;
 constexpr int kBK8 = 128;                            // K per stage: one 128-byte row of codes
 constexpr int kABufCols = kBK8 / 2;                  // TMEM columns of one A buffer (bf16 pairs)
 constexpr int kMaxABufs = 4;
 constexpr int kA8Bytes = kWRows * kBK8;              // codes per CTA per stage
 constexpr int kScaleBytes = kWRows * 4;              // four E8M0 scales per row per stage
 constexpr int kConvWarp0 = 6;
-// Converter warps: 16 in a CTA pair (four per TMEM lane quarter, one scale
-// block each), 8 alone (two per quarter, two blocks each).  Measured: with few
-// tokens the one-CTA tile's MMAs share the issue slots of the converters'
-// sub-partitions and 8 warps leave them more; with a CTA pair's large chunks
-// conversion is the longer side and 16 warps shorten it.
-__host__ __device__ constexpr int conv_warps(bool pair) { return pair ? 16 : 8; }
-__host__ __device__ constexpr int threads8(bool pair) { return (kConvWarp0 + conv_warps(pair)) * 32; }
+constexpr int kConvWarps = 4;                        // one per TMEM lane quarter
+constexpr int kBlkPerWarp = 16 / kConvWarps;         // 32-value scale blocks per warp per stage
+constexpr int kThreads8 = (kConvWarp0 + kConvWarps) * 32;
 constexpr int kMaxStages8 = 8;
 
 // 2^(byte - 127) as a float (byte 0: 2^-127, a subnormal).
@@ -577,15 +579,12 @@ __device__ __forceinline__ void e4m3x8_to_bf16(uint32_t lo, uint32_t hi, float s
   }
 }
 
-template <int KIND, bool PAIR>
+template <int KIND>
 __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
                                                      const TokenMapSet& tx, const Params& p) {
-  // one CTA's tile: 128 weight rows; a pair's tile spans two CTAs' rows
-  constexpr int kSlabH = PAIR ? 128 : 64;     // gate_up: h columns per tile
-  constexpr int kSlabRows = PAIR ? 256 : 128;  // down: y columns per tile
-  constexpr int kTokCap = PAIR ? kTokMax8 : kTokMax / 2;
-  constexpr int kConvWarps = conv_warps(PAIR);
-  constexpr int kBlkPerWarp = 16 / kConvWarps;  // 32-value scale blocks per warp per stage
+  // one CTA's tile: 128 weight rows and a chunk of up to 128 tokens
+  constexpr int kSlabH = 64;     // gate_up: h columns per tile (64 gate + 64 up rows)
+  constexpr int kSlabRows = 128;  // down: y columns per tile
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_ct[kMaxExperts + 1];
@@ -596,16 +595,12 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const bool leader = rank == 0;
-  const int pair = PAIR ? blockIdx.x >> 1 : blockIdx.x;
-  const int num_pairs = PAIR ? gridDim.x >> 1 : gridDim.x;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t a_full = smem_u32(&s_bar[0]);                    // own codes + scales landed
-  const uint32_t b_full = smem_u32(&s_bar[kMaxStages8]);          // leader: both CTAs' tokens
+  const uint32_t b_full = smem_u32(&s_bar[kMaxStages8]);          // tokens landed
   const uint32_t st_empty = smem_u32(&s_bar[2 * kMaxStages8]);    // stage consumed
-  const uint32_t conv_full = smem_u32(&s_bar[3 * kMaxStages8]);   // leader: A buffer converted
+  const uint32_t conv_full = smem_u32(&s_bar[3 * kMaxStages8]);   // A buffer converted
   const uint32_t conv_empty = conv_full + 8 * kMaxABufs;          // A buffer read by the MMAs
   const uint32_t tfull_bar = conv_empty + 8 * kMaxABufs;
   const uint32_t tempty_bar = tfull_bar + 16;
@@ -615,15 +610,15 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
     for (int s = 0; s < kMaxStages8; ++s) {
       mbar_init(a_full + 8 * s, 1);
       mbar_init(b_full + 8 * s, 1);
-      mbar_init(st_empty + 8 * s, 1 + kConvWarps);  // the MMA commit + this CTA's converters
+      mbar_init(st_empty + 8 * s, 1 + kConvWarps);  // the MMA commit + the converters
     }
     for (int b = 0; b < kMaxABufs; ++b) {
-      mbar_init(conv_full + 8 * b, (PAIR ? 2 : 1) * kConvWarps);  // the converters of the CTA(s)
+      mbar_init(conv_full + 8 * b, kConvWarps);
       mbar_init(conv_empty + 8 * b, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar + 8 * b, 1);
-      mbar_init(tempty_bar + 8 * b, PAIR ? kEpiArrivals : kEpiArrivals / 2);
+      mbar_init(tempty_bar + 8 * b, 4);  // the epilogue warps
     }
     mbar_init(drain_bar, 1);
     s_abort = 0;
@@ -633,33 +628,26 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
     for (int i = 0; i < kTokenMaps; ++i) tma_prefetch_desc(&tx.m[i]);
   }
   if (warp == 1) {
-    if constexpr (PAIR) {
-      tmem_alloc_pair(smem_u32(&s_tmem_base), kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_u32(&s_tmem_base), kTmemCols);
-      tmem_relinquish();
-    }
+    tmem_alloc(smem_u32(&s_tmem_base), kTmemCols);
+    tmem_relinquish();
   }
 
   pdl_wait_and_release();
 
   const int G = p.groups;
-  build_schedule(p, s_off, s_ct, &s_half_max, warp, lane, kTokCap);
+  build_schedule(p, s_off, s_ct, &s_half_max, warp, lane, kTokMax / 2);
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
   tc_fence_after_sync();
 
   const uint32_t tmem_base = s_tmem_base;
   const int total_tiles = s_ct[G] * p.slabs;
   const int num_ks = p.K / kBK8;  // K is a multiple of 128
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
-  // token rows this CTA holds per K box: half the largest chunk in a pair, all of it alone
-  const uint32_t b_sub_bytes = static_cast<uint32_t>((PAIR ? 1 : 2) * s_half_max) * kBK * 2;
+  // token rows per K box: the launch's largest chunk (twice its largest half)
+  const uint32_t b_sub_bytes = static_cast<uint32_t>(2 * s_half_max) * kBK * 2;
   const uint32_t stage_bytes = (kA8Bytes + kSub * b_sub_bytes + kScaleBytes + 1023u) & ~1023u;
   const uint32_t avail = static_cast<uint32_t>(p.smem_bytes) - (base - smem_u32(smem_raw));
-  // s_half_max: half the largest chunk (a pair CTA's share); accumulators hold the whole chunk
   const uint32_t acc_cols = static_cast<uint32_t>(2 * s_half_max);
   const int nst = min(kMaxStages8, static_cast<int>(avail / stage_bytes));
   // tensor memory: accumulators [0, acc_cols), [acc_cols, 2 acc_cols); A buffers after them
@@ -673,21 +661,18 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      const uint32_t b_leader = PAIR ? mapa_shared(b_full, 0) : b_full;
-      for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+      for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
         const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-        const int half = PAIR ? t.n / 2 : t.n;  // token rows this CTA loads
-        const CUtensorMap* tmap_x = &tx.m[half / (kUnit / 2) - 1];
-        const int trow = t.tok0 + static_cast<int>(rank) * half;
+        const CUtensorMap* tmap_x = &tx.m[t.n / (kUnit / 2) - 1];  // t.n <= 128 rows
         // this CTA's weight rows, and how many of them exist (the last slab may be ragged)
         int row0, row1 = 0, nrow;
         if (KIND == kGateUp) {
-          const int g0 = t.slab * kSlabH + static_cast<int>(rank) * 64;
+          const int g0 = t.slab * kSlabH;
           nrow = max(0, min(64, p.n_out - g0));
           row0 = t.e * p.w_rows_per_group + g0;
           row1 = row0 + p.up_offset;
         } else {
-          const int r0 = t.slab * kSlabRows + static_cast<int>(rank) * 128;
+          const int r0 = t.slab * kSlabRows;
           nrow = max(0, min(128, p.n_out - r0));
           row0 = t.e * p.w_rows_per_group + r0;
         }
@@ -710,40 +695,28 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
             if (KIND == kGateUp)
               bulk_load(s_dst + 256, sc + static_cast<size_t>(row1) * 4, nrow * 4, af);
           }
-          if (leader)
-            mbar_arrive_expect_tx(b_full + 8 * stage, (PAIR ? 2 : 1) * kSub * half * kBK * 2);
-          const uint32_t bf = b_leader + 8 * stage;
-          for (int sub = 0; sub < kSub; ++sub) {
-            if constexpr (PAIR)
-              tma_load_2d_pair(b_dst + sub * b_sub_bytes, tmap_x, bf, kx + sub * kBK, trow);
-            else
-              tma_load_2d(b_dst + sub * b_sub_bytes, tmap_x, b_full + 8 * stage, kx + sub * kBK,
-                          trow);
-          }
+          mbar_arrive_expect_tx(b_full + 8 * stage, kSub * t.n * kBK * 2);
+          for (int sub = 0; sub < kSub; ++sub)
+            tma_load_2d(b_dst + sub * b_sub_bytes, tmap_x, b_full + 8 * stage, kx + sub * kBK,
+                        t.tok0);
           ++issued;
           if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
       }
       for (int i = max(0, issued - nst); i < issued; ++i) {
         mbar_wait_drain(a_full + 8 * (i % nst), (i / nst) & 1, p.status);
-        if (leader) mbar_wait_drain(b_full + 8 * (i % nst), (i / nst) & 1, p.status);
-      }
-      if (PAIR && !leader && !ok) {
-        // the follower's token copies count on the leader's barrier
-        const unsigned long long t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 50000ull) {
-        }
+        mbar_wait_drain(b_full + 8 * (i % nst), (i / nst) & 1, p.status);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ---------------- MMA issuer (leader)
+    if (lane == 0) {
+      // ---------------- MMA issuer
       int stage = 0, cb = 0, acc = 0;
       uint32_t phase = 0, cphase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+      for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
         const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-        const uint32_t idesc = idesc_bf16_f32(PAIR ? 256 : 128, t.n);
+        const uint32_t idesc = idesc_bf16_f32(128, t.n);
         if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * acc_cols;
@@ -756,49 +729,35 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
 #pragma unroll
           for (int k = 0; k < kBK8 / 16; ++k) {
             const uint64_t bd = smem_desc_sw128(b_addr + (k >> 2) * b_sub_bytes + (k & 3) * 32);
-            if constexpr (PAIR)
-              mma_bf16_pair_tmem_a(d_tmem, a_tmem + k * 8, bd, idesc, (ks | k) != 0 ? 1u : 0u);
-            else
-              mma_bf16_tmem_a(d_tmem, a_tmem + k * 8, bd, idesc, (ks | k) != 0 ? 1u : 0u);
+            mma_bf16_tmem_a(d_tmem, a_tmem + k * 8, bd, idesc, (ks | k) != 0 ? 1u : 0u);
           }
-          if constexpr (PAIR) {
-            mma_commit_pair(st_empty + 8 * stage);  // the tokens of this stage, both CTAs
-            mma_commit_pair(conv_empty + 8 * cb);   // the A buffer, both CTAs
-          } else {
-            mma_commit(st_empty + 8 * stage);
-            mma_commit(conv_empty + 8 * cb);
-          }
+          mma_commit(st_empty + 8 * stage);  // the tokens of this stage
+          mma_commit(conv_empty + 8 * cb);   // the A buffer
           if (++stage == nst) { stage = 0; phase ^= 1u; }
           if (++cb == nbuf) { cb = 0; cphase ^= 1u; }
         }
         if (!ok) break;
-        if constexpr (PAIR) mma_commit_pair(tfull_bar + 8 * acc);
-        else mma_commit(tfull_bar + 8 * acc);
+        mma_commit(tfull_bar + 8 * acc);
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
-      if constexpr (PAIR) mma_commit_pair(drain_bar);
-      else mma_commit(drain_bar);
-      mbar_wait_drain(drain_bar, 0, p.status);
-    } else if (PAIR && lane == 0) {
+      mma_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0, p.status);
     }
   } else if (warp < kConvWarp0) {
     // ---------------- epilogue: warps 2..5
     const int q = warp & 3;
-    const uint32_t tempty_leader = mapa_shared(tempty_bar, 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tau = pair; tau < total_tiles; tau += num_pairs) {
+    for (int tau = blockIdx.x; tau < total_tiles; tau += gridDim.x) {
       const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
       const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
-      epilogue_tile<KIND, KIND == kGateUp ? kSlabH : kSlabRows>(t, t_row, live, p, q, lane, rank);
+      epilogue_tile<KIND, KIND == kGateUp ? kSlabH : kSlabRows>(t, t_row, live, p, q, lane, 0u);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        if (leader) mbar_arrive(tempty_bar + 8 * acc);
-        else mbar_arrive_cluster(tempty_leader + 8 * acc);
+        mbar_arrive(tempty_bar + 8 * acc);
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
@@ -810,19 +769,18 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
     const int q = warp & 3;
     const int kq = (warp - kConvWarp0) >> 2;
     const int r = q * 32 + lane;
-    const uint32_t conv_leader = mapa_shared(conv_full, 0);
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf0;
     int stage = 0, cb = 0;
     uint32_t phase = 0, cphase = 0;
     bool ok = true;
-    for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
+    for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
       const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
       int col, srow;
       if (KIND == kGateUp) {
-        col = t.slab * kSlabH + static_cast<int>(rank) * 64 + q * 16 + (lane & 15);
+        col = t.slab * kSlabH + q * 16 + (lane & 15);
         srow = lane < 16 ? q * 16 + lane : 64 + q * 16 + (lane - 16);
       } else {
-        col = t.slab * kSlabRows + static_cast<int>(rank) * 128 + r;
+        col = t.slab * kSlabRows + r;
         srow = r;
       }
       const bool row_ok = col < p.n_out;
@@ -835,6 +793,20 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
         uint32_t sc = 0;
         if (row_ok) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc) : "r"(s_src + srow * 4));
         const uint32_t t_buf = t_lane + cb * kABufCols;
+        // every code load of this warp's blocks first (two 16-byte chunks of
+        // the 128-byte row per block), then the conversions and TMEM stores:
+        // one shared-memory round trip per stage
+        uint32_t wv[kBlkPerWarp][8];
+#pragma unroll
+        for (int bi = 0; bi < kBlkPerWarp; ++bi)
+#pragma unroll
+          for (int hch = 0; hch < 2; ++hch) {
+            const int chunk = (kq * kBlkPerWarp + bi) * 2 + hch;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(wv[bi][4 * hch]), "=r"(wv[bi][4 * hch + 1]),
+                           "=r"(wv[bi][4 * hch + 2]), "=r"(wv[bi][4 * hch + 3])
+                         : "r"(a_src + r * 128 + ((chunk ^ (r & 7)) << 4)));
+          }
 #pragma unroll
         for (int bi = 0; bi < kBlkPerWarp; ++bi) {
           const int blk = kq * kBlkPerWarp + bi;  // 32 K values: one scale, 16 TMEM columns
@@ -845,22 +817,13 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
           const __nv_bfloat162 mul = *reinterpret_cast<const __nv_bfloat162*>(&mbits);
           const float scale = e8m0_to_float(sbyte);
           uint32_t out[16];
+          if (fast) {
 #pragma unroll
-          for (int hch = 0; hch < 2; ++hch) {
-            const int chunk = blk * 2 + hch;  // 16-byte chunk of the 128-byte row
-            uint32_t w0, w1, w2, w3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                         : "r"(a_src + r * 128 + ((chunk ^ (r & 7)) << 4)));
-            if (fast) {
-              e4m3x4_to_bf16_bits(w0, mul, out + hch * 8);
-              e4m3x4_to_bf16_bits(w1, mul, out + hch * 8 + 2);
-              e4m3x4_to_bf16_bits(w2, mul, out + hch * 8 + 4);
-              e4m3x4_to_bf16_bits(w3, mul, out + hch * 8 + 6);
-            } else {
-              e4m3x8_to_bf16(w0, w1, scale, out + hch * 8);
-              e4m3x8_to_bf16(w2, w3, scale, out + hch * 8 + 4);
-            }
+            for (int i = 0; i < 8; ++i) e4m3x4_to_bf16_bits(wv[bi][i], mul, out + 2 * i);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              e4m3x8_to_bf16(wv[bi][2 * i], wv[bi][2 * i + 1], scale, out + 4 * i);
           }
           if (!row_ok) {
 #pragma unroll
@@ -874,8 +837,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
-          if (leader) mbar_arrive(conv_full + 8 * cb);
-          else mbar_arrive_cluster(conv_leader + 8 * cb);
+          mbar_arrive(conv_full + 8 * cb);
         }
         if (++stage == nst) { stage = 0; phase ^= 1u; }
         if (++cb == nbuf) { cb = 0; cphase ^= 1u; }
@@ -885,39 +847,23 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
 
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
-    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
-    else tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads8(true), 1)
+__global__ void __launch_bounds__(kThreads8, 1)
     moe_gate_up_swiglu_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                     const __grid_constant__ TokenMapSet tx, const Params p) {
-  expert_gemm_fp8_body<kGateUp, true>(tmap_w, tx, p);
+  expert_gemm_fp8_body<kGateUp>(tmap_w, tx, p);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads8(true), 1)
+__global__ void __launch_bounds__(kThreads8, 1)
     moe_down_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
                           const __grid_constant__ TokenMapSet tx, const Params p) {
-  expert_gemm_fp8_body<kDown, true>(tmap_w, tx, p);
-}
-
-// One CTA per tile (M = 128 weight rows, the whole token chunk, chunks of at
-// most 128): no signal crosses SMs, which suits few tokens per expert.
-__global__ void __launch_bounds__(threads8(false), 1)
-    moe_gate_up_swiglu_mxfp8_1cta_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                                         const __grid_constant__ TokenMapSet tx, const Params p) {
-  expert_gemm_fp8_body<kGateUp, false>(tmap_w, tx, p);
-}
-
-__global__ void __launch_bounds__(threads8(false), 1)
-    moe_down_mxfp8_1cta_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                               const __grid_constant__ TokenMapSet tx, const Params p) {
-  expert_gemm_fp8_body<kDown, false>(tmap_w, tx, p);
+  expert_gemm_fp8_body<kDown>(tmap_w, tx, p);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -939,7 +885,7 @@ typedef void (*ExpertKernel)(const CUtensorMap, const TokenMapSet, const Params)
 // Set as the kernel's limit on first use per device; 0 on failure.
 int ensure_smem_attr(ExpertKernel k, int which) {
   static std::mutex mu;
-  static int bytes[6][64] = {};
+  static int bytes[4][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
@@ -1033,7 +979,7 @@ cudaError_t launch_expert_1cta(cudaStream_t s, const char* name, ExpertKernel k,
   p.smem_bytes = smem;
   const long long grid = std::max(1LL, std::min<long long>(device_sm_count(), tiles_bound));
   KernelScope scope(s, name);
-  return launch_kernel(k, dim3(static_cast<unsigned>(grid)), dim3(threads8(false)),
+  return launch_kernel(k, dim3(static_cast<unsigned>(grid)), dim3(kThreads8),
                        static_cast<size_t>(smem), s, mw, mx, p);
 }
 
@@ -1110,11 +1056,8 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
                                      const uint8_t* scales_gate_up, const uint8_t* codes_down,
                                      const uint8_t* scales_down, void* h, float* y,
                                      unsigned* status, unsigned long long timeout_ns) {
-  // Few rows per expert (decode): one CTA per tile, nothing signalled across SMs.
-  // Many: CTA pairs, which halve each SM's share of the tokens.
-  const bool one = rows <= 128LL * E;
-  const int cap = one ? kTokMax / 2 : kTokMax8;
-  const long long chunks_bound = rows / cap + std::min(E, rows);
+  // one CTA per tile, chunks of at most 128 tokens
+  const long long chunks_bound = rows / (kTokMax / 2) + std::min(E, rows);
 
   // codes of W_gate_up [E][2][I][d] viewed as (d, 16 rows, gate|up, I/16 row groups, E): one
   // box = 128 K of 4 row groups, each 16 gate rows followed by the 16 matching up rows
@@ -1131,7 +1074,7 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   if (e != cudaSuccess) return e;
   p.K = d;
   p.n_out = I;
-  p.slabs = one ? I / 64 : I / 128;
+  p.slabs = I / 64;
   p.groups = E;
   p.offsets = offsets;
   p.total_rows = rows;
@@ -1143,10 +1086,8 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   p.scale_rows = 2LL * I * E;
   p.status = status;
   p.timeout_ns = timeout_ns;
-  e = one ? launch_expert_1cta(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_1cta_kernel,
-                               4, mw, mx, p, chunks_bound * p.slabs)
-          : launch_expert(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_kernel, 2, mw, mx,
-                          p, chunks_bound * p.slabs, threads8(true));
+  e = launch_expert_1cta(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_kernel, 2, mw,
+                         mx, p, chunks_bound * p.slabs);
   if (e != cudaSuccess) return e;
 
   CUtensorMap mw2;
@@ -1160,7 +1101,7 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   Params q{};
   q.K = I;
   q.n_out = d;
-  q.slabs = one ? (d + 127) / 128 : (d + 255) / 256;
+  q.slabs = (d + 127) / 128;
   q.groups = E;
   q.offsets = offsets;
   q.total_rows = rows;
@@ -1171,10 +1112,8 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   q.scale_rows = static_cast<long long>(E) * d;
   q.status = status;
   q.timeout_ns = timeout_ns;
-  return one ? launch_expert_1cta(s, "moe_down_mxfp8", moe_down_mxfp8_1cta_kernel, 5, mw2, mx2, q,
-                                  chunks_bound * q.slabs)
-             : launch_expert(s, "moe_down_mxfp8", moe_down_mxfp8_kernel, 3, mw2, mx2, q,
-                             chunks_bound * q.slabs, threads8(true));
+  return launch_expert_1cta(s, "moe_down_mxfp8", moe_down_mxfp8_kernel, 3, mw2, mx2, q,
+                            chunks_bound * q.slabs);
 }
 
 }  // namespace moe

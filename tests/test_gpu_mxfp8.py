@@ -58,7 +58,7 @@ def _dequantised_bits(w):
 FORWARD_CASES = [
     # T, d, E, k, I, I_shared, zipf
     (64, 512, 32, 8, 256, 0, False),     # decode-like: a few rows per expert, 16-row chunks
-    (600, 512, 8, 4, 384, 0, False),     # ~300 rows per expert: two chunks, three slabs
+    (600, 512, 8, 4, 384, 0, False),     # ~300 rows per expert: three chunks, six slabs
     (200, 384, 16, 4, 128, 0, True),     # d = 384: the last down slab has one populated half
     (130, 768, 64, 8, 256, 128, True),   # bias and a (bf16) shared expert
 ]
