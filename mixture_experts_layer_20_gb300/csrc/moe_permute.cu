@@ -236,7 +236,10 @@ __global__ void __launch_bounds__(WARPS * 32)
 }
 
 // One warp copies one row: each lane issues all of its 16-byte loads of the
-// row (up to kGatherVec) before the stores, so a row is one round trip.
+// row (up to kGatherVec) before the stores, so a row is one round trip.  The
+// stores are marked streaming (evict first): measured on the prefill layer,
+// gather 88 -> 83 us and the layer 6 us faster although gate_up, which reads
+// x_perm next, finds less of it in L2.
 constexpr int kGatherVec = 16;  // uint4 per lane: rows of up to 32 * 16 * 8 = 4096 bf16
 
 __global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* __restrict__ perm,
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* 
 #pragma unroll
       for (int i = 0; i < kGatherVec; ++i) {
         const int v = v0 + lane + 32 * i;
-        if (v < vec_per_row) dst[v] = r[i];
+        if (v < vec_per_row) __stcs(dst + v, r[i]);  // streaming: x_perm exceeds L2
       }
     }
   }
