@@ -40,6 +40,20 @@ What the layer computes, and where each step comes from:
   clamped to E4M3's largest finite value.  A layer with MXFP8 weights is the
   layer computed with the dequantised weights (codes times scales), which the
   oracle obtains with mxfp8_quantize / mxfp8_dequantize.
+* NVFP4 expert weights ('PagedAttention, speculative decoding, MoE and
+  Blackwell', section 3: two-level micro-scaling, blocks of 16 values each
+  with its own FP8 scale, plus one FP32 scale for the whole tensor; 'Hosting
+  Qwen on Blackwell', "Quantization", names the format as considered).  The
+  elements are FP4 E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their
+  negatives).  The pages give no rule for choosing the scales; the oracle
+  takes the plainest one that uses both ranges fully: the tensor scale maps
+  the tensor's largest magnitude to 448 x 6 (the largest E4M3 scale times
+  the largest element), each block's scale is its largest magnitude / 6 in
+  units of the tensor scale, rounded to E4M3, and each element is the value
+  divided by (block scale x tensor scale) rounded to nearest-even E2M1,
+  saturating at 6.  These steps are taken in fp32 (IEEE, round to nearest) in
+  the order written, so that a GPU kernel doing the same operations produces
+  the same codes; the tensor is one expert's matrix.
 * Router bias.  A per-expert bias is added to the logits; by default it takes
   part in both the selection and the gates.  The variant the same section
   names for balancing (DeepSeek's bias adjustment) uses the bias only to pick
@@ -78,6 +92,10 @@ __all__ = [
     "round_to_e4m3",
     "mxfp8_quantize",
     "mxfp8_dequantize",
+    "e2m1_values",
+    "round_to_e2m1",
+    "nvfp4_quantize",
+    "nvfp4_dequantize",
 ]
 
 
@@ -244,6 +262,75 @@ def mxfp8_dequantize(codes, scales) -> np.ndarray:
     vals = e4m3_values()[codes].reshape(*codes.shape[:-1], K // MX_BLOCK, MX_BLOCK)
     x = 2.0 ** (np.asarray(scales, dtype=np.float64) - 127)
     return (vals * x[..., None]).reshape(codes.shape)
+
+
+E2M1_MAX = 6.0          # the largest E2M1 value
+NV_BLOCK = 16           # values that share one E4M3 scale
+NV_TENSOR_DIV = np.float32(E4M3_MAX * E2M1_MAX)   # 2688: tensor scale = amax / 2688
+
+
+def e2m1_values() -> np.ndarray:
+    """fp64 value of each of the 16 E2M1 codes (bit 3 sign, bits 2-1 the
+    exponent with bias 1, bit 0 the mantissa; exponent 0 is subnormal: m x 0.5)."""
+    vals = np.empty(16, dtype=np.float64)
+    for c in range(16):
+        sign = -1.0 if c & 0x8 else 1.0
+        e = (c >> 1) & 0x3
+        m = c & 0x1
+        vals[c] = sign * (m * 0.5 if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1))
+    return vals
+
+
+def round_to_e2m1(v) -> np.ndarray:
+    """Codes of the E2M1 values nearest to v (ties to the even code, i.e. the
+    one whose mantissa bit is 0), magnitudes above 6 saturating to 6; -0
+    encodes as +0."""
+    v = np.asarray(v, dtype=np.float64)
+    grid = e2m1_values()[:8]                        # 0, 0.5, 1, 1.5, 2, 3, 4, 6
+    a = np.minimum(np.abs(v), E2M1_MAX)
+    d = np.abs(a[..., None] - grid)                 # distance to every magnitude
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best                                # one, or two on a tie
+    even = cand & (np.arange(8) % 2 == 0)
+    mag = np.where(even.any(axis=-1), even.argmax(axis=-1), cand.argmax(axis=-1))
+    return np.where((v < 0) & (mag > 0), mag | 0x8, mag).astype(np.uint8)
+
+
+def nvfp4_quantize(w):
+    """Quantise one matrix (fp32-representable values, last axis a multiple
+    of 16 along the reduction dimension) to NVFP4.
+
+    Returns (codes uint8 [..., K] one E2M1 code per value, scales uint8
+    [..., K/16] E4M3 codes, tensor scale as np.float32).  All arithmetic is
+    fp32 with round to nearest: g = amax / 2688 (1 for an all-zero matrix);
+    per block s = round_to_e4m3((amax_block / 6) / g); each element
+    round_to_e2m1(w / (s * g)), or code 0 where s * g is 0."""
+    w = np.asarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    if K % NV_BLOCK:
+        raise ValueError("the quantised axis must be a multiple of 16")
+    amax_t = np.float32(np.abs(w).max()) if w.size else np.float32(0)
+    g = amax_t / NV_TENSOR_DIV if amax_t > 0 else np.float32(1)
+    blocks = w.reshape(*w.shape[:-1], K // NV_BLOCK, NV_BLOCK)
+    amax_b = np.abs(blocks).max(axis=-1).astype(np.float32)
+    s = (amax_b / np.float32(E2M1_MAX)) / g                          # fp32, in this order
+    s_q = round_to_e4m3(s.astype(np.float64)).astype(np.float32)      # exact in fp32
+    positive = e4m3_values()[:0x7F]
+    scale_codes = np.searchsorted(positive, s_q.astype(np.float64)).astype(np.uint8)
+    denom = (s_q * g).astype(np.float32)                             # fp32 product
+    with np.errstate(divide="ignore", invalid="ignore"):
+        x = np.where(denom[..., None] > 0, blocks / denom[..., None], np.float32(0))
+    codes = round_to_e2m1(x.astype(np.float32).astype(np.float64))
+    return codes.reshape(w.shape), scale_codes, np.float32(g)
+
+
+def nvfp4_dequantize(codes, scales, tensor_scale) -> np.ndarray:
+    """E2M1 value x E4M3 block scale x tensor scale, in fp64 (exact)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    K = codes.shape[-1]
+    vals = e2m1_values()[codes].reshape(*codes.shape[:-1], K // NV_BLOCK, NV_BLOCK)
+    s = e4m3_values()[np.asarray(scales, dtype=np.uint8)]
+    return (vals * s[..., None] * np.float64(tensor_scale)).reshape(codes.shape)
 
 
 # --------------------------------------------------------------------------

@@ -229,6 +229,71 @@ def check_mxfp8(o):
     assert ((top[nz] >= 256) & (top[nz] <= 448)).all()   # the largest maps into the top binade
 
 
+def check_nvfp4(o):
+    """E2M1 grid and rounding, NVFP4 scales and codes."""
+    vals = o.e2m1_values()
+    pos = vals[:8]
+    # a float format's positive codes increase with the code; 16 codes, sign in bit 3
+    assert np.all(np.diff(pos) > 0) and pos[0] == 0 and pos[-1] == 6.0
+    assert np.array_equal(vals[8:], -pos) and np.sum(vals == 0) == 2
+    # each magnitude has at most two significant bits and is a multiple of 0.5
+    m, _ = np.frexp(pos[1:])
+    assert set(np.round(m * 4).astype(int)) <= {2, 3}
+    assert np.array_equal(np.round(pos * 2), pos * 2)
+    # decode then round is the identity (+0 for -0)
+    codes = np.arange(16)
+    back = o.round_to_e2m1(vals)
+    assert np.array_equal(back, np.where(codes == 8, 0, codes))
+    # rounding = nearest by brute force; exact midpoints go to the code with mantissa bit 0
+    r = _rng(31)
+    v = np.concatenate([r.uniform(-7, 7, 4000), (pos[:-1] + pos[1:]) / 2,
+                        -(pos[:-1] + pos[1:]) / 2, [6.5, -100.0, 1e-9]])
+    got = o.round_to_e2m1(v)
+    for x, c in zip(v, got):
+        a = min(abs(x), 6.0)
+        dist = np.abs(pos - a)
+        near = np.flatnonzero(dist == dist.min())
+        want = near[0] if len(near) == 1 else [n for n in near if n % 2 == 0][0]
+        if x < 0 and want > 0:
+            want |= 8
+        assert c == want, (x, c, want)
+    # quantisation: scales through torch's E4M3 conversion, codes by nearest search
+    w = (r.standard_normal((6, 64)) * np.exp(r.uniform(-6, 2, (6, 1)))).astype(np.float32)
+    w[1, 16:32] = 0.0                                            # an all-zero block
+    codes, scales, g = o.nvfp4_quantize(w)
+    amax = np.float32(np.abs(w).max())
+    assert g == amax / np.float32(2688.0)
+    amax_b = np.abs(w.reshape(6, 4, 16)).max(axis=-1).astype(np.float32)
+    s = torch.from_numpy((amax_b / np.float32(6.0)) / g).to(torch.float8_e4m3fn)
+    assert np.array_equal(scales, s.view(torch.uint8).numpy())
+    s_val = s.to(torch.float64).numpy().astype(np.float32)
+    denom = (s_val * g).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        x = np.where(denom[..., None] > 0, w.reshape(6, 4, 16) / denom[..., None], 0).astype(np.float32)
+    assert np.array_equal(codes.reshape(6, 4, 16), o.round_to_e2m1(x.astype(np.float64)))
+    assert (codes.reshape(6, 4, 16)[1, 1] == 0).all() and scales[1, 1] == 0
+    # the largest magnitude of every non-zero block lands on 6 (its scale is within 1/16)
+    top = np.abs(o.e2m1_values()[codes.reshape(6, 4, 16)]).max(axis=-1)
+    assert np.all(top[amax_b > 0] == 6.0)
+    # error bound: half an E2M1 step (at most 1) times the block's scale
+    deq = o.nvfp4_dequantize(codes, scales, g)
+    step = np.where(np.abs(x) < 2, 0.5, np.where(np.abs(x) < 4, 1.0, 2.0))
+    assert np.all(np.abs(deq - w.reshape(6, 64)) <= (0.5 * step * denom[..., None]).reshape(6, 64) * (1 + 1e-6))
+    # values on the grid come back exactly: a block whose largest element is 6 x s x 2^-10
+    # (s an E4M3 value, one block with s = 448 so that the tensor scale is 2^-10)
+    bs = np.array([[448.0, 0.75], [13.0, 2.0 ** -3]])
+    grid = o.e2m1_values()[r.integers(0, 16, (2, 2, 16))] * bs[..., None] * 2.0 ** -10
+    grid[..., 0] = 6 * bs * 2.0 ** -10
+    grid = grid.reshape(2, 32)
+    c2, s2, g2 = o.nvfp4_quantize(grid.astype(np.float32))
+    assert g2 == np.float32(2.0 ** -10)
+    assert np.array_equal(o.e4m3_values()[s2], bs)
+    assert np.array_equal(o.nvfp4_dequantize(c2, s2, g2), grid)
+    # an all-zero matrix: tensor scale 1, every code and scale 0
+    c3, s3, g3 = o.nvfp4_quantize(np.zeros((2, 32), np.float32))
+    assert g3 == 1.0 and not c3.any() and not s3.any()
+
+
 # ---------------------------------------------------------------- grouping
 
 def check_permute(o):
@@ -353,6 +418,7 @@ def check_forward_tokens(o):
 ALL_CHECKS = [
     check_bf16_decode, check_bf16_round, check_logits_one_hot,
     check_topk_brute_force, check_tie_break, check_gates, check_selection_only_bias, check_mxfp8,
+    check_nvfp4,
     check_permute,
     check_swiglu_hand_example, check_single_expert_is_dense_ffn,
     check_identical_experts, check_brute_force_layer, check_down_scaling,

@@ -230,6 +230,36 @@ def _m_mx_no_clamp(o):
     o.E4M3_MAX = 512.0
 
 
+def _m_nv_no_tensor_scale(o):
+    o.NV_TENSOR_DIV = np.float32(1.0)
+
+
+def _m_nv_e2m1_truncates(o):
+    def round_to_e2m1(v):
+        v = np.asarray(v, dtype=np.float64)
+        grid = o.e2m1_values()[:8]
+        a = np.minimum(np.abs(v), 6.0)
+        mag = np.searchsorted(grid, a, side="right") - 1   # the grid value at or below
+        return np.where((v < 0) & (mag > 0), mag | 0x8, mag).astype(np.uint8)
+    o.round_to_e2m1 = round_to_e2m1
+
+
+def _m_nv_ties_away(o):
+    def round_to_e2m1(v):
+        v = np.asarray(v, dtype=np.float64)
+        grid = o.e2m1_values()[:8]
+        a = np.minimum(np.abs(v), 6.0)
+        d = np.abs(a[..., None] - grid)
+        best = d.min(axis=-1, keepdims=True)
+        mag = 7 - np.argmax((d == best)[..., ::-1], axis=-1)   # the larger of a tie
+        return np.where((v < 0) & (mag > 0), mag | 0x8, mag).astype(np.uint8)
+    o.round_to_e2m1 = round_to_e2m1
+
+
+def _m_nv_block_32(o):
+    o.NV_BLOCK = 32
+
+
 MUTATIONS = [
     _m_silu_sign, _m_gate_up_swapped, _m_no_h_rounding, _m_down_transposed,
     _m_tie_high_index, _m_slots_by_logit, _m_no_renormalise, _m_bias_dropped,
@@ -237,6 +267,7 @@ MUTATIONS = [
     _m_gather_wrong_index, _m_combine_ignores_gates, _m_combine_drops_shared,
     _m_expert_shift, _m_forward_tokens_no_gate, _m_selection_only_ignored,
     _m_selection_only_unbiased_pick, _m_mx_scale_off_by_one, _m_mx_truncates, _m_mx_no_clamp,
+    _m_nv_no_tensor_scale, _m_nv_e2m1_truncates, _m_nv_ties_away, _m_nv_block_32,
 ]
 
 
