@@ -225,12 +225,41 @@ moe_status_t moe_mxfp8_quantize(const moe_bf16* w, long long rows, int K, uint8_
  * expert (ext) and outputs are as in moe_forward_ex; the experts compute
  * with the dequantised weights (codes x 2^(scale - 127), exact in bf16) on
  * the bf16 tensor cores, half the weight bytes read from HBM.  d and I must
- * be multiples of 128 (else MOE_ERR_UNSUPPORTED); token chunks are capped at
- * 192 rows (tensor memory holds the dequantised weights too).  Same workspace
- * as moe_forward. */
+ * be multiples of 128 (else MOE_ERR_UNSUPPORTED); one CTA per tile of 128
+ * weight rows and at most 128 tokens.  Same workspace as moe_forward. */
 moe_status_t moe_forward_mxfp8(const moe_bf16* x, const moe_bf16* w_router,
                                const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
                                const uint8_t* codes_down, const uint8_t* scales_down, int T,
+                               int d, int E, int I, int top_k, moe_bf16* out, void* ws,
+                               size_t ws_bytes, moe_stream_t stream,
+                               const moe_forward_ext_t* ext);
+
+/* NVFP4 expert weights ('PagedAttention, speculative decoding, MoE and
+ * Blackwell', section 3: two-level micro-scaling, 16-value blocks with an FP8
+ * scale each and one FP32 scale per tensor).  Quantises `groups` matrices
+ * w [groups][rows_per_group][K] bf16 (K a multiple of 256; one matrix = one
+ * expert's W_gate_up or W_down) to E2M1 codes [groups*rows_per_group][K/2]
+ * (value 2i in the low nibble of byte i), E4M3 block scales
+ * [K/256][groups*rows_per_group][16] and one fp32 tensor scale per matrix.
+ * Rule (the pages give none; fp32, round to nearest, in this order):
+ * g = amax / (448 * 6) (1 for an all-zero matrix); block scale =
+ * E4M3((amax_block / 6) / g); element = E2M1(w / (scale * g)), nearest even,
+ * saturating at 6, -0 stored as +0.  Device pointers (codes, scales 16-byte
+ * aligned); asynchronous on `stream`. */
+moe_status_t moe_nvfp4_quantize(const moe_bf16* w, int groups, long long rows_per_group, int K,
+                                uint8_t* codes, uint8_t* scales, float* tensor_scales,
+                                moe_stream_t stream);
+
+/* The whole layer with NVFP4 expert weights (moe_nvfp4_quantize of W_gate_up
+ * as E matrices [2I, d] and of W_down as E matrices [d, I]).  The experts
+ * compute with E2M1 value x block scale (exact in bf16) on the bf16 tensor
+ * cores and apply each expert's tensor scale to the fp32 accumulators; the
+ * rest is moe_forward_ex.  d and I must be multiples of 256 (else
+ * MOE_ERR_UNSUPPORTED).  Same workspace as moe_forward. */
+moe_status_t moe_forward_nvfp4(const moe_bf16* x, const moe_bf16* w_router,
+                               const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
+                               const float* tscale_gate_up, const uint8_t* codes_down,
+                               const uint8_t* scales_down, const float* tscale_down, int T,
                                int d, int E, int I, int top_k, moe_bf16* out, void* ws,
                                size_t ws_bytes, moe_stream_t stream,
                                const moe_forward_ext_t* ext);

@@ -46,6 +46,9 @@ _SIGS = {
     "moe_mxfp8_quantize": (_st, [_vp, ctypes.c_longlong, _i, _vp, _vp, _vp]),
     "moe_forward_mxfp8": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz,
                                 _vp, _vp]),
+    "moe_nvfp4_quantize": (_st, [_vp, _i, ctypes.c_longlong, _i, _vp, _vp, _vp, _vp]),
+    "moe_forward_nvfp4": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
+                                _vp, _sz, _vp, _vp]),
     "moe_graph_destroy": (_st, [_vp]),
     "moe_permute": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute_static_scratch": (_st, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -321,6 +324,54 @@ def moe_mxfp8_quantize(w, stream=None):
     _check(_lib.moe_mxfp8_quantize(_p(w), rows, K, _p(codes), _p(scales), _stream(stream)),
            "moe_mxfp8_quantize")
     return codes, scales
+
+
+def moe_nvfp4_quantize(w, stream=None):
+    """bf16 [G, rows, K] weights (G matrices, one per expert) -> (codes uint8
+    [G*rows, K/2], scales uint8 [K/256, G*rows, 16], tensor scales float32 [G])
+    on the device."""
+    _want(w, torch.bfloat16, "w")
+    G, rows, K = w.shape
+    codes = torch.empty((G * rows, K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((K // 256, G * rows, 16), dtype=torch.uint8, device=w.device)
+    tscale = torch.empty((G,), dtype=torch.float32, device=w.device)
+    _check(_lib.moe_nvfp4_quantize(_p(w), G, rows, K, _p(codes), _p(scales), _p(tscale),
+                                   _stream(stream)), "moe_nvfp4_quantize")
+    return codes, scales, tscale
+
+
+def moe_forward_nvfp4(x, w_router, nv_gate_up, nv_down, top_k, out=None, ws=None,
+                      router_bias=None, w_gate_up_shared=None, w_down_shared=None, stream=None,
+                      bias_selection_only=False):
+    """The whole layer with NVFP4 expert weights: nv_gate_up / nv_down are the
+    (codes, scales, tensor scales) of moe_nvfp4_quantize for W_gate_up
+    [E,2I,d] and W_down [E,d,I].  Returns out [T, d] bf16."""
+    for t, n in ((x, "x"), (w_router, "w_router"), (w_gate_up_shared, "w_gate_up_shared"),
+                 (w_down_shared, "w_down_shared")):
+        _want(t, torch.bfloat16, n)
+    _want(router_bias, torch.float32, "router_bias")
+    cgu, sgu, tgu = nv_gate_up
+    cd, sd, td = nv_down
+    for t, n in ((cgu, "codes_gate_up"), (sgu, "scales_gate_up"), (cd, "codes_down"),
+                 (sd, "scales_down")):
+        _want(t, torch.uint8, n)
+    _want(tgu, torch.float32, "tscale_gate_up"); _want(td, torch.float32, "tscale_down")
+    T, d = x.shape
+    E = tgu.shape[0]
+    I = cgu.shape[0] // (2 * E)
+    I_s = w_down_shared.shape[1] if w_down_shared is not None else 0
+    if out is None:
+        out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device)
+    ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
+                     w_gate_up_shared.data_ptr() if I_s else None,
+                     w_down_shared.data_ptr() if I_s else None, I_s,
+                     1 if bias_selection_only else 0)
+    _check(_lib.moe_forward_nvfp4(_p(x), _p(w_router), _p(cgu), _p(sgu), _p(tgu), _p(cd), _p(sd),
+                                  _p(td), T, d, E, I, top_k, _p(out), _p(ws), ws.numel(),
+                                  _stream(stream), ctypes.byref(ext)), "moe_forward_nvfp4")
+    return out
 
 
 def moe_forward_mxfp8(x, w_router, mx_gate_up, mx_down, top_k, out=None, ws=None,

@@ -323,8 +323,11 @@ moe_status_t moe_combine(const float* y, const int32_t* slot_pos, const float* t
 namespace {
 
 // MXFP8 expert weights (codes and scales); null for bf16 weights.
+// Quantised expert weights: fmt 0 MXFP8, 1 NVFP4 (tensor scales used).
 struct MxWeights {
+  int fmt;
   const uint8_t *codes_gate_up, *scales_gate_up, *codes_down, *scales_down;
+  const float *tscale_gate_up, *tscale_down;
 };
 
 moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
@@ -333,8 +336,10 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
                           size_t ws_bytes, moe_stream_t stream, const moe_forward_ext_t* ext) {
   moe_status_t st = check_shapes(T, d, E, I, top_k);
   if (st != MOE_OK) return st;
-  if (mx && (d % 128 || I % 128))
+  if (mx && mx->fmt == 0 && (d % 128 || I % 128))
     return fail(MOE_ERR_UNSUPPORTED, "MXFP8 weights need d and I multiples of 128");
+  if (mx && mx->fmt == 1 && (d % 256 || I % 256))
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 weights need d and I multiples of 256");
   const float* bias = ext ? ext->router_bias : nullptr;
   const int bias_sel = ext ? ext->bias_selection_only : 0;
   const int I_shared = ext ? ext->I_shared : 0;
@@ -381,8 +386,9 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
                                  offsets, perm, slot_pos, x_perm, table, status);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   const TokenGather gather{x, perm, top_k, T};
-  e = mx ? launch_grouped_ffn_mxfp8(s, x_perm, offsets, rows, d, E, I, mx->codes_gate_up,
-                                    mx->scales_gate_up, mx->codes_down, mx->scales_down, h, y,
+  e = mx ? launch_grouped_ffn_quant(s, mx->fmt, x_perm, offsets, rows, d, E, I,
+                                    mx->codes_gate_up, mx->scales_gate_up, mx->tscale_gate_up,
+                                    mx->codes_down, mx->scales_down, mx->tscale_down, h, y,
                                     status, tmo)
          : launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status,
                               tmo, gather_rows ? &gather : nullptr);
@@ -418,7 +424,26 @@ moe_status_t moe_forward_mxfp8(const moe_bf16* x, const moe_bf16* w_router,
                 !aligned16(codes_gate_up) || !aligned16(scales_gate_up) ||
                 !aligned16(codes_down) || !aligned16(scales_down)))
     return fail(MOE_ERR_INVALID_ARG, "moe_forward_mxfp8: null or unaligned weight pointer");
-  const MxWeights mx{codes_gate_up, scales_gate_up, codes_down, scales_down};
+  const MxWeights mx{0, codes_gate_up, scales_gate_up, codes_down, scales_down, nullptr, nullptr};
+  // the bf16 weight pointers are not read on this path; pass the codes to pass the null checks
+  return forward_impl(x, w_router, reinterpret_cast<const moe_bf16*>(codes_gate_up),
+                      reinterpret_cast<const moe_bf16*>(codes_down), &mx, T, d, E, I, top_k, out,
+                      ws, ws_bytes, stream, ext);
+}
+
+moe_status_t moe_forward_nvfp4(const moe_bf16* x, const moe_bf16* w_router,
+                               const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
+                               const float* tscale_gate_up, const uint8_t* codes_down,
+                               const uint8_t* scales_down, const float* tscale_down, int T,
+                               int d, int E, int I, int top_k, moe_bf16* out, void* ws,
+                               size_t ws_bytes, moe_stream_t stream,
+                               const moe_forward_ext_t* ext) {
+  if (T > 0 && (!codes_gate_up || !scales_gate_up || !codes_down || !scales_down ||
+                !tscale_gate_up || !tscale_down || !aligned16(codes_gate_up) ||
+                !aligned16(scales_gate_up) || !aligned16(codes_down) || !aligned16(scales_down)))
+    return fail(MOE_ERR_INVALID_ARG, "moe_forward_nvfp4: null or unaligned weight pointer");
+  const MxWeights mx{1, codes_gate_up, scales_gate_up, codes_down, scales_down, tscale_gate_up,
+                     tscale_down};
   // the bf16 weight pointers are not read on this path; pass the codes to pass the null checks
   return forward_impl(x, w_router, reinterpret_cast<const moe_bf16*>(codes_gate_up),
                       reinterpret_cast<const moe_bf16*>(codes_down), &mx, T, d, E, I, top_k, out,
@@ -469,6 +494,22 @@ moe_status_t moe_mxfp8_quantize(const moe_bf16* w, long long rows, int K, uint8_
   const cudaError_t e =
       launch_mxfp8_quantize(reinterpret_cast<cudaStream_t>(stream), w, rows, K, codes, scales);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "mxfp8 quantize launch");
+}
+
+moe_status_t moe_nvfp4_quantize(const moe_bf16* w, int groups, long long rows_per_group, int K,
+                                uint8_t* codes, uint8_t* scales, float* tensor_scales,
+                                moe_stream_t stream) {
+  if (groups < 0 || rows_per_group < 0 || K <= 0 || K % 256)
+    return fail(MOE_ERR_INVALID_ARG, "moe_nvfp4_quantize: K must be a positive multiple of 256");
+  if (groups == 0 || rows_per_group == 0) return MOE_OK;
+  if (!w || !codes || !scales || !tensor_scales || !aligned16(w) || !aligned16(codes) ||
+      !aligned16(scales) || reinterpret_cast<uintptr_t>(tensor_scales) % 4)
+    return fail(MOE_ERR_INVALID_ARG, "moe_nvfp4_quantize: null or unaligned pointer");
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  const cudaError_t e = launch_nvfp4_quantize(reinterpret_cast<cudaStream_t>(stream), w, groups,
+                                              rows_per_group, K, codes, scales, tensor_scales);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "nvfp4 quantize launch");
 }
 
 moe_status_t moe_forward_graph(const moe_bf16* x, const moe_bf16* w_router,

@@ -92,8 +92,9 @@ struct Params {
   const int32_t* gather_perm;
   int gather_div;
   int gather_oob;
-  const uint8_t* scales;  // MXFP8 weights: E8M0 scales [K / 128][scale_rows][4]
-  long long scale_rows;   // MXFP8 weights: weight rows of the whole tensor
+  const uint8_t* scales;  // MXFP8 / NVFP4 weights: block scales [K / stage K][scale_rows][per row]
+  long long scale_rows;   // MXFP8 / NVFP4 weights: weight rows of the whole tensor
+  const float* tscale;    // NVFP4 weights: tensor scale per expert (null: none)
   int smem_bytes;         // dynamic shared memory of the launch
   int tok_cap;            // bf16 kernels: token rows per chunk, kTokMax or kTokMaxWide
   unsigned* status;
@@ -211,8 +212,10 @@ __device__ __forceinline__ void build_schedule(const Params& p, int* s_off, int*
 // down stores y in fp32; `live` false (a wait gave up) stores nothing.
 template <int KIND, int SLAB = (KIND == kGateUp ? 128 : 256)>
 __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, bool live,
-                                              const Params& p, int q, int lane, uint32_t rank) {
-  // SLAB: output columns of one tile (h columns for gate_up, y columns for down)
+                                              const Params& p, int q, int lane, uint32_t rank,
+                                              float tscale = 1.0f) {
+  // SLAB: output columns of one tile (h columns for gate_up, y columns for down).
+  // tscale: the weights' tensor scale (NVFP4), applied to the accumulators.
   if constexpr (KIND == kDown) {
     const int col = t.slab * SLAB + rank * 128 + q * 32 + lane;
     const bool col_ok = live && col < p.n_out;
@@ -221,6 +224,10 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, boo
       uint32_t v[16];
       tmem_ld_32x32b_x16(t_row + c, v);
       tmem_ld_wait();
+      if (tscale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * tscale);
+      }
       const int nvalid = min(16, t.tok_end - t.tok0 - c);  // uniform across the warp
       float* yp = static_cast<float*>(p.out) + (size_t)(t.tok0 + c) * p.ld_out + col;
       if (col_ok) {
@@ -249,6 +256,10 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, boo
       uint32_t v[16];
       tmem_ld_32x32b_x16(t_row + c, v);
       tmem_ld_wait();
+      if (tscale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * tscale);
+      }
       const int row0 = t.tok0 + c + (lo ? 0 : 8);
       const int nvalid = min(8, t.tok_end - row0);  // <= 0: rows past the expert's end
       __nv_bfloat16* hp = h + (size_t)row0 * p.ld_out;
@@ -525,11 +536,22 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 // (one per TMEM lane quarter, all four scale blocks of a row each) beat 8 and
 // 16 (decode 0.654 / 0.668 / 0.709 ms).
 
-constexpr int kBK8 = 128;                            // K per stage: one 128-byte row of codes
-constexpr int kABufCols = kBK8 / 2;                  // TMEM columns of one A buffer (bf16 pairs)
+// Weight formats: per pipeline stage a weight row brings one 128-byte row of
+// codes -- 128 E4M3 values (MXFP8) or 256 E2M1 values (NVFP4) -- and its
+// block scales: 4 E8M0 bytes (one per 32 values) or 16 E4M3 bytes (one per 16).
+enum WFormat : int { kMx8 = 0, kNv4 = 1 };
+template <int FMT> struct WFmt;
+template <> struct WFmt<kMx8> {
+  static constexpr int kStageK = 128;       // K values per stage
+  static constexpr int kScalesPerRow = 4;   // scale bytes per row per stage
+};
+template <> struct WFmt<kNv4> {
+  static constexpr int kStageK = 256;
+  static constexpr int kScalesPerRow = 16;
+};
+constexpr int kBK8 = 128;                            // code bytes per row per stage
 constexpr int kMaxABufs = 4;
 constexpr int kA8Bytes = kWRows * kBK8;              // codes per CTA per stage
-constexpr int kScaleBytes = kWRows * 4;              // four E8M0 scales per row per stage
 constexpr int kConvWarp0 = 6;
 constexpr int kConvWarps = 4;                        // one per TMEM lane quarter
 constexpr int kBlkPerWarp = 16 / kConvWarps;         // 32-value scale blocks per warp per stage
@@ -579,12 +601,45 @@ __device__ __forceinline__ void e4m3x8_to_bf16(uint32_t lo, uint32_t hi, float s
   }
 }
 
-template <int KIND>
+// 4 E2M1 codes (the low 16 bits of m_lo / signs from w's bits 3, 7, 11, 15)
+// as two bf16x2 of code value x scale.  The codes' 3-bit magnitudes index
+// byte tables of the bf16 patterns of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with prmt
+// (high bytes 00 3F 3F 3F 40 40 40 40, low bytes 00 00 80 C0 00 40 80 C0),
+// two more prmt interleave them into bf16 halves, the signs are or-ed in,
+// and one exact bf16x2 multiply applies the block scale.
+__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t w, __nv_bfloat162 mul, uint32_t* out) {
+  const uint32_t sel = w & 0x7777u;
+  uint32_t hi, lo, a, b;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(lo), "r"(hi));  // values 0, 1
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(lo), "r"(hi));  // values 2, 3
+  a |= ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
+  b |= ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
+  const __nv_bfloat162 pa = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), mul);
+  const __nv_bfloat162 pb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), mul);
+  out[0] = *reinterpret_cast<const uint32_t*>(&pa);
+  out[1] = *reinterpret_cast<const uint32_t*>(&pb);
+}
+
+// An E4M3 block scale as a bf16 pair (exact: 4 significant bits).
+__device__ __forceinline__ __nv_bfloat162 e4m3_scale_bf16x2(uint32_t code) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
+  const float f = __half2float(*reinterpret_cast<const __half*>(&h));
+  return __floats2bfloat162_rn(f, f);
+}
+
+template <int KIND, int FMT>
 __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
                                                      const TokenMapSet& tx, const Params& p) {
   // one CTA's tile: 128 weight rows and a chunk of up to 128 tokens
   constexpr int kSlabH = 64;     // gate_up: h columns per tile (64 gate + 64 up rows)
   constexpr int kSlabRows = 128;  // down: y columns per tile
+  constexpr int kStageK = WFmt<FMT>::kStageK;
+  constexpr int kSubF = kStageK / kBK;              // 64-wide token boxes per stage
+  constexpr int kSPR = WFmt<FMT>::kScalesPerRow;
+  constexpr int kABufCols = kStageK / 2;             // TMEM columns of one A buffer (bf16 pairs)
+  constexpr int kScaleBytes = kWRows * kSPR;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_ct[kMaxExperts + 1];
@@ -642,11 +697,11 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
 
   const uint32_t tmem_base = s_tmem_base;
   const int total_tiles = s_ct[G] * p.slabs;
-  const int num_ks = p.K / kBK8;  // K is a multiple of 128
+  const int num_ks = p.K / kStageK;  // K is a multiple of the stage's K
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
   // token rows per K box: the launch's largest chunk (twice its largest half)
   const uint32_t b_sub_bytes = static_cast<uint32_t>(2 * s_half_max) * kBK * 2;
-  const uint32_t stage_bytes = (kA8Bytes + kSub * b_sub_bytes + kScaleBytes + 1023u) & ~1023u;
+  const uint32_t stage_bytes = (kA8Bytes + kSubF * b_sub_bytes + kScaleBytes + 1023u) & ~1023u;
   const uint32_t avail = static_cast<uint32_t>(p.smem_bytes) - (base - smem_u32(smem_raw));
   const uint32_t acc_cols = static_cast<uint32_t>(2 * s_half_max);
   const int nst = min(kMaxStages8, static_cast<int>(avail / stage_bytes));
@@ -676,29 +731,29 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
           nrow = max(0, min(128, p.n_out - r0));
           row0 = t.e * p.w_rows_per_group + r0;
         }
-        const uint32_t scale_tx = (KIND == kGateUp ? 2 : 1) * static_cast<uint32_t>(nrow) * 4;
+        const uint32_t scale_tx = (KIND == kGateUp ? 2 : 1) * static_cast<uint32_t>(nrow) * kSPR;
         for (int ks = 0; ks < num_ks; ++ks) {
           if (!mbar_wait(st_empty + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t a_dst = base + stage * stage_bytes;
           const uint32_t b_dst = a_dst + kA8Bytes;
-          const uint32_t s_dst = b_dst + kSub * b_sub_bytes;
+          const uint32_t s_dst = b_dst + kSubF * b_sub_bytes;
           const uint32_t af = a_full + 8 * stage;
           mbar_arrive_expect_tx(af, kA8Bytes + scale_tx);
-          const int kx = ks * kBK8;
+          const int kx = ks * kBK8;  // code bytes
           if (KIND == kGateUp)
             tma_load_5d(a_dst, &tmap_w, af, kx, 0, 0, (row0 - t.e * p.w_rows_per_group) / 16, t.e);
           else
             tma_load_2d(a_dst, &tmap_w, af, kx, row0);
-          const uint8_t* sc = p.scales + (static_cast<size_t>(ks) * p.scale_rows) * 4;
+          const uint8_t* sc = p.scales + (static_cast<size_t>(ks) * p.scale_rows) * kSPR;
           if (nrow > 0) {
-            bulk_load(s_dst, sc + static_cast<size_t>(row0) * 4, nrow * 4, af);
+            bulk_load(s_dst, sc + static_cast<size_t>(row0) * kSPR, nrow * kSPR, af);
             if (KIND == kGateUp)
-              bulk_load(s_dst + 256, sc + static_cast<size_t>(row1) * 4, nrow * 4, af);
+              bulk_load(s_dst + 64 * kSPR, sc + static_cast<size_t>(row1) * kSPR, nrow * kSPR, af);
           }
-          mbar_arrive_expect_tx(b_full + 8 * stage, kSub * t.n * kBK * 2);
-          for (int sub = 0; sub < kSub; ++sub)
-            tma_load_2d(b_dst + sub * b_sub_bytes, tmap_x, b_full + 8 * stage, kx + sub * kBK,
-                        t.tok0);
+          mbar_arrive_expect_tx(b_full + 8 * stage, kSubF * t.n * kBK * 2);
+          for (int sub = 0; sub < kSubF; ++sub)
+            tma_load_2d(b_dst + sub * b_sub_bytes, tmap_x, b_full + 8 * stage,
+                        ks * kStageK + sub * kBK, t.tok0);
           ++issued;
           if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
@@ -727,7 +782,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
           const uint32_t b_addr = base + stage * stage_bytes + kA8Bytes;
           const uint32_t a_tmem = tmem_base + abuf0 + cb * kABufCols;
 #pragma unroll
-          for (int k = 0; k < kBK8 / 16; ++k) {
+          for (int k = 0; k < kStageK / 16; ++k) {
             const uint64_t bd = smem_desc_sw128(b_addr + (k >> 2) * b_sub_bytes + (k & 3) * 32);
             mma_bf16_tmem_a(d_tmem, a_tmem + k * 8, bd, idesc, (ks | k) != 0 ? 1u : 0u);
           }
@@ -753,7 +808,8 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
       const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
-      epilogue_tile<KIND, KIND == kGateUp ? kSlabH : kSlabRows>(t, t_row, live, p, q, lane, 0u);
+      epilogue_tile<KIND, KIND == kGateUp ? kSlabH : kSlabRows>(
+          t, t_row, live, p, q, lane, 0u, p.tscale ? __ldg(p.tscale + t.e) : 1.0f);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -789,10 +845,45 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
         if (!mbar_wait(conv_empty + 8 * cb, cphase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t a_src = base + stage * stage_bytes;
-        const uint32_t s_src = a_src + kA8Bytes + kSub * b_sub_bytes;
+        const uint32_t s_src = a_src + kA8Bytes + kSubF * b_sub_bytes;
+        const uint32_t t_buf = t_lane + cb * kABufCols;
+        if constexpr (FMT == kNv4) {
+          // NVFP4: the row's 16 block scales, then its 8 chunks of 32 codes (two
+          // blocks each), all loaded before converting; 16 TMEM columns per chunk
+          uint32_t scw[4] = {0u, 0u, 0u, 0u};
+          if (row_ok)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(scw[0]), "=r"(scw[1]), "=r"(scw[2]), "=r"(scw[3])
+                         : "r"(s_src + srow * 16));
+          uint32_t wv[8][4];
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(wv[ch][0]), "=r"(wv[ch][1]), "=r"(wv[ch][2]), "=r"(wv[ch][3])
+                         : "r"(a_src + r * 128 + ((ch ^ (r & 7)) << 4)));
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t out[16];
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {  // block 2 ch + hb: words 2 hb, 2 hb + 1
+              const int blk = 2 * ch + hb;
+              const __nv_bfloat162 mul = e4m3_scale_bf16x2((scw[blk >> 2] >> (8 * (blk & 3))) & 0xffu);
+#pragma unroll
+              for (int wi = 0; wi < 2; ++wi) {
+                const uint32_t w = wv[ch][2 * hb + wi];
+                e2m1x4_to_bf16(w, mul, out + 8 * hb + 4 * wi);
+                e2m1x4_to_bf16(w >> 16, mul, out + 8 * hb + 4 * wi + 2);
+              }
+            }
+            if (!row_ok) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) out[i] = 0u;
+            }
+            tmem_st_32x32b_x16(t_buf + ch * 16, out);
+          }
+        } else {
         uint32_t sc = 0;
         if (row_ok) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sc) : "r"(s_src + srow * 4));
-        const uint32_t t_buf = t_lane + cb * kABufCols;
         // every code load of this warp's blocks first (two 16-byte chunks of
         // the 128-byte row per block), then the conversions and TMEM stores:
         // one shared-memory round trip per stage
@@ -831,6 +922,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
           }
           tmem_st_32x32b_x16(t_buf + blk * 16, out);
         }
+        }
         tmem_st_wait();
         __syncwarp();
         if (lane == 0) mbar_arrive(st_empty + 8 * stage);  // codes and scales of this stage read
@@ -857,13 +949,25 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
 __global__ void __launch_bounds__(kThreads8, 1)
     moe_gate_up_swiglu_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                     const __grid_constant__ TokenMapSet tx, const Params p) {
-  expert_gemm_fp8_body<kGateUp>(tmap_w, tx, p);
+  expert_gemm_fp8_body<kGateUp, kMx8>(tmap_w, tx, p);
 }
 
 __global__ void __launch_bounds__(kThreads8, 1)
     moe_down_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
                           const __grid_constant__ TokenMapSet tx, const Params p) {
-  expert_gemm_fp8_body<kDown>(tmap_w, tx, p);
+  expert_gemm_fp8_body<kDown, kMx8>(tmap_w, tx, p);
+}
+
+__global__ void __launch_bounds__(kThreads8, 1)
+    moe_gate_up_swiglu_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                                    const __grid_constant__ TokenMapSet tx, const Params p) {
+  expert_gemm_fp8_body<kGateUp, kNv4>(tmap_w, tx, p);
+}
+
+__global__ void __launch_bounds__(kThreads8, 1)
+    moe_down_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                          const __grid_constant__ TokenMapSet tx, const Params p) {
+  expert_gemm_fp8_body<kDown, kNv4>(tmap_w, tx, p);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -885,7 +989,7 @@ typedef void (*ExpertKernel)(const CUtensorMap, const TokenMapSet, const Params)
 // Set as the kernel's limit on first use per device; 0 on failure.
 int ensure_smem_attr(ExpertKernel k, int which) {
   static std::mutex mu;
-  static int bytes[4][64] = {};
+  static int bytes[6][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
@@ -1051,22 +1155,27 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
                        q, chunks_bound * q.slabs);
 }
 
-cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_t* offsets,
-                                     int rows, int d, int E, int I, const uint8_t* codes_gate_up,
-                                     const uint8_t* scales_gate_up, const uint8_t* codes_down,
-                                     const uint8_t* scales_down, void* h, float* y,
-                                     unsigned* status, unsigned long long timeout_ns) {
+cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
+                                     const int32_t* offsets, int rows, int d, int E, int I,
+                                     const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
+                                     const float* tscale_gate_up, const uint8_t* codes_down,
+                                     const uint8_t* scales_down, const float* tscale_down,
+                                     void* h, float* y, unsigned* status,
+                                     unsigned long long timeout_ns) {
+  const bool nv = fmt == kNv4;
+  const uint64_t d_bytes = nv ? d / 2 : d;  // code bytes of a W_gate_up row
+  const uint64_t i_bytes = nv ? I / 2 : I;  // code bytes of a W_down row
   // one CTA per tile, chunks of at most 128 tokens
   const long long chunks_bound = rows / (kTokMax / 2) + std::min(E, rows);
 
   // codes of W_gate_up [E][2][I][d] viewed as (d, 16 rows, gate|up, I/16 row groups, E): one
-  // box = 128 K of 4 row groups, each 16 gate rows followed by the 16 matching up rows
+  // box = 128 code bytes of 4 row groups, each 16 gate rows followed by the 16 matching up rows
   CUtensorMap mw;
   TokenMapSet mx;
-  const uint64_t dims[5] = {static_cast<uint64_t>(d), 16, 2, static_cast<uint64_t>(I / 16),
+  const uint64_t dims[5] = {d_bytes, 16, 2, static_cast<uint64_t>(I / 16),
                             static_cast<uint64_t>(E)};
-  const uint64_t strides[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(I) * d,
-                               16ull * d, 2ull * I * d};
+  const uint64_t strides[4] = {d_bytes, static_cast<uint64_t>(I) * d_bytes, 16ull * d_bytes,
+                               2ull * I * d_bytes};
   const uint32_t box[5] = {kBK8, 16, 2, 4, 1};
   Params p{};
   cudaError_t e = make_u8_map_nd(&mw, codes_gate_up, 5, dims, strides, box);
@@ -1084,16 +1193,19 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   p.ld_out = I;
   p.scales = scales_gate_up;
   p.scale_rows = 2LL * I * E;
+  p.tscale = nv ? tscale_gate_up : nullptr;
   p.status = status;
   p.timeout_ns = timeout_ns;
-  e = launch_expert_1cta(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_kernel, 2, mw,
-                         mx, p, chunks_bound * p.slabs);
+  e = nv ? launch_expert_1cta(s, "moe_gate_up_swiglu_nvfp4", moe_gate_up_swiglu_nvfp4_kernel, 4,
+                              mw, mx, p, chunks_bound * p.slabs)
+         : launch_expert_1cta(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_kernel, 2,
+                              mw, mx, p, chunks_bound * p.slabs);
   if (e != cudaSuccess) return e;
 
   CUtensorMap mw2;
   TokenMapSet mx2;
-  const uint64_t dims2[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(E) * d};
-  const uint64_t strides2[1] = {static_cast<uint64_t>(I)};
+  const uint64_t dims2[2] = {i_bytes, static_cast<uint64_t>(E) * d};
+  const uint64_t strides2[1] = {i_bytes};
   const uint32_t box2[2] = {kBK8, 128};
   e = make_u8_map_nd(&mw2, codes_down, 2, dims2, strides2, box2);
   if (e == cudaSuccess) e = make_token_maps(mx2, h, rows, I);
@@ -1110,10 +1222,13 @@ cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_
   q.ld_out = d;
   q.scales = scales_down;
   q.scale_rows = static_cast<long long>(E) * d;
+  q.tscale = nv ? tscale_down : nullptr;
   q.status = status;
   q.timeout_ns = timeout_ns;
-  return launch_expert_1cta(s, "moe_down_mxfp8", moe_down_mxfp8_kernel, 3, mw2, mx2, q,
-                            chunks_bound * q.slabs);
+  return nv ? launch_expert_1cta(s, "moe_down_nvfp4", moe_down_nvfp4_kernel, 5, mw2, mx2, q,
+                                 chunks_bound * q.slabs)
+            : launch_expert_1cta(s, "moe_down_mxfp8", moe_down_mxfp8_kernel, 3, mw2, mx2, q,
+                                 chunks_bound * q.slabs);
 }
 
 }  // namespace moe

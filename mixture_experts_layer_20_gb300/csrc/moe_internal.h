@@ -134,13 +134,25 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
                                unsigned long long timeout_ns,
                                const TokenGather* gather = nullptr);
 
-// The same with MXFP8 expert weights: E4M3 codes [E, 2I, d] / [E, d, I] and
-// E8M0 scales [d/128][E*2I][4] / [I/128][E*d][4]; d and I multiples of 128.
-cudaError_t launch_grouped_ffn_mxfp8(cudaStream_t s, const void* a, const int32_t* offsets,
-                                     int rows, int d, int E, int I, const uint8_t* codes_gate_up,
-                                     const uint8_t* scales_gate_up, const uint8_t* codes_down,
-                                     const uint8_t* scales_down, void* h, float* y,
-                                     unsigned* status, unsigned long long timeout_ns);
+// The same with quantised expert weights (fmt 0: MXFP8, fmt 1: NVFP4):
+// codes [E, 2I, d] / [E, d, I] (one byte per value for MXFP8, two values per
+// byte for NVFP4) and block scales [K/128][rows][4] E8M0 (MXFP8) or
+// [K/256][rows][16] E4M3 (NVFP4), rows = E*2I (gate_up) or E*d (down); NVFP4
+// also a tensor scale per expert and matrix.  d and I multiples of 128
+// (MXFP8) or 256 (NVFP4).
+cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
+                                     const int32_t* offsets, int rows, int d, int E, int I,
+                                     const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
+                                     const float* tscale_gate_up, const uint8_t* codes_down,
+                                     const uint8_t* scales_down, const float* tscale_down,
+                                     void* h, float* y, unsigned* status,
+                                     unsigned long long timeout_ns);
+
+// NVFP4 quantisation of `groups` matrices [rows_per_group, K] (K a multiple of
+// 256) in one bf16 array: codes, scales as above, one tensor scale per matrix.
+cudaError_t launch_nvfp4_quantize(cudaStream_t s, const void* w, int groups,
+                                  long long rows_per_group, int K, uint8_t* codes,
+                                  uint8_t* scales, float* tensor_scales);
 
 // ---- grouping and combine (moe_permute.cu)
 

@@ -371,14 +371,22 @@ def permute(ids, E: int):
 # Expert FFN (SwiGLU, three matrices)
 # --------------------------------------------------------------------------
 
+def _weight_values(w) -> np.ndarray:
+    """Expert weights given as bf16 bit patterns (uint16), or as exact values
+    (float64, e.g. dequantised NVFP4 weights, which bf16 cannot hold)."""
+    w = np.asarray(w)
+    return w if w.dtype == np.float64 else bf16_bits_to_f64(w)
+
+
 def swiglu_ffn(x_rows, w_gate_up_bits, w_down_bits) -> np.ndarray:
     """One expert on a block of rows: fp64, with h rounded once to bf16.
 
-    x_rows: [m, d] fp64.  w_gate_up: [2I, d] bf16 bits, rows [0, I) = gate and
-    rows [I, 2I) = up.  w_down: [d, I] bf16 bits.  Returns y [m, d] fp64.
+    x_rows: [m, d] fp64.  w_gate_up: [2I, d] bf16 bits (or fp64 values), rows
+    [0, I) = gate and rows [I, 2I) = up.  w_down: [d, I] likewise.  Returns
+    y [m, d] fp64.
     """
-    w_gu = bf16_bits_to_f64(w_gate_up_bits)
-    w_d = bf16_bits_to_f64(w_down_bits)
+    w_gu = _weight_values(w_gate_up_bits)
+    w_d = _weight_values(w_down_bits)
     I = w_gu.shape[0] // 2
     gate = x_rows @ w_gu[:I].T
     up = x_rows @ w_gu[I:].T
