@@ -553,9 +553,11 @@ constexpr int kBK8 = 128;                            // code bytes per row per s
 constexpr int kMaxABufs = 4;
 constexpr int kA8Bytes = kWRows * kBK8;              // codes per CTA per stage
 constexpr int kConvWarp0 = 6;
-constexpr int kConvWarps = 4;                        // one per TMEM lane quarter
-constexpr int kBlkPerWarp = 16 / kConvWarps;         // 32-value scale blocks per warp per stage
-constexpr int kThreads8 = (kConvWarp0 + kConvWarps) * 32;
+constexpr int kConvWarpsMx = 4;                      // MXFP8: one per TMEM lane quarter
+constexpr int kConvWarpsNv = 8;                      // NVFP4: two per quarter, half the chunks each
+__host__ __device__ constexpr int conv_warps(int fmt) { return fmt == 1 ? kConvWarpsNv : kConvWarpsMx; }
+__host__ __device__ constexpr int threads_q(int fmt) { return (kConvWarp0 + conv_warps(fmt)) * 32; }
+constexpr int kBlkPerWarp = 16 / kConvWarpsMx;       // MXFP8: 32-value scale blocks per warp per stage
 constexpr int kMaxStages8 = 8;
 
 // 2^(byte - 127) as a float (byte 0: 2^-127, a subnormal).
@@ -640,6 +642,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
   constexpr int kSPR = WFmt<FMT>::kScalesPerRow;
   constexpr int kABufCols = kStageK / 2;             // TMEM columns of one A buffer (bf16 pairs)
   constexpr int kScaleBytes = kWRows * kSPR;
+  constexpr int kConvWarps = conv_warps(FMT);
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_ct[kMaxExperts + 1];
@@ -850,27 +853,32 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
         if constexpr (FMT == kNv4) {
           // NVFP4: the row's 16 block scales, then its 8 chunks of 32 codes (two
           // blocks each), all loaded before converting; 16 TMEM columns per chunk
-          uint32_t scw[4] = {0u, 0u, 0u, 0u};
+          constexpr int kCh = 8 / (kConvWarps / 4);  // chunks of this warp
+          static_assert(kCh == 4, "the scale words below cover four chunks");
+          uint32_t scw[2] = {0u, 0u};                // the 8 block scales of this warp's chunks
           if (row_ok)
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(scw[0]), "=r"(scw[1]), "=r"(scw[2]), "=r"(scw[3])
-                         : "r"(s_src + srow * 16));
-          uint32_t wv[8][4];
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                         : "=r"(scw[0]), "=r"(scw[1])
+                         : "r"(s_src + srow * 16 + kq * 8));
+          uint32_t wv[kCh][4];
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
+          for (int c = 0; c < kCh; ++c) {
+            const int ch = kq * kCh + c;
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(wv[ch][0]), "=r"(wv[ch][1]), "=r"(wv[ch][2]), "=r"(wv[ch][3])
+                         : "=r"(wv[c][0]), "=r"(wv[c][1]), "=r"(wv[c][2]), "=r"(wv[c][3])
                          : "r"(a_src + r * 128 + ((ch ^ (r & 7)) << 4)));
+          }
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
+          for (int c = 0; c < kCh; ++c) {
+            const int ch = kq * kCh + c;
             uint32_t out[16];
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {  // block 2 ch + hb: words 2 hb, 2 hb + 1
-              const int blk = 2 * ch + hb;
-              const __nv_bfloat162 mul = e4m3_scale_bf16x2((scw[blk >> 2] >> (8 * (blk & 3))) & 0xffu);
+              const int lb = 2 * c + hb;  // block within this warp's 8
+              const __nv_bfloat162 mul = e4m3_scale_bf16x2((scw[lb >> 2] >> (8 * (lb & 3))) & 0xffu);
 #pragma unroll
               for (int wi = 0; wi < 2; ++wi) {
-                const uint32_t w = wv[ch][2 * hb + wi];
+                const uint32_t w = wv[c][2 * hb + wi];
                 e2m1x4_to_bf16(w, mul, out + 8 * hb + 4 * wi);
                 e2m1x4_to_bf16(w >> 16, mul, out + 8 * hb + 4 * wi + 2);
               }
@@ -946,25 +954,25 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
   }
 }
 
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(threads_q(kMx8), 1)
     moe_gate_up_swiglu_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                     const __grid_constant__ TokenMapSet tx, const Params p) {
   expert_gemm_fp8_body<kGateUp, kMx8>(tmap_w, tx, p);
 }
 
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(threads_q(kMx8), 1)
     moe_down_mxfp8_kernel(const __grid_constant__ CUtensorMap tmap_w,
                           const __grid_constant__ TokenMapSet tx, const Params p) {
   expert_gemm_fp8_body<kDown, kMx8>(tmap_w, tx, p);
 }
 
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(threads_q(kNv4), 1)
     moe_gate_up_swiglu_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                     const __grid_constant__ TokenMapSet tx, const Params p) {
   expert_gemm_fp8_body<kGateUp, kNv4>(tmap_w, tx, p);
 }
 
-__global__ void __launch_bounds__(kThreads8, 1)
+__global__ void __launch_bounds__(threads_q(kNv4), 1)
     moe_down_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                           const __grid_constant__ TokenMapSet tx, const Params p) {
   expert_gemm_fp8_body<kDown, kNv4>(tmap_w, tx, p);
@@ -1074,7 +1082,7 @@ cudaError_t launch_expert(cudaStream_t s, const char* name, ExpertKernel k, int 
 // One CTA per SM (the kernels take all the shared memory), static stride over tiles.
 cudaError_t launch_expert_1cta(cudaStream_t s, const char* name, ExpertKernel k, int which,
                                const CUtensorMap& mw, const TokenMapSet& mx, Params p,
-                               long long tiles_bound) {
+                               long long tiles_bound, int threads) {
   const int smem = ensure_smem_attr(k, which);
   if (smem <= 0) {
     cudaGetLastError();
@@ -1083,7 +1091,7 @@ cudaError_t launch_expert_1cta(cudaStream_t s, const char* name, ExpertKernel k,
   p.smem_bytes = smem;
   const long long grid = std::max(1LL, std::min<long long>(device_sm_count(), tiles_bound));
   KernelScope scope(s, name);
-  return launch_kernel(k, dim3(static_cast<unsigned>(grid)), dim3(kThreads8),
+  return launch_kernel(k, dim3(static_cast<unsigned>(grid)), dim3(threads),
                        static_cast<size_t>(smem), s, mw, mx, p);
 }
 
@@ -1197,9 +1205,9 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
   p.status = status;
   p.timeout_ns = timeout_ns;
   e = nv ? launch_expert_1cta(s, "moe_gate_up_swiglu_nvfp4", moe_gate_up_swiglu_nvfp4_kernel, 4,
-                              mw, mx, p, chunks_bound * p.slabs)
+                              mw, mx, p, chunks_bound * p.slabs, threads_q(kNv4))
          : launch_expert_1cta(s, "moe_gate_up_swiglu_mxfp8", moe_gate_up_swiglu_mxfp8_kernel, 2,
-                              mw, mx, p, chunks_bound * p.slabs);
+                              mw, mx, p, chunks_bound * p.slabs, threads_q(kMx8));
   if (e != cudaSuccess) return e;
 
   CUtensorMap mw2;
@@ -1226,9 +1234,9 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
   q.status = status;
   q.timeout_ns = timeout_ns;
   return nv ? launch_expert_1cta(s, "moe_down_nvfp4", moe_down_nvfp4_kernel, 5, mw2, mx2, q,
-                                 chunks_bound * q.slabs)
+                                 chunks_bound * q.slabs, threads_q(kNv4))
             : launch_expert_1cta(s, "moe_down_mxfp8", moe_down_mxfp8_kernel, 3, mw2, mx2, q,
-                                 chunks_bound * q.slabs);
+                                 chunks_bound * q.slabs, threads_q(kMx8));
 }
 
 }  // namespace moe
