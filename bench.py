@@ -7,14 +7,15 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--also NAME,...] [--also-mxfp8 NAME,...]
+                  [--also-nvfp4 NAME,...]
 
 Default workload: the Qwen3-235B-A22B MoE layer on a 64-token decode batch
 (d=4096, E=128, top-8, I=1536).  Its 4.8 GB of expert weights exceed the
 129 MB L2, so every step streams them from HBM (no flush needed).
 --impl reference times the fp64 CPU oracle on the host cores instead.
 The "also" entries measure further workloads at N=1: --also with bf16
-weights, --also-mxfp8 with the expert weights quantised to MXFP8 once
-before timing (moe_forward_mxfp8).
+weights, --also-mxfp8 / --also-nvfp4 with the expert weights quantised to
+MXFP8 / NVFP4 once before timing (moe_forward_mxfp8 / moe_forward_nvfp4).
 Inside the timed region the dominant kernel is bracketed by CUDA events on
 every 10th step (for the roofline's achieved rate); the per-kernel breakdown
 ("kernels") comes from a traced pass of up to 50 steps just before it.
@@ -55,6 +56,8 @@ def parse_args():
                     help="comma-separated extra workloads measured at N=1 (empty for none)")
     ap.add_argument("--also-mxfp8", default=f"{W.DECODE},{W.PREFILL}",
                     help="workloads also measured at N=1 with MXFP8 expert weights (empty for none)")
+    ap.add_argument("--also-nvfp4", default=f"{W.DECODE},{W.PREFILL}",
+                    help="workloads also measured at N=1 with NVFP4 expert weights (empty for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (smaller cases for profiler captures)")
@@ -168,6 +171,7 @@ def ncu_traffic(kernel, workload):
 
 
 MX_BYTES = 1 + 1 / 32  # MXFP8 weight bytes per parameter: E4M3 code + E8M0 scale per 32
+NV_BYTES = 0.5 + 1 / 16  # NVFP4: E2M1 code + E4M3 scale per 16 (tensor scales negligible)
 
 
 def kernel_work(name, w, counts):
@@ -177,6 +181,10 @@ def kernel_work(name, w, counts):
     T, d, E, k, I, Is = w.T, w.d, w.E, w.top_k, w.I, w.I_shared
     rows = T * k
     touched = sum(1 for c in counts if c > 0)
+    if name == "moe_gate_up_swiglu_nvfp4":
+        return 4 * rows * d * I, int(touched * 2 * I * d * NV_BYTES) + rows * d * 2 + rows * I * 2
+    if name == "moe_down_nvfp4":
+        return 2 * rows * d * I, int(touched * d * I * NV_BYTES) + rows * I * 2 + rows * d * 4
     if name == "moe_gate_up_swiglu_mxfp8":
         return 4 * rows * d * I, int(touched * 2 * I * d * MX_BYTES) + rows * d * 2 + rows * I * 2
     if name == "moe_down_mxfp8":
@@ -204,9 +212,9 @@ def kernel_work(name, w, counts):
 # ------------------------------------------------------------------ our arm
 
 def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, peaks,
-            mxfp8=False):
-    """mxfp8: the expert weights are quantised to MXFP8 once, outside the
-    timed region, and every step runs moe_forward_mxfp8 on them."""
+            mxfp8=False, nvfp4=False):
+    """mxfp8 / nvfp4: the expert weights are quantised once, outside the
+    timed region, and every step runs moe_forward_mxfp8 / _nvfp4 on them."""
     import torch
     from mixture_experts_layer_20_gb300 import counters as C
     x = W.make_x(w, device="cuda")
@@ -220,6 +228,12 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
 
         def step():
             moe.moe_forward_mxfp8(x, params["w_router"], mx_gu, mx_d, w.top_k, **kw)
+    elif nvfp4:
+        nv_gu = moe.moe_nvfp4_quantize(params["w_gate_up"])
+        nv_d = moe.moe_nvfp4_quantize(params["w_down"])
+
+        def step():
+            moe.moe_forward_nvfp4(x, params["w_router"], nv_gu, nv_d, w.top_k, **kw)
     else:
         def step():
             moe.moe_forward(x, params["w_router"], params["w_gate_up"], params["w_down"], w.top_k,
@@ -314,9 +328,9 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
 
     flops = C.expert_flops(w.T, w.top_k, w.d, w.I, w.I_shared)
     abytes = C.algorithmic_bytes(counts, w.T, w.d, w.E, w.I, w.I_shared)
-    if mxfp8:  # routed expert weights at MX_BYTES per parameter instead of 2
+    if mxfp8 or nvfp4:  # routed expert weights at MX_BYTES / NV_BYTES per parameter, not 2
         tw = C.touched_weight_bytes(counts, w.d, w.I)
-        abytes += int(tw * MX_BYTES / 2) - tw
+        abytes += int(tw * (MX_BYTES if mxfp8 else NV_BYTES) / 2) - tw
     layer = {
         "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
         "tc_peak_frac": round(flops / (ms * 1e-3) / 1e12 / tensor_peak, 4),
@@ -522,14 +536,18 @@ def main():
             if not same:
                 del pa
             torch.cuda.empty_cache()
-        for name in [n for n in args.also_mxfp8.split(",") if n]:
+        quant = [(n, "mxfp8") for n in args.also_mxfp8.split(",") if n] + \
+            [(n, "nvfp4") for n in args.also_nvfp4.split(",") if n]
+        labels = {"mxfp8": "mxfp8 (E4M3 codes, E8M0 scale per 32)",
+                  "nvfp4": "nvfp4 (E2M1 codes, E4M3 scale per 16, fp32 scale per expert matrix)"}
+        for name, fmt in quant:
             wa = W.WORKLOADS[name]
             same = (wa.d, wa.E, wa.I, wa.I_shared, wa.zipf_bias, wa.seed) == \
                 (w.d, w.E, w.I, w.I_shared, w.zipf_bias, w.seed)
             pa = params if same else W.make_weights(wa, device="cuda")
             ra = measure(moe, W, wa, pa, max(3, args.steps // 10), 3, 0, 1, None, smi_index, peaks,
-                         mxfp8=True)
-            also.append({"workload": name, "weights": "mxfp8 (E4M3 codes, E8M0 scale per 32)",
+                         mxfp8=fmt == "mxfp8", nvfp4=fmt == "nvfp4")
+            also.append({"workload": name, "weights": labels[fmt],
                          "value": round(ra["tokens_per_s"], 1), "unit": "tokens/s",
                          "ms_per_step": round(ra["ms"], 4), "clocks": ra["clocks"],
                          "layer": ra["layer"], "roofline": ra["roofline"],
