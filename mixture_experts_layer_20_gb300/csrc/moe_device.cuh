@@ -217,21 +217,8 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// 32 lanes x 32 bits, 32 consecutive columns: thread i of the warp gets row
-// (lane base + i), columns [col, col+32).
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
+// 32 lanes x 32 bits, 16 consecutive columns: thread i of the warp gets row
+// (lane base + i), columns [col, col+16).
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -329,15 +316,6 @@ __device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar, int c0, int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map,
                                                  uint32_t bar, int c0, int c1, int c2, int c3,
                                                  int c4) {
@@ -399,12 +377,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
       " [%0], %1;" ::"r"(bar),
       "h"(static_cast<uint16_t>(3))
       : "memory");
-}
-
-// Barrier over `threads` threads (whole warps) with a fixed id (1..15).
-template <int ID>
-__device__ __forceinline__ void named_barrier_sync(uint32_t threads) {
-  asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
