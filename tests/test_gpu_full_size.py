@@ -68,3 +68,52 @@ def test_full_size_sampled(moe, name):
     got = f64(out[torch.as_tensor(tokens, device="cuda")])
     max_rel, mean_rel = assert_layer_close(got, ref, name)
     print(f"{name}: sampled {tokens.size} tokens max_rel={max_rel:.3e} mean_rel={mean_rel:.3e}")
+
+
+class _DequantisedExperts:
+    """Lazy per-expert oracle round trip (quantise, dequantise) of a [E, rows, K]
+    bf16 device weight tensor: bf16 bits for MXFP8 (exact), fp64 values for NVFP4."""
+
+    def __init__(self, t: torch.Tensor, fmt: str):
+        self.t, self.fmt, self.cache = t, fmt, {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            vals = oracle.bf16_bits_to_f64(W.to_bits(self.t[e]))
+            if self.fmt == "mxfp8":
+                deq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(vals))
+                self.cache[e] = oracle.f64_to_bf16_bits(deq)
+            else:
+                self.cache[e] = oracle.nvfp4_dequantize(*oracle.nvfp4_quantize(vals.astype(np.float32)))
+        return self.cache[e]
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_full_size_decode_quantised_weights_sampled(moe, fmt):
+    """The decode workload with MXFP8 / NVFP4 expert weights, as the benchmark
+    runs it: routing for every token, and two sampled tokens' outputs against
+    the oracle on its own quantisation of their experts' weights."""
+    w = W.WORKLOADS[W.DECODE]
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k)
+    if fmt == "mxfp8":
+        out = moe.moe_forward_mxfp8(x, p["w_router"], moe.moe_mxfp8_quantize(p["w_gate_up"]),
+                                    moe.moe_mxfp8_quantize(p["w_down"]), w.top_k, ws=ws)
+    else:
+        out = moe.moe_forward_nvfp4(x, p["w_router"], moe.moe_nvfp4_quantize(p["w_gate_up"]),
+                                    moe.moe_nvfp4_quantize(p["w_down"]), w.top_k, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, w.T, w.d, w.E, w.I, w.top_k)
+    ids_ref, gates_ref, logits = oracle.route(W.to_bits(x), W.to_bits(p["w_router"]), w.top_k)
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ids_ref, gates_ref, logits, w.top_k)
+    cand = np.setdiff1d(np.arange(w.T), differ)
+    tokens = np.array([cand[0], cand[-1]])
+    ref = oracle.forward_tokens(W.to_bits(x), tokens, ids_ref, gates_ref,
+                                _DequantisedExperts(p["w_gate_up"], fmt),
+                                _DequantisedExperts(p["w_down"], fmt), None, None)
+    got = f64(out[torch.as_tensor(tokens, device="cuda")])
+    max_rel, mean_rel = assert_layer_close(got, ref, f"decode {fmt}")
+    print(f"decode {fmt}: sampled {tokens.size} tokens max_rel={max_rel:.3e} mean_rel={mean_rel:.3e}")
