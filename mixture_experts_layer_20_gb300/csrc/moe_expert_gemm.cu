@@ -59,8 +59,11 @@ namespace {
 
 constexpr int kBK = 64;     // one 128-byte swizzle row of bf16: the K of one TMA box
 constexpr int kSub = 2;     // K boxes per pipeline stage: 8 MMAs per barrier round
-constexpr int kMaxStages = 4;                      // pipeline stages that fit when chunks are <= 192 tokens
+constexpr int kMaxStages = 4;                      // down: pipeline stages (3 for 256-token chunks)
+constexpr int kMaxStagesGateUp = 6;                // gate_up: more stages when chunks are small
 constexpr int kMaxStagesWide = 6;                  // one K box per stage (wide chunks)
+static_assert(kMaxStages <= kMaxStagesWide && kMaxStagesGateUp <= kMaxStagesWide,
+              "the barrier arrays hold kMaxStagesWide stages");
 constexpr int kTokMaxWide = 512;                   // wide chunks: two MMAs of up to 256 tokens
 constexpr int kWideRowsPerGroup = 256;             // launches with this many rows per expert go wide
 constexpr int kWRows = 128;                        // weight rows per CTA
@@ -351,7 +354,11 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   const uint32_t b_sub_bytes = static_cast<uint32_t>(s_half_max) * kBK * 2;
   const uint32_t stage_bytes = ksub * (kABytes + b_sub_bytes);
   const uint32_t avail = static_cast<uint32_t>(p.smem_bytes) - (base - smem_u32(smem_raw));
-  const int nst = min(wide ? kMaxStagesWide : kMaxStages, static_cast<int>(avail / stage_bytes));
+  // Measured at decode (16-token chunks): gate_up streams its weights at 6.95
+  // TB/s with six stages in flight against 6.85 with four; down, whose tiles
+  // are 12 stages long, is slower with more (248 against 239 us).
+  const int max_st = wide ? kMaxStagesWide : (KIND == kGateUp ? kMaxStagesGateUp : kMaxStages);
+  const int nst = min(max_st, static_cast<int>(avail / stage_bytes));
 
   if (warp == 0) {
     // ---------------- TMA producer (warp 0 of both CTAs, own shared memory;
