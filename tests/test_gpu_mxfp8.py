@@ -61,6 +61,7 @@ FORWARD_CASES = [
     (600, 512, 8, 4, 384, 0, False),     # ~300 rows per expert: three chunks, six slabs
     (200, 384, 16, 4, 128, 0, True),     # d = 384: the last down slab has one populated half
     (130, 768, 64, 8, 256, 128, True),   # bias and a (bf16) shared expert
+    (1, 256, 8, 2, 128, 0, False),       # one token
 ]
 
 

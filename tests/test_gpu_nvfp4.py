@@ -79,6 +79,7 @@ FORWARD_CASES = [
     (600, 512, 8, 4, 512, 0, False),     # ~300 rows per expert: three chunks
     (200, 768, 16, 4, 256, 0, True),     # d = 768: three 128-row down slabs
     (130, 1024, 32, 8, 256, 256, True),  # bias and a (bf16) shared expert
+    (1, 256, 8, 2, 256, 0, False),       # one token
 ]
 
 
