@@ -209,6 +209,30 @@ def kernel_work(name, w, counts):
     return 0, rows * 4 * 4
 
 
+# ------------------------------------------------------------------ ranks
+# Replicas: each rank runs the whole layer on its own batch; the job's time is
+# the slowest rank's and its throughput all ranks' tokens over that time.
+
+def slowest_rank(dist, ms, device):
+    """Max over ranks of a per-rank time (the identity without a process group)."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_rate(dist, per_rank_rate, world, device):
+    """Whole-job rate from per-rank rates: world x the slowest rank's rate."""
+    if not dist:
+        return per_rank_rate
+    import torch
+    t = torch.tensor([per_rank_rate], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return t.item() * world
+
+
 # ------------------------------------------------------------------ our arm
 
 def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, peaks,
@@ -290,11 +314,7 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
     if dist:
         dist.barrier()
     clocks = sampler.stop(t0, t1) if sampler else None
-    ms = start.elapsed_time(stop) / steps
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+    ms = slowest_rank(dist, start.elapsed_time(stop) / steps, "cuda")
     if moe.moe_get_device_status(ws) != moe.MOE_OK:
         raise RuntimeError("device status not OK after the timed region")
 
@@ -516,9 +536,7 @@ def main():
     r = measure(moe, W, w, params, args.steps, args.warmup, rank, world, dist, smi_index, peaks)
     e2e = measure_e2e(moe, w, params, r["ws"], r["x"], max(10, min(args.steps, 100)))
     if dist:
-        t = torch.tensor([e2e["value"]], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MIN)
-        e2e["value"] = round(t.item() * world, 1)
+        e2e["value"] = round(job_rate(dist, e2e["value"], world, "cuda"), 1)
 
     also = []
     if world == 1:
