@@ -184,26 +184,26 @@ def kernel_work(name, w, counts):
     if name == "moe_gate_up_swiglu_nvfp4":
         return 4 * rows * d * I, int(touched * 2 * I * d * NV_BYTES) + rows * d * 2 + rows * I * 2
     if name == "moe_down_nvfp4":
-        return 2 * rows * d * I, int(touched * d * I * NV_BYTES) + rows * I * 2 + rows * d * 4
+        return 2 * rows * d * I, int(touched * d * I * NV_BYTES) + rows * I * 2 + rows * d * 2
     if name == "moe_gate_up_swiglu_mxfp8":
         return 4 * rows * d * I, int(touched * 2 * I * d * MX_BYTES) + rows * d * 2 + rows * I * 2
     if name == "moe_down_mxfp8":
-        return 2 * rows * d * I, int(touched * d * I * MX_BYTES) + rows * I * 2 + rows * d * 4
+        return 2 * rows * d * I, int(touched * d * I * MX_BYTES) + rows * I * 2 + rows * d * 2
     if name == "moe_gate_up_swiglu":
         return 4 * rows * d * I, touched * 2 * I * d * 2 + rows * d * 2 + rows * I * 2
     if name == "moe_down":
-        return 2 * rows * d * I, touched * d * I * 2 + rows * I * 2 + rows * d * 4
+        return 2 * rows * d * I, touched * d * I * 2 + rows * I * 2 + rows * d * 2
     if name == "moe_shared_gate_up_swiglu":
         return 4 * T * d * Is, 2 * Is * d * 2 + T * d * 2 + T * Is * 2
     if name == "moe_shared_down":
-        return 2 * T * d * Is, d * Is * 2 + T * Is * 2 + T * d * 4
+        return 2 * T * d * Is, d * Is * 2 + T * Is * 2 + T * d * 2
     partial = ((d + 511) // 512) * T * ((E + 15) // 16 * 16) * 4
     if name == "moe_router_logits":
         return C.router_flops(T, d, E), T * d * 2 + E * d * 2 + partial
     if name == "moe_router_topk":
         return 0, partial + rows * 8
     if name == "moe_combine":
-        return 2 * rows * d, rows * d * 4 + T * d * 2 + rows * 8 + (T * d * 4 if Is else 0)
+        return 2 * rows * d, rows * d * 2 + T * d * 2 + rows * 8 + (T * d * 2 if Is else 0)
     if name == "moe_permute_gather":
         return 0, rows * d * 2 + T * d * 2 + rows * 4
     return 0, rows * 4 * 4

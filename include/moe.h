@@ -14,7 +14,7 @@
  *                 and a stable grouping of the T*k assignments by expert.
  *   3. expert   : each expert e is a SwiGLU FFN of three d x I matrices:
  *                 h = silu(x W_gate^T) * (x W_up^T), rounded to bf16;
- *                 y = h W_down^T, kept in fp32.
+ *                 y = h W_down^T, accumulated in fp32, stored in fp16.
  *   4. combine  : out[t] = sum_j gates[t,j] * y[slot_pos[t,j]] (+ shared
  *                 expert output), summed in fp32 in slot order, rounded once
  *                 to bf16.
@@ -35,7 +35,8 @@
  *     that must start at zero (moe_workspace_init).  Kernels record there what
  *     they find on the device: an expert id out of range, inconsistent
  *     offsets or slot positions (MOE_ERR_DEVICE_CHECK), a wait that gave up
- *     (MOE_ERR_TIMEOUT).  Such a kernel skips the bad work instead of faulting;
+ *     (MOE_ERR_TIMEOUT), an expert output outside fp16 range (MOE_ERR_RANGE).
+ *     Such a kernel skips the bad work instead of faulting;
  *     read the word with moe_get_device_status().
  *   - Calls that share a workspace must be ordered on one stream.
  */
@@ -56,10 +57,12 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,     /* workspace too small */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
   MOE_ERR_TIMEOUT = 5,       /* a device-side wait gave up (bounded) */
-  MOE_ERR_DEVICE_CHECK = 6   /* device-side validation found bad indices */
+  MOE_ERR_DEVICE_CHECK = 6,  /* device-side validation found bad indices */
+  MOE_ERR_RANGE = 7          /* an expert output left the fp16 range of y */
 } moe_status_t;
 
 typedef uint16_t moe_bf16;
+typedef uint16_t moe_f16;   /* raw bits of an IEEE binary16 value */
 typedef struct CUstream_st* moe_stream_t;  /* same type as cudaStream_t */
 
 /* Workspace bytes that moe_forward / moe_forward_ex need for these shapes;
@@ -145,7 +148,9 @@ moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, const moe_bf16*
 
 /* Step 3, grouped expert FFN.  Rows [expert_offsets[e], expert_offsets[e+1])
  * of x_perm [rows,d] go through expert e: w_gate_up [E,2I,d] (per expert,
- * rows [0,I) gate, [I,2I) up), w_down [E,d,I].  Writes y [rows,d] fp32.
+ * rows [0,I) gate, [I,2I) up), w_down [E,d,I].  Writes y [rows,d] fp16: the
+ * fp32 accumulators rounded to nearest; finite values beyond +-65504 are
+ * stored as +-65504 (inf and NaN as they are) and flag MOE_ERR_RANGE.
  * h is kept in the workspace as bf16.  Offsets that do not start at 0, go
  * down, or do not end at `rows` make the kernels skip all work and flag
  * MOE_ERR_DEVICE_CHECK.
@@ -153,17 +158,17 @@ moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, const moe_bf16*
  * expert, F_e(m) = 2 m P_e) and section 9.4.3 (grouped GEMM). */
 moe_status_t moe_expert_ffn(const moe_bf16* x_perm, const int32_t* expert_offsets,
                             const moe_bf16* w_gate_up, const moe_bf16* w_down,
-                            int rows, int d, int E, int I, float* y,
+                            int rows, int d, int E, int I, moe_f16* y,
                             void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Step 4, combine.  out[t] = bf16( sum_{j<top_k} topk_gates[t,j] *
  * y[slot_pos[t,j]] (+ y_shared[t]) ), fp32 sums in j order (deterministic).
- * y [rows,d] fp32 with rows = T*top_k, y_shared [T,d] fp32 or NULL.
+ * y [rows,d] fp16 with rows = T*top_k, y_shared [T,d] fp16 or NULL.
  * A slot position outside [0,rows) is skipped and flagged.
  * Cite: 'Chapter 9. Distributed inference', section 9.3.4, step four;
  * 'Hosting Qwen on Blackwell', "MoE Dispatch - Combine". */
-moe_status_t moe_combine(const float* y, const int32_t* slot_pos,
-                         const float* topk_gates, const float* y_shared,
+moe_status_t moe_combine(const moe_f16* y, const int32_t* slot_pos,
+                         const float* topk_gates, const moe_f16* y_shared,
                          int T, int d, int top_k, moe_bf16* out,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 

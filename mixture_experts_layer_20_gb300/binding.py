@@ -76,7 +76,7 @@ for _name, (_res, _args) in _SIGS.items():
     _f.restype, _f.argtypes = _res, _args
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, \
-    MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK = range(7)
+    MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK, MOE_ERR_RANGE = range(8)
 
 
 class MoeError(RuntimeError):
@@ -133,7 +133,7 @@ def new_workspace(T, d, E, I, top_k, I_shared=0, device="cuda") -> torch.Tensor:
 
 def moe_get_device_status(ws: torch.Tensor, stream=None) -> int:
     """Synchronise, read and clear the workspace's device status (MOE_OK,
-    MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK)."""
+    MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK or MOE_ERR_RANGE)."""
     return int(_lib.moe_get_device_status(_p(ws), ws.numel(), _stream(stream)))
 
 
@@ -236,8 +236,8 @@ def moe_expert_ffn(x_perm, expert_offsets, w_gate_up, w_down, y=None, ws=None, s
     E, I2, _ = w_gate_up.shape
     I = I2 // 2
     if y is None:
-        y = torch.empty((rows, d), dtype=torch.float32, device=x_perm.device)
-    _want(y, torch.float32, "y")
+        y = torch.empty((rows, d), dtype=torch.float16, device=x_perm.device)
+    _want(y, torch.float16, "y")
     if ws is None:
         ws = new_workspace(rows, d, E, I, 1, device=x_perm.device)
     _check(_lib.moe_expert_ffn(_p(x_perm), _p(expert_offsets), _p(w_gate_up), _p(w_down), rows, d,
@@ -246,8 +246,8 @@ def moe_expert_ffn(x_perm, expert_offsets, w_gate_up, w_down, y=None, ws=None, s
 
 
 def moe_combine(y, slot_pos, topk_gates, y_shared=None, out=None, ws=None, stream=None):
-    _want(y, torch.float32, "y"); _want(slot_pos, torch.int32, "slot_pos")
-    _want(topk_gates, torch.float32, "topk_gates"); _want(y_shared, torch.float32, "y_shared")
+    _want(y, torch.float16, "y"); _want(slot_pos, torch.int32, "slot_pos")
+    _want(topk_gates, torch.float32, "topk_gates"); _want(y_shared, torch.float16, "y_shared")
     T, k = slot_pos.shape
     d = y.shape[1]
     if out is None:
@@ -470,5 +470,5 @@ def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0) -> dict:
         "slot_pos": view(L["slot_pos"], n, torch.int32, (T, top_k)),
         "x_perm": view(L["x_perm"], n * d, torch.bfloat16, (n, d)),
         "h": view(L["h"], n * I, torch.bfloat16, (n, I)),
-        "y": view(L["y"], n * d, torch.float32, (n, d)),
+        "y": view(L["y"], n * d, torch.float16, (n, d)),
     }

@@ -101,8 +101,8 @@ Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
   L.x_perm = take(n * d * 2);
   L.h = take(n * I * 2);
   L.h_shared = take(static_cast<size_t>(T) * I_shared * 2);
-  L.y = take(n * d * 4);
-  L.y_shared = take(I_shared ? static_cast<size_t>(T) * d * 4 : 0);
+  L.y = take(n * d * 2);
+  L.y_shared = take(I_shared ? static_cast<size_t>(T) * d * 2 : 0);
   L.x_stage = take(static_cast<size_t>(T) * d * 2);
   L.out_stage = take(static_cast<size_t>(T) * d * 2);
   L.total = off;
@@ -283,7 +283,7 @@ moe_status_t moe_permute(const int32_t* topk_ids, const moe_bf16* x, int T, int 
 
 moe_status_t moe_expert_ffn(const moe_bf16* x_perm, const int32_t* expert_offsets,
                             const moe_bf16* w_gate_up, const moe_bf16* w_down, int rows, int d,
-                            int E, int I, float* y, void* ws, size_t ws_bytes,
+                            int E, int I, moe_f16* y, void* ws, size_t ws_bytes,
                             moe_stream_t stream) {
   moe_status_t st = check_shapes(rows, d, E, I, 1);
   if (st != MOE_OK) return st;
@@ -302,8 +302,8 @@ moe_status_t moe_expert_ffn(const moe_bf16* x_perm, const int32_t* expert_offset
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "expert FFN launch");
 }
 
-moe_status_t moe_combine(const float* y, const int32_t* slot_pos, const float* topk_gates,
-                         const float* y_shared, int T, int d, int top_k, moe_bf16* out, void* ws,
+moe_status_t moe_combine(const moe_f16* y, const int32_t* slot_pos, const float* topk_gates,
+                         const moe_f16* y_shared, int T, int d, int top_k, moe_bf16* out, void* ws,
                          size_t ws_bytes, moe_stream_t stream) {
   moe_status_t st = check_shapes(T, d, top_k, 64, top_k);
   if (st != MOE_OK) return st;
@@ -368,7 +368,7 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   int32_t* slot_pos = reinterpret_cast<int32_t*>(w + L.slot_pos);
   int32_t* table = reinterpret_cast<int32_t*>(w + L.chunk);
   void* h = w + L.h;
-  float* y = reinterpret_cast<float*>(w + L.y);
+  void* y = w + L.y;
   const unsigned long long tmo = g_timeout_ns.load();
   const int rows = T * top_k;
 
@@ -393,9 +393,9 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
          : launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status,
                               tmo, gather_rows ? &gather : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
-  float* y_shared = nullptr;
+  void* y_shared = nullptr;
   if (I_shared) {
-    y_shared = reinterpret_cast<float*>(w + L.y_shared);
+    y_shared = w + L.y_shared;
     e = launch_grouped_ffn(s, x, nullptr, T, d, 1, I_shared, wgu_s, wd_s, w + L.h_shared,
                            y_shared, status, tmo);
     if (e != cudaSuccess) return cuda_fail(e, "shared expert launch");
@@ -587,6 +587,8 @@ moe_status_t moe_get_device_status(void* ws, size_t ws_bytes, moe_stream_t strea
   }
   if (word & kStatusTimeout) return fail(MOE_ERR_TIMEOUT, "a device-side wait gave up");
   if (word & kStatusDeviceCheck) return fail(MOE_ERR_DEVICE_CHECK, "device-side check failed");
+  if (word & kStatusRange)
+    return fail(MOE_ERR_RANGE, "an expert output was outside the fp16 range of y");
   return MOE_OK;
 }
 
@@ -598,6 +600,7 @@ const char* moe_status_string(moe_status_t s) {
     case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_RANGE: return "MOE_ERR_RANGE";
     case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
   }
   return "MOE_ERR_UNKNOWN";

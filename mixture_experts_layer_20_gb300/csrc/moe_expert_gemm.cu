@@ -75,6 +75,7 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kEpiArrivals = 8;               // 4 epilogue warps x 2 CTAs
+constexpr float kHalfMax = 65504.0f;               // largest finite fp16
 
 enum Kind : int { kGateUp = 1, kDown = 2 };
 
@@ -87,7 +88,7 @@ struct Params {
   int total_rows;         // token rows of the B operand
   int w_rows_per_group;   // weight rows per expert in the A tensor map
   int up_offset;          // gate_up: I
-  void* out;              // gate_up: h bf16 [rows, I]; down: y fp32 [rows, d]
+  void* out;              // gate_up: h bf16 [rows, I]; down: y fp16 [rows, d]
   long long ld_out;
   // Token rows gathered on the fly (null: B is [total_rows, K] in row order):
   // B row of slot pos is row gather_perm[pos] / gather_div of the map over
@@ -212,7 +213,9 @@ __device__ __forceinline__ void build_schedule(const Params& p, int* s_off, int*
 
 // Epilogue of one tile (one of warps 2-5, q = warp % 4, reading TMEM lanes
 // 32 q .. 32 q + 31 from t_row): gate_up stores h = silu(gate) * up in bf16,
-// down stores y in fp32; `live` false (a wait gave up) stores nothing.
+// down stores y in fp16; `live` false (a wait gave up) stores nothing.
+// y in fp16: finite values beyond +-65504 are stored as +-65504, inf and NaN
+// as they are, and any of them sets kStatusRange.
 template <int KIND, int SLAB = (KIND == kGateUp ? 128 : 256)>
 __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, bool live,
                                               const Params& p, int q, int lane, uint32_t rank,
@@ -222,28 +225,36 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, boo
   if constexpr (KIND == kDown) {
     const int col = t.slab * SLAB + rank * 128 + q * 32 + lane;
     const bool col_ok = live && col < p.n_out;
+    bool out_of_range = false;
 #pragma unroll 1
     for (int c = 0; c < t.n; c += 16) {
       uint32_t v[16];
       tmem_ld_32x32b_x16(t_row + c, v);
       tmem_ld_wait();
-      if (tscale != 1.0f) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * tscale);
-      }
       const int nvalid = min(16, t.tok_end - t.tok0 - c);  // uniform across the warp
-      float* yp = static_cast<float*>(p.out) + (size_t)(t.tok0 + c) * p.ld_out + col;
+      __half hv[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float f = __uint_as_float(v[j]);
+        if (tscale != 1.0f) f *= tscale;
+        const float a = fabsf(f);
+        if (!(a <= kHalfMax) && j < nvalid) out_of_range = true;
+        if (a > kHalfMax && a < INFINITY) f = copysignf(kHalfMax, f);
+        hv[j] = __float2half_rn(f);
+      }
+      __half* yp = static_cast<__half*>(p.out) + (size_t)(t.tok0 + c) * p.ld_out + col;
       if (col_ok) {
         if (nvalid == 16) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) yp[(size_t)j * p.ld_out] = __uint_as_float(v[j]);
+          for (int j = 0; j < 16; ++j) yp[(size_t)j * p.ld_out] = hv[j];
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (j < nvalid) yp[(size_t)j * p.ld_out] = __uint_as_float(v[j]);
+            if (j < nvalid) yp[(size_t)j * p.ld_out] = hv[j];
         }
       }
     }
+    if (__any_sync(0xffffffffu, col_ok && out_of_range) && lane == 0) atomicOr(p.status, kStatusRange);
   } else {
     // In each warp's quarter of the TMEM lanes, lanes 0-15 hold 16 gate
     // rows and lanes 16-31 the matching up rows (the weight map
@@ -1106,7 +1117,7 @@ cudaError_t launch_expert_1cta(cudaStream_t s, const char* name, ExpertKernel k,
 
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
-                               void* h, float* y, unsigned* status,
+                               void* h, void* y, unsigned* status,
                                unsigned long long timeout_ns, const TokenGather* gather) {
   const int groups = offsets ? E : 1;
   // Down launches with at least 256 rows per expert take wide chunks (up to
@@ -1175,7 +1186,7 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
                                      const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
                                      const float* tscale_gate_up, const uint8_t* codes_down,
                                      const uint8_t* scales_down, const float* tscale_down,
-                                     void* h, float* y, unsigned* status,
+                                     void* h, void* y, unsigned* status,
                                      unsigned long long timeout_ns) {
   const bool nv = fmt == kNv4;
   const uint64_t d_bytes = nv ? d / 2 : d;  // code bytes of a W_gate_up row

@@ -28,6 +28,7 @@ inline size_t router_partial_bytes(int T, int d, int E) {
 // Bits of the workspace's device status word.
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusDeviceCheck = 2u;
+constexpr unsigned kStatusRange = 4u;  // an expert output outside the fp16 range of y
 
 // Programmatic dependent launch.  Every kernel of the layer is launched with
 // programmatic stream serialisation, so it may be scheduled while the kernel
@@ -127,10 +128,10 @@ struct TokenGather {
 // of a [rows, d] go through expert e (weights per expert: w_gate_up [2I, d],
 // w_down [d, I]).  offsets == nullptr: a single expert on all `rows` rows.
 // With `gather`, a is not read: gate_up gathers its rows (see TokenGather).
-// Writes h [rows, I] bf16 (scratch) and y [rows, d] fp32.
+// Writes h [rows, I] bf16 (scratch) and y [rows, d] fp16.
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
-                               void* h, float* y, unsigned* status,
+                               void* h, void* y, unsigned* status,
                                unsigned long long timeout_ns,
                                const TokenGather* gather = nullptr);
 
@@ -145,7 +146,7 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
                                      const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
                                      const float* tscale_gate_up, const uint8_t* codes_down,
                                      const uint8_t* scales_down, const float* tscale_down,
-                                     void* h, float* y, unsigned* status,
+                                     void* h, void* y, unsigned* status,
                                      unsigned long long timeout_ns);
 
 // NVFP4 quantisation of `groups` matrices [rows_per_group, K] (K a multiple of
@@ -161,8 +162,8 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
                            int32_t* slot_pos, void* x_perm, int32_t* chunk_table,
                            unsigned* status);
 
-cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_pos,
-                           const float* gates, const float* y_shared, int T, int d, int top_k,
+cudaError_t launch_combine(cudaStream_t s, const void* y, const int32_t* slot_pos,
+                           const float* gates, const void* y_shared, int T, int d, int top_k,
                            void* out, unsigned* status);
 
 // ---- MXFP8 weights (moe_mxfp8.cu)

@@ -18,10 +18,11 @@
 //
 // Combine ('Chapter 9. Distributed inference', section 9.3.4, step four;
 // 'Hosting Qwen on Blackwell', "MoE Dispatch - Combine": weighted
-// accumulation): each thread sums 4 columns of one token's k weighted rows in
-// fp32 in slot order, then rounds once to bf16.
+// accumulation): each thread sums 8 columns of one token's k weighted rows
+// (fp16 expert outputs) in fp32 in slot order, then rounds once to bf16.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "moe_device.cuh"
 #include "moe_internal.h"
@@ -274,19 +275,20 @@ __global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* 
   }
 }
 
-// One thread: 4 columns of one token, all k slot rows loaded before the sum
-// (k independent 16-byte loads in flight per thread), then the fp32 sum in
-// slot order and one bf16 rounding.  A block covers 1024 columns of a token.
+// One thread: 8 columns of one token, all k slot rows of fp16 y loaded before
+// the sum (k independent 16-byte loads in flight per thread), then the fp32
+// sum in slot order and one bf16 rounding.  A block covers 2048 columns of a
+// token.
 constexpr int kCombineThreads = 256;
-constexpr int kCombineCols = kCombineThreads * 4;
+constexpr int kCombineCols = kCombineThreads * 8;
 
 __global__ void __launch_bounds__(kCombineThreads) moe_combine_kernel(
-    const float* __restrict__ y, const int32_t* __restrict__ slot_pos,
-    const float* __restrict__ gates, const float* __restrict__ y_shared, int T, int d, int k,
+    const __half* __restrict__ y, const int32_t* __restrict__ slot_pos,
+    const float* __restrict__ gates, const __half* __restrict__ y_shared, int T, int d, int k,
     int rows, int blocks_per_token, __nv_bfloat16* __restrict__ out, unsigned* status) {
   pdl_wait_and_release();
   const int t = blockIdx.x / blocks_per_token;
-  const int c = (blockIdx.x - t * blocks_per_token) * kCombineCols + threadIdx.x * 4;
+  const int c = (blockIdx.x - t * blocks_per_token) * kCombineCols + threadIdx.x * 8;
   if (t >= T || c >= d) return;
   int pos[kMaxTopK];
   float g[kMaxTopK];
@@ -306,28 +308,40 @@ __global__ void __launch_bounds__(kCombineThreads) moe_combine_kernel(
     }
   }
   if (bad && c == 0) atomicOr(status, kStatusDeviceCheck);
-  float4 v[kMaxTopK];
+  // eight fp16 columns per thread: one 16-byte load per expert row
+  uint4 v[kMaxTopK];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j)
-    if (j < k) v[j] = __ldg(reinterpret_cast<const float4*>(y + (size_t)pos[j] * d + c));
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < k) v[j] = __ldg(reinterpret_cast<const uint4*>(y + (size_t)pos[j] * d + c));
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
     if (j < k) {
-      acc.x = fmaf(g[j], v[j].x, acc.x);
-      acc.y = fmaf(g[j], v[j].y, acc.y);
-      acc.z = fmaf(g[j], v[j].z, acc.z);
-      acc.w = fmaf(g[j], v[j].w, acc.w);
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        acc[2 * i] = fmaf(g[j], f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(g[j], f.y, acc[2 * i + 1]);
+      }
     }
   }
   if (y_shared) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c));
-    acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(y_shared + (size_t)t * d + c));
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      acc[2 * i] += f.x;
+      acc[2 * i + 1] += f.y;
+    }
   }
-  uint2 o;
-  o.x = pack_bf16x2(acc.x, acc.y);
-  o.y = pack_bf16x2(acc.z, acc.w);
-  *reinterpret_cast<uint2*>(out + (size_t)t * d + c) = o;
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(out + (size_t)t * d + c) = o;
 }
 
 }  // namespace
@@ -364,15 +378,16 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
                        status);
 }
 
-cudaError_t launch_combine(cudaStream_t s, const float* y, const int32_t* slot_pos,
-                           const float* gates, const float* y_shared, int T, int d, int top_k,
+cudaError_t launch_combine(cudaStream_t s, const void* y, const int32_t* slot_pos,
+                           const float* gates, const void* y_shared, int T, int d, int top_k,
                            void* out, unsigned* status) {
   const int blocks_per_token = (d + kCombineCols - 1) / kCombineCols;
   const long long grid = static_cast<long long>(T) * blocks_per_token;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   KernelScope scope(s, "moe_combine");
   return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(grid)),
-                       dim3(kCombineThreads), 0, s, y, slot_pos, gates, y_shared, T, d, top_k,
+                       dim3(kCombineThreads), 0, s, static_cast<const __half*>(y), slot_pos,
+                       gates, static_cast<const __half*>(y_shared), T, d, top_k,
                        T * top_k, blocks_per_token, static_cast<__nv_bfloat16*>(out), status);
 }
 

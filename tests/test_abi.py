@@ -76,13 +76,14 @@ def test_workspace_layout():
     assert all(o % 256 == 0 for o in offs)
     n = T * k
     assert lay["x_perm"] + n * d * 2 <= lay["h"]
-    assert lay["y"] + n * d * 4 <= lay["total"]
+    assert lay["y"] + n * d * 2 <= lay["x_stage"]          # y: fp16
     lay5 = b.moe_workspace_layout(8192, 7168, 256, 2048, 8, 2048)
-    assert lay5["y_shared"] + 8192 * 7168 * 4 <= lay5["x_stage"]
+    assert lay5["y_shared"] + 8192 * 7168 * 2 <= lay5["x_stage"]
     assert lay5["out_stage"] + 8192 * 7168 * 2 == lay5["total"]
 
 
 def test_status_strings():
     from mixture_experts_layer_20_gb300 import binding as b
     assert b._lib.moe_status_string(b.MOE_ERR_TIMEOUT) == b"MOE_ERR_TIMEOUT"
+    assert b._lib.moe_status_string(b.MOE_ERR_RANGE) == b"MOE_ERR_RANGE"
     assert b._lib.moe_status_string(b.MOE_OK) == b"MOE_OK"

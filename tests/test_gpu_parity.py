@@ -162,11 +162,11 @@ def test_expert_ffn(moe, counts, d, I):
 def test_combine(moe, T, d, k, shared):
     g = torch.Generator(device="cuda").manual_seed(T * 7 + k)
     rows = T * k
-    y = torch.randn((rows, d), generator=g, device="cuda")
+    y = torch.randn((rows, d), generator=g, device="cuda").half()
     slot_pos = torch.randperm(rows, generator=g, device="cuda").to(torch.int32).view(T, k)
     _, gates = W.random_routing(T, max(k, 8), k, seed=T)
     gates = gates.cuda()
-    ys = torch.randn((T, d), generator=g, device="cuda") if shared else None
+    ys = torch.randn((T, d), generator=g, device="cuda").half() if shared else None
     out = moe.moe_combine(y, slot_pos, gates, y_shared=ys)
     torch.cuda.synchronize()
     ref = oracle.combine(f64(y), slot_pos.cpu().numpy(), f64(gates),

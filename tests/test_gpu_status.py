@@ -52,7 +52,7 @@ def test_bad_offsets_are_flagged(moe):
 
 
 def test_bad_slot_positions_are_flagged(moe):
-    y = torch.ones((20, 64), device="cuda")
+    y = torch.ones((20, 64), dtype=torch.float16, device="cuda")
     slot_pos = torch.arange(20, dtype=torch.int32, device="cuda").view(10, 2).contiguous()
     slot_pos[3, 1] = 20
     gates = torch.full((10, 2), 0.5, device="cuda")
@@ -77,3 +77,31 @@ def test_wait_timeout_is_reported_and_recoverable(moe):
     again = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], w.top_k, ws=ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
     assert torch.equal(again, ref)
+
+
+def test_y_outside_fp16_range_saturates_and_is_flagged(moe):
+    """y is stored in fp16: finite outputs beyond +-65504 become +-65504 and
+    the status word reports MOE_ERR_RANGE; outputs inside the range are
+    unaffected.  W_down is scaled by a power of two, which scales the exact
+    y by the same factor."""
+    import numpy as np
+    import oracle
+    from tests.gpu_util import ExpertsOnHost, assert_layer_close, f64
+    w = W.Workload("r", 48, 256, 2, 1, 128, seed=5)
+    p = W.make_weights(w, device="cuda")
+    x_perm = W.make_x(w, device="cuda")
+    offsets = torch.tensor([0, 20, 48], dtype=torch.int32, device="cuda")
+    y_ref = oracle.expert_ffn(f64(x_perm), offsets.cpu().numpy(), ExpertsOnHost(p["w_gate_up"]),
+                              ExpertsOnHost(p["w_down"]))
+    s = 2.0 ** int(np.ceil(np.log2(4 * 65504 / np.abs(y_ref).max())))  # max |y| in [4, 8) x 65504
+    ws = moe.new_workspace(48, 256, 2, 128, 1)
+    y = moe.moe_expert_ffn(x_perm, offsets, p["w_gate_up"], p["w_down"] * s, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_RANGE
+    ref, got = y_ref * s, f64(y)
+    hi = np.abs(ref) > 65504 * (1 + 2.0**-9)
+    lo = np.abs(ref) < 65504 * (1 - 2.0**-9)
+    assert hi.any() and lo.any()
+    assert (got[hi] == np.sign(ref[hi]) * 65504).all()
+    assert_layer_close(got[lo], ref[lo], "y inside the fp16 range")
+    moe.moe_expert_ffn(x_perm, offsets, p["w_gate_up"], p["w_down"], ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
