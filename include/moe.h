@@ -150,7 +150,8 @@ moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, const moe_bf16*
  * of x_perm [rows,d] go through expert e: w_gate_up [E,2I,d] (per expert,
  * rows [0,I) gate, [I,2I) up), w_down [E,d,I].  Writes y [rows,d] fp16: the
  * fp32 accumulators rounded to nearest; finite values beyond +-65504 are
- * stored as +-65504 (inf and NaN as they are) and flag MOE_ERR_RANGE.
+ * stored as +-65504 and infinities as they are, and either flags
+ * MOE_ERR_RANGE (NaN passes through unflagged).
  * h is kept in the workspace as bf16.  Offsets that do not start at 0, go
  * down, or do not end at `rows` make the kernels skip all work and flag
  * MOE_ERR_DEVICE_CHECK.

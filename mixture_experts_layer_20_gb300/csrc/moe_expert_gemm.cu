@@ -214,8 +214,8 @@ __device__ __forceinline__ void build_schedule(const Params& p, int* s_off, int*
 // Epilogue of one tile (one of warps 2-5, q = warp % 4, reading TMEM lanes
 // 32 q .. 32 q + 31 from t_row): gate_up stores h = silu(gate) * up in bf16,
 // down stores y in fp16; `live` false (a wait gave up) stores nothing.
-// y in fp16: finite values beyond +-65504 are stored as +-65504, inf and NaN
-// as they are, and any of them sets kStatusRange.
+// y in fp16: finite values beyond +-65504 are stored as +-65504 and
+// infinities as they are, and either sets kStatusRange (NaN passes unflagged).
 template <int KIND, int SLAB = (KIND == kGateUp ? 128 : 256)>
 __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, bool live,
                                               const Params& p, int q, int lane, uint32_t rank,
@@ -232,25 +232,36 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, boo
       tmem_ld_32x32b_x16(t_row + c, v);
       tmem_ld_wait();
       const int nvalid = min(16, t.tok_end - t.tok0 - c);  // uniform across the warp
-      __half hv[16];
+      float f[16];
+      float m = 0.0f;  // largest |y| of the valid rows (NaN does not count)
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        float f = __uint_as_float(v[j]);
-        if (tscale != 1.0f) f *= tscale;
-        const float a = fabsf(f);
-        if (!(a <= kHalfMax) && j < nvalid) out_of_range = true;
-        if (a > kHalfMax && a < INFINITY) f = copysignf(kHalfMax, f);
-        hv[j] = __float2half_rn(f);
+        f[j] = __uint_as_float(v[j]) * tscale;
+        if (j < nvalid) m = fmaxf(m, fabsf(f[j]));
       }
+      if (m > kHalfMax) {  // rare: saturate the finite values beyond the fp16 range
+        out_of_range = true;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (fabsf(f[j]) > kHalfMax && fabsf(f[j]) < INFINITY) f[j] = copysignf(kHalfMax, f[j]);
+      }
+      __half2 hv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hv[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
       __half* yp = static_cast<__half*>(p.out) + (size_t)(t.tok0 + c) * p.ld_out + col;
       if (col_ok) {
         if (nvalid == 16) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) yp[(size_t)j * p.ld_out] = hv[j];
+          for (int i = 0; i < 8; ++i) {
+            yp[(size_t)(2 * i) * p.ld_out] = __low2half(hv[i]);
+            yp[(size_t)(2 * i + 1) * p.ld_out] = __high2half(hv[i]);
+          }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (j < nvalid) yp[(size_t)j * p.ld_out] = hv[j];
+          for (int i = 0; i < 8; ++i) {
+            if (2 * i < nvalid) yp[(size_t)(2 * i) * p.ld_out] = __low2half(hv[i]);
+            if (2 * i + 1 < nvalid) yp[(size_t)(2 * i + 1) * p.ld_out] = __high2half(hv[i]);
+          }
         }
       }
     }

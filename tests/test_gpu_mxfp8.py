@@ -101,6 +101,7 @@ def test_forward_mxfp8_extreme_codes(moe):
     x = W.make_x(w, device="cuda")
     wgu = p["w_gate_up"].clone()
     wgu[1, :, 0::32] *= 2.0 ** -14          # one value per run far below the run maximum
+    wgu[2, I:] *= 2.0 ** -20                # expert 2's up rows: h, and so y, scaled back
     wd = p["w_down"].clone()
     wd[2] *= 2.0 ** 20                      # run maxima near 2^19: scale bytes above 134
     mx_gu = moe.moe_mxfp8_quantize(wgu)
