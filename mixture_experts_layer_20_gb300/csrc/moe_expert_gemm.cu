@@ -2,7 +2,7 @@
 // expert weights on the M side.
 //
 //   gate_up : h[t, c] = silu(x[t] . W_gate[c]) * (x[t] . W_up[c]), bf16
-//   down    : y[t, c] = h[t] . W_down[c], fp32
+//   down    : y[t, c] = h[t] . W_down[c], accumulated in fp32, stored in fp16
 //
 // for every token row t of an expert's contiguous range of the grouped
 // activations ('Chapter 9. Distributed inference', section 9.3.2: three
@@ -61,11 +61,8 @@ constexpr int kBK = 64;     // one 128-byte swizzle row of bf16: the K of one TM
 constexpr int kSub = 2;     // K boxes per pipeline stage: 8 MMAs per barrier round
 constexpr int kMaxStages = 4;                      // down: pipeline stages (3 for 256-token chunks)
 constexpr int kMaxStagesGateUp = 6;                // gate_up: more stages when chunks are small
-constexpr int kMaxStagesWide = 6;                  // one K box per stage (wide chunks)
-static_assert(kMaxStages <= kMaxStagesWide && kMaxStagesGateUp <= kMaxStagesWide,
-              "the barrier arrays hold kMaxStagesWide stages");
-constexpr int kTokMaxWide = 512;                   // wide chunks: two MMAs of up to 256 tokens
-constexpr int kWideRowsPerGroup = 256;             // launches with this many rows per expert go wide
+constexpr int kMaxStagesAny = kMaxStagesGateUp;    // size of the barrier arrays
+static_assert(kMaxStages <= kMaxStagesAny, "the barrier arrays hold kMaxStagesAny stages");
 constexpr int kWRows = 128;                        // weight rows per CTA
 constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
 constexpr int kUnit = 16;                          // token rows: chunks are multiples of this
@@ -100,7 +97,6 @@ struct Params {
   long long scale_rows;   // MXFP8 / NVFP4 weights: weight rows of the whole tensor
   const float* tscale;    // NVFP4 weights: tensor scale per expert (null: none)
   int smem_bytes;         // dynamic shared memory of the launch
-  int tok_cap;            // bf16 kernels: token rows per chunk, kTokMax or kTokMaxWide
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -309,7 +305,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_ct[kMaxExperts + 1];
-  __shared__ alignas(8) uint64_t s_bar[2 * kMaxStagesWide + 5];
+  __shared__ alignas(8) uint64_t s_bar[2 * kMaxStagesAny + 5];
   __shared__ int s_half_max;
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
@@ -323,13 +319,13 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t full_bar = smem_u32(&s_bar[0]);
-  const uint32_t empty_bar = smem_u32(&s_bar[kMaxStagesWide]);
-  const uint32_t tfull_bar = smem_u32(&s_bar[2 * kMaxStagesWide]);
-  const uint32_t tempty_bar = smem_u32(&s_bar[2 * kMaxStagesWide + 2]);
-  const uint32_t drain_bar = smem_u32(&s_bar[2 * kMaxStagesWide + 4]);
+  const uint32_t empty_bar = smem_u32(&s_bar[kMaxStagesAny]);
+  const uint32_t tfull_bar = smem_u32(&s_bar[2 * kMaxStagesAny]);
+  const uint32_t tempty_bar = smem_u32(&s_bar[2 * kMaxStagesAny + 2]);
+  const uint32_t drain_bar = smem_u32(&s_bar[2 * kMaxStagesAny + 4]);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kMaxStagesWide; ++s) {
+    for (int s = 0; s < kMaxStagesAny; ++s) {
       mbar_init(full_bar + 8 * s, 1);  // leader: counts both CTAs' bytes; unused in the follower
       mbar_init(empty_bar + 8 * s, 1);
     }
@@ -352,7 +348,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   pdl_wait_and_release();
 
   const int G = p.groups;
-  build_schedule(p, s_off, s_ct, &s_half_max, warp, lane, p.tok_cap);
+  build_schedule(p, s_off, s_ct, &s_half_max, warp, lane, kTokMax);
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised before any remote arrive
@@ -362,24 +358,17 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   const int total_tiles = s_ct[G] * p.slabs;
   const int num_kb = p.K / kBK;                   // 64-wide K boxes
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
-  // Wide chunks (more than 256 tokens: launches with many rows per expert)
-  // hold twice the tokens per weight byte brought in: one accumulator set of
-  // up to 512 columns (no second one to overlap the epilogue), two MMAs per
-  // K step, one K box per stage so that enough stages fit.
-  const bool wide = s_half_max > kTokMax / 2;
-  const int nacc = wide ? 1 : 2;
-  const int ksub = wide ? 1 : kSub;
-  const int num_ks = (num_kb + ksub - 1) / ksub;  // pipeline stages per tile
-  // Stage geometry: a stage holds ksub K boxes of the weights and of the
+  const int num_ks = (num_kb + kSub - 1) / kSub;  // pipeline stages per tile
+  // Stage geometry: a stage holds kSub K boxes of the weights and of the
   // largest token-chunk half of this launch, so smaller chunks leave room for
   // more stages.  Both CTAs of a pair derive the same layout.
   const uint32_t b_sub_bytes = static_cast<uint32_t>(s_half_max) * kBK * 2;
-  const uint32_t stage_bytes = ksub * (kABytes + b_sub_bytes);
+  const uint32_t stage_bytes = kSub * (kABytes + b_sub_bytes);
   const uint32_t avail = static_cast<uint32_t>(p.smem_bytes) - (base - smem_u32(smem_raw));
   // Measured at decode (16-token chunks): gate_up streams its weights at 6.95
   // TB/s with six stages in flight against 6.85 with four; down, whose tiles
   // are 12 stages long, is slower with more (248 against 239 us).
-  const int max_st = wide ? kMaxStagesWide : (KIND == kGateUp ? kMaxStagesGateUp : kMaxStages);
+  const int max_st = KIND == kGateUp ? kMaxStagesGateUp : kMaxStages;
   const int nst = min(max_st, static_cast<int>(avail / stage_bytes));
 
   if (warp == 0) {
@@ -395,47 +384,37 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     const uint32_t full_leader = mapa_shared(full_bar, 0);
     for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
       const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-      const int half = t.n / 2;  // token rows per CTA: 8, 16, ..., 256
-      // A chunk of n tokens is one MMA of n0 = min(n, 256) tokens and, wide,
-      // one of n1 = n - n0; each CTA holds its half of each: rows tok0 +
-      // rank n0/2 .. (n0/2 of them) and tok0 + n0 + rank n1/2 .. after them.
-      const int n0 = min(t.n, static_cast<int>(kAccCols)), n1 = t.n - n0;
-      const CUtensorMap* tmap_x0 = &tx.m[n0 / kUnit - 1];
-      const CUtensorMap* tmap_x1 = &tx.m[max(n1, kUnit) / kUnit - 1];
+      const int half = t.n / 2;  // token rows per CTA: 8, 16, ..., 128
+      const CUtensorMap* tmap_x = &tx.m[t.n / kUnit - 1];
       const uint32_t tx_bytes = kABytes + half * 128;  // per CTA
-      const int trow = t.tok0 + rank * half;  // gathered rows (never wide)
-      const int trow0 = t.tok0 + rank * (n0 / 2);
-      const int trow1 = t.tok0 + n0 + rank * (n1 / 2);
+      const int trow = t.tok0 + rank * half;  // this CTA's first token row
       const int wrow = KIND == kGateUp ? t.slab * 128 + rank * 64
                                        : t.e * p.w_rows_per_group + t.slab * 256 + rank * 128;
       const GatherRows gr = gather_rows(p, trow, half, lane);
       for (int ks = 0; ks < num_ks; ++ks) {
-        const int nsub = min(ksub, num_kb - ks * ksub);
+        const int nsub = min(kSub, num_kb - ks * kSub);
         const bool got = lane == 0 ? mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc) : true;
         if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
         const uint32_t fb = full_leader + 8 * stage;
         const uint32_t a_dst = base + stage * stage_bytes;
-        const uint32_t b_dst = a_dst + ksub * kABytes;
+        const uint32_t b_dst = a_dst + kSub * kABytes;
         if (lane == 0) {
           if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * nsub * tx_bytes);
           for (int sub = 0; sub < nsub; ++sub) {
-            const int kx = (ks * ksub + sub) * kBK;
+            const int kx = (ks * kSub + sub) * kBK;
             // gate_up: one box holds 4 groups of {16 gate rows, the 16 matching up rows}
             if (KIND == kGateUp)
               tma_load_5d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, 0, 0, wrow / 16, t.e);
             else
               tma_load_2d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow);
-            if (p.gather_perm == nullptr) {
-              const uint32_t bs = b_dst + sub * b_sub_bytes;
-              tma_load_2d_pair(bs, tmap_x0, fb, kx, trow0);
-              if (n1 > 0) tma_load_2d_pair(bs + (n0 / 2) * 128, tmap_x1, fb, kx, trow1);
-            }
+            if (p.gather_perm == nullptr)
+              tma_load_2d_pair(b_dst + sub * b_sub_bytes, tmap_x, fb, kx, trow);
           }
         }
         if (gr.on) {
           for (int sub = 0; sub < nsub; ++sub)
             tma_gather4_pair(b_dst + sub * b_sub_bytes + lane * 512, &tx.m[0], fb,
-                             (ks * ksub + sub) * kBK, gr.r[0], gr.r[1], gr.r[2], gr.r[3]);
+                             (ks * kSub + sub) * kBK, gr.r[0], gr.r[1], gr.r[2], gr.r[3]);
         }
         ++issued;
         if (++stage == nst) { stage = 0; phase ^= 1u; }
@@ -463,43 +442,28 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       bool ok = true;
       for (int tau = pair; tau < total_tiles && ok; tau += num_pairs) {
         const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
-        const int n0 = min(t.n, static_cast<int>(kAccCols)), n1 = t.n - n0;
-        const uint32_t idesc0 = idesc_bf16_f32(256, n0);
-        const uint32_t idesc1 = idesc_bf16_f32(256, max(n1, kUnit));
+        const uint32_t idesc = idesc_bf16_f32(256, t.n);
         if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;  // TMEM column c: chunk token c
         for (int ks = 0; ks < num_ks; ++ks) {
-          const int nsub = min(ksub, num_kb - ks * ksub);
+          const int nsub = min(kSub, num_kb - ks * kSub);
           if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
           const uint32_t a_addr = base + stage * stage_bytes;
-          const uint32_t b_addr = a_addr + ksub * kABytes;
-          if (n1 == 0) {
-            for (int sub = 0; sub < nsub; ++sub) {
+          const uint32_t b_addr = a_addr + kSub * kABytes;
+          for (int sub = 0; sub < nsub; ++sub) {
 #pragma unroll
-              for (int k = 0; k < kBK / 16; ++k)
-                mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + sub * kABytes + k * 32),
-                              smem_desc_sw128(b_addr + sub * b_sub_bytes + k * 32), idesc0,
-                              (ks | sub | k) != 0 ? 1u : 0u);
-            }
-          } else {
-            for (int sub = 0; sub < nsub; ++sub) {
-#pragma unroll
-              for (int k = 0; k < kBK / 16; ++k) {
-                const uint64_t ad = smem_desc_sw128(a_addr + sub * kABytes + k * 32);
-                const uint32_t bs = b_addr + sub * b_sub_bytes + k * 32;
-                const uint32_t accum = (ks | sub | k) != 0 ? 1u : 0u;
-                mma_bf16_pair(d_tmem, ad, smem_desc_sw128(bs), idesc0, accum);
-                mma_bf16_pair(d_tmem + n0, ad, smem_desc_sw128(bs + (n0 / 2) * 128), idesc1, accum);
-              }
-            }
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_pair(d_tmem, smem_desc_sw128(a_addr + sub * kABytes + k * 32),
+                            smem_desc_sw128(b_addr + sub * b_sub_bytes + k * 32), idesc,
+                            (ks | sub | k) != 0 ? 1u : 0u);
           }
           mma_commit_pair(empty_bar + 8 * stage);  // frees this stage in both CTAs
           if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit_pair(tfull_bar + 8 * acc);     // accumulator ready in both CTAs
-        if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
       mma_commit_pair(drain_bar);
       mbar_wait_drain(drain_bar, 0, p.status);
@@ -527,7 +491,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
         if (leader) mbar_arrive(tempty_bar + 8 * acc);
         else mbar_arrive_cluster(tempty_leader + 8 * acc);
       }
-      if (++acc == nacc) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -1131,11 +1095,6 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
                                void* h, void* y, unsigned* status,
                                unsigned long long timeout_ns, const TokenGather* gather) {
   const int groups = offsets ? E : 1;
-  // Down launches with at least 256 rows per expert take wide chunks (up to
-  // 512 tokens).  Gate_up keeps chunks of at most 256 and its second
-  // accumulator: its SwiGLU epilogue is long enough that losing the overlap
-  // costs more than the wider tiles save (measured).
-  const int cap = rows < kWideRowsPerGroup * groups ? kTokMax : kTokMaxWide;
   const long long chunks_bound =
       offsets ? rows / kTokMax + std::min(E, rows) : (rows + kTokMax - 1) / kTokMax;
 
@@ -1164,7 +1123,6 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   p.ld_out = I;
   p.status = status;
   p.timeout_ns = timeout_ns;
-  p.tok_cap = kTokMax;
   e = launch_expert(s, offsets ? "moe_gate_up_swiglu" : "moe_shared_gate_up_swiglu",
                     moe_gate_up_swiglu_kernel, 0, mw, mx, p, chunks_bound * p.slabs);
   if (e != cudaSuccess) return e;
@@ -1187,7 +1145,6 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   q.ld_out = d;
   q.status = status;
   q.timeout_ns = timeout_ns;
-  q.tok_cap = cap;
   return launch_expert(s, offsets ? "moe_down" : "moe_shared_down", moe_down_kernel, 1, mw2, mx2,
                        q, chunks_bound * q.slabs);
 }

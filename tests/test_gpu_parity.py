@@ -133,8 +133,8 @@ FFN_CASES = [
     ([300, 17, 0, 64], 512, 384),     # I not a multiple of 128: ragged N tile
     ([1], 256, 64),
     ([130, 250, 5, 0, 0, 0, 1, 90, 60, 33, 7, 256], 768, 192),
-    # >= 256 rows per expert: wide chunks (up to 512 tokens, two MMAs per K
-    # step: 256 + 48, 256 + 16, 256 + 256 ...) mixed with small ones
+    # >= 256 rows per expert: several token chunks per expert (up to 256
+    # tokens each, sharing the expert's 16-row units) mixed with small ones
     ([600, 257, 512, 513, 16, 1000, 0, 300], 256, 128),
     ([700, 300, 260], 512, 384),
 ]
