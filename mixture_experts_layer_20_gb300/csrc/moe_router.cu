@@ -95,42 +95,40 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int
     }
   }
 
-  if (lane == 0) {
-    int e_of[kMaxTopK];
-    float w[kMaxTopK];
-    float sum = 0.0f;
-    float top = sel_g[0];
+  // The selections are the same in every lane.  Gates: softmax of the chosen
+  // logits (max subtracted, sum in selection order); lane j < k writes the
+  // selection whose expert id is the j-th smallest, so a token's slots hold
+  // ascending expert ids.
+  float top = sel_g[0];
 #pragma unroll
-    for (int j = 1; j < kMaxTopK; ++j)
-      if (j < k) top = fmaxf(top, sel_g[j]);
+  for (int j = 1; j < kMaxTopK; ++j)
+    if (j < k) top = fmaxf(top, sel_g[j]);
+  int e_of[kMaxTopK];
+  float w[kMaxTopK];
+  float sum = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      e_of[j] = j < k ? kMaxExperts - 1 - static_cast<int>(sel[j] & 0xffffffffu) : INT_MAX;
-      w[j] = j < k ? expf(sel_g[j] - top) : 0.0f;
-      sum += w[j];
-    }
-    // ascending expert id (unused slots hold INT_MAX and sort last)
+  for (int j = 0; j < kMaxTopK; ++j) {
+    e_of[j] = j < k ? kMaxExperts - 1 - static_cast<int>(sel[j] & 0xffffffffu) : INT_MAX;
+    w[j] = j < k ? expf(sel_g[j] - top) : 0.0f;
+    sum += w[j];
+  }
+  int my_e = INT_MAX;
+  float my_w = 0.0f;
 #pragma unroll
-    for (int a = 0; a < kMaxTopK - 1; ++a) {
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j == lane) { my_e = e_of[j]; my_w = w[j]; }
+  int rank = 0;
 #pragma unroll
-      for (int b = 0; b < kMaxTopK - 1 - a; ++b) {
-        if (e_of[b] > e_of[b + 1]) {
-          const int te = e_of[b]; e_of[b] = e_of[b + 1]; e_of[b + 1] = te;
-          const float tw = w[b]; w[b] = w[b + 1]; w[b + 1] = tw;
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k) {
-        ids[(size_t)t * k + j] = e_of[j];
-        gates[(size_t)t * k + j] = w[j] / sum;
-      }
-    }
+  for (int j = 0; j < kMaxTopK; ++j) rank += e_of[j] < my_e ? 1 : 0;
+  if (lane < k) {
+    ids[(size_t)t * k + rank] = my_e;
+    gates[(size_t)t * k + rank] = my_w / sum;
   }
 }
 
-__global__ void __launch_bounds__(kTokensPerCta * 32)
+// Five CTAs per SM (at most 51 registers a thread): a 6000-token batch is
+// one wave of warps.
+__global__ void __launch_bounds__(kTokensPerCta * 32, 5)
     moe_router_topk_kernel(const float* __restrict__ partial, int splits, int T, int npad, int E,
                            int k, const float* __restrict__ bias, int sel_only,
                            int32_t* __restrict__ ids, float* __restrict__ gates) {
