@@ -96,34 +96,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
 
   if (warp == 0) {
-    // ---------------- TMA producer: lane 0 waits and arms the stage, then
-    // lane 0 loads the token tile and lane 1 the router weights (one issuing
-    // thread moves about half the bytes per clock that two do).
-    const uint32_t tx_bytes = kABytes + static_cast<uint32_t>(p.mma_n) * kBK * 2;
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued = 0;
-    bool ok = true;
-    for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
-      const int row0 = (tau / p.k_splits) * kBM;
-      const int kb0 = (tau % p.k_splits) * p.kb_per_split;
-      const int kb1 = min(num_kb, kb0 + p.kb_per_split);
-      for (int kb = kb0; kb < kb1; ++kb) {
-        const bool got = lane == 0 ? mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc) : true;
-        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-        const uint32_t fb = full_bar + 8 * stage;
-        if (lane == 0) mbar_arrive_expect_tx(fb, tx_bytes);
-        __syncwarp();
-        if (lane == 0) tma_load_2d(a_base + stage * kABytes, &tmap_x, fb, kb * kBK, row0);
-        else if (lane == 1) tma_load_2d(b_base + stage * kBBytes, &tmap_w, fb, kb * kBK, 0);
-        ++issued;
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    if (lane == 0) {
+      // ---------------- TMA producer
+      const uint32_t tx_bytes = kABytes + static_cast<uint32_t>(p.mma_n) * kBK * 2;
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
+        const int row0 = (tau / p.k_splits) * kBM;
+        const int kb0 = (tau % p.k_splits) * p.kb_per_split;
+        const int kb1 = min(num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
+          const uint32_t fb = full_bar + 8 * stage;
+          mbar_arrive_expect_tx(fb, tx_bytes);
+          tma_load_2d(a_base + stage * kABytes, &tmap_x, fb, kb * kBK, row0);
+          tma_load_2d(b_base + stage * kBBytes, &tmap_w, fb, kb * kBK, 0);
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
       }
-    }
-    // Drain: the last (up to kStages) loads may still be landing.
-    if (lane == 0)
+      // Drain: the last (up to kStages) loads may still be landing.
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_wait_drain(full_bar + 8 * (i % kStages), (i / kStages) & 1, p.status);
+    }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
