@@ -59,11 +59,12 @@ namespace {
 
 constexpr int kBK = 64;     // one 128-byte swizzle row of bf16: the K of one TMA box
 constexpr int kSub = 2;     // K boxes per pipeline stage: 8 MMAs per barrier round
-static_assert(kSub == 2, "the MMA issue loop unrolls two K boxes per stage");
 constexpr int kMaxStages = 4;                      // down: pipeline stages (3 for 256-token chunks)
 constexpr int kMaxStagesGateUp = 6;                // gate_up: more stages when chunks are small
 constexpr int kMaxStagesAny = kMaxStagesGateUp;    // size of the barrier arrays
 static_assert(kMaxStages <= kMaxStagesAny, "the barrier arrays hold kMaxStagesAny stages");
+constexpr int kTileRing = 16;  // tile token counts passed from the producer to the MMA issuer
+static_assert(kMaxStagesAny + 1 < kTileRing, "the producer runs at most kMaxStagesAny tiles ahead");
 constexpr int kWRows = 128;                        // weight rows per CTA
 constexpr int kTokMax = 256;                       // tokens per tile (MMA N)
 constexpr int kUnit = 16;                          // token rows: chunks are multiples of this
@@ -311,10 +312,10 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   // Token count of the tile whose first stage the producer armed, by tile
-  // sequence number mod 8: the MMA issuer reads it after that stage's full
-  // barrier instead of decoding the tile itself (it is at most six stages,
-  // so six tiles, behind the producer).
-  __shared__ int s_tile_n[8];
+  // sequence number mod kTileRing: the MMA issuer reads it after that stage's
+  // full barrier instead of decoding the tile itself (it is at most
+  // kMaxStagesAny stages, so as many tiles, behind the producer).
+  __shared__ int s_tile_n[kTileRing];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -406,7 +407,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
         const uint32_t a_dst = base + stage * stage_bytes;
         const uint32_t b_dst = a_dst + kSub * kABytes;
         if (lane == 0) {
-          if (ks == 0) s_tile_n[seq & 7] = t.n;  // before the arrive that releases it
+          if (ks == 0) s_tile_n[seq % kTileRing] = t.n;  // before the arrive that releases it
           if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * nsub * tx_bytes);
           for (int sub = 0; sub < nsub; ++sub) {
             const int kx = (ks * kSub + sub) * kBK;
@@ -455,9 +456,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
         const uint32_t d_tmem = tmem_base + acc * kAccCols;  // TMEM column c: chunk token c
         uint32_t idesc = 0;
         for (int ks = 0; ks < num_ks; ++ks) {
-          const bool two = ks * kSub + 1 < num_kb;  // this stage holds a second K box
           if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
-          if (ks == 0) idesc = idesc_bf16_f32(256, s_tile_n[seq & 7]);
+          if (ks == 0) idesc = idesc_bf16_f32(256, s_tile_n[seq % kTileRing]);
           // Descriptors built once per stage; a K step of 16 moves 32 bytes,
           // i.e. 2 in the descriptor's 16-byte address field (no carry out of
           // it: shared addresses stay below 256 KB).
@@ -466,13 +466,13 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
           const uint64_t db = smem_desc_sw128(a_addr + kSub * kABytes);
           const uint32_t acc0 = ks != 0 ? 1u : 0u;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, k != 0 ? 1u : acc0);
-          if (two) {
-            const uint64_t da1 = da + (kABytes >> 4), db1 = db + (b_sub_bytes >> 4);
+          for (int sub = 0; sub < kSub; ++sub) {
+            if (sub == 0 || ks * kSub + sub < num_kb) {  // the last stage may hold fewer boxes
+              const uint64_t das = da + sub * (kABytes >> 4), dbs = db + sub * (b_sub_bytes >> 4);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              mma_bf16_pair(d_tmem, da1 + 2 * k, db1 + 2 * k, idesc, 1u);
+              for (int k = 0; k < kBK / 16; ++k)
+                mma_bf16_pair(d_tmem, das + 2 * k, dbs + 2 * k, idesc, (sub | k) != 0 ? 1u : acc0);
+            }
           }
           mma_commit_pair(empty_bar + 8 * stage);  // frees this stage in both CTAs
           if (++stage == nst) { stage = 0; phase ^= 1u; }
