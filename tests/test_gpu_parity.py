@@ -137,6 +137,10 @@ FFN_CASES = [
     # tokens each, sharing the expert's 16-row units) mixed with small ones
     ([600, 257, 512, 513, 16, 1000, 0, 300], 256, 128),
     ([700, 300, 260], 512, 384),
+    # d = 64: one pipeline stage per gate_up tile, 256 experts x 8 slabs = 2048
+    # tiles (~27 per CTA pair), so the producer runs several tiles ahead of the
+    # MMA issuer and the ring of tile sizes between them wraps
+    ([8, 0, 24, 9] * 64, 64, 1024),
 ]
 
 
