@@ -128,16 +128,20 @@ moe_status_t moe_permute(const int32_t* topk_ids, const moe_bf16* x,
  * every GPU that loads the library until the process exits.  This call
  * allocates and frees nothing.
  *
- * Limit: ceil(T*top_k / 4096) * E <= 65536, e.g. T*top_k <= 1,048,576 with
- * E = 256; larger sizes return MOE_ERR_UNSUPPORTED with a message naming the
- * limit (use moe_permute for them).
+ * Limit: the table has one entry per (chunk of 1024 assignments, expert):
+ * ceil(T*top_k / 1024) * E <= 65536, e.g. T*top_k <= 262,144 with E = 256
+ * (1,048,576 with E = 64); larger sizes return MOE_ERR_UNSUPPORTED with a
+ * message naming the limit (use moe_permute for them).
  * device_status: a device uint32 into which the kernels OR their status bits
  * (1 = a wait gave up, 2 = an expert id out of range was skipped); the caller
  * zeroes it.  If NULL, the bits go to the library's own status word, which
  * each call clears first and which cannot be read back.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the array: calls whose work
+ * (cudaGetSymbolAddress) with that device current and keeps it for that
+ * device's current CUDA context; a call made in a new context (after
+ * cudaDeviceReset, say) looks it up again.  Make the first call on a device,
+ * and the first after a reset, before any stream capture.  All calls share
+ * the array: calls whose work
  * can overlap on the GPU (unordered streams) race and may give wrong
  * results, so order them on one stream. */
 moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, const moe_bf16* x,
@@ -174,7 +178,10 @@ moe_status_t moe_combine(const moe_f16* y, const int32_t* slot_pos,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* The whole layer: steps 1-4 on one stream, intermediates in `ws`.
- * x [T,d], w_router [E,d], w_gate_up [E,2I,d], w_down [E,d,I] -> out [T,d]. */
+ * x [T,d], w_router [E,d], w_gate_up [E,2I,d], w_down [E,d,I] -> out [T,d].
+ * Cite: 'Chapter 9. Distributed inference', section 9.3.4 (the four steps of
+ * one MoE layer around Fig. 9-16: route, permute by expert, expert matrix
+ * multiplications, weighted combine). */
 moe_status_t moe_forward(const moe_bf16* x, const moe_bf16* w_router,
                          const moe_bf16* w_gate_up, const moe_bf16* w_down,
                          int T, int d, int E, int I, int top_k, moe_bf16* out,

@@ -198,8 +198,6 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation issued so far by this
-// thread has completed.
 // One-CTA MMA (M = 128) with A read from tensor memory: the CTA's 128 A rows
 // in TMEM lanes 0..127, K along the columns (two bf16 per 32-bit column).
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -214,6 +212,8 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+// Arrive once on `bar` when every tcgen05 operation issued so far by this
+// thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)

@@ -2,17 +2,19 @@
 // that cannot allocate device memory.
 //
 // The grouping kernels need one scratch buffer besides their inputs and
-// outputs: a table of per-chunk, per-expert counts (ceil(T*top_k/4096) x E
-// int32).  moe_permute takes it from the caller's workspace.  This variant
+// outputs: a table of per-chunk, per-expert counts (ceil(T*top_k/1024) x E
+// int32, chunks of kPermuteChunk = 1024 assignments).  moe_permute takes it from the caller's workspace.  This variant
 // keeps it in a fixed array in the library's own device memory instead, so
 // the caller passes only inputs and outputs.
 //
 // The array is a file-scope __device__ variable: every GPU on which the
 // library is loaded holds its 256 KB + 256 bytes until the process exits.
 // Its host-side name is only a stand-in for the symbol, never a device
-// address; the device address is looked up once per device with
-// cudaGetSymbolAddress (on the first call made with that device current)
-// and cached.
+// address; the device address is looked up with cudaGetSymbolAddress on the
+// first call made with that device current and cached together with the
+// unique id of the CUDA context it belongs to.  A device reset destroys that
+// context and the module with it; the next call runs in a context with a new
+// id and looks the address up again instead of using a stale one.
 //
 // Every call uses the same array.  The count kernel rewrites every table
 // entry it later reads, so the table needs no clearing; the status word in
@@ -20,6 +22,7 @@
 // whose work overlaps on the GPU (different streams, no ordering between
 // them) race on the array and may produce wrong results.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -38,23 +41,59 @@ constexpr size_t kScratchBytes = kStatusBytes + kMaxTableEntries * sizeof(int32_
 
 static __device__ __align__(256) unsigned char g_static_scratch[kScratchBytes];
 
+struct CachedAddress {
+  void* ptr;
+  unsigned long long ctx_id;  // 0: none cached
+};
 std::mutex g_addr_mu;
-void* g_addr[64] = {nullptr};
+CachedAddress g_addr[64] = {};
 
-// Device address of g_static_scratch on the current device (looked up once).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context (ids are never
+// reused within a process), or 0 when there is none or it cannot be read.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_static_scratch on the current device, looked up on the
+// first call in each context (with that device current) and cached for it.
 cudaError_t static_scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (g_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_addr[dev] = p;
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0 && g_addr[dev].ctx_id == ctx) {
+    *out = g_addr[dev].ptr;
+    return cudaSuccess;
   }
-  *out = g_addr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);  // makes the context current if needed
+  if (e != cudaSuccess) return e;
+  g_addr[dev] = CachedAddress{p, current_context_id()};
+  *out = p;
   return cudaSuccess;
 }
 

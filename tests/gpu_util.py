@@ -76,3 +76,15 @@ class ExpertsOnHost:
         if e not in self.cache:
             self.cache[e] = W.to_bits(self.t[e])
         return self.cache[e]
+
+
+class ExpertsStreamed:
+    """Per-expert host copies of a [E, ...] bf16 device weight tensor, made on
+    each access and not kept (a whole-layer oracle pass reads each expert
+    once; keeping them would hold every expert's weights in host memory)."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+
+    def __getitem__(self, e):
+        return W.to_bits(self.t[int(e)])

@@ -24,15 +24,16 @@ def moe():
     return binding
 
 
-def _call_c_abi(moe, ids, E, x, status):
-    """Direct ctypes call of the exported symbol (no binding helper)."""
+def _call_c_abi(moe, ids, E, x, status, d=None):
+    """Direct ctypes call of the exported symbol (no binding helper).  x may be
+    None (no gather; d then gives the row width the call is told)."""
     T, k = ids.shape
-    d = x.shape[1]
+    d = x.shape[1] if x is not None else d
     counts = torch.empty(E, dtype=torch.int32, device="cuda")
     offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
     slot_pos = torch.empty((T, k), dtype=torch.int32, device="cuda")
-    x_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device="cuda")
+    x_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device="cuda") if x is not None else None
     p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
     st = moe._lib.moe_permute_static_scratch(
         p(ids), p(x), T, d, E, k, p(counts), p(offsets), p(perm), p(slot_pos), p(x_perm),
@@ -55,6 +56,40 @@ def test_static_scratch_matches_workspace_version(moe, T, E, k, d):
         for a, b in zip(got, want):
             assert torch.equal(a, b)
         assert status.item() == 0
+
+
+def test_static_scratch_at_the_table_limit(moe):
+    """E = 256 and T*k = 262,144: ceil(T*k/1024) * E = 65,536 entries, the
+    whole fixed table.  Two calls in a row, bit for bit against moe_permute."""
+    T, k, E = 32768, 8, 256
+    for call in range(2):
+        ids, _ = W.random_routing(T, E, k, seed=31 + call)
+        ids[: T // 8] = ids[1]  # one group of experts hot
+        ids = ids.cuda()
+        want = moe.moe_permute(ids, E)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        st, got = _call_c_abi(moe, ids, E, None, status, d=64)
+        assert st == moe.MOE_OK, moe._lib.moe_last_error()
+        torch.cuda.synchronize()
+        for a, b in zip(got[:4], want[:4]):
+            assert torch.equal(a, b)
+        assert status.item() == 0
+
+
+def test_static_scratch_flags_out_of_range_ids(moe):
+    """Several chunks (T*k = 5600 > 4096 takes the two-kernel path) with two
+    expert ids out of range: the caller's status word gets bit 2 (device
+    check) and the call returns without a fault."""
+    T, k, E = 700, 8, 32
+    ids, _ = W.random_routing(T, E, k, seed=5)
+    ids[5, 3] = E + 3
+    ids[600, 0] = -1
+    ids = ids.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st, _ = _call_c_abi(moe, ids, E, None, status, d=64)
+    assert st == moe.MOE_OK, moe._lib.moe_last_error()
+    torch.cuda.synchronize()
+    assert status.item() & 2
 
 
 def test_static_scratch_without_status_word(moe):
