@@ -17,6 +17,9 @@ namespace moe {
 namespace {
 
 constexpr size_t kAlign = 256;
+// Quantised expert weights: the warp-level small-M kernels serve layers with
+// at most this many token rows per expert on average (decode batches).
+constexpr long long kSmallMRowsPerExpert = 16;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 std::atomic<unsigned long long> g_launches{0};
@@ -380,18 +383,26 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   // rows from x through perm (four rows per TMA gather), so no permuted copy
   // of x is written.  Many rows: one TMA box per K box of x_perm loads faster
   // than that many gathers.
+  // Quantised weights with few rows per expert (decode) take the warp-level
+  // small-M kernels, which read the token rows from x through perm.
   void* x_perm = w + L.x_perm;
-  const bool gather_rows = !mx && rows <= 128LL * E;
+  const bool small_m = mx && rows <= kSmallMRowsPerExpert * static_cast<long long>(E);
+  const bool gather_rows = small_m || (!mx && rows <= 128LL * E);
   cudaError_t e = launch_permute(s, ids, gather_rows ? nullptr : x, T, d, E, top_k, counts,
                                  offsets, perm, slot_pos, x_perm, table, status);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   const TokenGather gather{x, perm, top_k, T};
-  e = mx ? launch_grouped_ffn_quant(s, mx->fmt, x_perm, offsets, rows, d, E, I,
-                                    mx->codes_gate_up, mx->scales_gate_up, mx->tscale_gate_up,
-                                    mx->codes_down, mx->scales_down, mx->tscale_down, h, y,
-                                    status, tmo)
-         : launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status,
-                              tmo, gather_rows ? &gather : nullptr);
+  if (small_m)
+    e = launch_grouped_ffn_smallm(s, mx->fmt == 0 ? 1 : 2, x, perm, top_k, offsets, rows, d, E, I,
+                                  mx->codes_gate_up, mx->scales_gate_up, mx->tscale_gate_up,
+                                  mx->codes_down, mx->scales_down, mx->tscale_down, h, y, status);
+  else if (mx)
+    e = launch_grouped_ffn_quant(s, mx->fmt, x_perm, offsets, rows, d, E, I, mx->codes_gate_up,
+                                 mx->scales_gate_up, mx->tscale_gate_up, mx->codes_down,
+                                 mx->scales_down, mx->tscale_down, h, y, status, tmo);
+  else
+    e = launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status,
+                           tmo, gather_rows ? &gather : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
   void* y_shared = nullptr;
   if (I_shared) {

@@ -51,6 +51,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include "moe_convert.cuh"
 #include "moe_device.cuh"
 #include "moe_internal.h"
 
@@ -125,21 +126,50 @@ __device__ __forceinline__ GatherRows gather_rows(const Params& p, int row0, int
   return g;
 }
 
-__device__ __forceinline__ Tile decode_tile(int tau, int slabs, int groups, const int* s_off,
-                                            const int* s_ct) {
-  int lo = 0, hi = groups - 1;
+// The launch's tiles, as built by build_schedule in shared memory.  Experts
+// with several token chunks ("multi") reuse each weight slab from L2 for
+// their second and later chunks, so their tiles lean on the tensor cores;
+// single-chunk experts stream every slab from HBM.  Tile position tau of the
+// launch interleaves the two classes in proportion (multi-chunk tile number
+// floor(tau * n_multi / n_all) comes next whenever that count grows at tau),
+// so the pairs working at the same time mix both kinds and the two roofs
+// overlap instead of adding up one after the other (a skewed routing gives a
+// few experts many chunks and most one).  Within a class tiles stay in
+// (expert, slab, chunk) order: the chunks of one slab sit in neighbouring
+// positions and run at the same time, so the slab is read from HBM once.
+// With one class only (prefill: all experts multi-chunk; decode: all single)
+// the order is plain (expert, slab, chunk).
+struct Sched {
+  const int* off;      // [G + 1] token row offsets
+  const int* pre_multi;   // [G + 1] exclusive chunk prefix of multi-chunk experts
+  const int* pre_single;  // [G + 1] the same for single-chunk experts
+  int slabs, groups;
+  long long n_multi;   // tiles of multi-chunk experts
+  long long n_all;     // all tiles
+};
+
+__device__ __forceinline__ Tile decode_tile(int tau, const Sched& sc) {
+  const long long before = static_cast<long long>(tau) * sc.n_multi / sc.n_all;
+  const bool multi = (static_cast<long long>(tau) + 1) * sc.n_multi / sc.n_all > before;
+  const int idx = multi ? static_cast<int>(before) : tau - static_cast<int>(before);
+  const int* pre = multi ? sc.pre_multi : sc.pre_single;
+  const int slabs = sc.slabs;
+  // the expert whose tiles of this class hold idx: the last with pre * slabs <= idx
+  // (experts without tiles in the class repeat the prefix and are passed over)
+  int lo = 0, hi = sc.groups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_ct[mid] * slabs <= tau) lo = mid; else hi = mid - 1;
+    if (pre[mid] * slabs <= idx) lo = mid; else hi = mid - 1;
   }
   Tile t;
   t.e = lo;
-  const int ch = s_ct[lo + 1] - s_ct[lo];
-  const int local = tau - s_ct[lo] * slabs;
+  const int ch = pre[lo + 1] - pre[lo];
+  const int local = idx - pre[lo] * slabs;
   t.slab = local / ch;
   const int c = local - t.slab * ch;
   // the expert's ceil(m / 16) row units, spread over its ch chunks as evenly as
   // possible (the first `rem` chunks take one unit more)
+  const int* s_off = sc.off;
   const int m = s_off[lo + 1] - s_off[lo];
   const int u = (m + kUnit - 1) / kUnit;
   const int base_u = u / ch, rem = u - base_u * ch;
@@ -157,18 +187,20 @@ struct TokenMapSet {
 };
 
 // Schedule (all threads of the CTA): token chunks per expert (at most TOKCAP
-// tokens each) and their exclusive prefix in s_ct, and the largest chunk half
-// of the launch in *s_half_max.  Inconsistent offsets give an empty schedule
-// and MOE_ERR_DEVICE_CHECK.
-__device__ __forceinline__ void build_schedule(const Params& p, int* s_off, int* s_ct,
-                                               int* s_half_max, int warp, int lane, int TOKCAP) {
+// tokens each), their exclusive prefix per class (s_pre[0]: experts with two
+// or more chunks, s_pre[1]: experts with one; entry G holds the class total),
+// and the largest chunk half of the launch in *s_half_max.  Inconsistent
+// offsets give an empty schedule and MOE_ERR_DEVICE_CHECK.
+__device__ __forceinline__ void build_schedule(const Params& p, int* s_off,
+                                               int (*s_pre)[kMaxExperts + 1], int* s_half_max,
+                                               int warp, int lane, int TOKCAP) {
   const int G = p.groups;
   for (int i = threadIdx.x; i <= G; i += blockDim.x)
     s_off[i] = p.offsets ? __ldg(p.offsets + i) : (i == 0 ? 0 : p.total_rows);
   __syncthreads();
   if (warp == 0) {
     const int per = (G + 31) / 32;
-    int local = 0;
+    int local_m = 0, local_s = 0;
     int half_max = kUnit / 2;
     bool bad = false;
     for (int j = 0; j < per; ++j) {
@@ -178,35 +210,56 @@ __device__ __forceinline__ void build_schedule(const Params& p, int* s_off, int*
         bad |= m < 0;
         if (m > 0) {
           const int ch = (m + TOKCAP - 1) / TOKCAP;
-          local += ch;
+          if (ch > 1) local_m += ch; else local_s += 1;
           half_max = max(half_max, (((m + kUnit - 1) / kUnit + ch - 1) / ch) * (kUnit / 2));
         }
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) half_max = max(half_max, __shfl_xor_sync(0xffffffffu, half_max, o));
-    int incl = local;
+    int incl_m = local_m, incl_s = local_s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      const int vm = __shfl_up_sync(0xffffffffu, incl_m, o);
+      const int vs = __shfl_up_sync(0xffffffffu, incl_s, o);
+      if (lane >= o) { incl_m += vm; incl_s += vs; }
     }
-    int run = incl - local;
+    int run_m = incl_m - local_m, run_s = incl_s - local_s;
     for (int j = 0; j < per; ++j) {
       const int g = lane * per + j;
       if (g < G) {
-        s_ct[g] = run;
+        s_pre[0][g] = run_m;
+        s_pre[1][g] = run_s;
         const int m = s_off[g + 1] - s_off[g];
-        run += m > 0 ? (m + TOKCAP - 1) / TOKCAP : 0;
+        const int ch = m > 0 ? (m + TOKCAP - 1) / TOKCAP : 0;
+        if (ch > 1) run_m += ch; else run_s += ch;
       }
     }
     bad |= (s_off[0] != 0) || (s_off[G] != p.total_rows);
     bad = __any_sync(0xffffffffu, bad);
     __syncwarp();
-    if (lane == 31) s_ct[G] = bad ? 0 : incl;
+    if (lane == 31) {
+      s_pre[0][G] = bad ? 0 : incl_m;
+      s_pre[1][G] = bad ? 0 : incl_s;
+    }
     if (lane == 0) *s_half_max = bad ? TOKCAP / 2 : min(half_max, TOKCAP / 2);
     if (bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusDeviceCheck);
   }
+}
+
+// The launch's tile list over the schedule in shared memory (after the
+// barrier that follows build_schedule).
+__device__ __forceinline__ Sched make_sched(const Params& p, const int* s_off,
+                                            const int (*s_pre)[kMaxExperts + 1]) {
+  Sched sc;
+  sc.off = s_off;
+  sc.pre_multi = s_pre[0];
+  sc.pre_single = s_pre[1];
+  sc.slabs = p.slabs;
+  sc.groups = p.groups;
+  sc.n_multi = static_cast<long long>(s_pre[0][p.groups]) * p.slabs;
+  sc.n_all = sc.n_multi + static_cast<long long>(s_pre[1][p.groups]) * p.slabs;
+  return sc;
 }
 
 // Epilogue of one tile (one of warps 2-5, q = warp % 4, reading TMEM lanes
@@ -306,7 +359,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
                                                  const Params& p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
-  __shared__ int s_ct[kMaxExperts + 1];
+  __shared__ int s_pre[2][kMaxExperts + 1];
   __shared__ alignas(8) uint64_t s_bar[2 * kMaxStagesAny + 5];
   __shared__ int s_half_max;
   __shared__ uint32_t s_tmem_base;
@@ -354,15 +407,15 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
 
   pdl_wait_and_release();
 
-  const int G = p.groups;
-  build_schedule(p, s_off, s_ct, &s_half_max, warp, lane, kTokMax);
+  build_schedule(p, s_off, s_pre, &s_half_max, warp, lane, kTokMax);
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised before any remote arrive
   tc_fence_after_sync();
 
   const uint32_t tmem_base = s_tmem_base;
-  const int total_tiles = s_ct[G] * p.slabs;
+  const Sched sched = make_sched(p, s_off, s_pre);
+  const int total_tiles = static_cast<int>(sched.n_all);
   const int num_kb = p.K / kBK;                   // 64-wide K boxes
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
   const int num_ks = (num_kb + kSub - 1) / kSub;  // pipeline stages per tile
@@ -391,7 +444,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     int seq = 0;
     const uint32_t full_leader = mapa_shared(full_bar, 0);
     for (int tau = pair; tau < total_tiles && ok; tau += num_pairs, ++seq) {
-      const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+      const Tile t = decode_tile(tau, sched);
       const int half = t.n / 2;  // token rows per CTA: 8, 16, ..., 128
       const CUtensorMap* tmap_x = &tx.m[t.n / kUnit - 1];
       const uint32_t tx_bytes = kABytes + half * 128;  // per CTA
@@ -496,7 +549,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     // After a wait gives up, the loop still runs to the end (later waits fail
     // at once) with its stores switched off.
     for (int tau = pair; tau < total_tiles; tau += num_pairs) {
-      const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+      const Tile t = decode_tile(tau, sched);
       const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
@@ -569,77 +622,6 @@ __host__ __device__ constexpr int threads_q(int fmt) { return (kConvWarp0 + conv
 constexpr int kBlkPerWarp = 16 / kConvWarpsMx;       // MXFP8: 32-value scale blocks per warp per stage
 constexpr int kMaxStages8 = 8;
 
-// 2^(byte - 127) as a float (byte 0: 2^-127, a subnormal).
-__device__ __forceinline__ float e8m0_to_float(uint32_t byte) {
-  return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
-}
-
-// 4 E4M3 codes (a 32-bit word, lowest byte first) times 2^(S - 127) as two
-// bf16x2, by bits: a code's seven magnitude bits placed at bf16 bit 4 and its
-// sign at bit 15 form the bf16 (normal, or subnormal for a subnormal code)
-// whose value is the code's times 2^-120; one exact bf16x2 multiply by
-// mul = 2^(S - 7) applies the scale.  Valid while 2^(S - 7) is a finite bf16
-// (S <= 134); larger scales take e4m3x8_to_bf16.  The byte permute
-// sign-extends each code to 16 bits (prmt selector nibbles with bit 3 set
-// replicate the selected byte's sign), so one shift moves the magnitude to
-// bits 4-10 and a sign copy to bit 15, and one mask clears the rest.
-__device__ __forceinline__ void e4m3x4_to_bf16_bits(uint32_t w, __nv_bfloat162 mul,
-                                                    uint32_t* out) {
-  uint32_t a, b;
-  asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));  // sext16(code 0) | sext16(code 1) << 16
-  asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));  // codes 2 and 3
-  a = (a << 4) & 0x87F087F0u;
-  b = (b << 4) & 0x87F087F0u;
-  const __nv_bfloat162 pa = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), mul);
-  const __nv_bfloat162 pb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), mul);
-  out[0] = *reinterpret_cast<const uint32_t*>(&pa);
-  out[1] = *reinterpret_cast<const uint32_t*>(&pb);
-}
-
-// 8 E4M3 codes (a 64-bit word, lowest byte first) times `scale` as 4 bf16x2,
-// through the hardware conversions (any scale).
-__device__ __forceinline__ void e4m3x8_to_bf16(uint32_t lo, uint32_t hi, float scale,
-                                               uint32_t* out) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t w = i < 2 ? lo : hi;
-    const __nv_fp8x2_storage_t two =
-        static_cast<__nv_fp8x2_storage_t>((w >> (16 * (i & 1))) & 0xffffu);
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-    out[i] = *reinterpret_cast<const uint32_t*>(&b);
-  }
-}
-
-// 4 E2M1 codes (the low 16 bits of m_lo / signs from w's bits 3, 7, 11, 15)
-// as two bf16x2 of code value x scale.  The codes' 3-bit magnitudes index
-// byte tables of the bf16 patterns of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with prmt
-// (high bytes 00 3F 3F 3F 40 40 40 40, low bytes 00 00 80 C0 00 40 80 C0),
-// two more prmt interleave them into bf16 halves, the signs are or-ed in,
-// and one exact bf16x2 multiply applies the block scale.
-__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t w, __nv_bfloat162 mul, uint32_t* out) {
-  const uint32_t sel = w & 0x7777u;
-  uint32_t hi, lo, a, b;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
-  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(lo), "r"(hi));  // values 0, 1
-  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(lo), "r"(hi));  // values 2, 3
-  a |= ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
-  b |= ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
-  const __nv_bfloat162 pa = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), mul);
-  const __nv_bfloat162 pb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), mul);
-  out[0] = *reinterpret_cast<const uint32_t*>(&pa);
-  out[1] = *reinterpret_cast<const uint32_t*>(&pb);
-}
-
-// An E4M3 block scale as a bf16 pair (exact: 4 significant bits).
-__device__ __forceinline__ __nv_bfloat162 e4m3_scale_bf16x2(uint32_t code) {
-  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
-  const float f = __half2float(*reinterpret_cast<const __half*>(&h));
-  return __floats2bfloat162_rn(f, f);
-}
-
 template <int KIND, int FMT>
 __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
                                                      const TokenMapSet& tx, const Params& p) {
@@ -654,7 +636,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
   constexpr int kConvWarps = conv_warps(FMT);
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
-  __shared__ int s_ct[kMaxExperts + 1];
+  __shared__ int s_pre[2][kMaxExperts + 1];
   __shared__ alignas(8) uint64_t s_bar[3 * kMaxStages8 + 2 * kMaxABufs + 5];
   __shared__ int s_half_max;
   __shared__ uint32_t s_tmem_base;
@@ -701,14 +683,14 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
 
   pdl_wait_and_release();
 
-  const int G = p.groups;
-  build_schedule(p, s_off, s_ct, &s_half_max, warp, lane, kTokMax / 2);
+  build_schedule(p, s_off, s_pre, &s_half_max, warp, lane, kTokMax / 2);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
 
   const uint32_t tmem_base = s_tmem_base;
-  const int total_tiles = s_ct[G] * p.slabs;
+  const Sched sched = make_sched(p, s_off, s_pre);
+  const int total_tiles = static_cast<int>(sched.n_all);
   const int num_ks = p.K / kStageK;  // K is a multiple of the stage's K
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
   // token rows per K box: the launch's largest chunk (twice its largest half)
@@ -729,7 +711,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
       int issued = 0;
       bool ok = true;
       for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
-        const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+        const Tile t = decode_tile(tau, sched);
         const CUtensorMap* tmap_x = &tx.m[t.n / (kUnit / 2) - 1];  // t.n <= 128 rows
         // this CTA's weight rows, and how many of them exist (the last slab may be ragged)
         int row0, row1 = 0, nrow;
@@ -782,7 +764,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
       uint32_t phase = 0, cphase = 0, acc_phase = 0;
       bool ok = true;
       for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
-        const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+        const Tile t = decode_tile(tau, sched);
         const uint32_t idesc = idesc_bf16_f32(128, t.n);
         if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after_sync();
@@ -829,7 +811,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tau = blockIdx.x; tau < total_tiles; tau += gridDim.x) {
-      const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+      const Tile t = decode_tile(tau, sched);
       const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
@@ -855,7 +837,7 @@ __device__ __forceinline__ void expert_gemm_fp8_body(const CUtensorMap& tmap_w,
     uint32_t phase = 0, cphase = 0;
     bool ok = true;
     for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
-      const Tile t = decode_tile(tau, p.slabs, G, s_off, s_ct);
+      const Tile t = decode_tile(tau, sched);
       int col, srow;
       if (KIND == kGateUp) {
         col = t.slab * kSlabH + q * 16 + (lane & 15);

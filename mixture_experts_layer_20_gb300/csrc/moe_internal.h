@@ -149,6 +149,20 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
                                      void* h, void* y, unsigned* status,
                                      unsigned long long timeout_ns);
 
+// Grouped SwiGLU FFN for few token rows per expert (decode): warp-level
+// tensor-core MMAs, weights decoded in registers (moe_smallm.cu).  fmt 0:
+// bf16 weights, 1: MXFP8, 2: NVFP4 (scales and tensor scales as for
+// launch_grouped_ffn_quant).  Gate_up's token rows are a[perm[pos] / div]
+// (perm != nullptr) or a[pos]; d and I multiples of 128 (256 for NVFP4).
+// Writes h [rows, I] bf16 and y [rows, d] fp16.
+cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
+                                      const int32_t* perm, int div, const int32_t* offsets,
+                                      int rows, int d, int E, int I, const void* w_gate_up,
+                                      const uint8_t* scales_gate_up, const float* tscale_gate_up,
+                                      const void* w_down, const uint8_t* scales_down,
+                                      const float* tscale_down, void* h, void* y,
+                                      unsigned* status);
+
 // NVFP4 quantisation of `groups` matrices [rows_per_group, K] (K a multiple of
 // 256) in one bf16 array: codes, scales as above, one tensor scale per matrix.
 cudaError_t launch_nvfp4_quantize(cudaStream_t s, const void* w, int groups,

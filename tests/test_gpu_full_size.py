@@ -12,6 +12,7 @@ import torch
 import oracle
 from mixture_experts_layer_20_gb300 import counters
 from mixture_experts_layer_20_gb300 import workloads as W
+from tests import oracle_pool
 from tests.gpu_util import ExpertsStreamed, assert_layer_close, compare_routing, f64
 
 pytestmark = pytest.mark.gpu
@@ -70,21 +71,6 @@ def test_full_size_whole_layer(moe, name):
           f"max_rel={max_rel:.3e} mean_rel={mean_rel:.3e}")
 
 
-class _DequantisedExperts:
-    """Per-expert oracle round trip (quantise, dequantise) of a [E, rows, K]
-    bf16 device weight tensor, made on each access: bf16 bits for MXFP8
-    (exact), fp64 values for NVFP4."""
-
-    def __init__(self, t: torch.Tensor, fmt: str):
-        self.t, self.fmt = t, fmt
-
-    def __getitem__(self, e):
-        vals = oracle.bf16_bits_to_f64(W.to_bits(self.t[int(e)]))
-        if self.fmt == "mxfp8":
-            return oracle.f64_to_bf16_bits(oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(vals)))
-        return oracle.nvfp4_dequantize(*oracle.nvfp4_quantize(vals.astype(np.float32)))
-
-
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 def test_full_size_decode_quantised_weights(moe, fmt):
     """The decode workload with MXFP8 / NVFP4 expert weights, as the benchmark
@@ -107,9 +93,10 @@ def test_full_size_decode_quantised_weights(moe, fmt):
     differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
                              ids_ref, gates_ref, logits, w.top_k)
     tokens = np.setdiff1d(np.arange(w.T), differ)
-    ref = oracle.forward_tokens(W.to_bits(x), tokens, ids_ref, gates_ref,
-                                _DequantisedExperts(p["w_gate_up"], fmt),
-                                _DequantisedExperts(p["w_down"], fmt), None, None)
+    # the oracle quantises each expert itself; experts run in host worker processes
+    ref = oracle_pool.layer_out(
+        W.to_bits(x), ids_ref, gates_ref, w.E,
+        lambda e: (W.to_bits(p["w_gate_up"][e]), W.to_bits(p["w_down"][e])), fmt=fmt)[tokens]
     got = f64(out[torch.as_tensor(tokens, device="cuda")])
     assert got.shape == (w.T - differ.size, w.d)
     max_rel, mean_rel = assert_layer_close(got, ref, f"decode {fmt}")
