@@ -7,7 +7,7 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--also NAME,...] [--also-mxfp8 NAME,...]
-                  [--also-nvfp4 NAME,...]
+                  [--also-nvfp4 NAME,...] [--also-single NAME,...]
 
 Default workload: the Qwen3-235B-A22B MoE layer on a 64-token decode batch
 (d=4096, E=128, top-8, I=1536).  Its 4.8 GB of expert weights exceed the
@@ -15,7 +15,8 @@ Default workload: the Qwen3-235B-A22B MoE layer on a 64-token decode batch
 --impl reference times the fp64 CPU oracle on the host cores instead.
 The "also" entries measure further workloads at N=1: --also with bf16
 weights, --also-mxfp8 / --also-nvfp4 with the expert weights quantised to
-MXFP8 / NVFP4 once before timing (moe_forward_mxfp8 / moe_forward_nvfp4).
+MXFP8 / NVFP4 once before timing (moe_forward_mxfp8 / moe_forward_nvfp4),
+--also-single with the whole layer as one kernel launch (single_launch).
 A bf16 "also" entry times max(3, K/50) steps (tens of ms, like the burst
 bf16 peak: single GEMMs at full clocks); the prefill entry also times,
 as a second row, enough steps for about 2 s (like the sustained peak: a
@@ -63,10 +64,17 @@ def parse_args():
     ap.add_argument("--workload", default=W.DECODE, choices=sorted(W.WORKLOADS))
     ap.add_argument("--also", default=f"{W.PREFILL},{W.SKEWED},{W.DEEPSEEK},{W.TINY}",
                     help="comma-separated extra workloads measured at N=1 (empty for none)")
+    ap.add_argument("--also-single", default=W.DECODE,
+                    help="workloads also measured at N=1 as one kernel launch (empty for none)")
     ap.add_argument("--also-mxfp8", default=f"{W.DECODE},{W.PREFILL}",
                     help="workloads also measured at N=1 with MXFP8 expert weights (empty for none)")
     ap.add_argument("--also-nvfp4", default=f"{W.DECODE},{W.PREFILL}",
                     help="workloads also measured at N=1 with NVFP4 expert weights (empty for none)")
+    ap.add_argument("--weights", choices=["bf16", "mxfp8", "nvfp4"], default="bf16",
+                    help="expert weights of the main workload (profiler captures of the "
+                         "quantised kernels; e2e is measured for bf16 only)")
+    ap.add_argument("--single-launch", action="store_true",
+                    help="run the main workload as one kernel launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (smaller cases for profiler captures)")
@@ -190,6 +198,9 @@ def kernel_work(name, w, counts):
     T, d, E, k, I, Is = w.T, w.d, w.E, w.top_k, w.I, w.I_shared
     rows = T * k
     name = name.removesuffix("_smallm")  # the small-M kernels do the same work
+    if name == "moe_decode_fused":  # the whole layer in one launch
+        return (C.expert_flops(T, k, d, I, Is) + C.router_flops(T, d, E) + 2 * rows * d,
+                C.algorithmic_bytes(counts, T, d, E, I, Is))
     touched = sum(1 for c in counts if c > 0)
     if name == "moe_gate_up_swiglu_nvfp4":
         return 4 * rows * d * I, int(touched * 2 * I * d * NV_BYTES) + rows * d * 2 + rows * I * 2
@@ -278,9 +289,10 @@ def job_rate(dist, per_rank_rate, world, device):
 # ------------------------------------------------------------------ our arm
 
 def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, peaks,
-            mxfp8=False, nvfp4=False):
+            mxfp8=False, nvfp4=False, single_launch=False):
     """mxfp8 / nvfp4: the expert weights are quantised once, outside the
-    timed region, and every step runs moe_forward_mxfp8 / _nvfp4 on them."""
+    timed region, and every step runs moe_forward_mxfp8 / _nvfp4 on them.
+    single_launch: every step runs the layer as one kernel launch."""
     import torch
     from mixture_experts_layer_20_gb300 import counters as C
     x = W.make_x(w, device="cuda")
@@ -288,6 +300,7 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
     out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
     kw = dict(out=out, ws=ws, router_bias=params["router_bias"],
               w_gate_up_shared=params["w_gate_up_shared"], w_down_shared=params["w_down_shared"])
+    fwd_kw = dict(single_launch=True) if single_launch else {}
     if mxfp8:
         mx_gu = moe.moe_mxfp8_quantize(params["w_gate_up"])
         mx_d = moe.moe_mxfp8_quantize(params["w_down"])
@@ -303,7 +316,7 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
     else:
         def step():
             moe.moe_forward(x, params["w_router"], params["w_gate_up"], params["w_down"], w.top_k,
-                            **kw)
+                            **kw, **fwd_kw)
 
     for _ in range(max(warmup, 3)):
         step()
@@ -406,7 +419,7 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
             "x": x, "ws": ws, "counts": counts}
 
 
-def measure_e2e(moe, w, params, ws, x, steps):
+def measure_e2e(moe, w, params, ws, x, steps, single_launch=False):
     """Tokens/s end to end through the public API, host buffers in and out: the
     layer captured once as a graph over pinned x_host / out_host
     (moe_forward_graph with host buffers: H2D of x, the layer, D2H of out) and
@@ -430,9 +443,10 @@ def measure_e2e(moe, w, params, ws, x, steps):
         return w.T * steps / (time.perf_counter() - t0)
 
     plain = timed(lambda: moe.moe_forward_host(x_host, params["w_router"], params["w_gate_up"],
-                                               params["w_down"], w.top_k, out_host, ws, **kw))
+                                               params["w_down"], w.top_k, out_host, ws,
+                                               single_launch=single_launch, **kw))
     graph = moe.ForwardGraph(x_host, params["w_router"], params["w_gate_up"], params["w_down"],
-                             w.top_k, out_host, ws, **kw)
+                             w.top_k, out_host, ws, single_launch=single_launch, **kw)
     replay = timed(lambda: graph.launch())
     graph.close()
     nbytes = w.T * w.d * 2
@@ -575,10 +589,15 @@ def main():
 
     w = pick_workload(W, args)
     params = W.make_weights(w, device="cuda")
-    r = measure(moe, W, w, params, args.steps, args.warmup, rank, world, dist, smi_index, peaks)
-    e2e = measure_e2e(moe, w, params, r["ws"], r["x"], max(10, min(args.steps, 100)))
-    if dist:
-        e2e["value"] = round(job_rate(dist, e2e["value"], world, "cuda"), 1)
+    r = measure(moe, W, w, params, args.steps, args.warmup, rank, world, dist, smi_index, peaks,
+                mxfp8=args.weights == "mxfp8", nvfp4=args.weights == "nvfp4",
+                single_launch=args.single_launch)
+    e2e = None
+    if args.weights == "bf16":
+        e2e = measure_e2e(moe, w, params, r["ws"], r["x"], max(10, min(args.steps, 100)),
+                          single_launch=args.single_launch)
+        if dist:
+            e2e["value"] = round(job_rate(dist, e2e["value"], world, "cuda"), 1)
 
     also = []
     details = [detail_line(w.name + " bf16", r)]
@@ -602,6 +621,20 @@ def main():
                 also.append(also_row(name, "bf16", rs, "sustained"))
                 details.append(detail_line(name + " bf16 sustained", rs))
                 del rs
+            if not same:
+                del pa
+            torch.cuda.empty_cache()
+        for name in [n for n in args.also_single.split(",") if n]:
+            wa = W.WORKLOADS[name]
+            same = (wa.d, wa.E, wa.I, wa.I_shared, wa.zipf_bias, wa.seed) == \
+                (w.d, w.E, w.I, w.I_shared, w.zipf_bias, w.seed)
+            pa = params if same else W.make_weights(wa, device="cuda")
+            n_s = max(3, args.steps // 10)
+            ra = measure(moe, W, wa, pa, n_s, 3, 0, 1, None, smi_index, peaks, single_launch=True)
+            also.append(also_row(name, "bf16 1-launch", ra,
+                                 "sustained" if ra["ms"] * n_s * 1e-3 > 1.0 else "burst"))
+            details.append(detail_line(f"{name} bf16 single launch", ra))
+            del ra
             if not same:
                 del pa
             torch.cuda.empty_cache()
@@ -633,7 +666,9 @@ def main():
             "metric": METRIC, "value": round(r["tokens_per_s"], 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(r["ms"], 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Gaussian x and weights)",
+            "vs_baseline": None, "dtype": "bf16" if args.weights == "bf16" else
+            f"bf16 activations, {args.weights} expert weights",
+            "data": "synthetic (seeded Gaussian x and weights)",
             "config": bench_config(w, world),
             "clocks": r["clocks"], "e2e": e2e, "gpu_launches": r["launches"],
             "roofline": r["roofline"], "cpu_baseline": cpu, "layer": r["layer"],

@@ -192,13 +192,27 @@ moe_status_t moe_forward(const moe_bf16* x, const moe_bf16* w_router,
  * only (see moe_route_ex).  Shared expert ('PagedAttention, speculative
  * decoding, MoE and Blackwell', section 2: experts that process every token):
  * w_gate_up_shared [2*I_shared,d], w_down_shared [d,I_shared]; its output is
- * added with weight 1.  Zero-initialise the struct: later fields default to 0. */
+ * added with weight 1.
+ * single_launch = 1: the whole layer runs as one kernel launch ('Hosting Qwen
+ * on Blackwell', "Expert parallelism": decode fuses dispatch, GEMMs and
+ * combine into one kernel): a cooperative launch whose phases (router,
+ * top-k, grouping, gate_up, down, combine) are separated by grid-wide
+ * barriers bounded by the wait timeout.  For decode-sized batches with bf16
+ * expert weights: d and I multiples of 128, no shared expert, T*top_k <= 4096
+ * and at most 16 rows per expert on average (else MOE_ERR_UNSUPPORTED).  The
+ * barrier counters live in the workspace's first 256 bytes, which must start
+ * at zero (moe_workspace_init) like the status word.  The router sums its
+ * logits over 128-wide ranges of d here (512 otherwise), so a near-tie may
+ * route differently from the multi-launch layer; both are checked against
+ * the same reference.
+ * Zero-initialise the struct: later fields default to 0. */
 typedef struct {
   const float* router_bias;
   const moe_bf16* w_gate_up_shared;
   const moe_bf16* w_down_shared;
   int I_shared;
   int bias_selection_only;
+  int single_launch;
 } moe_forward_ext_t;
 
 moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,

@@ -32,7 +32,7 @@ class WorkspaceLayout(ctypes.Structure):
 
 class ForwardExt(ctypes.Structure):
     _fields_ = [("router_bias", _vp), ("w_gate_up_shared", _vp), ("w_down_shared", _vp),
-                ("I_shared", _i), ("bias_selection_only", _i)]
+                ("I_shared", _i), ("bias_selection_only", _i), ("single_launch", _i)]
 
 
 _SIGS = {
@@ -261,8 +261,10 @@ def moe_combine(y, slot_pos, topk_gates, y_shared=None, out=None, ws=None, strea
 
 
 def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router_bias=None,
-                w_gate_up_shared=None, w_down_shared=None, stream=None, bias_selection_only=False):
-    """The whole layer.  Returns out [T, d] bf16."""
+                w_gate_up_shared=None, w_down_shared=None, stream=None, bias_selection_only=False,
+                single_launch=False):
+    """The whole layer.  Returns out [T, d] bf16.  single_launch: one kernel
+    launch for the whole layer (decode-sized batches, see moe_forward_ext_t)."""
     for t, n in ((x, "x"), (w_router, "w_router"), (w_gate_up, "w_gate_up"), (w_down, "w_down"),
                  (w_gate_up_shared, "w_gate_up_shared"), (w_down_shared, "w_down_shared")):
         _want(t, torch.bfloat16, n)
@@ -277,14 +279,14 @@ def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router
     if ws is None:
         ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device)
     s = _stream(stream)
-    if router_bias is None and I_s == 0:
+    if router_bias is None and I_s == 0 and not single_launch:
         st = _lib.moe_forward(_p(x), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E, I, top_k,
                               _p(out), _p(ws), ws.numel(), s)
     else:
         ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
                          w_gate_up_shared.data_ptr() if I_s else None,
                          w_down_shared.data_ptr() if I_s else None, I_s,
-                         1 if bias_selection_only else 0)
+                         1 if bias_selection_only else 0, 1 if single_launch else 0)
         st = _lib.moe_forward_ex(_p(x), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E, I,
                                  top_k, _p(out), _p(ws), ws.numel(), s, ctypes.byref(ext))
     _check(st, "moe_forward")
@@ -292,7 +294,8 @@ def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router
 
 
 def moe_forward_host(x_host, w_router, w_gate_up, w_down, top_k, out_host, ws,
-                     router_bias=None, w_gate_up_shared=None, w_down_shared=None, stream=None):
+                     router_bias=None, w_gate_up_shared=None, w_down_shared=None, stream=None,
+                     single_launch=False):
     """The whole layer on host tensors (pinned for async copies); queued on
     the stream, not synchronised."""
     if x_host.is_cuda or out_host.is_cuda or x_host.dtype != torch.bfloat16 \
@@ -306,7 +309,8 @@ def moe_forward_host(x_host, w_router, w_gate_up, w_down, top_k, out_host, ws,
     I_s = w_down_shared.shape[1] if w_down_shared is not None else 0
     ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
                      w_gate_up_shared.data_ptr() if I_s else None,
-                     w_down_shared.data_ptr() if I_s else None, I_s)
+                     w_down_shared.data_ptr() if I_s else None, I_s, 0,
+                     1 if single_launch else 0)
     _check(_lib.moe_forward_host(_p(x_host), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E,
                                  I2 // 2, top_k, _p(out_host), _p(ws), ws.numel(), _stream(stream),
                                  ctypes.byref(ext)), "moe_forward_host")
@@ -414,7 +418,8 @@ class ForwardGraph:
     replays, not the tensor; every buffer is kept alive by this object."""
 
     def __init__(self, x, w_router, w_gate_up, w_down, top_k, out, ws, router_bias=None,
-                 w_gate_up_shared=None, w_down_shared=None, bias_selection_only=False):
+                 w_gate_up_shared=None, w_down_shared=None, bias_selection_only=False,
+                 single_launch=False):
         host = not x.is_cuda
         if x.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or out.is_cuda == host:
             raise ValueError("x and out must be bf16 tensors on the same side (device or host)")
@@ -428,7 +433,7 @@ class ForwardGraph:
         self._ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
                                w_gate_up_shared.data_ptr() if I_s else None,
                                w_down_shared.data_ptr() if I_s else None, I_s,
-                               1 if bias_selection_only else 0)
+                               1 if bias_selection_only else 0, 1 if single_launch else 0)
         self._keep = (x, w_router, w_gate_up, w_down, out, ws, router_bias, w_gate_up_shared,
                       w_down_shared)
         self._h = ctypes.c_void_p()

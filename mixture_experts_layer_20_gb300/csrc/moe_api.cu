@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -93,7 +94,12 @@ Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t at = off; off += align_up(bytes); return at; };
   L.status = take(kAlign);
-  L.logits = take(router_partial_bytes(T, d, E));
+  // decode-sized layers may run as one launch, whose router keeps partial
+  // sums over 128-wide ranges of d (four times the 512-wide ones)
+  const bool decode_sized = d % 128 == 0 && n <= static_cast<size_t>(kPermuteSmallMax) &&
+                            n <= static_cast<size_t>(kSmallMRowsPerExpert) * E;
+  L.logits = take(decode_sized ? std::max(router_partial_bytes(T, d, E), fused_partial_bytes(T, d, E))
+                               : router_partial_bytes(T, d, E));
   L.ids = take(n * 4);
   L.gates = take(n * 4);
   L.counts = take(static_cast<size_t>(E) * 4);
@@ -345,6 +351,7 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
     return fail(MOE_ERR_UNSUPPORTED, "NVFP4 weights need d and I multiples of 256");
   const float* bias = ext ? ext->router_bias : nullptr;
   const int bias_sel = ext ? ext->bias_selection_only : 0;
+  const bool single = ext && ext->single_launch;
   const int I_shared = ext ? ext->I_shared : 0;
   const moe_bf16* wgu_s = ext ? ext->w_gate_up_shared : nullptr;
   const moe_bf16* wd_s = ext ? ext->w_down_shared : nullptr;
@@ -358,6 +365,12 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
     return fail(MOE_ERR_INVALID_ARG, "moe_forward: pointers must be 16-byte aligned");
   const Layout L = forward_layout(T, d, E, I, top_k, I_shared);
   if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "moe_forward: workspace too small");
+  if (single && (mx || I_shared || d % 128 || I % 128 ||
+                 static_cast<long long>(T) * top_k > kPermuteSmallMax ||
+                 static_cast<long long>(T) * top_k > kSmallMRowsPerExpert * E))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "single_launch needs bf16 expert weights, no shared expert, d and I multiples of "
+                "128, T*top_k <= 4096 and at most 16 rows per expert on average");
   if ((st = check_device()) != MOE_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -376,6 +389,34 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   const int rows = T * top_k;
 
   float* partial = reinterpret_cast<float*>(w + L.logits);
+  if (single) {
+    FusedLayer F{};
+    F.x = x;
+    F.w_router = w_router;
+    F.bias = bias;
+    F.bias_selection_only = bias_sel;
+    F.w_gate_up = w_gate_up;
+    F.w_down = w_down;
+    F.T = T;
+    F.d = d;
+    F.E = E;
+    F.I = I;
+    F.k = top_k;
+    F.partial = partial;
+    F.ids = ids;
+    F.gates = gates;
+    F.counts = counts;
+    F.offsets = offsets;
+    F.perm = perm;
+    F.slot_pos = slot_pos;
+    F.h = h;
+    F.y = y;
+    F.out = out;
+    F.status = status;
+    F.timeout_ns = tmo;
+    const cudaError_t fe = launch_decode_fused(s, F);
+    return fe == cudaSuccess ? MOE_OK : cuda_fail(fe, "single-launch layer");
+  }
   if ((st = route_impl(x, w_router, bias, bias_sel, T, d, E, top_k, ids, gates, partial, status,
                        s)) != MOE_OK)
     return st;

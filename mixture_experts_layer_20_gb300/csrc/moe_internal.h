@@ -25,6 +25,13 @@ inline size_t router_partial_bytes(int T, int d, int E) {
   return static_cast<size_t>(router_splits(d)) * T * router_npad(E) * sizeof(float);
 }
 
+// Words of the workspace's 256-byte status region: word 0 is the status word;
+// the single-launch decode kernel keeps its grid-barrier counters in three
+// more, each on its own 64-byte line (moe_workspace_init zeroes all of them).
+constexpr int kBarrierCountWord = 16;
+constexpr int kBarrierGenWord = 32;
+constexpr int kExitCountWord = 48;
+
 // Bits of the workspace's device status word.
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusDeviceCheck = 2u;
@@ -46,6 +53,16 @@ __device__ __forceinline__ void pdl_wait_and_release() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
+}
+
+// A load of data the kernel only reads.  COHERENT = false: written by an
+// earlier kernel (the read-only path, __ldg).  COHERENT = true: written by
+// another CTA of the same kernel before a grid-wide barrier, so it is read
+// from L2 (__ldcg), never from a possibly stale L1 line.
+template <bool COHERENT, typename T>
+__device__ __forceinline__ T ld_in(const T* p) {
+  if constexpr (COHERENT) return __ldcg(p);
+  else return __ldg(p);
 }
 
 template <typename... KArgs, typename... Args>
@@ -162,6 +179,32 @@ cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
                                       const void* w_down, const uint8_t* scales_down,
                                       const float* tscale_down, void* h, void* y,
                                       unsigned* status);
+
+// The whole layer in one cooperative launch, for decode-sized batches with
+// bf16 expert weights and no shared expert (moe_fused.cu).  Requires d and I
+// multiples of 128, E <= 256 and T * k <= kPermuteSmallMax; partial holds
+// fused_partial_bytes(T, d, E) bytes; status points at the workspace's status
+// region (its barrier words must start at zero).
+struct FusedLayer {
+  const void* x;
+  const void* w_router;
+  const float* bias;
+  int bias_selection_only;
+  const void* w_gate_up;
+  const void* w_down;
+  int T, d, E, I, k;
+  float* partial;
+  int32_t* ids;
+  float* gates;
+  int32_t *counts, *offsets, *perm, *slot_pos;
+  void* h;    // [T k, I] bf16
+  void* y;    // [T k, d] fp16
+  void* out;  // [T, d] bf16
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+size_t fused_partial_bytes(int T, int d, int E);
+cudaError_t launch_decode_fused(cudaStream_t s, const FusedLayer& L);
 
 // NVFP4 quantisation of `groups` matrices [rows_per_group, K] (K a multiple of
 // 256) in one bf16 array: codes, scales as above, one tensor scale per matrix.

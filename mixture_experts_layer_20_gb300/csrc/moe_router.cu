@@ -14,117 +14,12 @@
 #include <climits>
 
 #include "moe_internal.h"
+#include "moe_router.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kTokensPerCta = 8;  // one warp each
-
-// A float's bits mapped to an unsigned key with the same order.
-__device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-template <int SLOTS>  // experts per lane: lane, lane + 32, ... (SLOTS * 32 >= E)
-__device__ __forceinline__ void topk_warp(const float* __restrict__ partial, int splits, int T,
-                                          int npad, int E, int k, const float* __restrict__ bias,
-                                          int sel_only, int t, int lane,
-                                          int32_t* __restrict__ ids, float* __restrict__ gates) {
-  // K ranges summed in range order (a token's logits do not depend on the
-  // batch); all loads of a range are issued before its adds
-  float L[SLOTS];
-#pragma unroll
-  for (int i = 0; i < SLOTS; ++i) L[i] = 0.0f;
-#pragma unroll 4
-  for (int sp = 0; sp < splits; ++sp) {
-    const float* row = partial + ((size_t)sp * T + t) * npad;
-    float v[SLOTS];
-#pragma unroll
-    for (int i = 0; i < SLOTS; ++i) v[i] = lane + 32 * i < E ? __ldg(row + lane + 32 * i) : 0.0f;
-#pragma unroll
-    for (int i = 0; i < SLOTS; ++i) L[i] += v[i];
-  }
-  // 64-bit keys: selection-logit order in the high word, lower expert index
-  // wins ties.  Each key carries the logit its gate is computed from: the
-  // same biased logit, or the unbiased one when the bias only selects.
-  unsigned long long key[SLOTS];
-  float gl[SLOTS];
-#pragma unroll
-  for (int i = 0; i < SLOTS; ++i) {
-    const int e = lane + 32 * i;
-    float l = e < E ? L[i] + (bias ? __ldg(bias + e) : 0.0f) : -INFINITY;
-    gl[i] = sel_only ? L[i] : l;
-    if (l == 0.0f) l = 0.0f;  // -0 and +0 compare equal: one key for both
-    key[i] = e < E ? (static_cast<unsigned long long>(order_key(l)) << 32) |
-                         static_cast<uint32_t>(kMaxExperts - 1 - e)
-                   : 0ull;
-  }
-  // each lane sorts its own keys, descending
-#pragma unroll
-  for (int a = 0; a < SLOTS - 1; ++a)
-#pragma unroll
-    for (int b = 0; b < SLOTS - 1 - a; ++b)
-      if (key[b] < key[b + 1]) {
-        const unsigned long long x = key[b]; key[b] = key[b + 1]; key[b + 1] = x;
-        const float y = gl[b]; gl[b] = gl[b + 1]; gl[b + 1] = y;
-      }
-
-  // k rounds: the warp's largest head wins; its lane pops it
-  unsigned long long sel[kMaxTopK];
-  float sel_g[kMaxTopK];
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    sel[j] = 0ull;
-    sel_g[j] = 0.0f;
-    if (j < k) {
-      unsigned long long best = key[0];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-        best = o > best ? o : best;
-      }
-      const unsigned owner = __ballot_sync(0xffffffffu, key[0] == best);
-      sel[j] = best;
-      sel_g[j] = __shfl_sync(0xffffffffu, gl[0], __ffs(owner) - 1);
-      if (key[0] == best) {
-#pragma unroll
-        for (int i = 0; i < SLOTS - 1; ++i) { key[i] = key[i + 1]; gl[i] = gl[i + 1]; }
-        key[SLOTS - 1] = 0ull;
-      }
-    }
-  }
-
-  // The selections are the same in every lane.  Gates: softmax of the chosen
-  // logits (max subtracted, sum in selection order); lane j < k writes the
-  // selection whose expert id is the j-th smallest, so a token's slots hold
-  // ascending expert ids.
-  float top = sel_g[0];
-#pragma unroll
-  for (int j = 1; j < kMaxTopK; ++j)
-    if (j < k) top = fmaxf(top, sel_g[j]);
-  int e_of[kMaxTopK];
-  float w[kMaxTopK];
-  float sum = 0.0f;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    e_of[j] = j < k ? kMaxExperts - 1 - static_cast<int>(sel[j] & 0xffffffffu) : INT_MAX;
-    w[j] = j < k ? expf(sel_g[j] - top) : 0.0f;
-    sum += w[j];
-  }
-  int my_e = INT_MAX;
-  float my_w = 0.0f;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j)
-    if (j == lane) { my_e = e_of[j]; my_w = w[j]; }
-  int rank = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) rank += e_of[j] < my_e ? 1 : 0;
-  if (lane < k) {
-    ids[(size_t)t * k + rank] = my_e;
-    gates[(size_t)t * k + rank] = my_w / sum;
-  }
-}
 
 // Five CTAs per SM (at most 51 registers a thread): a 6000-token batch is
 // one wave of warps.
