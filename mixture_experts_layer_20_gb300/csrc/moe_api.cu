@@ -427,7 +427,8 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   // Quantised weights with few rows per expert (decode) take the warp-level
   // small-M kernels, which read the token rows from x through perm.
   void* x_perm = w + L.x_perm;
-  const bool small_m = mx && rows <= kSmallMRowsPerExpert * static_cast<long long>(E);
+  const bool small_m = mx && rows <= kSmallMRowsPerExpert * static_cast<long long>(E) &&
+                       d % 256 == 0 && I % 256 == 0;
   const bool gather_rows = small_m || (!mx && rows <= 128LL * E);
   cudaError_t e = launch_permute(s, ids, gather_rows ? nullptr : x, T, d, E, top_k, counts,
                                  offsets, perm, slot_pos, x_perm, table, status);

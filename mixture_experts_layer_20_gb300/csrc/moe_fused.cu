@@ -40,6 +40,8 @@
 namespace moe {
 namespace {
 
+constexpr int kRouterRange = 128;  // the router's partial sums: 128-wide ranges of d
+
 struct FusedParams {
   const __nv_bfloat16* x;         // [T, d]
   const __nv_bfloat16* w_router;  // [E, d]
@@ -104,7 +106,7 @@ __device__ __forceinline__ void router_partials(const FusedParams& p) {
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
   const int groups = (p.E + 15) / 16;
-  const int ranges = p.d / kSmChunkK;
+  const int ranges = p.d / kRouterRange;
   const int passes = (p.T + 15) / 16;
   const int total = groups * ranges * passes;
   const int W = gridDim.x * kSmWarps;
@@ -113,7 +115,7 @@ __device__ __forceinline__ void router_partials(const FusedParams& p) {
     const int rest = tau / groups;
     const int r = rest % ranges;
     const int pass = rest / ranges;
-    const int k0 = r * kSmChunkK;
+    const int k0 = r * kRouterRange;
     uint4 a[2][4], b[2][4];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kSmThreads, 2) moe_decode_fused_kernel(const F
   bool alive = grid_sync(p);
 
   if (alive) {
-    const int splits = p.d / kSmChunkK;
+    const int splits = p.d / kRouterRange;
     for (int t = blockIdx.x * kSmWarps + warp; t < p.T; t += gridDim.x * kSmWarps) {
       if (p.E <= 64)
         topk_warp<2, true>(p.partial, splits, p.T, p.npad, p.E, p.k, p.bias, p.sel_only, t, lane,
@@ -239,11 +241,11 @@ int fused_blocks_per_sm() {
 }  // namespace
 
 size_t fused_partial_bytes(int T, int d, int E) {
-  return static_cast<size_t>(d / kSmChunkK) * T * router_npad(E) * sizeof(float);
+  return static_cast<size_t>(d / kRouterRange) * T * router_npad(E) * sizeof(float);
 }
 
 cudaError_t launch_decode_fused(cudaStream_t s, const FusedLayer& L) {
-  if (L.d % kSmChunkK || L.I % kSmChunkK || L.E > kMaxExperts || L.k > kMaxTopK ||
+  if (L.d % kRouterRange || L.I % kRouterRange || L.E > kMaxExperts || L.k > kMaxTopK ||
       L.T * L.k > kPermuteSmallMax)
     return cudaErrorInvalidValue;
   const int per_sm = fused_blocks_per_sm();

@@ -82,12 +82,13 @@ cudaError_t sm_ffn(cudaStream_t s, const char* gu_name, const char* dn_name, con
                    const float* t_gate_up, const uint8_t* w_down, const uint8_t* s_down,
                    const float* t_down, void* h, void* y, unsigned* status) {
   using F = SmF<FMT>;
+  if (d % sm_chunk_k<FMT>() || I % sm_chunk_k<FMT>()) return cudaErrorInvalidValue;
   SmParams p{};
   p.w = w_gate_up;
   p.scales = s_gate_up;
   p.tscale = t_gate_up;
   p.scale_rows = 2LL * I * E;
-  p.row_bytes = static_cast<long long>(d) * F::kValBytesX2 / 2;
+  p.row_bytes = static_cast<long long>(d) * F::kBytesX2 / 2;
   p.K = d;
   p.n_out = I;
   p.w_rows_per_expert = 2 * I;
@@ -109,7 +110,7 @@ cudaError_t sm_ffn(cudaStream_t s, const char* gu_name, const char* dn_name, con
   q.scales = s_down;
   q.tscale = t_down;
   q.scale_rows = static_cast<long long>(E) * d;
-  q.row_bytes = static_cast<long long>(I) * F::kValBytesX2 / 2;
+  q.row_bytes = static_cast<long long>(I) * F::kBytesX2 / 2;
   q.K = I;
   q.n_out = d;
   q.w_rows_per_expert = d;
@@ -132,7 +133,7 @@ cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
                                       const void* w_down, const uint8_t* scales_down,
                                       const float* tscale_down, void* h, void* y,
                                       unsigned* status) {
-  if (d % kSmChunkK || I % kSmChunkK || E > kMaxExperts) return cudaErrorInvalidValue;
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
   const uint8_t* wg = static_cast<const uint8_t*>(w_gate_up);
   const uint8_t* wd = static_cast<const uint8_t*>(w_down);
   switch (fmt) {
@@ -145,7 +146,6 @@ cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
                             perm, div, offsets, rows, d, E, I, wg, scales_gate_up, nullptr, wd,
                             scales_down, nullptr, h, y, status);
     case 2:
-      if (d % 256 || I % 256) return cudaErrorInvalidValue;
       return sm_ffn<kSmNv4>(s, "moe_gate_up_swiglu_nvfp4_smallm", "moe_down_nvfp4_smallm", a,
                             perm, div, offsets, rows, d, E, I, wg, scales_gate_up, tscale_gate_up,
                             wd, scales_down, tscale_down, h, y, status);

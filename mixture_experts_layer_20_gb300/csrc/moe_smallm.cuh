@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -18,28 +19,37 @@ enum SmKind : int { kSmGateUp = 1, kSmDown = 2 };
 
 constexpr int kSmWarps = 8;               // warps per CTA
 constexpr int kSmThreads = kSmWarps * 32;
-constexpr int kSmChunkK = 128;            // reduction values per pipeline step
-constexpr int kSmNT = 2;                  // 8-token MMA tiles per pass: 16 tokens
-constexpr int kSmTokPass = 8 * kSmNT;
-constexpr int kSmScaleSlot = 16;          // bytes of block scales per lane per stage
+constexpr int kSmTok = 8;                 // tokens per pass (the MMA's N)
 constexpr float kSmHalfMax = 65504.0f;
 
-// V: values per 16-byte unit; U: units per lane and row per chunk; NS: ring
-// stages; SB: scale bytes per weight row per chunk (copied per lane).
+// Per weight format: V values per 16-byte unit; U units per lane and weight
+// row per chunk, so a chunk covers KC = 4 V U values of the reduction; NS
+// ring stages; SB block-scale bytes per weight row per chunk (0: none).
 template <int FMT> struct SmF;
 template <> struct SmF<kSmBf16> {
-  static constexpr int V = 8, U = 4, NS = 3, SB = 0, kValBytesX2 = 4;  // 2 bytes / value
+  static constexpr int V = 8, U = 4, NS = 3, SB = 0;
+  static constexpr int kBytesX2 = 4;  // twice the bytes per value
 };
 template <> struct SmF<kSmMx8> {
-  static constexpr int V = 16, U = 2, NS = 5, SB = 4, kValBytesX2 = 2;  // 1 byte / value
+  static constexpr int V = 16, U = 4, NS = 3, SB = 8;
+  static constexpr int kBytesX2 = 2;
 };
 template <> struct SmF<kSmNv4> {
-  static constexpr int V = 32, U = 1, NS = 8, SB = 8, kValBytesX2 = 1;  // half a byte / value
+  static constexpr int V = 32, U = 2, NS = 4, SB = 16;
+  static constexpr int kBytesX2 = 1;
 };
-
+template <int FMT>
+__host__ __device__ constexpr int sm_chunk_k() {
+  return 4 * SmF<FMT>::V * SmF<FMT>::U;
+}
+// Block-scale bytes a lane keeps per stage: both of its rows' scales.
+template <int FMT>
+__host__ __device__ constexpr int sm_scale_slot() {
+  return 2 * SmF<FMT>::SB;
+}
 template <int FMT>
 __host__ __device__ constexpr int sm_stage_bytes() {
-  return 2 * SmF<FMT>::U * 32 * 16 + (SmF<FMT>::SB ? 32 * kSmScaleSlot : 0);
+  return 2 * SmF<FMT>::U * 32 * 16 + 32 * sm_scale_slot<FMT>();
 }
 template <int FMT>
 __host__ __device__ constexpr int sm_smem_bytes() {
@@ -52,7 +62,7 @@ struct SmParams {
   const float* tscale;       // NVFP4: one scale per expert (null: none)
   long long scale_rows;      // weight rows of the whole tensor
   long long row_bytes;
-  int K;                     // reduction length (a multiple of 128)
+  int K;                     // reduction length (a multiple of the chunk)
   int n_out;                 // gate_up: I (h columns); down: d (y columns)
   int w_rows_per_expert;     // 2I or d
   int up_offset;             // gate_up: I
@@ -70,9 +80,6 @@ struct SmParams {
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
@@ -108,73 +115,94 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// One task: 16 weight rows of one expert (see the file comment) over the
-// whole reduction, for all of the expert's tokens (passes of 16).
+// One task: 16 weight rows of one expert (see the file comment of
+// moe_smallm.cu) over the whole reduction, for all of the expert's tokens in
+// passes of 8.  Pointers are this lane's: its two weight rows (fragment rows
+// g and g + 8) at its first unit, and their block scales.
 struct SmTask {
   int e, m, row_off;      // expert, its token rows, first row in the grouped layout
-  long long r0, r1;       // weight rows of fragment rows g and g + 8 (this lane)
   int col;                // gate_up: h column c0 + g; down: y column r0 + g
   int npass;
+  const uint8_t* w0;
+  const uint8_t* w1;
+  const uint8_t* s0;
+  const uint8_t* s1;
 };
 
-template <int KIND>
+template <int FMT, int KIND>
 __device__ __forceinline__ SmTask sm_task(const SmParams& p, const int* s_act, const int* s_off,
-                                          int tau, int tpe, int g) {
+                                          int tau, int tpe, int g, int tig) {
   SmTask t;
   const int a = tau / tpe;
   const int cg = tau - a * tpe;
   t.e = s_act[a];
   t.row_off = s_off[t.e];
   t.m = s_off[t.e + 1] - t.row_off;
-  t.npass = (t.m + kSmTokPass - 1) / kSmTokPass;
+  t.npass = (t.m + kSmTok - 1) / kSmTok;
   const long long base = static_cast<long long>(t.e) * p.w_rows_per_expert;
+  long long r0, r1;
   if (KIND == kSmGateUp) {
     t.col = cg * 8 + g;
-    t.r0 = base + t.col;
-    t.r1 = t.r0 + p.up_offset;
+    r0 = base + t.col;
+    r1 = r0 + p.up_offset;
   } else {
     t.col = cg * 16 + g;
-    t.r0 = base + t.col;
-    t.r1 = t.r0 + 8;
+    r0 = base + t.col;
+    r1 = r0 + 8;
+  }
+  t.w0 = p.w + r0 * p.row_bytes + 16 * tig;
+  t.w1 = p.w + r1 * p.row_bytes + 16 * tig;
+  if constexpr (FMT == kSmMx8) {
+    t.s0 = p.scales + r0 * 4;
+    t.s1 = p.scales + r1 * 4;
+  } else if constexpr (FMT == kSmNv4) {
+    t.s0 = p.scales + r0 * 16;
+    t.s1 = p.scales + r1 * 16;
+  } else {
+    t.s0 = t.s1 = nullptr;
   }
   return t;
 }
 
-// Copies of one chunk of a task's weights (and scales) into ring slot `slot`.
+// Copies of chunk c of a task's weights (and scales) into ring slot `slot`:
+// unit i of row half rr at ((rr U + i) 32 + lane) 16, the lane's scale bytes
+// after the units.
 template <int FMT>
 __device__ __forceinline__ void sm_fetch(const SmParams& p, const SmTask& t, int c, uint32_t slot,
-                                         int lane, int tig) {
+                                         int lane) {
   using F = SmF<FMT>;
-  constexpr int kChunkBytes = kSmChunkK * F::kValBytesX2 / 2;
-  const uint8_t* rows[2] = {p.w + t.r0 * p.row_bytes + static_cast<long long>(c) * kChunkBytes,
-                            p.w + t.r1 * p.row_bytes + static_cast<long long>(c) * kChunkBytes};
+  constexpr int kChunkBytes = sm_chunk_k<FMT>() * F::kBytesX2 / 2;  // = 64 U
+  const long long off = static_cast<long long>(c) * kChunkBytes;
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-    for (int i = 0; i < F::U; ++i)
-      cp_async_16(slot + ((rr * F::U + i) * 32 + lane) * 16, rows[rr] + 64 * i + 16 * tig);
+  for (int i = 0; i < F::U; ++i) {
+    cp_async_16(slot + (i * 32 + lane) * 16, t.w0 + off + 64 * i);
+    cp_async_16(slot + ((F::U + i) * 32 + lane) * 16, t.w1 + off + 64 * i);
+  }
+  const uint32_t s = slot + 2 * F::U * 32 * 16 + lane * sm_scale_slot<FMT>();
   if constexpr (FMT == kSmMx8) {
-    const uint32_t s = slot + 2 * F::U * 32 * 16 + lane * kSmScaleSlot;
-    const uint8_t* base = p.scales + static_cast<long long>(c) * p.scale_rows * 4;
-    cp_async_4(s, base + t.r0 * 4);
-    cp_async_4(s + 4, base + t.r1 * 4);
+    // a 256-wide chunk spans two 128-wide scale stages: one word per row each
+    const long long st = 2LL * c * p.scale_rows * 4;
+    const long long st2 = st + p.scale_rows * 4;
+    cp_async_4(s, t.s0 + st);
+    cp_async_4(s + 4, t.s0 + st2);
+    cp_async_4(s + 8, t.s1 + st);
+    cp_async_4(s + 12, t.s1 + st2);
   } else if constexpr (FMT == kSmNv4) {
-    const uint32_t s = slot + 2 * F::U * 32 * 16 + lane * kSmScaleSlot;
-    const uint8_t* base =
-        p.scales + static_cast<long long>(c >> 1) * p.scale_rows * 16 + 8 * (c & 1);
-    cp_async_8(s, base + t.r0 * 16);
-    cp_async_8(s + 8, base + t.r1 * 16);
+    const long long st = static_cast<long long>(c) * p.scale_rows * 16;  // one stage per chunk
+    cp_async_16(s, t.s0 + st);
+    cp_async_16(s + 16, t.s1 + st);
   }
 }
 
-// One grouped GEMM (gate_up or down) by all warps of the grid.  ring: the
-// block's dynamic shared memory (sm_smem_bytes<FMT>()).  COHERENT: the offsets,
-// the permutation and (down) the token rows h were written by this kernel
-// before a grid-wide barrier (see ld_in).  Ends with every copy landed and a
-// block-wide barrier.
+// One grouped GEMM (gate_up or down) by all warps of the grid.  sm_raw: the
+// block's dynamic shared memory (sm_smem_bytes<FMT>()).  COHERENT: the
+// offsets, the permutation and (down) the token rows h were written by this
+// kernel before a grid-wide barrier (see ld_in).  Ends with every copy landed
+// and a block-wide barrier.
 template <int FMT, int KIND, bool COHERENT = false>
 __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
   using F = SmF<FMT>;
+  constexpr int KC = sm_chunk_k<FMT>();
   constexpr bool kBCoherent = COHERENT && KIND == kSmDown;  // h rows; x is an input
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_act[kMaxExperts];
@@ -209,172 +237,178 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
   const int tpe = KIND == kSmGateUp ? p.n_out / 8 : p.n_out / 16;  // tasks per expert
   const int total = n_act * tpe;
   const int W = gridDim.x * kSmWarps;
-  const int nch = p.K / kSmChunkK;
+  const int nch = p.K / KC;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(sm_raw)) +
                         warp * F::NS * sm_stage_bytes<FMT>();
 
   // Fetch cursor: runs NS - 1 chunks ahead of the compute cursor over the
   // warp's stream of (task, pass, chunk).
   int f_tau = blockIdx.x * kSmWarps + warp;
-  int f_pass = 0, f_c = 0, f_slot = 0;
+  int f_pass = 0, f_c = 0;
+  uint32_t f_slot = ring;
   SmTask ft;
-  if (f_tau < total) ft = sm_task<KIND>(p, s_act, s_off, f_tau, tpe, g);
+  if (f_tau < total) ft = sm_task<FMT, KIND>(p, s_act, s_off, f_tau, tpe, g, tig);
   auto fetch_next = [&]() {
     if (f_tau < total) {
-      sm_fetch<FMT>(p, ft, f_c, ring + f_slot * sm_stage_bytes<FMT>(), lane, tig);
+      sm_fetch<FMT>(p, ft, f_c, f_slot, lane);
       if (++f_c == nch) {
         f_c = 0;
         if (++f_pass == ft.npass) {
           f_pass = 0;
           f_tau += W;
-          if (f_tau < total) ft = sm_task<KIND>(p, s_act, s_off, f_tau, tpe, g);
+          if (f_tau < total) ft = sm_task<FMT, KIND>(p, s_act, s_off, f_tau, tpe, g, tig);
         }
       }
     }
     cp_async_commit();  // an empty group once the stream has ended
-    if (++f_slot == F::NS) f_slot = 0;
+    f_slot += sm_stage_bytes<FMT>();
+    if (f_slot == ring + F::NS * sm_stage_bytes<FMT>()) f_slot = ring;
   };
 #pragma unroll 1
   for (int i = 0; i < F::NS - 1; ++i) fetch_next();
 
-  int slot = 0;
+  uint32_t st = ring;
   bool range_flag = false;
 #pragma unroll 1
   for (int tau = blockIdx.x * kSmWarps + warp; tau < total; tau += W) {
-    const SmTask t = sm_task<KIND>(p, s_act, s_off, tau, tpe, g);
+    const SmTask t = sm_task<FMT, KIND>(p, s_act, s_off, tau, tpe, g, tig);
     const float ts = (FMT == kSmNv4 && p.tscale) ? __ldg(p.tscale + t.e) : 1.0f;
 #pragma unroll 1
     for (int pass = 0; pass < t.npass; ++pass) {
-      // this lane's token of each 8-token tile: n = pass * 16 + nt * 8 + g
-      const __nv_bfloat16* brow[kSmNT];
-      bool nt_on[kSmNT];
-#pragma unroll
-      for (int nt = 0; nt < kSmNT; ++nt) {
-        const int n0 = pass * kSmTokPass + nt * 8;
-        nt_on[nt] = n0 < t.m;  // warp-uniform
-        const int n = n0 + g;
-        brow[nt] = nullptr;
+      // this lane's token: n = 8 pass + g (none past the expert's rows)
+      const __nv_bfloat16* brow = nullptr;
+      {
+        const int n = pass * kSmTok + g;
         if (n < t.m) {
           const int pos = t.row_off + n;
           const long long src = p.perm ? ld_in<COHERENT>(p.perm + pos) / p.div : pos;
-          if (src >= 0 && src < p.b_rows) brow[nt] = p.b + src * p.K;
+          if (src >= 0 && src < p.b_rows) brow = p.b + src * p.K;
           else atomicOr(p.status, kStatusDeviceCheck);  // a bad permutation: read zeros
         }
       }
-      float acc[kSmNT][4];
+      // kAcc accumulators, taken in turn by a unit's MMAs, break the MMA
+      // dependency chain; they are added in a fixed order at the end
+      constexpr int kAcc = F::V / 4 < 4 ? F::V / 4 : 4;
+      float acc[kAcc][4];
 #pragma unroll
-      for (int nt = 0; nt < kSmNT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+      for (int q = 0; q < kAcc; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
 
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
-        // token values of this chunk: per tile, unit i's V values (V / 8 x 16 bytes)
-        uint4 bv[kSmNT][4];
+        // token values of this chunk, unit by unit: values V (4 i + tig) + [0, V)
+        uint4 bv[F::U][F::V / 8];
 #pragma unroll
-        for (int nt = 0; nt < kSmNT; ++nt)
+        for (int i = 0; i < F::U; ++i)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = q / (F::V / 8), h = q % (F::V / 8);
-            bv[nt][q] = make_uint4(0u, 0u, 0u, 0u);
-            if (brow[nt])
-              bv[nt][q] = ld_in<kBCoherent>(reinterpret_cast<const uint4*>(
-                  brow[nt] + c * kSmChunkK + F::V * (4 * i + tig) + 8 * h));
-          }
+          for (int h = 0; h < F::V / 8; ++h)
+            bv[i][h] = brow ? ld_in<kBCoherent>(reinterpret_cast<const uint4*>(
+                                  brow + c * KC + F::V * (4 * i + tig) + 8 * h))
+                            : make_uint4(0u, 0u, 0u, 0u);
         fetch_next();
         cp_async_wait<F::NS - 1>();
-        const uint32_t st = ring + slot * sm_stage_bytes<FMT>();
-        if (++slot == F::NS) slot = 0;
-        uint4 av[2][F::U];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-          for (int i = 0; i < F::U; ++i) av[rr][i] = lds128(st + ((rr * F::U + i) * 32 + lane) * 16);
-        uint32_t sc0 = 0, sc1 = 0, sc2 = 0, sc3 = 0;
-        if constexpr (F::SB > 0) {
-          const uint4 s = lds128(st + 2 * F::U * 32 * 16 + lane * kSmScaleSlot);
-          sc0 = s.x; sc1 = s.y; sc2 = s.z; sc3 = s.w;
+        const uint32_t cur = st;
+        st += sm_stage_bytes<FMT>();
+        if (st == ring + F::NS * sm_stage_bytes<FMT>()) st = ring;
+        const uint32_t sslot = cur + 2 * F::U * 32 * 16 + lane * sm_scale_slot<FMT>();
+        uint4 sc = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (F::SB > 0) sc = lds128(sslot);
+        uint4 sc2 = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (FMT == kSmNv4) sc2 = lds128(sslot + 16);
+        // MXFP8: a scale byte above 134 (weights beyond 2^7 in a block) needs
+        // the general conversion; decided once per chunk for the whole warp
+        // MXFP8: a scale byte above 134 (weights beyond 2^7 in a block) needs
+        // the general conversion; decided once per chunk for the whole warp, so
+        // each variant of the chunk body below is one straight-line block
+        bool slow = false;
+        if constexpr (FMT == kSmMx8) {
+          const unsigned big = __vcmpgtu4(sc.x, 0x86868686u) | __vcmpgtu4(sc.y, 0x86868686u) |
+                               __vcmpgtu4(sc.z, 0x86868686u) | __vcmpgtu4(sc.w, 0x86868686u);
+          slow = __any_sync(0xffffffffu, big != 0u);
         }
+        auto chunk_body = [&](auto slow_tag) {
+          constexpr bool kSlow = decltype(slow_tag)::value;
+          (void)kSlow;
 #pragma unroll
-        for (int i = 0; i < F::U; ++i) {
-#pragma unroll
-          for (int j = 0; j < F::V / 4; ++j) {
-            uint32_t a[2][2];  // [row g / g + 8][values 4j, 4j+1 | 4j+2, 4j+3]
-            if constexpr (FMT == kSmBf16) {
-#pragma unroll
-              for (int rr = 0; rr < 2; ++rr) {
-                a[rr][0] = word_of(av[rr][i], 2 * j);
-                a[rr][1] = word_of(av[rr][i], 2 * j + 1);
-              }
-            } else if constexpr (FMT == kSmMx8) {
-              // unit i: 16 codes in the 32-value block 2 i + tig / 2 of the chunk
+          for (int i = 0; i < F::U; ++i) {
+            const uint4 a0 = lds128(cur + (i * 32 + lane) * 16);
+            const uint4 a1 = lds128(cur + ((F::U + i) * 32 + lane) * 16);
+            // MXFP8: unit i holds 16 codes of the 32-value block 2 i + tig / 2 of
+            // the chunk (scale word: row half, block / 4; byte: block % 4)
+            uint32_t sb[2] = {0u, 0u};
+            (void)sb;
+            if constexpr (FMT == kSmMx8) {
               const int blk = 2 * i + (tig >> 1);
-#pragma unroll
-              for (int rr = 0; rr < 2; ++rr) {
-                const uint32_t sbyte = ((rr ? sc1 : sc0) >> (8 * blk)) & 0xffu;
-                uint32_t o[2];
-                if (sbyte <= 134u) {
-                  const uint32_t mbits = ((sbyte + 120u) << 7) * 0x00010001u;
-                  e4m3x4_to_bf16_bits(word_of(av[rr][i], j),
-                                      *reinterpret_cast<const __nv_bfloat162*>(&mbits), o);
-                } else {
-                  e4m3x4_to_bf16_scaled(word_of(av[rr][i], j), e8m0_to_float(sbyte), o);
-                }
-                a[rr][0] = o[0];
-                a[rr][1] = o[1];
-              }
-            } else {
-              // one unit of 32 codes: blocks 2 tig (j < 4) and 2 tig + 1 of the
-              // chunk's 8; MMA j takes codes 4 j .. 4 j + 3 (word j / 2)
-              const int blk = 2 * tig + (j >> 2);  // byte of the 8 scale bytes
-#pragma unroll
-              for (int rr = 0; rr < 2; ++rr) {
-                const uint32_t lo = rr ? sc2 : sc0, hi = rr ? sc3 : sc1;
-                const uint32_t sbyte = ((blk < 4 ? lo : hi) >> (8 * (blk & 3))) & 0xffu;
-                const uint32_t w = word_of(av[rr][0], j >> 1) >> (16 * (j & 1));
-                uint32_t o[2];
-                e2m1x4_to_bf16(w, e4m3_scale_bf16x2(sbyte), o);
-                a[rr][0] = o[0];
-                a[rr][1] = o[1];
-              }
+              sb[0] = ((i < 2 ? sc.x : sc.y) >> (8 * (blk & 3))) & 0xffu;
+              sb[1] = ((i < 2 ? sc.z : sc.w) >> (8 * (blk & 3))) & 0xffu;
             }
 #pragma unroll
-            for (int nt = 0; nt < kSmNT; ++nt) {
-              if (!nt_on[nt]) continue;
-              // tokens: values V (4 i + tig) + 4 j + {0..3} of unit i
-              const int q = i * (F::V / 8) + (4 * j) / 8;
+            for (int j = 0; j < F::V / 4; ++j) {
+              uint32_t a[2][2];  // [row g / g + 8][values 4j, 4j+1 | 4j+2, 4j+3]
+              if constexpr (FMT == kSmBf16) {
+                a[0][0] = word_of(a0, 2 * j);
+                a[0][1] = word_of(a0, 2 * j + 1);
+                a[1][0] = word_of(a1, 2 * j);
+                a[1][1] = word_of(a1, 2 * j + 1);
+              } else if constexpr (FMT == kSmMx8) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                  const uint32_t codes = word_of(rr ? a1 : a0, j);
+                  if constexpr (!kSlow) {
+                    const uint32_t mbits = ((sb[rr] + 120u) << 7) * 0x00010001u;
+                    e4m3x4_to_bf16_bits(codes, *reinterpret_cast<const __nv_bfloat162*>(&mbits),
+                                        a[rr]);
+                  } else {
+                    e4m3x4_to_bf16_scaled(codes, e8m0_to_float(sb[rr]), a[rr]);
+                  }
+                }
+              } else {
+                // unit i: 32 codes = blocks 8 i + 2 tig (j < 4) and + 1 of the
+                // chunk's 16; MMA j takes codes 4 j .. 4 j + 3 (word j / 2)
+                const int blk = 8 * i + 2 * tig + (j >> 2);
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                  const uint4& s4 = rr ? sc2 : sc;
+                  const uint32_t sbyte = (word_of(s4, blk >> 2) >> (8 * (blk & 3))) & 0xffu;
+                  const uint32_t w = word_of(rr ? a1 : a0, j >> 1) >> (16 * (j & 1));
+                  e2m1x4_to_bf16(w, e4m3_scale_bf16x2(sbyte), a[rr]);
+                }
+              }
+              // tokens: values V (4 i + tig) + 4 j + {0..3}: 16-byte piece (4 j) / 8
+              const uint4& bq = bv[i][(4 * j) / 8];
               const int wsel = ((4 * j) % 8) / 2;
-              const uint32_t b0 = word_of(bv[nt][q], wsel), b1 = word_of(bv[nt][q], wsel + 1);
-              mma_16816(acc[nt], a[0][0], a[1][0], a[0][1], a[1][1], b0, b1);
+              mma_16816(acc[j % kAcc], a[0][0], a[1][0], a[0][1], a[1][1], word_of(bq, wsel),
+                        word_of(bq, wsel + 1));
             }
           }
-        }
+        };
+        if (FMT == kSmMx8 && slow) chunk_body(std::true_type{});
+        else chunk_body(std::false_type{});
       }
 
-      // epilogue: acc[nt] = {(row g, token 2 tig), (g, 2 tig + 1), (g + 8, 2 tig), (g + 8, 2 tig + 1)}
+      // epilogue: acc = {(row g, token 2 tig), (g, 2 tig + 1), (g + 8, 2 tig), (g + 8, 2 tig + 1)}
 #pragma unroll
-      for (int nt = 0; nt < kSmNT; ++nt) {
-        if (!nt_on[nt]) continue;
-        const int n0 = pass * kSmTokPass + nt * 8 + 2 * tig;
+      for (int q = 1; q < kAcc; ++q)
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          const int n = n0 + hlf;
-          if (n >= t.m) continue;
-          const size_t orow = static_cast<size_t>(t.row_off + n) * p.ld_out;
-          if constexpr (KIND == kSmGateUp) {
-            const float gt = acc[nt][hlf] * ts, up = acc[nt][2 + hlf] * ts;
-            static_cast<__nv_bfloat16*>(p.out)[orow + t.col] =
-                __float2bfloat16_rn(__fdividef(gt, 1.0f + __expf(-gt)) * up);
-          } else {
+        for (int v = 0; v < 4; ++v) acc[0][v] += acc[q][v];
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-              float v = acc[nt][2 * rr + hlf] * ts;
-              if (fabsf(v) > kSmHalfMax) {
-                range_flag = true;
-                if (fabsf(v) < INFINITY) v = copysignf(kSmHalfMax, v);
-              }
-              static_cast<__half*>(p.out)[orow + t.col + 8 * rr] = __float2half_rn(v);
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int n = pass * kSmTok + 2 * tig + hlf;
+        if (n >= t.m) continue;
+        const size_t orow = static_cast<size_t>(t.row_off + n) * p.ld_out;
+        if constexpr (KIND == kSmGateUp) {
+          const float gt = acc[0][hlf] * ts;
+          const float up = acc[0][2 + hlf] * ts;
+          static_cast<__nv_bfloat16*>(p.out)[orow + t.col] =
+              __float2bfloat16_rn(__fdividef(gt, 1.0f + __expf(-gt)) * up);
+        } else {
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            float v = acc[0][2 * rr + hlf] * ts;
+            if (fabsf(v) > kSmHalfMax) {
+              range_flag = true;
+              if (fabsf(v) < INFINITY) v = copysignf(kSmHalfMax, v);
             }
+            static_cast<__half*>(p.out)[orow + t.col + 8 * rr] = __float2half_rn(v);
           }
         }
       }

@@ -55,16 +55,18 @@ def _dequantised_bits(w):
     return bits
 
 
-# Layers with at most 16 token rows per expert on average take the warp-level
-# small-M kernels; the others the tcgen05 tile kernels.
+# Layers with at most 16 token rows per expert on average (and d, I multiples
+# of 256) take the warp-level small-M kernels; the others the tcgen05 tile
+# kernels.
 FORWARD_CASES = [
     # T, d, E, k, I, I_shared, zipf
-    (64, 512, 32, 8, 256, 0, False),     # small-M: 16 rows per expert, some in two passes
-    (60, 768, 64, 8, 384, 128, True),    # small-M: bias (hot experts: several passes), shared expert
+    (64, 512, 32, 8, 256, 0, False),     # small-M: 16 rows per expert, two or three passes
+    (60, 768, 64, 8, 512, 128, True),    # small-M: bias (hot experts: several passes), shared expert
     (600, 512, 8, 4, 384, 0, False),     # ~300 rows per expert: three chunks, six slabs
     (200, 384, 16, 4, 128, 0, True),     # d = 384: the last down slab has one populated half
     (130, 768, 64, 8, 256, 128, True),   # bias and a (bf16) shared expert
-    (1, 256, 8, 2, 128, 0, False),       # one token
+    (1, 256, 8, 2, 128, 0, False),       # one token (I = 128: tile kernels)
+    (1, 256, 8, 2, 256, 0, False),       # one token, small-M
 ]
 
 
