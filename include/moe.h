@@ -252,8 +252,11 @@ moe_status_t moe_mxfp8_quantize(const moe_bf16* w, long long rows, int K, uint8_
  * expert (ext) and outputs are as in moe_forward_ex; the experts compute
  * with the dequantised weights (codes x 2^(scale - 127), exact in bf16) on
  * the bf16 tensor cores, half the weight bytes read from HBM.  d and I must
- * be multiples of 128 (else MOE_ERR_UNSUPPORTED); one CTA per tile of 128
- * weight rows and at most 128 tokens.  Same workspace as moe_forward. */
+ * be multiples of 128 (else MOE_ERR_UNSUPPORTED).  Layers with at most 8
+ * token rows per expert on average (decode) and d, I multiples of 256 run
+ * warp-level kernels that decode the codes in registers next to their MMAs;
+ * the others one CTA per tile of 128 weight rows and at most 128 tokens.
+ * Same workspace as moe_forward. */
 moe_status_t moe_forward_mxfp8(const moe_bf16* x, const moe_bf16* w_router,
                                const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
                                const uint8_t* codes_down, const uint8_t* scales_down, int T,
@@ -282,7 +285,9 @@ moe_status_t moe_nvfp4_quantize(const moe_bf16* w, int groups, long long rows_pe
  * compute with E2M1 value x block scale (exact in bf16) on the bf16 tensor
  * cores and apply each expert's tensor scale to the fp32 accumulators; the
  * rest is moe_forward_ex.  d and I must be multiples of 256 (else
- * MOE_ERR_UNSUPPORTED).  Same workspace as moe_forward. */
+ * MOE_ERR_UNSUPPORTED).  Layers with at most 8 token rows per expert on
+ * average (decode) run warp-level kernels that decode the codes in registers
+ * next to their MMAs.  Same workspace as moe_forward. */
 moe_status_t moe_forward_nvfp4(const moe_bf16* x, const moe_bf16* w_router,
                                const uint8_t* codes_gate_up, const uint8_t* scales_gate_up,
                                const float* tscale_gate_up, const uint8_t* codes_down,

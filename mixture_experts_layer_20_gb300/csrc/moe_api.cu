@@ -19,8 +19,13 @@ namespace {
 
 constexpr size_t kAlign = 256;
 // Quantised expert weights: the warp-level small-M kernels serve layers with
-// at most this many token rows per expert on average (decode batches).
-constexpr long long kSmallMRowsPerExpert = 16;
+// at most this many token rows per expert on average (decode batches).  They
+// take 8 tokens per pass over an expert's weights, so an expert with more rows
+// reads its weights again; measured at 16 rows per expert, the second pass
+// came from DRAM (the other warps' streams evict it from L2).
+constexpr long long kSmallMRowsPerExpert = 8;
+// single_launch: decode-sized layers, at most this many rows per expert on average.
+constexpr long long kSingleLaunchRowsPerExpert = 16;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 std::atomic<unsigned long long> g_launches{0};
@@ -97,7 +102,7 @@ Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
   // decode-sized layers may run as one launch, whose router keeps partial
   // sums over 128-wide ranges of d (four times the 512-wide ones)
   const bool decode_sized = d % 128 == 0 && n <= static_cast<size_t>(kPermuteSmallMax) &&
-                            n <= static_cast<size_t>(kSmallMRowsPerExpert) * E;
+                            n <= static_cast<size_t>(kSingleLaunchRowsPerExpert) * E;
   L.logits = take(decode_sized ? std::max(router_partial_bytes(T, d, E), fused_partial_bytes(T, d, E))
                                : router_partial_bytes(T, d, E));
   L.ids = take(n * 4);
@@ -367,7 +372,7 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "moe_forward: workspace too small");
   if (single && (mx || I_shared || d % 128 || I % 128 ||
                  static_cast<long long>(T) * top_k > kPermuteSmallMax ||
-                 static_cast<long long>(T) * top_k > kSmallMRowsPerExpert * E))
+                 static_cast<long long>(T) * top_k > kSingleLaunchRowsPerExpert * E))
     return fail(MOE_ERR_UNSUPPORTED,
                 "single_launch needs bf16 expert weights, no shared expert, d and I multiples of "
                 "128, T*top_k <= 4096 and at most 16 rows per expert on average");

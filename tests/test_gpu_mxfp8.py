@@ -55,12 +55,13 @@ def _dequantised_bits(w):
     return bits
 
 
-# Layers with at most 16 token rows per expert on average (and d, I multiples
+# Layers with at most 8 token rows per expert on average (and d, I multiples
 # of 256) take the warp-level small-M kernels; the others the tcgen05 tile
 # kernels.
 FORWARD_CASES = [
     # T, d, E, k, I, I_shared, zipf
-    (64, 512, 32, 8, 256, 0, False),     # small-M: 16 rows per expert, two or three passes
+    (64, 512, 32, 8, 256, 0, False),     # 16 rows per expert: tile kernels, 16-row chunks
+    (32, 512, 32, 8, 256, 0, False),     # small-M: 8 rows per expert, some in two passes
     (60, 768, 64, 8, 512, 128, True),    # small-M: bias (hot experts: several passes), shared expert
     (600, 512, 8, 4, 384, 0, False),     # ~300 rows per expert: three chunks, six slabs
     (200, 384, 16, 4, 128, 0, True),     # d = 384: the last down slab has one populated half
@@ -97,7 +98,7 @@ def test_forward_mxfp8(moe, T, d, E, k, I, Is, zipf):
     assert_layer_close(f64(out), ref["out"], "out")
 
 
-@pytest.mark.parametrize("T", [96, 32])  # tile kernels; small-M kernels (8 rows per expert)
+@pytest.mark.parametrize("T", [96, 32])  # tile kernels (24 rows per expert); small-M (8)
 def test_forward_mxfp8_extreme_codes(moe, T):
     """Subnormal E4M3 codes (tiny weights inside a block) and scales above
     2^7 (the converter's general path) still match the oracle."""

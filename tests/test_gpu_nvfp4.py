@@ -73,12 +73,13 @@ def test_quantize_all_zero_matrix(moe):
     assert np.array_equal(tsc.cpu().numpy(), rt)
 
 
-# Layers with at most 16 token rows per expert on average take the warp-level
+# Layers with at most 8 token rows per expert on average take the warp-level
 # small-M kernels; the others the tcgen05 tile kernels.
 FORWARD_CASES = [
     # T, d, E, k, I, I_shared, zipf
-    (64, 512, 32, 8, 256, 0, False),     # small-M: 16 rows per expert, some in two passes
-    (40, 1024, 32, 8, 512, 256, True),   # small-M: bias (hot experts: several passes), shared expert
+    (64, 512, 32, 8, 256, 0, False),     # 16 rows per expert: tile kernels, 16-row chunks
+    (32, 512, 32, 8, 256, 0, False),     # small-M: 8 rows per expert, some in two passes
+    (32, 1024, 32, 8, 512, 256, True),   # small-M: bias (hot experts: several passes), shared expert
     (600, 512, 8, 4, 512, 0, False),     # ~300 rows per expert: three chunks
     (200, 768, 16, 4, 256, 0, True),     # d = 768: three 128-row down slabs
     (130, 1024, 32, 8, 256, 256, True),  # bias and a (bf16) shared expert
