@@ -67,21 +67,27 @@ __device__ __forceinline__ void e4m3x4_to_bf16_scaled(uint32_t w, float scale, u
   }
 }
 
-// 4 E2M1 codes (the low 16 bits of m_lo / signs from w's bits 3, 7, 11, 15)
-// as two bf16x2 of code value x scale.  The codes' 3-bit magnitudes index
-// byte tables of the bf16 patterns of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with prmt
-// (high bytes 00 3F 3F 3F 40 40 40 40, low bytes 00 00 80 C0 00 40 80 C0),
-// two more prmt interleave them into bf16 halves, the signs are or-ed in,
-// and one exact bf16x2 multiply applies the block scale.
+// 4 E2M1 codes (the low 16 bits of w, code i in bits 4i .. 4i + 3) as two
+// bf16x2 of code value x scale.  The codes' 3-bit magnitudes index byte
+// tables of the bf16 patterns of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with prmt (high
+// bytes 00 3F 3F 3F 40 40 40 40, low bytes 00 00 80 C0 00 40 80 C0), two more
+// prmt interleave them into bf16 halves, and one exact bf16x2 multiply
+// applies the block scale.  Signs: code 2i + 1's sign bit is bit 7 of byte i
+// of w and code 2i's is bit 7 of byte i of w << 4, so one sign-replicating
+// byte select per pair (selector nibbles 8 | byte) lays them over bits 15
+// and 31, and one masked or merges them.
 __device__ __forceinline__ void e2m1x4_to_bf16(uint32_t w, __nv_bfloat162 mul, uint32_t* out) {
   const uint32_t sel = w & 0x7777u;
-  uint32_t hi, lo, a, b;
+  uint32_t hi, lo, a, b, sa, sb;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x3F3F3F00u), "r"(0x40404040u), "r"(sel));
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0xC0800000u), "r"(0xC0804000u), "r"(sel));
   asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(lo), "r"(hi));  // values 0, 1
   asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(lo), "r"(hi));  // values 2, 3
-  a |= ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
-  b |= ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
+  const uint32_t w4 = w << 4;
+  asm("prmt.b32 %0, %1, %2, 0xC080;" : "=r"(sa) : "r"(w4), "r"(w));  // signs of codes 0, 1
+  asm("prmt.b32 %0, %1, %2, 0xD090;" : "=r"(sb) : "r"(w4), "r"(w));  // signs of codes 2, 3
+  a |= sa & 0x80008000u;
+  b |= sb & 0x80008000u;
   const __nv_bfloat162 pa = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), mul);
   const __nv_bfloat162 pb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), mul);
   out[0] = *reinterpret_cast<const uint32_t*>(&pa);

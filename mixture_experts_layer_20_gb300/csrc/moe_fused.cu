@@ -2,28 +2,33 @@
 //
 // 'Hosting Qwen on Blackwell', "Expert parallelism": for decode the dispatch,
 // the expert GEMMs and the combine run as one kernel, while prefill splits
-// them.  Here one persistent cooperative launch (every CTA resident at once)
-// runs the layer's steps as phases separated by grid-wide barriers:
+// them.  Here one persistent cooperative launch of CTA pairs (2-CTA clusters,
+// every CTA resident at once, one per SM) runs the layer's steps as phases
+// separated by grid-wide barriers:
 //
 //   1. router logits: fp32 partial sums of x W_r^T over 128-wide ranges of d,
 //      warp-level tensor-core MMAs (16 experts x 8 tokens per MMA tile);
 //   2. top-k and gates: one warp per token adds the ranges in range order
 //      (the same warp code as the standalone router);
 //   3. grouping: counts, offsets and the stable permutation, by one CTA;
-//   4. gate_up with the SwiGLU epilogue and 5. down: the small-M grouped
-//      GEMMs (warp-level MMAs, weights streamed through per-warp cp.async
-//      rings), token rows taken from x through the permutation;
+//   4. gate_up with the SwiGLU epilogue and 5. down: the bf16 expert GEMM body
+//      of the grouped kernels (2-SM tcgen05 MMAs, weights on M, TMA rings,
+//      accumulators in tensor memory), gate_up gathering its token rows from
+//      x through the permutation;
 //   6. combine: fp32 sum of each token's k rows in slot order, one bf16
 //      rounding.
 //
-// A grid-wide barrier is an arrival counter and a generation word in the
-// workspace's status region; thread 0 of each CTA arrives and waits for the
-// generation to move, bounded by %globaltimer.  A wait that runs out records
-// MOE_ERR_TIMEOUT and its CTA skips the rest of the layer (the others then
-// run out too), so a missing CTA cannot hang the GPU.  The last CTA to leave
-// resets the counters, so the next launch starts clean even after a timeout.
-// Data one phase writes and a later phase reads goes through L2 (ld_in with
-// COHERENT = true).
+// The pair's 512 tensor-memory columns are allocated once for both GEMM
+// phases.  A grid-wide barrier is an arrival counter and a generation word in
+// the workspace's status region; thread 0 of each CTA arrives and waits for
+// the generation to move, bounded by %globaltimer.  A wait that runs out
+// records MOE_ERR_TIMEOUT and the CTA carries on (the results are then not to
+// be used): every CTA runs every phase, so the cluster barriers inside the
+// GEMM phases always meet their peer, and since every wait is bounded the
+// kernel always ends.  The last CTA to leave resets the arrival counter for
+// the next launch.  Data one phase writes and a later phase reads with
+// ordinary loads goes through L2 (ld_in with COHERENT = true); h, which the
+// down phase's TMA reads, is ordered by proxy fences on both sides.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -32,17 +37,24 @@
 #include <mutex>
 
 #include "moe_device.cuh"
+#include "moe_expert_gemm.cuh"
 #include "moe_internal.h"
 #include "moe_permute.cuh"
 #include "moe_router.cuh"
-#include "moe_smallm.cuh"
+#include "moe_smallm.cuh"  // mma_16816, word_of
 
 namespace moe {
 namespace {
 
-constexpr int kRouterRange = 128;  // the router's partial sums: 128-wide ranges of d
+constexpr int kRouterRange = 128;         // the router's partial sums: 128-wide ranges of d
+constexpr int kFuWarps = kThreads / 32;   // warps per CTA (the GEMM body's six roles)
 
 struct FusedParams {
+  CUtensorMap mw_gu;              // W_gate_up, interleaved 5-D map
+  CUtensorMap mw_dn;              // W_down as [E d, I]
+  TokenMapSet tx_gu;              // gate_up token rows: one-row boxes over x (gathered)
+  TokenMapSet tx_dn;              // down token rows: boxes over h
+  Params gu, dn;                  // the two GEMM phases
   const __nv_bfloat16* x;         // [T, d]
   const __nv_bfloat16* w_router;  // [E, d]
   const float* bias;              // [E] or null
@@ -52,8 +64,7 @@ struct FusedParams {
   int npad;
   int32_t *ids, *counts, *offsets, *perm, *slot_pos;
   float* gates;
-  SmParams gu, dn;                // the two grouped GEMMs
-  const __half* y;                // [T k, d] (dn.out)
+  const __half* y;                // [T k, d]
   __nv_bfloat16* out;             // [T, d]
   unsigned* status;
   unsigned* bar_count;            // arrivals at the current barrier
@@ -68,13 +79,11 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
-// Grid-wide barrier (every thread of every CTA).  Returns false when the wait
-// ran out; the caller then skips the rest of the layer.
-__device__ __forceinline__ bool grid_sync(const FusedParams& p) {
-  __shared__ int s_ok;
+// Grid-wide barrier (every thread of every CTA).  A wait that runs out sets
+// MOE_ERR_TIMEOUT; the CTA then goes on (see the file comment).
+__device__ __forceinline__ void grid_sync(const FusedParams& p) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    int ok = 1;
     const unsigned gen = ld_acquire_gpu(p.bar_gen);
     __threadfence();  // this CTA's writes before its arrival
     if (atomicAdd(p.bar_count, 1u) == gridDim.x - 1) {
@@ -86,16 +95,13 @@ __device__ __forceinline__ bool grid_sync(const FusedParams& p) {
       while (ld_acquire_gpu(p.bar_gen) == gen) {
         if (globaltimer_ns() - t0 > p.timeout_ns) {
           atomicOr(p.status, kStatusTimeout);
-          ok = 0;
           break;
         }
       }
     }
     __threadfence();
-    s_ok = ok;
   }
   __syncthreads();
-  return s_ok != 0;
 }
 
 // Phase 1: partial[r][t][e] = sum over the 128 values of range r of
@@ -109,8 +115,8 @@ __device__ __forceinline__ void router_partials(const FusedParams& p) {
   const int ranges = p.d / kRouterRange;
   const int passes = (p.T + 15) / 16;
   const int total = groups * ranges * passes;
-  const int W = gridDim.x * kSmWarps;
-  for (int tau = blockIdx.x * kSmWarps + (threadIdx.x >> 5); tau < total; tau += W) {
+  const int W = gridDim.x * kFuWarps;
+  for (int tau = blockIdx.x * kFuWarps + (threadIdx.x >> 5); tau < total; tau += W) {
     const int rg = tau % groups;
     const int rest = tau / groups;
     const int r = rest % ranges;
@@ -158,56 +164,67 @@ __device__ __forceinline__ void router_partials(const FusedParams& p) {
   }
 }
 
-__global__ void __launch_bounds__(kSmThreads, 2) moe_decode_fused_kernel(const FusedParams p) {
-  extern __shared__ __align__(16) uint8_t sm_raw[];
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    moe_decode_fused_kernel(const __grid_constant__ FusedParams p) {
+  __shared__ uint32_t s_tmem;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // the pair's tensor memory, for both GEMM phases
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&s_tmem), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
   router_partials(p);
-  bool alive = grid_sync(p);
+  grid_sync(p);
 
-  if (alive) {
-    const int splits = p.d / kRouterRange;
-    for (int t = blockIdx.x * kSmWarps + warp; t < p.T; t += gridDim.x * kSmWarps) {
-      if (p.E <= 64)
-        topk_warp<2, true>(p.partial, splits, p.T, p.npad, p.E, p.k, p.bias, p.sel_only, t, lane,
-                           p.ids, p.gates);
-      else if (p.E <= 128)
-        topk_warp<4, true>(p.partial, splits, p.T, p.npad, p.E, p.k, p.bias, p.sel_only, t, lane,
-                           p.ids, p.gates);
-      else
-        topk_warp<8, true>(p.partial, splits, p.T, p.npad, p.E, p.k, p.bias, p.sel_only, t, lane,
-                           p.ids, p.gates);
-    }
-    alive = grid_sync(p);
+  const int splits = p.d / kRouterRange;
+  for (int t = blockIdx.x * kFuWarps + warp; t < p.T; t += gridDim.x * kFuWarps) {
+    if (p.E <= 64)
+      topk_warp<2, true>(p.partial, splits, p.T, p.npad, p.E, p.k, p.bias, p.sel_only, t, lane,
+                         p.ids, p.gates);
+    else if (p.E <= 128)
+      topk_warp<4, true>(p.partial, splits, p.T, p.npad, p.E, p.k, p.bias, p.sel_only, t, lane,
+                         p.ids, p.gates);
+    else
+      topk_warp<8, true>(p.partial, splits, p.T, p.npad, p.E, p.k, p.bias, p.sel_only, t, lane,
+                         p.ids, p.gates);
   }
-  if (alive) {
-    if (blockIdx.x == 0)
-      permute_small_block<kSmWarps, true>(p.ids, p.T * p.k, p.E, p.counts, p.offsets, p.perm,
-                                          p.slot_pos, p.status);
-    alive = grid_sync(p);
-  }
-  if (alive) {
-    sm_phase<kSmBf16, kSmGateUp, true>(p.gu, sm_raw);
-    alive = grid_sync(p);
-  }
-  if (alive) {
-    sm_phase<kSmBf16, kSmDown, true>(p.dn, sm_raw);
-    alive = grid_sync(p);
-  }
-  if (alive) {
-    const int cpr = p.d / 8;  // 8-column groups per token
-    const int n = p.T * cpr;
-    for (int i = blockIdx.x * kSmThreads + threadIdx.x; i < n; i += gridDim.x * kSmThreads) {
-      const int t = i / cpr;
-      combine_cols<true>(p.y, p.slot_pos, p.gates, nullptr, p.d, p.k, p.T * p.k, t,
-                         (i - t * cpr) * 8, p.out, p.status);
-    }
+  grid_sync(p);
+
+  if (blockIdx.x == 0)
+    permute_small_block<kFuWarps, true>(p.ids, p.T * p.k, p.E, p.counts, p.offsets, p.perm,
+                                        p.slot_pos, p.status);
+  grid_sync(p);
+
+  expert_gemm_body<kGateUp, true>(p.mw_gu, p.tx_gu, p.gu, tmem);
+  grid_sync(p);
+  expert_gemm_body<kDown, true>(p.mw_dn, p.tx_dn, p.dn, tmem);
+  grid_sync(p);
+
+  const int cpr = p.d / 8;  // 8-column groups per token
+  const int n = p.T * cpr;
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < n; i += gridDim.x * kThreads) {
+    const int t = i / cpr;
+    combine_cols<true>(p.y, p.slot_pos, p.gates, nullptr, p.d, p.k, p.T * p.k, t,
+                       (i - t * cpr) * 8, p.out, p.status);
   }
 
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
   // The last CTA to leave resets the arrival counter (after a timeout it may
   // hold stale arrivals) for the next launch.
-  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(p.exit_count, 1u) == gridDim.x - 1) {
@@ -218,24 +235,45 @@ __global__ void __launch_bounds__(kSmThreads, 2) moe_decode_fused_kernel(const F
   }
 }
 
-// CTAs per SM that can be resident with the kernel's shared memory (0 on error).
-int fused_blocks_per_sm() {
+// Dynamic shared memory (all a block may use beside the kernel's static
+// shared memory) and the number of co-resident CTA pairs; 0 on error.
+struct FusedLaunchShape {
+  int smem, pairs;
+};
+
+FusedLaunchShape fused_launch_shape() {
   static std::once_flag once[64];
-  static int blocks[64];
+  static FusedLaunchShape shape[64];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return {0, 0};
   std::call_once(once[dev], [&] {
-    constexpr int smem = sm_smem_bytes<kSmBf16>();
-    int n = 0;
-    if (cudaFuncSetAttribute(moe_decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe_decode_fused_kernel, kSmThreads,
-                                                      smem) == cudaSuccess)
-      blocks[dev] = std::min(n, 2);
-    else
+    int optin = 0;
+    cudaFuncAttributes fa{};
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaFuncGetAttributes(&fa, moe_decode_fused_kernel) != cudaSuccess) {
       cudaGetLastError();
+      return;
+    }
+    const int smem = optin - static_cast<int>(fa.sharedSizeBytes);
+    if (cudaFuncSetAttribute(moe_decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, moe_decode_fused_kernel, &cfg) != cudaSuccess ||
+        n <= 0) {
+      cudaGetLastError();
+      return;
+    }
+    shape[dev] = {smem, std::min(n, device_sm_count() / 2)};
   });
-  return blocks[dev];
+  return shape[dev];
 }
 
 }  // namespace
@@ -248,10 +286,47 @@ cudaError_t launch_decode_fused(cudaStream_t s, const FusedLayer& L) {
   if (L.d % kRouterRange || L.I % kRouterRange || L.E > kMaxExperts || L.k > kMaxTopK ||
       L.T * L.k > kPermuteSmallMax)
     return cudaErrorInvalidValue;
-  const int per_sm = fused_blocks_per_sm();
-  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+  const FusedLaunchShape shape = fused_launch_shape();
+  if (shape.pairs <= 0) return cudaErrorInvalidConfiguration;
   const int rows = L.T * L.k;
   FusedParams p{};
+  // gate_up: interleaved weight map, token rows gathered from x through perm
+  cudaError_t e = make_gate_up_weight_map(&p.mw_gu, L.w_gate_up, L.d, L.I, L.E);
+  const TokenGather gather{L.x, L.perm, L.k, L.T};
+  if (e == cudaSuccess) e = make_gate_up_token_maps(p.tx_gu, p.gu, L.x, rows, L.d, &gather);
+  // down: W_down as [E d, I] in 128-row boxes, token rows = h
+  if (e == cudaSuccess)
+    e = make_bf16_map(&p.mw_dn, L.w_down, static_cast<uint64_t>(L.E) * L.d, L.I, 128);
+  if (e == cudaSuccess) e = make_token_maps(p.tx_dn, L.h, rows, L.I);
+  if (e != cudaSuccess) return e;
+  Params& gu = p.gu;
+  gu.K = L.d;
+  gu.n_out = L.I;
+  gu.slabs = (L.I + 127) / 128;
+  gu.groups = L.E;
+  gu.offsets = L.offsets;
+  gu.total_rows = rows;
+  gu.w_rows_per_group = 2 * L.I;
+  gu.up_offset = L.I;
+  gu.out = L.h;
+  gu.ld_out = L.I;
+  gu.smem_bytes = shape.smem;
+  gu.status = L.status;
+  gu.timeout_ns = L.timeout_ns;
+  Params& dn = p.dn;
+  dn.K = L.I;
+  dn.n_out = L.d;
+  dn.slabs = (L.d + 255) / 256;
+  dn.groups = L.E;
+  dn.offsets = L.offsets;
+  dn.total_rows = rows;
+  dn.w_rows_per_group = L.d;
+  dn.up_offset = 0;
+  dn.out = L.y;
+  dn.ld_out = L.d;
+  dn.smem_bytes = shape.smem;
+  dn.status = L.status;
+  dn.timeout_ns = L.timeout_ns;
   p.x = static_cast<const __nv_bfloat16*>(L.x);
   p.w_router = static_cast<const __nv_bfloat16*>(L.w_router);
   p.bias = L.bias;
@@ -268,37 +343,6 @@ cudaError_t launch_decode_fused(cudaStream_t s, const FusedLayer& L) {
   p.offsets = L.offsets;
   p.perm = L.perm;
   p.slot_pos = L.slot_pos;
-  SmParams& gu = p.gu;
-  gu.w = static_cast<const uint8_t*>(L.w_gate_up);
-  gu.row_bytes = static_cast<long long>(L.d) * 2;
-  gu.K = L.d;
-  gu.n_out = L.I;
-  gu.w_rows_per_expert = 2 * L.I;
-  gu.up_offset = L.I;
-  gu.E = L.E;
-  gu.offsets = L.offsets;
-  gu.total_rows = rows;
-  gu.b = p.x;
-  gu.b_rows = L.T;
-  gu.perm = L.perm;
-  gu.div = L.k;
-  gu.out = L.h;
-  gu.ld_out = L.I;
-  gu.status = L.status;
-  SmParams& dn = p.dn;
-  dn = gu;
-  dn.w = static_cast<const uint8_t*>(L.w_down);
-  dn.row_bytes = static_cast<long long>(L.I) * 2;
-  dn.K = L.I;
-  dn.n_out = L.d;
-  dn.w_rows_per_expert = L.d;
-  dn.up_offset = 0;
-  dn.b = static_cast<const __nv_bfloat16*>(L.h);
-  dn.b_rows = rows;
-  dn.perm = nullptr;
-  dn.div = 1;
-  dn.out = L.y;
-  dn.ld_out = L.d;
   p.y = static_cast<const __half*>(L.y);
   p.out = static_cast<__nv_bfloat16*>(L.out);
   p.status = L.status;
@@ -308,9 +352,9 @@ cudaError_t launch_decode_fused(cudaStream_t s, const FusedLayer& L) {
   p.timeout_ns = L.timeout_ns;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(per_sm * device_sm_count());
-  cfg.blockDim = dim3(kSmThreads);
-  cfg.dynamicSmemBytes = sm_smem_bytes<kSmBf16>();
+  cfg.gridDim = dim3(2 * shape.pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = shape.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -167,10 +167,10 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
                                      unsigned long long timeout_ns);
 
 // Grouped SwiGLU FFN for few token rows per expert (decode): warp-level
-// tensor-core MMAs, weights decoded in registers (moe_smallm.cu).  fmt 0:
-// bf16 weights, 1: MXFP8, 2: NVFP4 (scales and tensor scales as for
-// launch_grouped_ffn_quant).  Gate_up's token rows are a[perm[pos] / div]
-// (perm != nullptr) or a[pos]; d and I multiples of 128 (bf16) or 256.
+// tensor-core MMAs, weights decoded in registers (moe_smallm.cu).  fmt 1:
+// MXFP8, 2: NVFP4 (scales and tensor scales as for launch_grouped_ffn_quant).
+// Gate_up's token rows are a[perm[pos] / div] (perm != nullptr) or a[pos];
+// d and I multiples of 256.
 // Writes h [rows, I] bf16 and y [rows, d] fp16.
 cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
                                       const int32_t* perm, int div, const int32_t* offsets,

@@ -71,13 +71,28 @@ __device__ __forceinline__ void permute_small_block(const int32_t* ids, int n, i
     s_scan[e] = total;
   }
   __syncthreads();
-  for (int o = 1; o < kMaxExperts; o <<= 1) {
-    int v = 0;
-    if (threadIdx.x < kMaxExperts && threadIdx.x >= o) v = s_scan[threadIdx.x - o];
-    __syncthreads();
-    if (threadIdx.x < kMaxExperts) s_scan[threadIdx.x] += v;
-    __syncthreads();
+  // inclusive scan over the 256 entries by warp 0 (any block size): lane l
+  // takes entries 8 l .. 8 l + 7, then a warp scan of the lanes' sums
+  if (w == 0) {
+    constexpr int kPer = kMaxExperts / 32;
+    int v[kPer];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      sum += s_scan[lane * kPer + i];
+      v[i] = sum;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int before = incl - sum;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) s_scan[lane * kPer + i] = before + v[i];
   }
+  __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = e > 0 ? s_scan[e - 1] : 0;
     offsets[e] = run;

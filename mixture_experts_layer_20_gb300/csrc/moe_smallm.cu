@@ -1,5 +1,5 @@
 // Small-M expert GEMMs: the grouped SwiGLU FFN when experts receive few token
-// rows (decode batches), for bf16, MXFP8 and NVFP4 expert weights.
+// rows (decode batches), for MXFP8 and NVFP4 expert weights.
 //
 // At decode every active expert sees a handful of tokens, so the layer is
 // bound by streaming the expert weights from HBM ('Hosting Qwen on
@@ -19,11 +19,11 @@
 //   down    : 16 consecutive rows of W_down (16 y columns); y stored in fp16
 //             with the same range rule as the large-M kernels.
 //
-// The reduction is consumed in chunks of 128 values.  Lane (g, t) of a warp
+// The reduction is consumed in chunks of 256 values.  Lane (g, t) of a warp
 // (g = lane / 4, t = lane % 4) loads 16-byte units of its rows g and g + 8 at
 // byte offsets 64 i + 16 t of the row's chunk, so four lanes read 64
-// contiguous bytes of a row per instruction.  A unit holds V values (8 bf16,
-// 16 E4M3 or 32 E2M1 codes) at reduction indices V (4 i + t) + [0, V), and
+// contiguous bytes of a row per instruction.  A unit holds V values (16 E4M3
+// or 32 E2M1 codes) at reduction indices V (4 i + t) + [0, V), and
 // the MMA whose fragment k-positions {2t, 2t+1, 2t+8, 2t+9} stand for
 // indices V (4 i + t) + 4 j + {0, 1, 2, 3} takes the same indices of the
 // tokens: a fixed permutation of the reduction, applied to both operands,
@@ -137,10 +137,6 @@ cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
   const uint8_t* wg = static_cast<const uint8_t*>(w_gate_up);
   const uint8_t* wd = static_cast<const uint8_t*>(w_down);
   switch (fmt) {
-    case 0:
-      return sm_ffn<kSmBf16>(s, "moe_gate_up_swiglu_smallm", "moe_down_smallm", a, perm, div,
-                             offsets, rows, d, E, I, wg, nullptr, nullptr, wd, nullptr, nullptr,
-                             h, y, status);
     case 1:
       return sm_ffn<kSmMx8>(s, "moe_gate_up_swiglu_mxfp8_smallm", "moe_down_mxfp8_smallm", a,
                             perm, div, offsets, rows, d, E, I, wg, scales_gate_up, nullptr, wd,

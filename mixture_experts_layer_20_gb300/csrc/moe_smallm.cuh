@@ -1,7 +1,7 @@
 // Warp-level small-M expert GEMM (mma.sync m16n8k16) for the decode case of
-// the grouped SwiGLU FFN: the device code shared by the standalone small-M
-// kernels (moe_smallm.cu) and the single-launch decode kernel.  The design is
-// described at the top of moe_smallm.cu.
+// the grouped SwiGLU FFN with quantised expert weights (moe_smallm.cu, where
+// the design is described); mma_16816 and word_of also serve the router
+// phase of the single-launch layer.
 #pragma once
 
 #include <cstdint>
@@ -14,7 +14,7 @@
 
 namespace moe {
 
-enum SmFmt : int { kSmBf16 = 0, kSmMx8 = 1, kSmNv4 = 2 };
+enum SmFmt : int { kSmMx8 = 1, kSmNv4 = 2 };
 enum SmKind : int { kSmGateUp = 1, kSmDown = 2 };
 
 constexpr int kSmWarps = 8;               // warps per CTA
@@ -26,13 +26,9 @@ constexpr float kSmHalfMax = 65504.0f;
 // row per chunk, so a chunk covers KC = 4 V U values of the reduction; NS
 // ring stages; SB block-scale bytes per weight row per chunk (0: none).
 template <int FMT> struct SmF;
-template <> struct SmF<kSmBf16> {
-  static constexpr int V = 8, U = 4, NS = 3, SB = 0;
-  static constexpr int kBytesX2 = 4;  // twice the bytes per value
-};
 template <> struct SmF<kSmMx8> {
   static constexpr int V = 16, U = 4, NS = 3, SB = 8;
-  static constexpr int kBytesX2 = 2;
+  static constexpr int kBytesX2 = 2;  // twice the bytes per value
 };
 template <> struct SmF<kSmNv4> {
   static constexpr int V = 32, U = 2, NS = 4, SB = 16;
@@ -57,7 +53,7 @@ __host__ __device__ constexpr int sm_smem_bytes() {
 }
 
 struct SmParams {
-  const uint8_t* w;          // weight rows (bf16 values or codes), row_bytes each
+  const uint8_t* w;          // weight rows (codes), row_bytes each
   const uint8_t* scales;     // MXFP8 [K/128][scale_rows][4], NVFP4 [K/256][scale_rows][16]
   const float* tscale;       // NVFP4: one scale per expert (null: none)
   long long scale_rows;      // weight rows of the whole tensor
@@ -155,11 +151,9 @@ __device__ __forceinline__ SmTask sm_task(const SmParams& p, const int* s_act, c
   if constexpr (FMT == kSmMx8) {
     t.s0 = p.scales + r0 * 4;
     t.s1 = p.scales + r1 * 4;
-  } else if constexpr (FMT == kSmNv4) {
+  } else {
     t.s0 = p.scales + r0 * 16;
     t.s1 = p.scales + r1 * 16;
-  } else {
-    t.s0 = t.s1 = nullptr;
   }
   return t;
 }
@@ -187,7 +181,7 @@ __device__ __forceinline__ void sm_fetch(const SmParams& p, const SmTask& t, int
     cp_async_4(s + 4, t.s0 + st2);
     cp_async_4(s + 8, t.s1 + st);
     cp_async_4(s + 12, t.s1 + st2);
-  } else if constexpr (FMT == kSmNv4) {
+  } else {
     const long long st = static_cast<long long>(c) * p.scale_rows * 16;  // one stage per chunk
     cp_async_16(s, t.s0 + st);
     cp_async_16(s + 16, t.s1 + st);
@@ -310,8 +304,7 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
         st += sm_stage_bytes<FMT>();
         if (st == ring + F::NS * sm_stage_bytes<FMT>()) st = ring;
         const uint32_t sslot = cur + 2 * F::U * 32 * 16 + lane * sm_scale_slot<FMT>();
-        uint4 sc = make_uint4(0u, 0u, 0u, 0u);
-        if constexpr (F::SB > 0) sc = lds128(sslot);
+        const uint4 sc = lds128(sslot);
         uint4 sc2 = make_uint4(0u, 0u, 0u, 0u);
         if constexpr (FMT == kSmNv4) sc2 = lds128(sslot + 16);
         // MXFP8: a scale byte above 134 (weights beyond 2^7 in a block) needs
@@ -344,12 +337,7 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
 #pragma unroll
             for (int j = 0; j < F::V / 4; ++j) {
               uint32_t a[2][2];  // [row g / g + 8][values 4j, 4j+1 | 4j+2, 4j+3]
-              if constexpr (FMT == kSmBf16) {
-                a[0][0] = word_of(a0, 2 * j);
-                a[0][1] = word_of(a0, 2 * j + 1);
-                a[1][0] = word_of(a1, 2 * j);
-                a[1][1] = word_of(a1, 2 * j + 1);
-              } else if constexpr (FMT == kSmMx8) {
+              if constexpr (FMT == kSmMx8) {
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                   const uint32_t codes = word_of(rr ? a1 : a0, j);
