@@ -170,6 +170,9 @@ def source_sha(files):
 GEMM_SOURCES = ["mixture_experts_layer_20_gb300/csrc/moe_gemm.cu",
                 "mixture_experts_layer_20_gb300/csrc/moe_expert_gemm.cu",
                 "mixture_experts_layer_20_gb300/csrc/moe_expert_gemm.cuh",
+                "mixture_experts_layer_20_gb300/csrc/moe_smallm.cu",
+                "mixture_experts_layer_20_gb300/csrc/moe_smallm.cuh",
+                "mixture_experts_layer_20_gb300/csrc/moe_convert.cuh",
                 "mixture_experts_layer_20_gb300/csrc/moe_device.cuh"]
 
 
