@@ -41,3 +41,19 @@ def test_untouched_experts_are_not_counted():
     assert by_mx == int(64 * d * I * bench.MX_BYTES) + rows * I * 2 + rows * d * 2
     _, by_nv = bench.kernel_work("moe_down_nvfp4", w, counts)
     assert by_nv == int(64 * d * I * bench.NV_BYTES) + rows * I * 2 + rows * d * 2
+
+
+def test_small_m_and_single_launch_accounting():
+    """The small-M kernels do the tile kernels' work; the single-launch layer
+    counts the whole layer: every expert FLOP, the router and the combine,
+    and the layer's algorithmic bytes."""
+    w = W.WORKLOADS["qwen3_235b_decode_T64"]
+    T, d, E, k, I = w.T, w.d, w.E, w.top_k, w.I
+    counts = [T * k // 64] * 64 + [0] * 64
+    for fmt in ("mxfp8", "nvfp4"):
+        for kind in ("gate_up_swiglu", "down"):
+            assert bench.kernel_work(f"moe_{kind}_{fmt}_smallm", w, counts) == \
+                bench.kernel_work(f"moe_{kind}_{fmt}", w, counts)
+    fl, by = bench.kernel_work("moe_decode_fused", w, counts)
+    assert fl == counters.expert_flops(T, k, d, I) + counters.router_flops(T, d, E) + 2 * T * k * d
+    assert by == counters.algorithmic_bytes(counts, T, d, E, I)
