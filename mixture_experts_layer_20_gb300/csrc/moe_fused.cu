@@ -351,8 +351,13 @@ cudaError_t launch_decode_fused(cudaStream_t s, const FusedLayer& L) {
   p.exit_count = L.status + kExitCountWord;
   p.timeout_ns = L.timeout_ns;
 
+  // As many pairs as the larger GEMM phase has tiles at most (every expert
+  // active, one token chunk each): a small layer waits at its grid barriers
+  // for fewer CTAs.
+  const long long tiles = static_cast<long long>(L.E) * std::max(gu.slabs, dn.slabs);
+  const int pairs = static_cast<int>(std::max(1LL, std::min<long long>(shape.pairs, tiles)));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * shape.pairs);
+  cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = shape.smem;
   cfg.stream = s;
