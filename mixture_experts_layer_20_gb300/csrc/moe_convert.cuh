@@ -94,6 +94,50 @@ __device__ __forceinline__ void e2m1x4_to_bf16(uint32_t w, __nv_bfloat162 mul, u
   out[1] = *reinterpret_cast<const uint32_t*>(&pb);
 }
 
+// 8 E2M1 codes (a 32-bit word, code q in bits 4q .. 4q + 3) as four bf16x2
+// pairs, out[q] = (code q, code q + 4) x mul for q = 0..3: the two codes of a
+// pair lie 16 bits apart, so one shift places both.  A code's magnitude bits
+// e1 e0 m placed at bf16 bits 8..6 form the bf16 with exponent field e1 e0 and
+// mantissa m/2: 2^(e - 127) (1 + m/2) for e > 0 and 2^-126 m/2 (a subnormal)
+// for e = 0, i.e. the code's value times 2^-126; its sign goes to bit 15.
+// mul is the block scale times 2^118 (e4m3_scale_x2p118), so the products are
+// the weights times 2^-8, exact in bf16 (at most 6 significant bits, and
+// normal); the caller multiplies its fp32 sums by 2^8.  Ten integer-pipe
+// operations (masks, two right shifts), five left shifts that may run as
+// integer multiply-adds, and four bf16x2 multiplies per eight codes.
+__device__ __forceinline__ void e2m1x8_to_bf16_pairs(uint32_t x, __nv_bfloat162 mul,
+                                                     uint32_t* out) {
+  uint32_t r[4];
+  r[0] = ((x << 6) & 0x01C001C0u) | ((x << 12) & 0x80008000u);  // codes 0, 4
+  r[1] = ((x << 2) & 0x01C001C0u) | ((x << 8) & 0x80008000u);   // codes 1, 5
+  r[2] = ((x >> 2) & 0x01C001C0u) | ((x << 4) & 0x80008000u);   // codes 2, 6
+  r[3] = ((x >> 6) & 0x01C001C0u) | (x & 0x80008000u);          // codes 3, 7
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&r[q]), mul);
+    out[q] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
+// Byte b (0..3) of an E4M3 scale word as a bf16 pair of value x 2^118, for
+// e2m1x8_to_bf16_pairs.  sel = e4m3_scale_sel(b).  The byte, sign-extended
+// into both halves by one byte permute and shifted so that its seven
+// magnitude bits sit at bf16 bits 10..4, is the bf16 of value x 2^-120
+// (normal, or subnormal for a subnormal code; the trick of
+// e4m3x4_to_bf16_bits); two exact multiplies by 2^119 give value x 2^118,
+// finite for every finite E4M3 value (at most 448 x 2^118 < 2^127).
+__host__ __device__ constexpr uint32_t e4m3_scale_sel(uint32_t b) {
+  return b | ((b | 8u) << 4) | (b << 8) | ((b | 8u) << 12);
+}
+__device__ __forceinline__ __nv_bfloat162 e4m3_scale_x2p118(uint32_t word, uint32_t sel) {
+  uint32_t t;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(word), "r"(sel));
+  t = (t << 4) & 0x87F087F0u;
+  const uint32_t k2p119 = 0x7B007B00u;  // bf16 2^119 in both halves
+  const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&k2p119);
+  return __hmul2(__hmul2(*reinterpret_cast<const __nv_bfloat162*>(&t), c), c);
+}
+
 // An E4M3 block scale as a bf16 pair (exact: 4 significant bits).
 __device__ __forceinline__ __nv_bfloat162 e4m3_scale_bf16x2(uint32_t code) {
   const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);

@@ -23,11 +23,20 @@
 // (g = lane / 4, t = lane % 4) loads 16-byte units of its rows g and g + 8 at
 // byte offsets 64 i + 16 t of the row's chunk, so four lanes read 64
 // contiguous bytes of a row per instruction.  A unit holds V values (16 E4M3
-// or 32 E2M1 codes) at reduction indices V (4 i + t) + [0, V), and
-// the MMA whose fragment k-positions {2t, 2t+1, 2t+8, 2t+9} stand for
-// indices V (4 i + t) + 4 j + {0, 1, 2, 3} takes the same indices of the
-// tokens: a fixed permutation of the reduction, applied to both operands,
-// which leaves the sum unchanged.
+// or 32 E2M1 codes) at reduction indices V (4 i + t) + [0, V).  MXFP8: the
+// MMA whose fragment k-positions {2t, 2t+1, 2t+8, 2t+9} stand for indices
+// V (4 i + t) + 4 j + {0, 1, 2, 3} takes the same indices of the tokens.
+// NVFP4: the two MMAs of 32-bit word m of a unit stand for V (4 i + t) +
+// 8 m + {0, 4, 1, 5} and {2, 6, 3, 7}: codes 16 bits apart share a bf16 pair,
+// so one shift places both (e2m1x8_to_bf16_pairs), and one byte permute per
+// pair pairs the token values alike.  Either way a fixed permutation of the
+// reduction, applied to both operands, leaves the sum unchanged.
+//
+// Decoding E2M1 codes bounds the NVFP4 kernels (integer and bf16 multiply
+// pipes, not HBM): the codes' magnitude bits go straight into bf16 exponent
+// and mantissa fields (the weight times 2^-8 after the block-scale multiply;
+// the fp32 sums are multiplied by 2^8 with the tensor scale), so a code costs
+// about two instructions.
 //
 // Weights (and their block scales) reach shared memory through a per-warp
 // ring of cp.async copies several chunks ahead, across task boundaries; each

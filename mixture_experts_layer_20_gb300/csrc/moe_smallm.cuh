@@ -263,10 +263,18 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
 
   uint32_t st = ring;
   bool range_flag = false;
+  // NVFP4: byte selectors of this lane's two block scales in a scale word
+  const uint32_t ssel0 = e4m3_scale_sel(2u * (tig & 1));
+  const uint32_t ssel1 = e4m3_scale_sel(2u * (tig & 1) + 1u);
+  (void)ssel0;
+  (void)ssel1;
 #pragma unroll 1
   for (int tau = blockIdx.x * kSmWarps + warp; tau < total; tau += W) {
     const SmTask t = sm_task<FMT, KIND>(p, s_act, s_off, tau, tpe, g, tig);
-    const float ts = (FMT == kSmNv4 && p.tscale) ? __ldg(p.tscale + t.e) : 1.0f;
+    // NVFP4: the tensor scale, times 2^8 for the MMAs' weights x 2^-8 (see
+    // e2m1x8_to_bf16_pairs)
+    const float ts =
+        FMT == kSmNv4 ? (p.tscale ? __ldg(p.tscale + t.e) : 1.0f) * 256.0f : 1.0f;
 #pragma unroll 1
     for (int pass = 0; pass < t.npass; ++pass) {
       // this lane's token: n = 8 pass + g (none past the expert's rows)
@@ -308,8 +316,6 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
         uint4 sc2 = make_uint4(0u, 0u, 0u, 0u);
         if constexpr (FMT == kSmNv4) sc2 = lds128(sslot + 16);
         // MXFP8: a scale byte above 134 (weights beyond 2^7 in a block) needs
-        // the general conversion; decided once per chunk for the whole warp
-        // MXFP8: a scale byte above 134 (weights beyond 2^7 in a block) needs
         // the general conversion; decided once per chunk for the whole warp, so
         // each variant of the chunk body below is one straight-line block
         bool slow = false;
@@ -325,19 +331,16 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
           for (int i = 0; i < F::U; ++i) {
             const uint4 a0 = lds128(cur + (i * 32 + lane) * 16);
             const uint4 a1 = lds128(cur + ((F::U + i) * 32 + lane) * 16);
-            // MXFP8: unit i holds 16 codes of the 32-value block 2 i + tig / 2 of
-            // the chunk (scale word: row half, block / 4; byte: block % 4)
-            uint32_t sb[2] = {0u, 0u};
-            (void)sb;
             if constexpr (FMT == kSmMx8) {
+              // unit i holds 16 codes of the 32-value block 2 i + tig / 2 of the
+              // chunk (scale word: row half, block / 4; byte: block % 4)
               const int blk = 2 * i + (tig >> 1);
+              uint32_t sb[2];
               sb[0] = ((i < 2 ? sc.x : sc.y) >> (8 * (blk & 3))) & 0xffu;
               sb[1] = ((i < 2 ? sc.z : sc.w) >> (8 * (blk & 3))) & 0xffu;
-            }
 #pragma unroll
-            for (int j = 0; j < F::V / 4; ++j) {
-              uint32_t a[2][2];  // [row g / g + 8][values 4j, 4j+1 | 4j+2, 4j+3]
-              if constexpr (FMT == kSmMx8) {
+              for (int j = 0; j < F::V / 4; ++j) {
+                uint32_t a[2][2];  // [row g / g + 8][values 4j, 4j+1 | 4j+2, 4j+3]
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                   const uint32_t codes = word_of(rr ? a1 : a0, j);
@@ -349,23 +352,40 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
                     e4m3x4_to_bf16_scaled(codes, e8m0_to_float(sb[rr]), a[rr]);
                   }
                 }
-              } else {
-                // unit i: 32 codes = blocks 8 i + 2 tig (j < 4) and + 1 of the
-                // chunk's 16; MMA j takes codes 4 j .. 4 j + 3 (word j / 2)
-                const int blk = 8 * i + 2 * tig + (j >> 2);
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                  const uint4& s4 = rr ? sc2 : sc;
-                  const uint32_t sbyte = (word_of(s4, blk >> 2) >> (8 * (blk & 3))) & 0xffu;
-                  const uint32_t w = word_of(rr ? a1 : a0, j >> 1) >> (16 * (j & 1));
-                  e2m1x4_to_bf16(w, e4m3_scale_bf16x2(sbyte), a[rr]);
-                }
+                // tokens: values V (4 i + tig) + 4 j + {0..3}: 16-byte piece (4 j) / 8
+                const uint4& bq = bv[i][(4 * j) / 8];
+                const int wsel = ((4 * j) % 8) / 2;
+                mma_16816(acc[j % kAcc], a[0][0], a[1][0], a[0][1], a[1][1], word_of(bq, wsel),
+                          word_of(bq, wsel + 1));
               }
-              // tokens: values V (4 i + tig) + 4 j + {0..3}: 16-byte piece (4 j) / 8
-              const uint4& bq = bv[i][(4 * j) / 8];
-              const int wsel = ((4 * j) % 8) / 2;
-              mma_16816(acc[j % kAcc], a[0][0], a[1][0], a[0][1], a[1][1], word_of(bq, wsel),
-                        word_of(bq, wsel + 1));
+            } else {
+              // unit i: 32 codes = blocks 8 i + 2 tig and + 1 of the chunk's 16
+              // (scale word 2 i + tig / 2, bytes 2 (tig & 1) and + 1); word m of
+              // the unit holds codes 8 m .. 8 m + 7, of block m / 2
+              __nv_bfloat162 mul[2][2];
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                const uint32_t sw = word_of(rr ? sc2 : sc, 2 * i + (tig >> 1));
+                mul[rr][0] = e4m3_scale_x2p118(sw, ssel0);
+                mul[rr][1] = e4m3_scale_x2p118(sw, ssel1);
+              }
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                uint32_t q[2][4];  // [row g / g + 8][code pairs (0,4) (1,5) (2,6) (3,7)]
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr)
+                  e2m1x8_to_bf16_pairs(word_of(rr ? a1 : a0, m), mul[rr][m >> 1], q[rr]);
+                // the token values of the same positions, paired alike: the
+                // 16-byte piece m holds values 8 m .. 8 m + 7 as 4 bf16 pairs
+                const uint4& bq = bv[i][m];
+                uint32_t b04, b15, b26, b37;
+                asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(b04) : "r"(bq.x), "r"(bq.z));
+                asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(b15) : "r"(bq.x), "r"(bq.z));
+                asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(b26) : "r"(bq.y), "r"(bq.w));
+                asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(b37) : "r"(bq.y), "r"(bq.w));
+                mma_16816(acc[(2 * m) % kAcc], q[0][0], q[1][0], q[0][1], q[1][1], b04, b15);
+                mma_16816(acc[(2 * m + 1) % kAcc], q[0][2], q[1][2], q[0][3], q[1][3], b26, b37);
+              }
             }
           }
         };

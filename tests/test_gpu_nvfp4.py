@@ -124,3 +124,37 @@ def test_nvfp4_rejects_unaligned_dims(moe):
                torch.ones((4,), dtype=torch.float32, device="cuda"))
     with pytest.raises(RuntimeError, match="UNSUPPORTED"):
         moe.moe_forward_nvfp4(x, p["w_router"], fake_gu, nv_d, 2)
+
+
+def test_forward_nvfp4_subnormal_block_scales(moe):
+    """Small-M path with blocks whose E4M3 scale is subnormal: every 16-value
+    block of the weights is multiplied by a power of ten down to 1e-6, so that
+    the smallest blocks' scales (448 x block amax / tensor amax) fall below
+    the E4M3 normal range 2^-6, and every code magnitude, 0.5 included, occurs."""
+    T, d, E, k, I = 32, 512, 16, 4, 256
+    w = W.Workload("nv_sub", T, d, E, k, I, seed=7)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    g = torch.Generator().manual_seed(11)
+
+    def spread(t):
+        rows, K = t.shape[-2], t.shape[-1]
+        f = 10.0 ** -torch.randint(0, 7, (t.shape[0], rows, K // 16, 1), generator=g)
+        t32 = t.float().cpu().reshape(t.shape[0], rows, K // 16, 16) * f
+        return t32.reshape(t.shape).to(torch.bfloat16).to(t.device)
+
+    wgu, wd = spread(p["w_gate_up"]), spread(p["w_down"])
+    nv_gu, nv_d = moe.moe_nvfp4_quantize(wgu), moe.moe_nvfp4_quantize(wd)
+    sc = np.concatenate([nv_gu[1].cpu().numpy().ravel(), nv_d[1].cpu().numpy().ravel()])
+    assert (((sc & 0x78) == 0) & ((sc & 0x07) != 0)).any()  # subnormal scales occur
+    ws = moe.new_workspace(T, d, E, I, k, 0)
+    out = moe.moe_forward_nvfp4(x, p["w_router"], nv_gu, nv_d, k, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, T, d, E, I, k, 0)
+    ref = oracle.forward(W.to_bits(x), W.to_bits(p["w_router"]), _dequantised(wgu),
+                         _dequantised(wd), k)
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ref["ids"], ref["gates"], ref["logits"], k)
+    assert differ.size == 0
+    assert_layer_close(f64(v["y"]), ref["y"], "y")
+    assert_layer_close(f64(out), ref["out"], "out")
