@@ -384,7 +384,7 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
         avg = tot / n
         kernels[name] = {"launches": n, "avg_ms": round(avg, 5), "share": None,
                          "tflops": round(fl / (avg * 1e-3) / 1e12, 2),
-                         "gbs": round(by / (avg * 1e-3) / 1e9, 1)}
+                         "gbs": round(by / (avg * 1e-3) / 1e9, 1), "alg_bytes": int(by)}
     total_k = sum(v[1] for v in prof.values()) or 1.0
     for name, (n, tot) in prof.items():
         kernels[name]["share"] = round(tot / total_k, 4)
