@@ -133,3 +133,13 @@ def test_single_launch_rejects_unsupported(moe):
     x = W.make_x(w, device="cuda")
     with pytest.raises(RuntimeError, match="UNSUPPORTED"):
         _run(moe, w, p, x)
+
+
+def test_single_launch_zero_tokens(moe):
+    """An empty batch launches nothing and returns an empty output."""
+    w = W.Workload("fused0", 4, 256, 8, 2, 128, seed=3)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")[:0]
+    out = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], 2, single_launch=True)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256)

@@ -120,3 +120,14 @@ def test_forward_mxfp8_extreme_codes(moe, T):
     ref = oracle.forward(W.to_bits(x), W.to_bits(p["w_router"]), _dequantised_bits(wgu),
                          _dequantised_bits(wd), k)
     assert_layer_close(f64(out), ref["out"], "out")
+
+
+def test_mxfp8_zero_tokens(moe):
+    """An empty batch launches nothing and returns an empty output."""
+    w = W.Workload("mxfp80", 4, 256, 8, 2, 256, seed=3)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")[:0]
+    out = moe.moe_forward_mxfp8(x, p["w_router"], moe.moe_mxfp8_quantize(p["w_gate_up"]),
+                               moe.moe_mxfp8_quantize(p["w_down"]), 2)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256)

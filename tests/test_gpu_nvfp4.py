@@ -158,3 +158,14 @@ def test_forward_nvfp4_subnormal_block_scales(moe):
     assert differ.size == 0
     assert_layer_close(f64(v["y"]), ref["y"], "y")
     assert_layer_close(f64(out), ref["out"], "out")
+
+
+def test_nvfp4_zero_tokens(moe):
+    """An empty batch launches nothing and returns an empty output."""
+    w = W.Workload("nvfp40", 4, 256, 8, 2, 256, seed=3)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")[:0]
+    out = moe.moe_forward_nvfp4(x, p["w_router"], moe.moe_nvfp4_quantize(p["w_gate_up"]),
+                               moe.moe_nvfp4_quantize(p["w_down"]), 2)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256)
