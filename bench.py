@@ -424,16 +424,21 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
 
 
 def measure_e2e(moe, w, params, ws, x, steps, single_launch=False):
-    """Tokens/s end to end through the public API, host buffers in and out: the
-    layer captured once as a graph over pinned x_host / out_host
-    (moe_forward_graph with host buffers: H2D of x, the layer, D2H of out) and
-    replayed with moe_graph_launch plus a stream synchronisation every step.
-    The same loop through the plain moe_forward_host call is reported beside it."""
+    """Tokens/s end to end through the public API, from pinned host x to pinned
+    host out, as a serving loop runs it: two device buffer sets, each with the
+    layer captured as a graph (moe_forward_graph over device x / out) and
+    replayed with moe_graph_launch; step i's x goes up on a copy stream while
+    step i - 1 computes, its out comes back on another while step i + 1
+    computes, and the host waits for step i's copy-back and reads the result
+    after queueing step i + 1.  Every step moves its own x in and its out back.
+    Reported beside it: a graph over the host buffers themselves (H2D, layer,
+    D2H on one stream) with a stream synchronisation after every step, and the
+    plain moe_forward_host call the same way."""
     import torch
-    x_host = x.cpu().pin_memory()
-    out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    x_hosts = [x.cpu().pin_memory() for _ in range(2)]
+    out_hosts = [torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     kw = dict(router_bias=params["router_bias"], w_gate_up_shared=params["w_gate_up_shared"],
-              w_down_shared=params["w_down_shared"])
+              w_down_shared=params["w_down_shared"], single_launch=single_launch)
     s = torch.cuda.current_stream()
 
     def timed(call):
@@ -446,17 +451,50 @@ def measure_e2e(moe, w, params, ws, x, steps, single_launch=False):
             s.synchronize()
         return w.T * steps / (time.perf_counter() - t0)
 
-    plain = timed(lambda: moe.moe_forward_host(x_host, params["w_router"], params["w_gate_up"],
-                                               params["w_down"], w.top_k, out_host, ws,
-                                               single_launch=single_launch, **kw))
-    graph = moe.ForwardGraph(x_host, params["w_router"], params["w_gate_up"], params["w_down"],
-                             w.top_k, out_host, ws, single_launch=single_launch, **kw)
-    replay = timed(lambda: graph.launch())
-    graph.close()
+    wts = (params["w_router"], params["w_gate_up"], params["w_down"])
+    plain = timed(lambda: moe.moe_forward_host(x_hosts[0], *wts, w.top_k, out_hosts[0], ws, **kw))
+    g_host = moe.ForwardGraph(x_hosts[0], *wts, w.top_k, out_hosts[0], ws, **kw)
+    synced = timed(lambda: g_host.launch())
+    g_host.close()
+
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    out_dev = [torch.empty((w.T, w.d), dtype=torch.bfloat16, device=x.device) for _ in range(2)]
+    graphs = [moe.ForwardGraph(x_dev[j], *wts, w.top_k, out_dev[j], ws, **kw) for j in range(2)]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    seen = []
+
+    def run(n):
+        for i in range(n):
+            j = i % 2  # buffers of step i - 2: its copy-back was waited for below
+            with torch.cuda.stream(up):
+                x_dev[j].copy_(x_hosts[j], non_blocking=True)
+                ev_in[j].record(up)
+            s.wait_event(ev_in[j])
+            graphs[j].launch()
+            ev_done[j].record(s)
+            down.wait_event(ev_done[j])
+            with torch.cuda.stream(down):
+                out_hosts[j].copy_(out_dev[j], non_blocking=True)
+                ev_out[j].record(down)
+            if i:
+                ev_out[1 - j].synchronize()
+                seen.append(out_hosts[1 - j][0, 0].item())  # the host reads step i - 1
+        ev_out[(n - 1) % 2].synchronize()
+        seen.append(out_hosts[(n - 1) % 2][0, 0].item())
+
+    run(3)
+    t0 = time.perf_counter()
+    run(steps)
+    value = w.T * steps / (time.perf_counter() - t0)
+    for g in graphs:
+        g.close()
     nbytes = w.T * w.d * 2
-    return {"value": round(replay, 1), "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
-            "d2h_bytes_per_step": nbytes, "api": "moe_forward_graph(host buffers)+moe_graph_launch",
-            "plain_call_value": round(plain, 1)}
+    return {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": nbytes, "api": "moe_forward_graph+moe_graph_launch, copy streams",
+            "synced_value": round(synced, 1), "plain_call_value": round(plain, 1)}
 
 
 def cpu_baseline(W, w, params, x, target_s=15.0):
