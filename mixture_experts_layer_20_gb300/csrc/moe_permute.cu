@@ -13,7 +13,8 @@
 //             the grouping of a prefill batch (48k assignments) ~50 CTAs.  Positions are thus
 //             offsets[e] + (number of earlier f with the same e): a stable
 //             counting sort, deterministic with no global atomics.
-//   gather  : x_perm[p] = x[perm[p] / k], one warp per row, 16-byte copies.
+//   gather  : x_perm[slot_pos[t k + j]] = x[t], one warp per token: its row
+//             read once, written to its k slots, 16-byte copies.
 // Up to 4096 assignments, one CTA does count, scan and scatter.
 //
 // Combine ('Chapter 9. Distributed inference', section 9.3.4, step four;
@@ -146,29 +147,35 @@ __global__ void __launch_bounds__(WARPS * 32)
   permute_small_block<WARPS>(ids, n, E, counts, offsets, perm, slot_pos, status);
 }
 
-// One warp copies one row: each lane issues all of its 16-byte loads of the
-// row (up to kGatherVec) before the stores, so a row is one round trip.  The
-// stores are marked streaming (evict first): measured on the prefill layer,
-// gather 88 -> 83 us and the layer 6 us faster although gate_up, which reads
-// x_perm next, finds less of it in L2.
-constexpr int kGatherVec = 16;  // uint4 per lane: rows of up to 32 * 16 * 8 = 4096 bf16
+// One warp per token: its row of x is loaded once (each lane issues all of its
+// 16-byte loads of the row, up to kGatherVec, before any store) and stored to
+// each of its k slots x_perm[slot_pos[t k + j]].  Reading x once in token order,
+// instead of once per slot in slot order, keeps the reads sequential and
+// independent of L2 holding x (the DeepSeek-like layer's x is about L2-sized).
+// The stores are streaming (evict first): x_perm exceeds L2, and measured on
+// the prefill layer the layer was faster although gate_up, which reads x_perm
+// next, finds less of it in L2.
+constexpr int kGatherVec = 16;  // uint4 per lane and pass: 32 * 16 * 8 = 4096 bf16
 
-__global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* __restrict__ perm,
-                                                             const uint4* __restrict__ x, int n,
-                                                             int k, int vec_per_row,
-                                                             uint4* __restrict__ x_perm,
-                                                             unsigned* status) {
+__global__ void __launch_bounds__(256) moe_permute_gather_kernel(
+    const int32_t* __restrict__ slot_pos, const uint4* __restrict__ x, int T, int k, int n,
+    int vec_per_row, uint4* __restrict__ x_perm, unsigned* status) {
   pdl_wait_and_release();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n; pos += warps) {
-    const int f = __ldg(perm + pos);
-    if (static_cast<unsigned>(f) >= static_cast<unsigned>(n)) {
-      if (lane == 0) atomicOr(status, kStatusDeviceCheck);
-      continue;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    int pos[kMaxTopK];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      pos[j] = j < k ? __ldg(slot_pos + (size_t)t * k + j) : -1;
+      if (j < k && static_cast<unsigned>(pos[j]) >= static_cast<unsigned>(n)) {
+        bad = true;
+        pos[j] = -1;  // a bad slot position: that copy is skipped
+      }
     }
-    const uint4* src = x + (size_t)(f / k) * vec_per_row;
-    uint4* dst = x_perm + (size_t)pos * vec_per_row;
+    if (bad && lane == 0) atomicOr(status, kStatusDeviceCheck);
+    const uint4* src = x + (size_t)t * vec_per_row;
     for (int v0 = 0; v0 < vec_per_row; v0 += 32 * kGatherVec) {
       uint4 r[kGatherVec];
 #pragma unroll
@@ -177,9 +184,14 @@ __global__ void __launch_bounds__(256) moe_permute_gather_kernel(const int32_t* 
         if (v < vec_per_row) r[i] = __ldg(src + v);
       }
 #pragma unroll
-      for (int i = 0; i < kGatherVec; ++i) {
-        const int v = v0 + lane + 32 * i;
-        if (v < vec_per_row) __stcs(dst + v, r[i]);  // streaming: x_perm exceeds L2
+      for (int j = 0; j < kMaxTopK; ++j) {
+        if (pos[j] < 0) continue;
+        uint4* dst = x_perm + (size_t)pos[j] * vec_per_row;
+#pragma unroll
+        for (int i = 0; i < kGatherVec; ++i) {
+          const int v = v0 + lane + 32 * i;
+          if (v < vec_per_row) __stcs(dst + v, r[i]);
+        }
       }
     }
   }
@@ -223,11 +235,11 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
   }
   if (e != cudaSuccess || x == nullptr) return e;
   const int warps_per_cta = 8;
-  const int grid = std::min((n + warps_per_cta - 1) / warps_per_cta, device_sm_count() * 8);
+  const int grid = std::min((T + warps_per_cta - 1) / warps_per_cta, device_sm_count() * 8);
   KernelScope scope(s, "moe_permute_gather");
-  return launch_kernel(moe_permute_gather_kernel, dim3(grid), dim3(warps_per_cta * 32), 0, s, perm,
-                       static_cast<const uint4*>(x), n, top_k, d / 8, static_cast<uint4*>(x_perm),
-                       status);
+  return launch_kernel(moe_permute_gather_kernel, dim3(grid), dim3(warps_per_cta * 32), 0, s,
+                       slot_pos, static_cast<const uint4*>(x), T, top_k, n, d / 8,
+                       static_cast<uint4*>(x_perm), status);
 }
 
 cudaError_t launch_combine(cudaStream_t s, const void* y, const int32_t* slot_pos,
