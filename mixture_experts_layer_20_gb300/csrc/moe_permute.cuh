@@ -133,10 +133,8 @@ __device__ __forceinline__ void permute_small_block(const int32_t* ids, int n, i
 
 // One thread: 8 columns of one token, all k slot rows of fp16 y loaded before
 // the sum (k independent 16-byte loads in flight per thread), then the fp32
-// sum in slot order and one bf16 rounding.  A block covers 2048 columns of a
-// token.
+// sum in slot order and one bf16 rounding.
 constexpr int kCombineThreads = 256;
-constexpr int kCombineCols = kCombineThreads * 8;
 
 // Columns c .. c + 7 of token t (c a multiple of 8, c < d).
 template <bool COHERENT = false>
