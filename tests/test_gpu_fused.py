@@ -39,6 +39,7 @@ CASES = [
     (40, 768, 256, 8, 384, True, True),     # 256 experts, bias used for selection only
     (16, 256, 8, 8, 128, False, False),     # k = E
     (17, 640, 16, 1, 256, False, False),    # k = 1: gate exactly 1
+    (512, 256, 256, 8, 128, False, False),  # the limits: T k = 4096, 16 rows per expert
 ]
 
 
