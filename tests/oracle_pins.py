@@ -280,11 +280,12 @@ def check_nvfp4(o):
     step = np.where(np.abs(x) < 2, 0.5, np.where(np.abs(x) < 4, 1.0, 2.0))
     assert np.all(np.abs(deq - w.reshape(6, 64)) <= (0.5 * step * denom[..., None]).reshape(6, 64) * (1 + 1e-6))
     # values on the grid come back exactly: a block whose largest element is 6 x s x 2^-10
-    # (s an E4M3 value, one block with s = 448 so that the tensor scale is 2^-10)
-    bs = np.array([[448.0, 0.75], [13.0, 2.0 ** -3]])
-    grid = o.e2m1_values()[r.integers(0, 16, (2, 2, 16))] * bs[..., None] * 2.0 ** -10
+    # (s an E4M3 value, one block with s = 448 so that the tensor scale is 2^-10; two
+    # blocks with subnormal E4M3 scales, 2^-8 and 3 x 2^-9)
+    bs = np.array([[448.0, 0.75, 2.0 ** -8], [13.0, 2.0 ** -3, 3 * 2.0 ** -9]])
+    grid = o.e2m1_values()[r.integers(0, 16, (2, 3, 16))] * bs[..., None] * 2.0 ** -10
     grid[..., 0] = 6 * bs * 2.0 ** -10
-    grid = grid.reshape(2, 32)
+    grid = grid.reshape(2, 48)
     c2, s2, g2 = o.nvfp4_quantize(grid.astype(np.float32))
     assert g2 == np.float32(2.0 ** -10)
     assert np.array_equal(o.e4m3_values()[s2], bs)
