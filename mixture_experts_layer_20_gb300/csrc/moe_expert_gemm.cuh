@@ -373,7 +373,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_pre[2][kMaxExperts + 1];
-  __shared__ alignas(8) uint64_t s_bar[2 * kMaxStagesAny + 5];
+  __shared__ alignas(8) uint64_t s_bar[(kSub + 1) * kMaxStagesAny + 5];
   __shared__ int s_half_max;
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
@@ -391,16 +391,28 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   const int num_pairs = gridDim.x >> 1;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  // full: one per stage.  empty: gate_up releases each K box of a stage on
+  // its own barrier (box 0 of stage s at empty_bar + 8 s, box b > 0 at
+  // empty_hi + 8 ((b - 1) kMaxStagesAny + s)), so a box is refilled as soon as the MMAs that read it are done while the
+  // stage's other box is still in use; down releases a stage at once (box 0's
+  // barrier).  Measured on one box: gate_up -2 % at prefill, -9 % on the
+  // DeepSeek-like layer; down at decode +3 % with per-box release (its short
+  // 16-token tiles pay for the extra commit and wait per stage).
+  constexpr bool kBoxRelease = KIND == kGateUp;
   const uint32_t full_bar = smem_u32(&s_bar[0]);
   const uint32_t empty_bar = smem_u32(&s_bar[kMaxStagesAny]);
   const uint32_t tfull_bar = smem_u32(&s_bar[2 * kMaxStagesAny]);
   const uint32_t tempty_bar = smem_u32(&s_bar[2 * kMaxStagesAny + 2]);
   const uint32_t drain_bar = smem_u32(&s_bar[2 * kMaxStagesAny + 4]);
+  const uint32_t empty_hi = smem_u32(&s_bar[2 * kMaxStagesAny + 5]);
+  auto empty_box = [&](int b, int st) {
+    return b == 0 ? empty_bar + 8 * st : empty_hi + 8 * ((b - 1) * kMaxStagesAny + st);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStagesAny; ++s) {
       mbar_init(full_bar + 8 * s, 1);  // leader: counts both CTAs' bytes; unused in the follower
-      mbar_init(empty_bar + 8 * s, 1);
+      for (int b = 0; b < kSub; ++b) mbar_init(empty_box(b, s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar + 8 * a, 1);
@@ -466,34 +478,72 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       const int wrow = KIND == kGateUp ? t.slab * 128 + rank * 64
                                        : t.e * p.w_rows_per_group + t.slab * 256 + rank * 128;
       const GatherRows gr = gather_rows<FUSED>(p, trow, half, lane);
-      for (int ks = 0; ks < num_ks; ++ks) {
-        const int nsub = min(kSub, num_kb - ks * kSub);
-        const bool got = lane == 0 ? mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc) : true;
-        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-        const uint32_t fb = full_leader + 8 * stage;
-        const uint32_t a_dst = base + stage * stage_bytes;
-        const uint32_t b_dst = a_dst + kSub * kABytes;
-        if (lane == 0) {
-          if (ks == 0) s_tile_n[seq % kTileRing] = t.n;  // before the arrive that releases it
-          if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * nsub * tx_bytes);
-          for (int sub = 0; sub < nsub; ++sub) {
-            const int kx = (ks * kSub + sub) * kBK;
-            // gate_up: one box holds 4 groups of {16 gate rows, the 16 matching up rows}
-            if (KIND == kGateUp)
-              tma_load_5d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, 0, 0, wrow / 16, t.e);
-            else
-              tma_load_2d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow);
-            if (p.gather_perm == nullptr)
-              tma_load_2d_pair(b_dst + sub * b_sub_bytes, tmap_x, fb, kx, trow);
+      if constexpr (!kBoxRelease) {
+        for (int ks = 0; ks < num_ks; ++ks) {
+          const int nsub = min(kSub, num_kb - ks * kSub);
+          const bool got = lane == 0 ? mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc) : true;
+          if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+          const uint32_t fb = full_leader + 8 * stage;
+          const uint32_t a_dst = base + stage * stage_bytes;
+          const uint32_t b_dst = a_dst + kSub * kABytes;
+          if (lane == 0) {
+            if (ks == 0) s_tile_n[seq % kTileRing] = t.n;  // before the arrive that releases it
+            if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * nsub * tx_bytes);
+            for (int sub = 0; sub < nsub; ++sub) {
+              const int kx = (ks * kSub + sub) * kBK;
+              if (KIND == kGateUp)
+                tma_load_5d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, 0, 0, wrow / 16, t.e);
+              else
+                tma_load_2d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow);
+              if (p.gather_perm == nullptr)
+                tma_load_2d_pair(b_dst + sub * b_sub_bytes, tmap_x, fb, kx, trow);
+            }
           }
+          if (gr.on) {
+            for (int sub = 0; sub < nsub; ++sub)
+              tma_gather4_pair(b_dst + sub * b_sub_bytes + lane * 512, &tx.m[0], fb,
+                               (ks * kSub + sub) * kBK, gr.r[0], gr.r[1], gr.r[2], gr.r[3]);
+          }
+          ++issued;
+          if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
-        if (gr.on) {
-          for (int sub = 0; sub < nsub; ++sub)
-            tma_gather4_pair(b_dst + sub * b_sub_bytes + lane * 512, &tx.m[0], fb,
-                             (ks * kSub + sub) * kBK, gr.r[0], gr.r[1], gr.r[2], gr.r[3]);
+      } else {
+        for (int ks = 0; ks < num_ks && ok; ++ks) {
+          const int nsub = min(kSub, num_kb - ks * kSub);
+          const uint32_t fb = full_leader + 8 * stage;
+          const uint32_t a_dst = base + stage * stage_bytes;
+          const uint32_t b_dst = a_dst + kSub * kABytes;
+          bool armed = false;  // the stage's barrier is armed and its first box on the way
+#pragma unroll
+          for (int sub = 0; sub < kSub; ++sub) {
+            // box `sub` of this stage is free once the MMAs that read it are done
+            const bool got = lane == 0 ? mbar_wait(empty_box(sub, stage), phase ^ 1u, wc) : true;
+            if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+            armed = true;
+            if (lane == 0) {
+              if (sub == 0) {
+                if (ks == 0) s_tile_n[seq % kTileRing] = t.n;  // before the arrive that releases it
+                if (leader) mbar_arrive_expect_tx(full_bar + 8 * stage, 2 * nsub * tx_bytes);
+              }
+              if (sub < nsub) {
+                const int kx = (ks * kSub + sub) * kBK;
+                // gate_up: one box holds 4 groups of {16 gate rows, the 16 matching up rows}
+                if (KIND == kGateUp)
+                  tma_load_5d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, 0, 0, wrow / 16, t.e);
+                else
+                  tma_load_2d_pair(a_dst + sub * kABytes, &tmap_w, fb, kx, wrow);
+                if (p.gather_perm == nullptr)
+                  tma_load_2d_pair(b_dst + sub * b_sub_bytes, tmap_x, fb, kx, trow);
+              }
+            }
+            if (gr.on && sub < nsub)
+              tma_gather4_pair(b_dst + sub * b_sub_bytes + lane * 512, &tx.m[0], fb,
+                               (ks * kSub + sub) * kBK, gr.r[0], gr.r[1], gr.r[2], gr.r[3]);
+          }
+          if (armed) ++issued;  // drained at the end even if a later box never came
+          if (!ok) break;
+          if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
-        ++issued;
-        if (++stage == nst) { stage = 0; phase ^= 1u; }
       }
     }
     if (lane == 0) {
@@ -540,8 +590,12 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
               for (int k = 0; k < kBK / 16; ++k)
                 mma_bf16_pair(d_tmem, das + 2 * k, dbs + 2 * k, idesc, (sub | k) != 0 ? 1u : acc0);
             }
+            // frees box `sub` of this stage in both CTAs (also when the box is
+            // absent, so every box barrier completes one phase per stage), or
+            // the whole stage after its last box
+            if (kBoxRelease) mma_commit_pair(empty_box(sub, stage));
+            else if (sub == kSub - 1) mma_commit_pair(empty_bar + 8 * stage);
           }
-          mma_commit_pair(empty_bar + 8 * stage);  // frees this stage in both CTAs
           if (++stage == nst) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
