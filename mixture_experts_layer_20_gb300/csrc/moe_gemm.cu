@@ -195,6 +195,203 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The same logits for large batches in one pass per tile: a tile is 128
+// tokens by a chunk of at most 128 experts, and it runs over all 512-wide
+// ranges of d.  Each range is accumulated into one of two TMEM accumulators
+// (so the next range's MMAs overlap the epilogue of this one); the epilogue
+// threads (one token row each) add the ranges into a running sum in
+// registers, starting from +0 and in range order, exactly as the top-k
+// kernel adds the partial sums, so the logits are bit for bit those of the
+// split kernel above.  Only the final sums are written (one range of
+// partial), so the top-k kernel reads T x E values instead of splits times as
+// many.
+constexpr int kAccMaxN = 128;  // experts per tile
+constexpr int kAccBBytes = kAccMaxN * kBK * 2;  // 16 KB
+constexpr int kAccStages = 6;  // 6 x 32 KB: the split kernel's shared memory
+static_assert(kAccStages * (kABytes + kAccBBytes) + 1024 <= kSmemBytes, "fits the same allocation");
+
+struct RouterAccParams {
+  int T, K;
+  int n_per;           // experts per tile (multiple of 16, <= kAccMaxN)
+  int n_chunks;        // expert chunks: tiles = m tiles x n_chunks
+  int npad;            // row length of partial (E rounded up to 16)
+  int k_splits;        // 512-wide ranges of d
+  int kb_per_split;    // 64-wide K blocks per range
+  float* partial;      // [T][npad]: the logits
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_router_logits_accum_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                                   const __grid_constant__ CUtensorMap tmap_w,
+                                   const RouterAccParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ alignas(8) uint64_t s_bar[2 * kAccStages + 5];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t a_base = base;
+  const uint32_t b_base = base + kAccStages * kABytes;
+  const uint32_t full_bar = smem_u32(&s_bar[0]);
+  const uint32_t empty_bar = smem_u32(&s_bar[kAccStages]);
+  const uint32_t tfull_bar = smem_u32(&s_bar[2 * kAccStages]);
+  const uint32_t tempty_bar = smem_u32(&s_bar[2 * kAccStages + 2]);
+  const uint32_t drain_bar = smem_u32(&s_bar[2 * kAccStages + 4]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAccStages; ++s) {
+      mbar_init(full_bar + 8 * s, 1);
+      mbar_init(empty_bar + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar + 8 * a, 1);
+      mbar_init(tempty_bar + 8 * a, kEpiThreads);
+    }
+    mbar_init(drain_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(&tmap_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem_base), 2 * kAccMaxN);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  pdl_wait_and_release();
+
+  const uint32_t tmem_base = s_tmem_base;
+  const int m_tiles = (p.T + kBM - 1) / kBM;
+  const int total_tiles = m_tiles * p.n_chunks;
+  const int num_kb = p.K / kBK;
+  const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer: every K block of the tile, in order
+      const uint32_t tx_bytes = kABytes + static_cast<uint32_t>(p.n_per) * kBK * 2;
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
+        const int row0 = (tau / p.n_chunks) * kBM;
+        const int e0 = (tau % p.n_chunks) * p.n_per;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty_bar + 8 * stage, phase ^ 1u, wc)) { ok = false; break; }
+          const uint32_t fb = full_bar + 8 * stage;
+          mbar_arrive_expect_tx(fb, tx_bytes);
+          tma_load_2d(a_base + stage * kABytes, &tmap_x, fb, kb * kBK, row0);
+          tma_load_2d(b_base + stage * kAccBBytes, &tmap_w, fb, kb * kBK, e0);
+          ++issued;
+          if (++stage == kAccStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int i = max(0, issued - kAccStages); i < issued; ++i)
+        mbar_wait_drain(full_bar + 8 * (i % kAccStages), (i / kAccStages) & 1, p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: one accumulation per range
+      const uint32_t idesc = idesc_bf16_f32(kBM, p.n_per);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
+        for (int sp = 0; sp < p.k_splits && ok; ++sp) {
+          if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + acc * kAccMaxN;
+          const int kb0 = sp * p.kb_per_split;
+          const int kb1 = min(num_kb, kb0 + p.kb_per_split);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(full_bar + 8 * stage, phase, wc)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t a_addr = a_base + stage * kABytes;
+            const uint32_t b_addr = b_base + stage * kAccBBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_ss(d_tmem, smem_desc_sw128(a_addr + k * 32),
+                          smem_desc_sw128(b_addr + k * 32), idesc,
+                          (kb != kb0 || k != 0) ? 1u : 0u);
+            mma_commit(empty_bar + 8 * stage);
+            if (++stage == kAccStages) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          mma_commit(tfull_bar + 8 * acc);  // this range's sums ready for the epilogue
+          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+      }
+      mma_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0, p.status);
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5, TMEM lane = token row of the tile
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool live = true;
+    for (int tau = blockIdx.x; tau < total_tiles && live; tau += gridDim.x) {
+      const int row = (tau / p.n_chunks) * kBM + q * 32 + lane;
+      const int e0 = (tau % p.n_chunks) * p.n_per;
+      float sum[kAccMaxN];
+#pragma unroll
+      for (int i = 0; i < kAccMaxN; ++i) sum[i] = 0.0f;
+      for (int sp = 0; sp < p.k_splits; ++sp) {
+        const bool ok = mbar_wait(tfull_bar + 8 * acc, acc_phase, wc);
+        if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
+        tc_fence_after_sync();
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccMaxN;
+#pragma unroll
+        for (int c = 0; c < kAccMaxN; c += 16) {
+          if (c < p.n_per) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(t_row + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sum[c + i] += __uint_as_float(v[i]);
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(tempty_bar + 8 * acc);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (live && row < p.T) {
+        // the last chunk may reach past the row's npad columns: not stored
+        const int n_valid = min(p.n_per, p.npad - e0);
+        float* dst = p.partial + (size_t)row * p.npad + e0;
+#pragma unroll
+        for (int c = 0; c < kAccMaxN; c += 16) {
+          if (c < n_valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(__float_as_uint(sum[c + 4 * i]), __float_as_uint(sum[c + 4 * i + 1]),
+                                 __float_as_uint(sum[c + 4 * i + 2]),
+                                 __float_as_uint(sum[c + 4 * i + 3]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 2 * kAccMaxN);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -224,6 +421,9 @@ cudaError_t ensure_router_smem_attr() {
   if (dev < 32 && (done_mask >> dev) & 1u) return cudaSuccess;
   e = cudaFuncSetAttribute(moe_router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(moe_router_logits_accum_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && dev < 32) done_mask |= 1u << dev;
   return e;
 }
@@ -281,24 +481,70 @@ cudaError_t make_u8_map_nd(CUtensorMap* m, const void* base, int rank, const uin
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// One pass per tile over all ranges (moe_router_logits_accum) when the batch
+// has at least 16 token tiles and the partial sums of the split kernel would
+// move (written, then read) more than 1.5 times the bytes of x; otherwise one
+// tile per range, which spreads a tile's K over many SMs.  Both give the same
+// logits.  Measured (router logits + top-k): the DeepSeek-like layer (d = 7168,
+// 14 ranges, E = 256) 64 against 108 us; the 6000-token Qwen3 prefill (8
+// ranges, E = 128) 40 against 37 us, so it keeps the split kernel.
+constexpr int kAccumMinTiles = 16;
+
+int router_ranges_written(int T, int d, int E) {
+  const long long partial_bytes = 8LL * router_splits(d) * router_npad(E);  // per token
+  const long long x_bytes = 2LL * d;
+  const bool accum = (T + kBM - 1) / kBM >= kAccumMinTiles && 2 * partial_bytes > 3 * x_bytes;
+  return accum ? 1 : router_splits(d);
+}
+
 cudaError_t launch_router_logits(cudaStream_t s, const void* x, const void* w_router, int T,
                                  int d, int E, float* partial, unsigned* status,
                                  unsigned long long timeout_ns) {
+  const int m_tiles = (T + kBM - 1) / kBM;
+  const int npad = router_npad(E);
+  cudaError_t e = ensure_router_smem_attr();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mx, mw;
+  e = make_bf16_map(&mx, x, T, d, kBM);
+  if (e != cudaSuccess) return e;
+  if (router_ranges_written(T, d, E) == 1) {
+    RouterAccParams p{};
+    p.T = T;
+    p.K = d;
+    p.npad = npad;
+    p.k_splits = router_splits(d);
+    p.kb_per_split = kRouterSplitK / kBK;
+    // expert chunks: enough tiles for every SM, at most kAccMaxN experts each
+    const int sms = device_sm_count();
+    int chunks = std::max((npad + kAccMaxN - 1) / kAccMaxN, std::min(npad / 16, sms / m_tiles));
+    p.n_per = ((npad + chunks - 1) / chunks + 15) / 16 * 16;
+    p.n_chunks = (npad + p.n_per - 1) / p.n_per;
+    p.partial = partial;
+    p.status = status;
+    p.timeout_ns = timeout_ns;
+    e = make_bf16_map(&mw, w_router, E, d, p.n_per);
+    if (e != cudaSuccess) return e;
+    const long long tiles = static_cast<long long>(m_tiles) * p.n_chunks;
+    const long long grid = std::max(1LL, std::min<long long>(sms, tiles));
+    KernelScope scope(s, "moe_router_logits");
+    cudaError_t le = launch_kernel(moe_router_logits_accum_kernel,
+                                   dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
+                                   s, mx, mw, p);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+  }
   RouterParams p{};
   p.T = T;
   p.K = d;
-  p.mma_n = router_npad(E);
+  p.mma_n = npad;
   p.k_splits = router_splits(d);
   p.kb_per_split = kRouterSplitK / kBK;
   p.partial = partial;
   p.status = status;
   p.timeout_ns = timeout_ns;
-  CUtensorMap mx, mw;
-  cudaError_t e = make_bf16_map(&mx, x, T, d, kBM);
-  if (e == cudaSuccess) e = make_bf16_map(&mw, w_router, E, d, p.mma_n);
-  if (e == cudaSuccess) e = ensure_router_smem_attr();
+  e = make_bf16_map(&mw, w_router, E, d, p.mma_n);
   if (e != cudaSuccess) return e;
-  const long long tiles = static_cast<long long>((T + kBM - 1) / kBM) * p.k_splits;
+  const long long tiles = static_cast<long long>(m_tiles) * p.k_splits;
   const long long grid = std::max(1LL, std::min<long long>(device_sm_count(), tiles));
   KernelScope scope(s, "moe_router_logits");
   cudaError_t le = launch_kernel(moe_router_logits_kernel, dim3(static_cast<unsigned>(grid)),

@@ -15,15 +15,19 @@ constexpr int kMaxTopK = 8;
 constexpr int kPermuteChunk = 1024;     // assignments per count / scatter CTA
 constexpr int kPermuteSmallMax = 4096;  // up to this many, one CTA groups them all
 
-// The router's logits are computed in K ranges of 512 on the tensor cores
-// and summed in range order by the top-k kernel.  The number of ranges
-// depends on d only, so a token's logits do not depend on the batch.
+// The router's logits are sums over K ranges of 512 on the tensor cores,
+// added in range order starting from +0 (by the top-k kernel, or, for large
+// batches, already by the logits kernel, which then writes one range).  The
+// number of ranges depends on d only, so a token's logits do not depend on
+// the batch.
 constexpr int kRouterSplitK = 512;
 inline int router_splits(int d) { return (d + kRouterSplitK - 1) / kRouterSplitK; }
 inline int router_npad(int E) { return (E + 15) / 16 * 16; }
 inline size_t router_partial_bytes(int T, int d, int E) {
   return static_cast<size_t>(router_splits(d)) * T * router_npad(E) * sizeof(float);
 }
+// Ranges the logits kernel writes for a batch of T tokens (moe_gemm.cu).
+int router_ranges_written(int T, int d, int E);
 
 // Words of the workspace's 256-byte status region: word 0 is the status word;
 // the single-launch decode kernel keeps its grid-barrier counters in three
@@ -118,7 +122,8 @@ cudaError_t make_u8_map_nd(CUtensorMap* map, const void* base, int rank, const u
 // ---- tcgen05 GEMM launchers.  Return a CUDA error code.
 
 // Router logits of x [T,d] against w_router [E,d] on the tensor cores:
-// partial sums over each 512-wide K range, partial [splits][T][npad] fp32.
+// partial [router_ranges_written(T, d, E)][T][npad] fp32 (the partial sums over
+// each 512-wide K range, or, for large batches, their in-order sum).
 cudaError_t launch_router_logits(cudaStream_t s, const void* x, const void* w_router, int T,
                                  int d, int E, float* partial, unsigned* status,
                                  unsigned long long timeout_ns);

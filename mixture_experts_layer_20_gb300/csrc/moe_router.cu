@@ -4,8 +4,9 @@
 // the token to its top-K experts ('PagedAttention, speculative decoding, MoE
 // and Blackwell', section 2; 'Chapter 9. Distributed inference', section
 // 9.3.4: the router picks eight experts per token).  The logits come from the
-// tensor-core kernel as fp32 partial sums over 512-wide K ranges; here one
-// warp per token adds the ranges in range order (deterministic), adds the
+// tensor-core kernel as fp32 partial sums over 512-wide K ranges (for large
+// batches already added, in the same order, by that kernel: one range); here
+// one warp per token adds the ranges in range order (deterministic), adds the
 // router bias, selects the k largest logits (an equal logit loses to a lower
 // expert index) by k rounds of a warp-wide arg-max, and computes the gates
 // as the softmax of the chosen logits, which equals the full softmax
@@ -46,7 +47,7 @@ cudaError_t launch_router(cudaStream_t s, const void* x, const void* w_router, c
   if (e != cudaSuccess) return e;
   KernelScope scope(s, "moe_router_topk");
   return launch_kernel(moe_router_topk_kernel, dim3((T + kTokensPerCta - 1) / kTokensPerCta),
-                       dim3(kTokensPerCta * 32), 0, s, partial, router_splits(d), T,
+                       dim3(kTokensPerCta * 32), 0, s, partial, router_ranges_written(T, d, E), T,
                        router_npad(E), E, top_k, bias, bias_selection_only ? 1 : 0, ids, gates);
 }
 

@@ -46,6 +46,11 @@ ROUTE_CASES = [
     (1, 256, 8, 1, False),       # one token, k = 1
     (513, 1024, 128, 8, False),  # Qwen3 expert count
     (200, 512, 256, 8, True),    # maximum expert count
+    (2100, 1024, 128, 8, False), # 17 token tiles, one tile per K range
+    # 16 token tiles or more with many experts: one logits pass per tile over all K ranges
+    (2048, 640, 256, 8, True),   # expert chunks to fill the SMs; a 128-wide last K range
+    (1921, 512, 256, 3, True),   # exactly 16 tiles
+    (5000, 1024, 256, 8, False), # 40 tiles: three chunks of 96 experts, the last one partial
 ]
 
 
@@ -61,6 +66,17 @@ def test_route(moe, T, d, E, k, bias):
     assert torch.allclose(gates.sum(1), torch.ones(T, device="cuda"), atol=1e-6)
     if k == 1:
         assert (gates == 1.0).all()
+
+
+def test_route_does_not_depend_on_the_batch(moe):
+    """A token's routing is the same in a large batch (logits in one pass per
+    tile) and alone with a few others (one tile per K range): bit for bit."""
+    w, x, p = _layer(2304, 1024, 256, 8, 64, zipf=True, seed=5)
+    ids, gates = moe.moe_route(x, p["w_router"], 8, router_bias=p["router_bias"])
+    ids_s, gates_s = moe.moe_route(x[:100].contiguous(), p["w_router"], 8,
+                                   router_bias=p["router_bias"])
+    torch.cuda.synchronize()
+    assert torch.equal(ids[:100], ids_s) and torch.equal(gates[:100], gates_s)
 
 
 def test_route_ties(moe):
