@@ -205,6 +205,13 @@ moe_status_t moe_forward(const moe_bf16* x, const moe_bf16* w_router,
  * logits over 128-wide ranges of d here (512 otherwise), so a near-tie may
  * route differently from the multi-launch layer; both are checked against
  * the same reference.
+ * y_fp32 = 1: the expert outputs y (and the shared expert's) are kept in fp32
+ * instead of fp16 between the down GEMM and the combine, so an output beyond
+ * the fp16 range (|y| > 65504) is neither saturated nor flagged
+ * (MOE_ERR_RANGE cannot occur); the down GEMM's stores and the combine's
+ * reads of y double, and the workspace must hold moe_workspace_size_ex(...,
+ * ext) bytes (MOE_ERR_WORKSPACE otherwise).  Not with single_launch
+ * (MOE_ERR_UNSUPPORTED).
  * Zero-initialise the struct: later fields default to 0. */
 typedef struct {
   const float* router_bias;
@@ -213,7 +220,14 @@ typedef struct {
   int I_shared;
   int bias_selection_only;
   int single_launch;
+  int y_fp32;
 } moe_forward_ext_t;
+
+/* Workspace bytes for moe_forward_ex (and the other calls taking ext) with
+ * these options: the shared expert (ext->I_shared) and fp32 y (ext->y_fp32);
+ * ext may be NULL (then equal to moe_workspace_size(..., 0)). */
+size_t moe_workspace_size_ex(int T, int d, int E, int I, int top_k,
+                             const moe_forward_ext_t* ext);
 
 moe_status_t moe_forward_ex(const moe_bf16* x, const moe_bf16* w_router,
                             const moe_bf16* w_gate_up, const moe_bf16* w_down,
@@ -327,6 +341,11 @@ typedef struct {
 
 moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,
                                   moe_workspace_layout_t* layout);
+/* The same for the options in ext (fp32 y: y and y_shared take 4 bytes a
+ * value); ext may be NULL. */
+moe_status_t moe_workspace_layout_ex(int T, int d, int E, int I, int top_k,
+                                     const moe_forward_ext_t* ext,
+                                     moe_workspace_layout_t* layout);
 
 /* Synchronise `stream`, read and clear the workspace's device status word. */
 moe_status_t moe_get_device_status(void* ws, size_t ws_bytes, moe_stream_t stream);

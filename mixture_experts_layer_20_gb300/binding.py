@@ -32,7 +32,8 @@ class WorkspaceLayout(ctypes.Structure):
 
 class ForwardExt(ctypes.Structure):
     _fields_ = [("router_bias", _vp), ("w_gate_up_shared", _vp), ("w_down_shared", _vp),
-                ("I_shared", _i), ("bias_selection_only", _i), ("single_launch", _i)]
+                ("I_shared", _i), ("bias_selection_only", _i), ("single_launch", _i),
+                ("y_fp32", _i)]
 
 
 _SIGS = {
@@ -61,6 +62,9 @@ _SIGS = {
     "moe_forward_host": (_st, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp,
                                ctypes.POINTER(ForwardExt)]),
     "moe_workspace_layout": (_st, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(WorkspaceLayout)]),
+    "moe_workspace_size_ex": (_sz, [_i, _i, _i, _i, _i, ctypes.POINTER(ForwardExt)]),
+    "moe_workspace_layout_ex": (_st, [_i, _i, _i, _i, _i, ctypes.POINTER(ForwardExt),
+                                      ctypes.POINTER(WorkspaceLayout)]),
     "moe_get_device_status": (_st, [_vp, _sz, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_st]),
     "moe_last_error": (ctypes.c_char_p, []),
@@ -110,14 +114,22 @@ def _want(t, dtype, name):
 
 # ---------------------------------------------------------------- workspace
 
-def moe_workspace_size(T, d, E, I, top_k, I_shared=0) -> int:
-    return int(_lib.moe_workspace_size(T, d, E, I, top_k, I_shared))
+def moe_workspace_size(T, d, E, I, top_k, I_shared=0, y_fp32=False) -> int:
+    if not y_fp32:
+        return int(_lib.moe_workspace_size(T, d, E, I, top_k, I_shared))
+    ext = ForwardExt(None, None, None, I_shared, 0, 0, 1)
+    return int(_lib.moe_workspace_size_ex(T, d, E, I, top_k, ctypes.byref(ext)))
 
 
-def moe_workspace_layout(T, d, E, I, top_k, I_shared=0) -> dict:
+def moe_workspace_layout(T, d, E, I, top_k, I_shared=0, y_fp32=False) -> dict:
     lay = WorkspaceLayout()
-    _check(_lib.moe_workspace_layout(T, d, E, I, top_k, I_shared, ctypes.byref(lay)),
-           "moe_workspace_layout")
+    if not y_fp32:
+        _check(_lib.moe_workspace_layout(T, d, E, I, top_k, I_shared, ctypes.byref(lay)),
+               "moe_workspace_layout")
+    else:
+        ext = ForwardExt(None, None, None, I_shared, 0, 0, 1)
+        _check(_lib.moe_workspace_layout_ex(T, d, E, I, top_k, ctypes.byref(ext),
+                                            ctypes.byref(lay)), "moe_workspace_layout_ex")
     return {n: getattr(lay, n) for n, _ in WorkspaceLayout._fields_}
 
 
@@ -125,9 +137,9 @@ def moe_workspace_init(ws: torch.Tensor, stream=None):
     _check(_lib.moe_workspace_init(_p(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
 
 
-def new_workspace(T, d, E, I, top_k, I_shared=0, device="cuda") -> torch.Tensor:
-    """A zeroed uint8 device workspace for these shapes."""
-    n = max(moe_workspace_size(T, d, E, I, top_k, I_shared), 256)
+def new_workspace(T, d, E, I, top_k, I_shared=0, device="cuda", y_fp32=False) -> torch.Tensor:
+    """A zeroed uint8 device workspace for these shapes (and fp32 y)."""
+    n = max(moe_workspace_size(T, d, E, I, top_k, I_shared, y_fp32), 256)
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
@@ -262,9 +274,10 @@ def moe_combine(y, slot_pos, topk_gates, y_shared=None, out=None, ws=None, strea
 
 def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router_bias=None,
                 w_gate_up_shared=None, w_down_shared=None, stream=None, bias_selection_only=False,
-                single_launch=False):
+                single_launch=False, y_fp32=False):
     """The whole layer.  Returns out [T, d] bf16.  single_launch: one kernel
-    launch for the whole layer (decode-sized batches, see moe_forward_ext_t)."""
+    launch for the whole layer (decode-sized batches, see moe_forward_ext_t);
+    y_fp32: expert outputs kept in fp32 (needs new_workspace(..., y_fp32=True))."""
     for t, n in ((x, "x"), (w_router, "w_router"), (w_gate_up, "w_gate_up"), (w_down, "w_down"),
                  (w_gate_up_shared, "w_gate_up_shared"), (w_down_shared, "w_down_shared")):
         _want(t, torch.bfloat16, n)
@@ -277,16 +290,17 @@ def moe_forward(x, w_router, w_gate_up, w_down, top_k, out=None, ws=None, router
         out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
     _want(out, torch.bfloat16, "out")
     if ws is None:
-        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device)
+        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device, y_fp32=y_fp32)
     s = _stream(stream)
-    if router_bias is None and I_s == 0 and not single_launch:
+    if router_bias is None and I_s == 0 and not single_launch and not y_fp32:
         st = _lib.moe_forward(_p(x), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E, I, top_k,
                               _p(out), _p(ws), ws.numel(), s)
     else:
         ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
                          w_gate_up_shared.data_ptr() if I_s else None,
                          w_down_shared.data_ptr() if I_s else None, I_s,
-                         1 if bias_selection_only else 0, 1 if single_launch else 0)
+                         1 if bias_selection_only else 0, 1 if single_launch else 0,
+                         1 if y_fp32 else 0)
         st = _lib.moe_forward_ex(_p(x), _p(w_router), _p(w_gate_up), _p(w_down), T, d, E, I,
                                  top_k, _p(out), _p(ws), ws.numel(), s, ctypes.byref(ext))
     _check(st, "moe_forward")
@@ -346,7 +360,7 @@ def moe_nvfp4_quantize(w, stream=None):
 
 def moe_forward_nvfp4(x, w_router, nv_gate_up, nv_down, top_k, out=None, ws=None,
                       router_bias=None, w_gate_up_shared=None, w_down_shared=None, stream=None,
-                      bias_selection_only=False):
+                      bias_selection_only=False, y_fp32=False):
     """The whole layer with NVFP4 expert weights: nv_gate_up / nv_down are the
     (codes, scales, tensor scales) of moe_nvfp4_quantize for W_gate_up
     [E,2I,d] and W_down [E,d,I].  Returns out [T, d] bf16."""
@@ -367,11 +381,11 @@ def moe_forward_nvfp4(x, w_router, nv_gate_up, nv_down, top_k, out=None, ws=None
     if out is None:
         out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
     if ws is None:
-        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device)
+        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device, y_fp32=y_fp32)
     ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
                      w_gate_up_shared.data_ptr() if I_s else None,
                      w_down_shared.data_ptr() if I_s else None, I_s,
-                     1 if bias_selection_only else 0)
+                     1 if bias_selection_only else 0, 0, 1 if y_fp32 else 0)
     _check(_lib.moe_forward_nvfp4(_p(x), _p(w_router), _p(cgu), _p(sgu), _p(tgu), _p(cd), _p(sd),
                                   _p(td), T, d, E, I, top_k, _p(out), _p(ws), ws.numel(),
                                   _stream(stream), ctypes.byref(ext)), "moe_forward_nvfp4")
@@ -380,7 +394,7 @@ def moe_forward_nvfp4(x, w_router, nv_gate_up, nv_down, top_k, out=None, ws=None
 
 def moe_forward_mxfp8(x, w_router, mx_gate_up, mx_down, top_k, out=None, ws=None,
                       router_bias=None, w_gate_up_shared=None, w_down_shared=None, stream=None,
-                      bias_selection_only=False):
+                      bias_selection_only=False, y_fp32=False):
     """The whole layer with MXFP8 expert weights: mx_gate_up / mx_down are the
     (codes, scales) pairs of moe_mxfp8_quantize for W_gate_up [E,2I,d] and
     W_down [E,d,I].  Returns out [T, d] bf16."""
@@ -400,11 +414,11 @@ def moe_forward_mxfp8(x, w_router, mx_gate_up, mx_down, top_k, out=None, ws=None
     if out is None:
         out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
     if ws is None:
-        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device)
+        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device, y_fp32=y_fp32)
     ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
                      w_gate_up_shared.data_ptr() if I_s else None,
                      w_down_shared.data_ptr() if I_s else None, I_s,
-                     1 if bias_selection_only else 0)
+                     1 if bias_selection_only else 0, 0, 1 if y_fp32 else 0)
     _check(_lib.moe_forward_mxfp8(_p(x), _p(w_router), _p(cgu), _p(sgu), _p(cd), _p(sd), T, d, E,
                                   I, top_k, _p(out), _p(ws), ws.numel(), _stream(stream),
                                   ctypes.byref(ext)), "moe_forward_mxfp8")
@@ -457,9 +471,9 @@ class ForwardGraph:
             pass
 
 
-def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0) -> dict:
+def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0, y_fp32=False) -> dict:
     """Typed views of moe_forward's intermediates inside its workspace."""
-    L = moe_workspace_layout(T, d, E, I, top_k, I_shared)
+    L = moe_workspace_layout(T, d, E, I, top_k, I_shared, y_fp32)
     n = T * top_k
 
     def view(off, count, dtype, shape):
@@ -475,5 +489,5 @@ def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0) -> dict:
         "slot_pos": view(L["slot_pos"], n, torch.int32, (T, top_k)),
         "x_perm": view(L["x_perm"], n * d, torch.bfloat16, (n, d)),
         "h": view(L["h"], n * I, torch.bfloat16, (n, I)),
-        "y": view(L["y"], n * d, torch.float16, (n, d)),
+        "y": view(L["y"], n * d, torch.float32 if y_fp32 else torch.float16, (n, d)),
     }

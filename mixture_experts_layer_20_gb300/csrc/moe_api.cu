@@ -92,7 +92,8 @@ struct Layout {
       y, y_shared, x_stage, out_stage, total;
 };
 
-Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
+// y_fp32: the expert outputs y and y_shared kept in fp32 (else fp16).
+Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared, bool y_fp32 = false) {
   const size_t n = static_cast<size_t>(T) * top_k;
   const size_t nchunks = (n + kPermuteChunk - 1) / kPermuteChunk;
   Layout L{};
@@ -115,8 +116,9 @@ Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared) {
   L.x_perm = take(n * d * 2);
   L.h = take(n * I * 2);
   L.h_shared = take(static_cast<size_t>(T) * I_shared * 2);
-  L.y = take(n * d * 2);
-  L.y_shared = take(I_shared ? static_cast<size_t>(T) * d * 2 : 0);
+  const size_t ybytes = y_fp32 ? 4 : 2;
+  L.y = take(n * d * ybytes);
+  L.y_shared = take(I_shared ? static_cast<size_t>(T) * d * ybytes : 0);
   L.x_stage = take(static_cast<size_t>(T) * d * 2);
   L.out_stage = take(static_cast<size_t>(T) * d * 2);
   L.total = off;
@@ -216,11 +218,18 @@ size_t moe_workspace_size(int T, int d, int E, int I, int top_k, int I_shared) {
   return forward_layout(T, d, E, I, top_k, I_shared).total;
 }
 
-moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,
-                                  moe_workspace_layout_t* out) {
+size_t moe_workspace_size_ex(int T, int d, int E, int I, int top_k,
+                             const moe_forward_ext_t* ext) {
+  const int I_shared = ext ? ext->I_shared : 0;
+  if (T < 0 || d <= 0 || E <= 0 || I <= 0 || top_k <= 0 || I_shared < 0) return 0;
+  return forward_layout(T, d, E, I, top_k, I_shared, ext && ext->y_fp32).total;
+}
+
+static moe_status_t workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,
+                                     bool y_fp32, moe_workspace_layout_t* out) {
   if (!out || T < 0 || d <= 0 || E <= 0 || I <= 0 || top_k <= 0 || I_shared < 0)
     return fail(MOE_ERR_INVALID_ARG, "bad arguments to moe_workspace_layout");
-  const Layout L = forward_layout(T, d, E, I, top_k, I_shared);
+  const Layout L = forward_layout(T, d, E, I, top_k, I_shared, y_fp32);
   out->status = L.status;
   out->router_logits = L.logits;
   out->topk_ids = L.ids;
@@ -239,6 +248,16 @@ moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_s
   out->out_stage = L.out_stage;
   out->total = L.total;
   return MOE_OK;
+}
+
+moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,
+                                  moe_workspace_layout_t* out) {
+  return workspace_layout(T, d, E, I, top_k, I_shared, false, out);
+}
+
+moe_status_t moe_workspace_layout_ex(int T, int d, int E, int I, int top_k,
+                                     const moe_forward_ext_t* ext, moe_workspace_layout_t* out) {
+  return workspace_layout(T, d, E, I, top_k, ext ? ext->I_shared : 0, ext && ext->y_fp32, out);
 }
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
@@ -357,6 +376,7 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   const float* bias = ext ? ext->router_bias : nullptr;
   const int bias_sel = ext ? ext->bias_selection_only : 0;
   const bool single = ext && ext->single_launch;
+  const bool y32 = ext && ext->y_fp32;
   const int I_shared = ext ? ext->I_shared : 0;
   const moe_bf16* wgu_s = ext ? ext->w_gate_up_shared : nullptr;
   const moe_bf16* wd_s = ext ? ext->w_down_shared : nullptr;
@@ -368,8 +388,10 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) ||
       !aligned16(out) || !aligned16(ws) || (I_shared && (!aligned16(wgu_s) || !aligned16(wd_s))))
     return fail(MOE_ERR_INVALID_ARG, "moe_forward: pointers must be 16-byte aligned");
-  const Layout L = forward_layout(T, d, E, I, top_k, I_shared);
+  const Layout L = forward_layout(T, d, E, I, top_k, I_shared, y32);
   if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "moe_forward: workspace too small");
+  if (single && y32)
+    return fail(MOE_ERR_UNSUPPORTED, "single_launch keeps y in fp16 (y_fp32 unsupported)");
   if (single && (mx || I_shared || d % 128 || I % 128 ||
                  static_cast<long long>(T) * top_k > kPermuteSmallMax ||
                  static_cast<long long>(T) * top_k > kSingleLaunchRowsPerExpert * E))
@@ -442,23 +464,24 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   if (small_m)
     e = launch_grouped_ffn_smallm(s, mx->fmt == 0 ? 1 : 2, x, perm, top_k, offsets, rows, d, E, I,
                                   mx->codes_gate_up, mx->scales_gate_up, mx->tscale_gate_up,
-                                  mx->codes_down, mx->scales_down, mx->tscale_down, h, y, status);
+                                  mx->codes_down, mx->scales_down, mx->tscale_down, h, y, status,
+                                  y32);
   else if (mx)
     e = launch_grouped_ffn_quant(s, mx->fmt, x_perm, offsets, rows, d, E, I, mx->codes_gate_up,
                                  mx->scales_gate_up, mx->tscale_gate_up, mx->codes_down,
-                                 mx->scales_down, mx->tscale_down, h, y, status, tmo);
+                                 mx->scales_down, mx->tscale_down, h, y, status, tmo, y32);
   else
     e = launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status,
-                           tmo, gather_rows ? &gather : nullptr);
+                           tmo, gather_rows ? &gather : nullptr, y32);
   if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
   void* y_shared = nullptr;
   if (I_shared) {
     y_shared = w + L.y_shared;
     e = launch_grouped_ffn(s, x, nullptr, T, d, 1, I_shared, wgu_s, wd_s, w + L.h_shared,
-                           y_shared, status, tmo);
+                           y_shared, status, tmo, nullptr, y32);
     if (e != cudaSuccess) return cuda_fail(e, "shared expert launch");
   }
-  e = launch_combine(s, y, slot_pos, gates, y_shared, T, d, top_k, out, status);
+  e = launch_combine(s, y, slot_pos, gates, y_shared, T, d, top_k, out, status, y32);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
 }
 
@@ -524,7 +547,7 @@ moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
   if (T == 0) return MOE_OK;
   if (!x_host || !out_host || !ws) return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: null pointer");
   const int I_shared = ext ? ext->I_shared : 0;
-  const Layout L = forward_layout(T, d, E, I, top_k, I_shared);
+  const Layout L = forward_layout(T, d, E, I, top_k, I_shared, ext && ext->y_fp32);
   if (ws_bytes < L.total || !aligned16(ws))
     return fail(MOE_ERR_WORKSPACE, "moe_forward_host: workspace too small");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -521,7 +521,8 @@ cudaError_t launch_expert_1cta(cudaStream_t s, const char* name, ExpertKernel k,
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
                                void* h, void* y, unsigned* status,
-                               unsigned long long timeout_ns, const TokenGather* gather) {
+                               unsigned long long timeout_ns, const TokenGather* gather,
+                               bool y_fp32) {
   const int groups = offsets ? E : 1;
   const long long chunks_bound =
       offsets ? rows / kTokMax + std::min(E, rows) : (rows + kTokMax - 1) / kTokMax;
@@ -564,6 +565,7 @@ cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* off
   q.up_offset = 0;
   q.out = y;
   q.ld_out = d;
+  q.y_fp32 = y_fp32 ? 1 : 0;
   q.status = status;
   q.timeout_ns = timeout_ns;
   return launch_expert(s, offsets ? "moe_down" : "moe_shared_down", moe_down_kernel, 1, mw2, mx2,
@@ -576,7 +578,7 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
                                      const float* tscale_gate_up, const uint8_t* codes_down,
                                      const uint8_t* scales_down, const float* tscale_down,
                                      void* h, void* y, unsigned* status,
-                                     unsigned long long timeout_ns) {
+                                     unsigned long long timeout_ns, bool y_fp32) {
   const bool nv = fmt == kNv4;
   const uint64_t d_bytes = nv ? d / 2 : d;  // code bytes of a W_gate_up row
   const uint64_t i_bytes = nv ? I / 2 : I;  // code bytes of a W_down row
@@ -635,6 +637,7 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
   q.w_rows_per_group = d;
   q.out = y;
   q.ld_out = d;
+  q.y_fp32 = y_fp32 ? 1 : 0;
   q.scales = scales_down;
   q.scale_rows = static_cast<long long>(E) * d;
   q.tscale = nv ? tscale_down : nullptr;

@@ -101,6 +101,7 @@ struct Params {
   long long scale_rows;   // MXFP8 / NVFP4 weights: weight rows of the whole tensor
   const float* tscale;    // NVFP4 weights: tensor scale per expert (null: none)
   int smem_bytes;         // dynamic shared memory of the launch
+  int y_fp32;             // down: y in fp32 (else fp16, saturated at the fp16 range)
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -295,6 +296,15 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, uint32_t t_row, boo
       for (int j = 0; j < 16; ++j) {
         f[j] = __uint_as_float(v[j]) * tscale;
         if (j < nvalid) m = fmaxf(m, fabsf(f[j]));
+      }
+      if (p.y_fp32) {  // the full fp32 range, no saturation
+        float* yq = static_cast<float*>(p.out) + (size_t)(t.tok0 + c) * p.ld_out + col;
+        if (col_ok) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < nvalid) yq[(size_t)j * p.ld_out] = f[j];
+        }
+        continue;
       }
       if (m > kHalfMax) {  // rare: saturate the finite values beyond the fp16 range
         out_of_range = true;

@@ -211,7 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int n = p.T * cpr;
   for (int i = blockIdx.x * kThreads + threadIdx.x; i < n; i += gridDim.x * kThreads) {
     const int t = i / cpr;
-    combine_cols<true>(p.y, p.slot_pos, p.gates, nullptr, p.d, p.k, p.T * p.k, t,
+    combine_cols<true, __half>(p.y, p.slot_pos, p.gates, nullptr, p.d, p.k, p.T * p.k, t,
                        (i - t * cpr) * 8, p.out, p.status);
   }
 

@@ -150,12 +150,12 @@ struct TokenGather {
 // of a [rows, d] go through expert e (weights per expert: w_gate_up [2I, d],
 // w_down [d, I]).  offsets == nullptr: a single expert on all `rows` rows.
 // With `gather`, a is not read: gate_up gathers its rows (see TokenGather).
-// Writes h [rows, I] bf16 (scratch) and y [rows, d] fp16.
+// Writes h [rows, I] bf16 (scratch) and y [rows, d] fp16 (fp32 with y_fp32).
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
                                void* h, void* y, unsigned* status,
                                unsigned long long timeout_ns,
-                               const TokenGather* gather = nullptr);
+                               const TokenGather* gather = nullptr, bool y_fp32 = false);
 
 // The same with quantised expert weights (fmt 0: MXFP8, fmt 1: NVFP4):
 // codes [E, 2I, d] / [E, d, I] (one byte per value for MXFP8, two values per
@@ -169,21 +169,21 @@ cudaError_t launch_grouped_ffn_quant(cudaStream_t s, int fmt, const void* a,
                                      const float* tscale_gate_up, const uint8_t* codes_down,
                                      const uint8_t* scales_down, const float* tscale_down,
                                      void* h, void* y, unsigned* status,
-                                     unsigned long long timeout_ns);
+                                     unsigned long long timeout_ns, bool y_fp32 = false);
 
 // Grouped SwiGLU FFN for few token rows per expert (decode): warp-level
 // tensor-core MMAs, weights decoded in registers (moe_smallm.cu).  fmt 1:
 // MXFP8, 2: NVFP4 (scales and tensor scales as for launch_grouped_ffn_quant).
 // Gate_up's token rows are a[perm[pos] / div] (perm != nullptr) or a[pos];
 // d and I multiples of 256.
-// Writes h [rows, I] bf16 and y [rows, d] fp16.
+// Writes h [rows, I] bf16 and y [rows, d] fp16 (fp32 with y_fp32).
 cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
                                       const int32_t* perm, int div, const int32_t* offsets,
                                       int rows, int d, int E, int I, const void* w_gate_up,
                                       const uint8_t* scales_gate_up, const float* tscale_gate_up,
                                       const void* w_down, const uint8_t* scales_down,
                                       const float* tscale_down, void* h, void* y,
-                                      unsigned* status);
+                                      unsigned* status, bool y_fp32 = false);
 
 // The whole layer in one cooperative launch, for decode-sized batches with
 // bf16 expert weights and no shared expert (moe_fused.cu).  Requires d and I
@@ -224,9 +224,10 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
                            int32_t* slot_pos, void* x_perm, int32_t* chunk_table,
                            unsigned* status);
 
+// y (and y_shared) fp16, or fp32 with y_fp32.
 cudaError_t launch_combine(cudaStream_t s, const void* y, const int32_t* slot_pos,
                            const float* gates, const void* y_shared, int T, int d, int top_k,
-                           void* out, unsigned* status);
+                           void* out, unsigned* status, bool y_fp32 = false);
 
 // ---- MXFP8 weights (moe_mxfp8.cu)
 

@@ -199,17 +199,19 @@ __global__ void __launch_bounds__(256) moe_permute_gather_kernel(
 
 // One thread per (token, 8-column group), numbered token-major, so a warp's
 // threads take consecutive column groups and every thread has work whatever d.
+// YT: the type of y, __half or float.
+template <typename YT>
 __global__ void __launch_bounds__(kCombineThreads) moe_combine_kernel(
-    const __half* __restrict__ y, const int32_t* __restrict__ slot_pos,
-    const float* __restrict__ gates, const __half* __restrict__ y_shared, int d, int k,
-    int rows, long long groups, __nv_bfloat16* __restrict__ out, unsigned* status) {
+    const YT* __restrict__ y, const int32_t* __restrict__ slot_pos,
+    const float* __restrict__ gates, const YT* __restrict__ y_shared, int d, int k, int rows,
+    long long groups, __nv_bfloat16* __restrict__ out, unsigned* status) {
   pdl_wait_and_release();
   const long long i = static_cast<long long>(blockIdx.x) * kCombineThreads + threadIdx.x;
   if (i >= groups) return;
   const int cpr = d / 8;  // column groups per token
   const int t = static_cast<int>(i / cpr);
   const int c = static_cast<int>(i - static_cast<long long>(t) * cpr) * 8;
-  combine_cols(y, slot_pos, gates, y_shared, d, k, rows, t, c, out, status);
+  combine_cols<false, YT>(y, slot_pos, gates, y_shared, d, k, rows, t, c, out, status);
 }
 
 }  // namespace
@@ -248,12 +250,17 @@ cudaError_t launch_permute(cudaStream_t s, const int32_t* ids, const void* x, in
 
 cudaError_t launch_combine(cudaStream_t s, const void* y, const int32_t* slot_pos,
                            const float* gates, const void* y_shared, int T, int d, int top_k,
-                           void* out, unsigned* status) {
+                           void* out, unsigned* status, bool y_fp32) {
   const long long groups = static_cast<long long>(T) * (d / 8);
   const long long grid = (groups + kCombineThreads - 1) / kCombineThreads;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   KernelScope scope(s, "moe_combine");
-  return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(grid)),
+  if (y_fp32)
+    return launch_kernel(moe_combine_kernel<float>, dim3(static_cast<unsigned>(grid)),
+                         dim3(kCombineThreads), 0, s, static_cast<const float*>(y), slot_pos,
+                         gates, static_cast<const float*>(y_shared), d, top_k, T * top_k,
+                         groups, static_cast<__nv_bfloat16*>(out), status);
+  return launch_kernel(moe_combine_kernel<__half>, dim3(static_cast<unsigned>(grid)),
                        dim3(kCombineThreads), 0, s, static_cast<const __half*>(y), slot_pos,
                        gates, static_cast<const __half*>(y_shared), d, top_k, T * top_k, groups,
                        static_cast<__nv_bfloat16*>(out), status);

@@ -131,17 +131,41 @@ __device__ __forceinline__ void permute_small_block(const int32_t* ids, int n, i
   __syncthreads();
 }
 
-// One thread: 8 columns of one token, all k slot rows of fp16 y loaded before
-// the sum (k independent 16-byte loads in flight per thread), then the fp32
-// sum in slot order and one bf16 rounding.
+// One thread: 8 columns of one token, all k slot rows of y loaded before the
+// sum (k independent 16-byte loads in flight per thread, two each for fp32
+// y), then the fp32 sum in slot order and one bf16 rounding.
 constexpr int kCombineThreads = 256;
 
-// Columns c .. c + 7 of token t (c a multiple of 8, c < d).
-template <bool COHERENT = false>
-__device__ __forceinline__ void combine_cols(const __half* y, const int32_t* slot_pos,
-                                             const float* gates, const __half* y_shared, int d,
+// 8 columns of y (fp16 or fp32) as floats, from the 16-byte pieces raw[].
+template <typename YT>
+__device__ __forceinline__ void y8_to_float(const uint4* raw, float (&f)[8]) {
+  if constexpr (sizeof(YT) == 4) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      f[4 * u + 0] = __uint_as_float(raw[u].x);
+      f[4 * u + 1] = __uint_as_float(raw[u].y);
+      f[4 * u + 2] = __uint_as_float(raw[u].z);
+      f[4 * u + 3] = __uint_as_float(raw[u].w);
+    }
+  } else {
+    const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = p.x;
+      f[2 * i + 1] = p.y;
+    }
+  }
+}
+
+// Columns c .. c + 7 of token t (c a multiple of 8, c < d).  YT: the type
+// of y and y_shared, __half or float.
+template <bool COHERENT = false, typename YT = __half>
+__device__ __forceinline__ void combine_cols(const YT* y, const int32_t* slot_pos,
+                                             const float* gates, const YT* y_shared, int d,
                                              int k, int rows, int t, int c,
                                              __nv_bfloat16* __restrict__ out, unsigned* status) {
+  constexpr int kPieces = sizeof(YT) == 4 ? 2 : 1;  // 16-byte loads per row
   int pos[kMaxTopK];
   float g[kMaxTopK];
   bool bad = false;
@@ -160,33 +184,33 @@ __device__ __forceinline__ void combine_cols(const __half* y, const int32_t* slo
     }
   }
   if (bad && c == 0) atomicOr(status, kStatusDeviceCheck);
-  // eight fp16 columns per thread: one 16-byte load per expert row
-  uint4 v[kMaxTopK];
+  // all k rows' loads first
+  uint4 v[kMaxTopK][kPieces];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j)
-    if (j < k) v[j] = ld_in<COHERENT>(reinterpret_cast<const uint4*>(y + (size_t)pos[j] * d + c));
+    if (j < k)
+#pragma unroll
+      for (int u = 0; u < kPieces; ++u)
+        v[j][u] = ld_in<COHERENT>(reinterpret_cast<const uint4*>(y + (size_t)pos[j] * d + c) + u);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
     if (j < k) {
-      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      float f[8];
+      y8_to_float<YT>(v[j], f);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-        acc[2 * i] = fmaf(g[j], f.x, acc[2 * i]);
-        acc[2 * i + 1] = fmaf(g[j], f.y, acc[2 * i + 1]);
-      }
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(g[j], f[i], acc[i]);
     }
   }
   if (y_shared) {
-    const uint4 a = ld_in<COHERENT>(reinterpret_cast<const uint4*>(y_shared + (size_t)t * d + c));
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint4 a[kPieces];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-      acc[2 * i] += f.x;
-      acc[2 * i + 1] += f.y;
-    }
+    for (int u = 0; u < kPieces; ++u)
+      a[u] = ld_in<COHERENT>(reinterpret_cast<const uint4*>(y_shared + (size_t)t * d + c) + u);
+    float f[8];
+    y8_to_float<YT>(a, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += f[i];
   }
   uint4 o;
   o.x = pack_bf16x2(acc[0], acc[1]);

@@ -89,7 +89,7 @@ cudaError_t sm_ffn(cudaStream_t s, const char* gu_name, const char* dn_name, con
                    const int32_t* perm, int div, const int32_t* offsets, int rows, int d, int E,
                    int I, const uint8_t* w_gate_up, const uint8_t* s_gate_up,
                    const float* t_gate_up, const uint8_t* w_down, const uint8_t* s_down,
-                   const float* t_down, void* h, void* y, unsigned* status) {
+                   const float* t_down, void* h, void* y, unsigned* status, bool y_fp32) {
   using F = SmF<FMT>;
   if (d % sm_chunk_k<FMT>() || I % sm_chunk_k<FMT>()) return cudaErrorInvalidValue;
   SmParams p{};
@@ -130,6 +130,7 @@ cudaError_t sm_ffn(cudaStream_t s, const char* gu_name, const char* dn_name, con
   q.div = 1;
   q.out = y;
   q.ld_out = d;
+  q.y_fp32 = y_fp32 ? 1 : 0;
   return sm_launch<FMT, kSmDown>(s, dn_name, q);
 }
 
@@ -141,7 +142,7 @@ cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
                                       const uint8_t* scales_gate_up, const float* tscale_gate_up,
                                       const void* w_down, const uint8_t* scales_down,
                                       const float* tscale_down, void* h, void* y,
-                                      unsigned* status) {
+                                      unsigned* status, bool y_fp32) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   const uint8_t* wg = static_cast<const uint8_t*>(w_gate_up);
   const uint8_t* wd = static_cast<const uint8_t*>(w_down);
@@ -149,11 +150,11 @@ cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
     case 1:
       return sm_ffn<kSmMx8>(s, "moe_gate_up_swiglu_mxfp8_smallm", "moe_down_mxfp8_smallm", a,
                             perm, div, offsets, rows, d, E, I, wg, scales_gate_up, nullptr, wd,
-                            scales_down, nullptr, h, y, status);
+                            scales_down, nullptr, h, y, status, y_fp32);
     case 2:
       return sm_ffn<kSmNv4>(s, "moe_gate_up_swiglu_nvfp4_smallm", "moe_down_nvfp4_smallm", a,
                             perm, div, offsets, rows, d, E, I, wg, scales_gate_up, tscale_gate_up,
-                            wd, scales_down, tscale_down, h, y, status);
+                            wd, scales_down, tscale_down, h, y, status, y_fp32);
   }
   return cudaErrorInvalidValue;
 }

@@ -71,6 +71,7 @@ struct SmParams {
   int div;
   void* out;                 // gate_up: h bf16 [rows, I]; down: y fp16 [rows, d]
   int ld_out;
+  int y_fp32;                // down: y in fp32 (else fp16, saturated at the fp16 range)
   unsigned* status;
 };
 
@@ -412,6 +413,10 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             float v = acc[0][2 * rr + hlf] * ts;
+            if (p.y_fp32) {  // the full fp32 range, no saturation
+              static_cast<float*>(p.out)[orow + t.col + 8 * rr] = v;
+              continue;
+            }
             if (fabsf(v) > kSmHalfMax) {
               range_flag = true;
               if (fabsf(v) < INFINITY) v = copysignf(kSmHalfMax, v);

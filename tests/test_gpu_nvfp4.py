@@ -169,3 +169,29 @@ def test_nvfp4_zero_tokens(moe):
                                moe.moe_nvfp4_quantize(p["w_down"]), 2)
     torch.cuda.synchronize()
     assert out.shape == (0, 256)
+
+
+@pytest.mark.parametrize("T,d,E,k,I,Is", [(32, 512, 32, 8, 256, 0),     # small-M kernels
+                                          (600, 512, 8, 4, 256, 128)])  # tile kernels, shared expert
+def test_forward_nvfp4_fp32_y(moe, T, d, E, k, I, Is):
+    """y kept in fp32 (moe_forward_ext_t.y_fp32) with NVFP4 weights."""
+    w = W.Workload("nvfp432", T, d, E, k, I, I_shared=Is, seed=T + 3)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    q_gu = moe.moe_nvfp4_quantize(p["w_gate_up"])
+    q_d = moe.moe_nvfp4_quantize(p["w_down"])
+    ws = moe.new_workspace(T, d, E, I, k, Is, y_fp32=True)
+    out = moe.moe_forward_nvfp4(x, p["w_router"], q_gu, q_d, k, ws=ws, y_fp32=True,
+                              w_gate_up_shared=p["w_gate_up_shared"],
+                              w_down_shared=p["w_down_shared"])
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, T, d, E, I, k, Is, y_fp32=True)
+    ref = oracle.forward(
+        W.to_bits(x), W.to_bits(p["w_router"]), _dequantised(p["w_gate_up"]), _dequantised(p["w_down"]), k,
+        w_gate_up_shared=None if p["w_gate_up_shared"] is None else W.to_bits(p["w_gate_up_shared"]),
+        w_down_shared=None if p["w_down_shared"] is None else W.to_bits(p["w_down_shared"]))
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ref["ids"], ref["gates"], ref["logits"], k)
+    assert differ.size == 0
+    assert_layer_close(f64(v["y"]), ref["y"], "y")
+    assert_layer_close(f64(out), ref["out"], "out")

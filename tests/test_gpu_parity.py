@@ -231,6 +231,51 @@ def test_forward(moe, T, d, E, k, I, Is, zipf):
     assert_layer_close(f64(out), ref["out"], "out")
 
 
+FP32_Y_CASES = [
+    # T, d, E, k, I, I_shared, zipf
+    (300, 512, 16, 4, 384, 0, True),      # tile GEMMs on x_perm
+    (48, 256, 8, 2, 128, 128, False),     # decode-sized (rows gathered from x), shared expert
+]
+
+
+@pytest.mark.parametrize("T,d,E,k,I,Is,zipf", FP32_Y_CASES)
+def test_forward_fp32_y(moe, T, d, E, k, I, Is, zipf):
+    """y kept in fp32 (moe_forward_ext_t.y_fp32): the same routing, y and out
+    within the layer tolerance of the oracle, and out close to the fp16-y
+    layer's (the difference is fp16 rounding of y, relative to the largest
+    output: a sum that nearly cancels may differ by more than its own ulp)."""
+    w, x, p = _layer(T, d, E, k, I, I_shared=Is, zipf=zipf, seed=T + E + 1)
+    kw = dict(router_bias=p["router_bias"], w_gate_up_shared=p["w_gate_up_shared"],
+              w_down_shared=p["w_down_shared"])
+    ws = moe.new_workspace(T, d, E, I, k, Is, y_fp32=True)
+    assert ws.numel() > moe.moe_workspace_size(T, d, E, I, k, Is)
+    out = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], k, ws=ws, y_fp32=True,
+                          **kw)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, T, d, E, I, k, Is, y_fp32=True)
+    assert v["y"].dtype == torch.float32
+    ref = _oracle_forward(x, p, k)
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ref["ids"], ref["gates"], ref["logits"], k)
+    assert differ.size == 0
+    assert_layer_close(f64(v["y"]), ref["y"], "y")
+    assert_layer_close(f64(out), ref["out"], "out")
+    out16 = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], k, **kw)
+    torch.cuda.synchronize()
+    a, b = f64(out), f64(out16)
+    assert np.abs(a - b).max() <= np.abs(b).max() * 2.0**-6  # about one bf16 ulp at the top
+
+
+def test_forward_fp32_y_needs_its_workspace(moe):
+    w, x, p = _layer(64, 256, 8, 2, 128, seed=3)
+    with pytest.raises(RuntimeError):
+        moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], 2,
+                        ws=moe.new_workspace(64, 256, 8, 128, 2), y_fp32=True)
+    with pytest.raises(RuntimeError):
+        moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], 2, y_fp32=True,
+                        single_launch=True)
+
+
 def test_forward_bias_selection_only(moe):
     T, d, E, k, I = 250, 512, 16, 4, 256
     w, x, p = _layer(T, d, E, k, I, zipf=True, seed=21)

@@ -105,3 +105,32 @@ def test_y_outside_fp16_range_saturates_and_is_flagged(moe):
     assert_layer_close(got[lo], ref[lo], "y inside the fp16 range")
     moe.moe_expert_ffn(x_perm, offsets, p["w_gate_up"], p["w_down"], ws=ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
+
+
+def test_y_beyond_fp16_range_with_fp32_y(moe):
+    """With y kept in fp32 an expert output beyond the fp16 range is neither
+    saturated nor flagged: the whole layer with W_down scaled by a power of
+    two (max |y| in [4, 8) x 65504) matches the oracle on the scaled weights,
+    while the fp16-y layer reports MOE_ERR_RANGE."""
+    import numpy as np
+    import oracle
+    from tests.gpu_util import ExpertsOnHost, assert_layer_close, f64
+    w = W.Workload("r32", 48, 256, 4, 2, 128, seed=9)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    ref1 = oracle.forward(W.to_bits(x), W.to_bits(p["w_router"]), ExpertsOnHost(p["w_gate_up"]),
+                          ExpertsOnHost(p["w_down"]), 2)
+    s = 2.0 ** int(np.ceil(np.log2(4 * 65504 / np.abs(ref1["y"]).max())))
+    wd = (p["w_down"] * s).contiguous()
+    ref = oracle.forward(W.to_bits(x), W.to_bits(p["w_router"]), ExpertsOnHost(p["w_gate_up"]),
+                         ExpertsOnHost(wd), 2)
+    assert np.abs(ref["y"]).max() > 65504
+    ws = moe.new_workspace(48, 256, 4, 128, 2, y_fp32=True)
+    out = moe.moe_forward(x, p["w_router"], p["w_gate_up"], wd, 2, ws=ws, y_fp32=True)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, 48, 256, 4, 128, 2, y_fp32=True)
+    assert_layer_close(f64(v["y"]), ref["y"], "fp32 y beyond the fp16 range")
+    assert_layer_close(f64(out), ref["out"], "out")
+    ws16 = moe.new_workspace(48, 256, 4, 128, 2)
+    moe.moe_forward(x, p["w_router"], p["w_gate_up"], wd, 2, ws=ws16)
+    assert moe.moe_get_device_status(ws16) == moe.MOE_ERR_RANGE
