@@ -207,6 +207,11 @@ FORWARD_CASES = [
     (1, 512, 32, 8, 256, 0, False),
     (250, 1024, 64, 6, 256, 256, False),  # with an always-on shared expert
     (130, 768, 256, 8, 128, 128, False),  # 256 experts, most with zero or one row
+    # more than 4096 rows and 128 per expert: grouping by count and scatter kernels,
+    # x_perm written by the gather kernel
+    (1500, 512, 16, 4, 384, 0, True),     # biased router: hot experts with many chunks
+    (2100, 256, 8, 2, 128, 0, False),     # 4200 rows: a last 16-row unit of 8 rows
+    (1100, 1024, 64, 8, 256, 256, False),  # with a shared expert
 ]
 
 
@@ -227,6 +232,8 @@ def test_forward(moe, T, d, E, k, I, Is, zipf):
     assert np.array_equal(v["expert_offsets"].cpu().numpy(), ref["offsets"])
     assert np.array_equal(v["perm"].cpu().numpy(), ref["perm"])
     assert np.array_equal(v["slot_pos"].cpu().numpy(), ref["slot_pos"])
+    if T * k > 128 * E:  # x_perm written (fewer rows: gate_up gathers them from x itself)
+        assert torch.equal(v["x_perm"], x[v["perm"].long() // k])
     assert_layer_close(f64(v["y"]), ref["y"], "y")
     assert_layer_close(f64(out), ref["out"], "out")
 
