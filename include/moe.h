@@ -32,7 +32,9 @@
  *     A failed launch returns MOE_ERR_CUDA (details: moe_last_error()).
  *   - `ws` is a device workspace of at least moe_workspace_size() bytes for
  *     the shapes in use; its first 256 bytes hold a sticky device status word
- *     that must start at zero (moe_workspace_init).  Kernels record there what
+ *     and the expert GEMMs' tile counters (which every launch leaves at zero
+ *     again), and must start at zero (moe_workspace_init); calls that share
+ *     one workspace must run one after another.  Kernels record there what
  *     they find on the device: an expert id out of range, inconsistent
  *     offsets or slot positions (MOE_ERR_DEVICE_CHECK), a wait that gave up
  *     (MOE_ERR_TIMEOUT), an expert output outside fp16 range (MOE_ERR_RANGE).

@@ -331,7 +331,8 @@ moe_status_t moe_expert_ffn(const moe_bf16* x_perm, const int32_t* expert_offset
   void* h = static_cast<char*>(ws) + kAlign;
   cudaError_t e = launch_grouped_ffn(reinterpret_cast<cudaStream_t>(stream), x_perm,
                                      expert_offsets, rows, d, E, I, w_gate_up, w_down, h, y,
-                                     status_word(ws), g_timeout_ns.load());
+                                     status_word(ws), g_timeout_ns.load(), nullptr, false,
+                                     status_word(ws));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "expert FFN launch");
 }
 
@@ -472,13 +473,13 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
                                  mx->scales_down, mx->tscale_down, h, y, status, tmo, y32);
   else
     e = launch_grouped_ffn(s, x_perm, offsets, rows, d, E, I, w_gate_up, w_down, h, y, status,
-                           tmo, gather_rows ? &gather : nullptr, y32);
+                           tmo, gather_rows ? &gather : nullptr, y32, status);
   if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
   void* y_shared = nullptr;
   if (I_shared) {
     y_shared = w + L.y_shared;
     e = launch_grouped_ffn(s, x, nullptr, T, d, 1, I_shared, wgu_s, wd_s, w + L.h_shared,
-                           y_shared, status, tmo, nullptr, y32);
+                           y_shared, status, tmo, nullptr, y32, status);
     if (e != cudaSuccess) return cuda_fail(e, "shared expert launch");
   }
   e = launch_combine(s, y, slot_pos, gates, y_shared, T, d, top_k, out, status, y32);

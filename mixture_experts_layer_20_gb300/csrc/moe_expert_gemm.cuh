@@ -28,7 +28,11 @@
 // tile's tensor work.  The stages are sized for the launch's largest chunk:
 // 3 fit in shared memory for 256-token chunks, 4 when no chunk exceeds 192.
 // Tiles are ordered (expert, slab, chunk): pairs running at the same time
-// read the same weight slab, which is then read from HBM once.
+// read the same weight slab, which is then read from HBM once.  Pair p takes
+// tiles p, p + pairs, ...; or, for decode-sized layers, the pairs take them
+// in order from a counter in global memory (a scheduler warp of the leader
+// fetches the next indices and publishes them to both CTAs of its pair), so
+// a pair that streams its weights faster takes more tiles.
 //
 // gate_up: rank r of the pair holds the gate rows [128 s + 64 r, +64) of slab
 // s and the matching up rows, interleaved in groups of 16 (A rows 32 j .. 32 j
@@ -39,7 +43,8 @@
 // a warp's lanes are consecutive output columns, so every store of one token
 // row is contiguous.
 //
-// Roles, per CTA (192 threads): warp 0 loads both operands with TMA into its
+// Roles, per CTA (192 threads, 224 with the scheduler warp 6 of the dynamic
+// schedule): warp 0 loads both operands with TMA into its
 // own shared memory, counting the bytes of both CTAs on the leader's full
 // barrier; warp 1 owns the tensor memory (512 columns: two accumulators of up
 // to 256 fp32 columns) and, in the leader, one of its threads issues the MMAs
@@ -73,6 +78,10 @@ constexpr int kUnit = 16;                          // token rows: chunks are mul
 constexpr int kABytes = kWRows * kBK * 2;          // 16 KB per K box
 constexpr int kMinStages = 3;                      // 3 stages of the largest (256-token) chunks
 constexpr int kThreads = 192;
+// With the dynamic schedule a seventh warp fetches the tiles (kSchedAhead at
+// most ahead of the producer).
+constexpr int kThreadsSched = kThreads + 32;
+constexpr int kSchedAhead = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kEpiArrivals = 8;               // 4 epilogue warps x 2 CTAs
@@ -102,6 +111,11 @@ struct Params {
   const float* tscale;    // NVFP4 weights: tensor scale per expert (null: none)
   int smem_bytes;         // dynamic shared memory of the launch
   int y_fp32;             // down: y in fp32 (else fp16, saturated at the fp16 range)
+  // Dynamic schedule (null: tile pair + i * pairs for the i-th tile of a
+  // pair): the leader of each pair takes its next tile from *tile_ctr, in
+  // order; the last CTA to leave (*exit_ctr) resets both to zero.
+  unsigned* tile_ctr;
+  unsigned* exit_ctr;
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -392,6 +406,16 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   // full barrier instead of decoding the tile itself (it is at most
   // kMaxStagesAny stages, so as many tiles, behind the producer).
   __shared__ int s_tile_n[kTileRing];
+  // Dynamic schedule: tile index by tile sequence number mod kTileRing (-1:
+  // no more tiles), written in both CTAs by the leader's scheduler warp
+  // before it arrives on s_tbar of that slot (locally and remotely); every
+  // other role of both CTAs waits there.  The scheduler stays at most
+  // kSchedAhead tiles ahead of the leader's producer (s_prod_next: tiles the
+  // producer has taken) and at most kMaxStagesAny + 3 tiles separate the
+  // producer from the slowest reader, so a slot is read before it is reused.
+  __shared__ int s_tau[kTileRing];
+  __shared__ alignas(8) uint64_t s_tbar[kTileRing];
+  __shared__ int s_prod_next;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -415,6 +439,7 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   const uint32_t tempty_bar = smem_u32(&s_bar[2 * kMaxStagesAny + 2]);
   const uint32_t drain_bar = smem_u32(&s_bar[2 * kMaxStagesAny + 4]);
   const uint32_t empty_hi = smem_u32(&s_bar[2 * kMaxStagesAny + 5]);
+  const uint32_t tbar = smem_u32(&s_tbar[0]);
   auto empty_box = [&](int b, int st) {
     return b == 0 ? empty_bar + 8 * st : empty_hi + 8 * ((b - 1) * kMaxStagesAny + st);
   };
@@ -429,6 +454,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       mbar_init(tempty_bar + 8 * a, kEpiArrivals);
     }
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < kTileRing; ++i) mbar_init(tbar + 8 * i, 1);
+    s_prod_next = 0;
     s_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap_w);
@@ -453,6 +480,25 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   const int total_tiles = static_cast<int>(sched.n_all);
   const int num_kb = p.K / kBK;                   // 64-wide K boxes
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
+  const bool dyn = !FUSED && p.tile_ctr != nullptr;
+  // Tile of sequence number `seq` of this pair (one thread): the static
+  // stride, or the index the leader's producer published; -1 past the last
+  // tile, or once a wait has given up.
+  auto tile_at = [&](int seq) -> int {
+    if (!dyn) {
+      const long long t = pair + static_cast<long long>(seq) * num_pairs;
+      return t < total_tiles ? static_cast<int>(t) : -1;
+    }
+    const int slot = seq % kTileRing;
+    if (!mbar_wait_cluster(tbar + 8 * slot, (seq / kTileRing) & 1, wc)) return -1;
+    return s_tau[slot];
+  };
+  // The same for a whole warp (lane 0 waits).
+  auto tile_at_warp = [&](int seq) -> int {
+    int t = 0;
+    if (lane == 0) t = tile_at(seq);
+    return __shfl_sync(0xffffffffu, t, 0);
+  };
   const int num_ks = (num_kb + kSub - 1) / kSub;  // pipeline stages per tile
   // Stage geometry: a stage holds kSub K boxes of the weights and of the
   // largest token-chunk half of this launch, so smaller chunks leave room for
@@ -479,7 +525,10 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     int seq = 0;
     const uint32_t full_leader = mapa_shared(full_bar, 0);
     if (FUSED) fence_proxy_async_global();  // earlier phases' generic stores before this TMA
-    for (int tau = pair; tau < total_tiles && ok; tau += num_pairs, ++seq) {
+    for (;; ++seq) {
+      const int tau = ok ? tile_at_warp(seq) : -1;
+      if (tau < 0) break;
+      if (dyn && leader && lane == 0) *static_cast<volatile int*>(&s_prod_next) = seq + 1;
       const Tile t = decode_tile(tau, sched);
       const int half = t.n / 2;  // token rows per CTA: 8, 16, ..., 128
       const CUtensorMap* tmap_x = &tx.m[t.n / kUnit - 1];
@@ -576,8 +625,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      int seq = 0;
-      for (int tau = pair; tau < total_tiles && ok; tau += num_pairs, ++seq) {
+      for (int seq = 0; ok; ++seq) {
+        if (tile_at(seq) < 0) break;
         if (!mbar_wait(tempty_bar + 8 * acc, acc_phase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;  // TMEM column c: chunk token c
@@ -618,6 +667,35 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
       // follower: the leader's last commit also arrives here once its MMAs are done
       mbar_wait_drain(drain_bar, 0, p.status);
     }
+  } else if (warp >= kThreads / 32) {
+    // ---------------- scheduler (dynamic schedule, leader, lane 0): takes
+    // the next tile from the global counter and publishes it to both CTAs.
+    // Its own thread waits out the atomic's round trip, so the producer's
+    // barrier arrives (release operations) never wait for it.
+    if (dyn && leader && lane == 0) {
+      for (int seq = 0;; ++seq) {
+        bool go = !*wc.abort_flag;
+        if (go && seq >= *static_cast<volatile int*>(&s_prod_next) + kSchedAhead) {
+          const unsigned long long t0 = globaltimer_ns();
+          while (seq >= *static_cast<volatile int*>(&s_prod_next) + kSchedAhead) {
+            if (*wc.abort_flag) { go = false; break; }
+            if (globaltimer_ns() - t0 > wc.timeout_ns) { go = give_up(wc); break; }
+            __nanosleep(64);
+          }
+        }
+        int v = -1;
+        if (go) {
+          const unsigned got = atomicAdd(p.tile_ctr, 1u);
+          if (got < static_cast<unsigned>(total_tiles)) v = static_cast<int>(got);
+        }
+        const int slot = seq % kTileRing;
+        s_tau[slot] = v;
+        st_shared_cluster_u32(mapa_shared(smem_u32(&s_tau[slot]), 1), static_cast<uint32_t>(v));
+        mbar_arrive(tbar + 8 * slot);
+        mbar_arrive_cluster(mapa_shared(tbar + 8 * slot, 1));
+        if (v < 0) break;
+      }
+    }
   } else {
     // ---------------- epilogue: warps 2..5, TMEM lanes 32 (warp % 4) + lane
     const int q = warp & 3;
@@ -625,8 +703,11 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     int acc = 0;
     uint32_t acc_phase = 0;
     // After a wait gives up, the loop still runs to the end (later waits fail
-    // at once) with its stores switched off.
-    for (int tau = pair; tau < total_tiles; tau += num_pairs) {
+    // at once; with the dynamic schedule, to the last tile published) with its
+    // stores switched off.
+    for (int seq = 0;; ++seq) {
+      const int tau = tile_at_warp(seq);
+      if (tau < 0) break;
       const Tile t = decode_tile(tau, sched);
       const bool live = __all_sync(0xffffffffu, mbar_wait(tfull_bar + 8 * acc, acc_phase, wc));
       tc_fence_after_sync();
@@ -650,6 +731,16 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  // Dynamic schedule: the last CTA to leave (every CTA has taken its last
+  // tile by now) resets the counters for the next launch.
+  if (dyn && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.exit_ctr, 1u) == gridDim.x - 1) {
+      atomicExch(p.tile_ctr, 0u);
+      atomicExch(p.exit_ctr, 0u);
+      __threadfence();
+    }
   }
 }
 

@@ -35,6 +35,11 @@ int router_ranges_written(int T, int d, int E);
 constexpr int kBarrierCountWord = 16;
 constexpr int kBarrierGenWord = 32;
 constexpr int kExitCountWord = 48;
+// The bf16 expert GEMMs' tile counter and exit counter (dynamic schedule):
+// the next tile to hand out, and the CTAs that have left (the last one resets
+// both to zero for the next launch).
+constexpr int kTileCounterWord = 24;
+constexpr int kTileExitWord = 40;
 
 // Bits of the workspace's device status word.
 constexpr unsigned kStatusTimeout = 1u;
@@ -151,11 +156,15 @@ struct TokenGather {
 // w_down [d, I]).  offsets == nullptr: a single expert on all `rows` rows.
 // With `gather`, a is not read: gate_up gathers its rows (see TokenGather).
 // Writes h [rows, I] bf16 (scratch) and y [rows, d] fp16 (fp32 with y_fp32).
+// sched_words: the workspace's status region (its tile and exit counters, at
+// zero); the kernels then hand their tiles out in order through the counter
+// instead of by a static stride.  Null: the static stride.
 cudaError_t launch_grouped_ffn(cudaStream_t s, const void* a, const int32_t* offsets, int rows,
                                int d, int E, int I, const void* w_gate_up, const void* w_down,
                                void* h, void* y, unsigned* status,
                                unsigned long long timeout_ns,
-                               const TokenGather* gather = nullptr, bool y_fp32 = false);
+                               const TokenGather* gather = nullptr, bool y_fp32 = false,
+                               unsigned* sched_words = nullptr);
 
 // The same with quantised expert weights (fmt 0: MXFP8, fmt 1: NVFP4):
 // codes [E, 2I, d] / [E, d, I] (one byte per value for MXFP8, two values per
