@@ -62,11 +62,22 @@ def test_bad_slot_positions_are_flagged(moe):
     assert out[0].float().eq(1.0).all()
 
 
-def test_wait_timeout_is_reported_and_recoverable(moe):
-    w, x, p = _layer()
+def _control_words_clear(ws):
+    """Words 1.. of the status region: the expert GEMMs' tile counters, which
+    every launch leaves at zero (moe.h), and the single-launch layer's
+    counters, untouched here."""
+    return bool(ws[:256].view(torch.int32)[1:].eq(0).all())
+
+
+# 75 rows per expert: the GEMMs' static tile stride; 8: decode-sized, tiles
+# taken from the workspace's counter by a scheduler warp.
+@pytest.mark.parametrize("T", [300, 32])
+def test_wait_timeout_is_reported_and_recoverable(moe, T):
+    w, x, p = _layer(T=T)
     ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k)
     ref = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], w.top_k, ws=ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    assert _control_words_clear(ws)
     try:
         moe.moe_set_wait_timeout_ns(1)
         moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], w.top_k, ws=ws)
@@ -74,9 +85,11 @@ def test_wait_timeout_is_reported_and_recoverable(moe):
     finally:
         moe.moe_set_wait_timeout_ns(0)
     assert st == moe.MOE_ERR_TIMEOUT
+    assert _control_words_clear(ws)   # also after every wait gave up
     again = moe.moe_forward(x, p["w_router"], p["w_gate_up"], p["w_down"], w.top_k, ws=ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
     assert torch.equal(again, ref)
+    assert _control_words_clear(ws)
 
 
 def test_y_outside_fp16_range_saturates_and_is_flagged(moe):
