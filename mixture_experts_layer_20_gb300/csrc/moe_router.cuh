@@ -71,7 +71,10 @@ __device__ __forceinline__ void topk_warp(const float* partial, int splits, int 
         const float y = gl[b]; gl[b] = gl[b + 1]; gl[b + 1] = y;
       }
 
-  // k rounds: the warp's largest head wins; its lane pops it
+  // k rounds: the warp's largest head wins; its lane pops it.  The 64-bit
+  // maximum is taken as two 32-bit warp reductions: the largest high word
+  // (the logit's order), then the largest low word among the lanes holding
+  // it (the lowest expert index).
   unsigned long long sel[kMaxTopK];
   float sel_g[kMaxTopK];
 #pragma unroll
@@ -79,12 +82,11 @@ __device__ __forceinline__ void topk_warp(const float* partial, int splits, int 
     sel[j] = 0ull;
     sel_g[j] = 0.0f;
     if (j < k) {
-      unsigned long long best = key[0];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-        best = o > best ? o : best;
-      }
+      const uint32_t hi = static_cast<uint32_t>(key[0] >> 32);
+      const uint32_t m_hi = __reduce_max_sync(0xffffffffu, hi);
+      const uint32_t m_lo =
+          __reduce_max_sync(0xffffffffu, hi == m_hi ? static_cast<uint32_t>(key[0]) : 0u);
+      const unsigned long long best = (static_cast<unsigned long long>(m_hi) << 32) | m_lo;
       const unsigned owner = __ballot_sync(0xffffffffu, key[0] == best);
       sel[j] = best;
       sel_g[j] = __shfl_sync(0xffffffffu, gl[0], __ffs(owner) - 1);
