@@ -480,7 +480,8 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
   const int total_tiles = static_cast<int>(sched.n_all);
   const int num_kb = p.K / kBK;                   // 64-wide K boxes
   const WaitCtx wc{p.timeout_ns, p.status, &s_abort};
-  const bool dyn = !FUSED && p.tile_ctr != nullptr;
+  // (the scheduler warp must exist: launched with kThreadsSched threads)
+  const bool dyn = !FUSED && p.tile_ctr != nullptr && blockDim.x >= kThreadsSched;
   // Tile of sequence number `seq` of this pair (one thread): the static
   // stride, or the index the leader's producer published; -1 past the last
   // tile, or once a wait has given up.
