@@ -116,6 +116,7 @@ struct Params {
   // order; the last CTA to leave (*exit_ctr) resets both to zero.
   unsigned* tile_ctr;
   unsigned* exit_ctr;
+  int prefetch_boxes;     // dynamic schedule: K boxes of weights to warm L2 with before the wait
   unsigned* status;
   unsigned long long timeout_ns;
 };
@@ -467,6 +468,27 @@ __device__ __forceinline__ void expert_gemm_body(const CUtensorMap& tmap_w, cons
     tmem_relinquish_pair();
   }
 
+  // Decode-sized launches: the weights do not depend on the kernels before
+  // this one (routing, grouping), so while they finish, each CTA warms L2
+  // with the first kPrefetchBoxes K boxes of its half of the tile its pair
+  // would take first if every expert had tokens (at decode nearly all do);
+  // a wrong guess costs only the bandwidth.
+  if (!FUSED && p.tile_ctr != nullptr && p.prefetch_boxes > 0 && threadIdx.x == 0) {
+    const int e = pair / p.slabs, slab = pair - (pair / p.slabs) * p.slabs;
+    // whole boxes inside the weight tensor only (a partial last slab is skipped)
+    const bool inside = KIND == kGateUp ? (slab * 128 + static_cast<int>(rank) * 64 + 64) * 2 <= p.w_rows_per_group
+                                        : slab * 256 + static_cast<int>(rank) * 128 + 128 <= p.w_rows_per_group;
+    if (e < p.groups && inside) {
+      const int nb = min(p.prefetch_boxes, p.K / kBK);
+      for (int kb = 0; kb < nb; ++kb) {
+        if (KIND == kGateUp)
+          tma_prefetch_l2_5d(&tmap_w, kb * kBK, 0, 0, (slab * 128 + static_cast<int>(rank) * 64) / 16, e);
+        else
+          tma_prefetch_l2_2d(&tmap_w, kb * kBK,
+                             e * p.w_rows_per_group + slab * 256 + static_cast<int>(rank) * 128);
+      }
+    }
+  }
   pdl_wait_and_release();
 
   build_schedule<FUSED>(p, s_off, s_pre, &s_half_max, warp, lane, kTokMax);
