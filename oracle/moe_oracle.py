@@ -40,6 +40,13 @@ What the layer computes, and where each step comes from:
   clamped to E4M3's largest finite value.  A layer with MXFP8 weights is the
   layer computed with the dequantised weights (codes times scales), which the
   oracle obtains with mxfp8_quantize / mxfp8_dequantize.
+* MXFP8 activations (``act_mxfp8``).  The same section says micro-scaling is
+  what the tensor cores need for the best throughput; the deployed format
+  then also carries the activations as MXFP8.  The pages do not say which
+  activations or where; the plainest reading, taken here: each expert GEMM's
+  token operand is quantised like its weights, along the reduction axis in
+  runs of 32 -- x before gate_up, and h (after its rounding to bf16) before
+  down -- and the GEMM is then the exact product of the dequantised values.
 * NVFP4 expert weights ('PagedAttention, speculative decoding, MoE and
   Blackwell', section 3: two-level micro-scaling, blocks of 16 values each
   with its own FP8 scale, plus one FP32 scale for the whole tensor; 'Hosting
@@ -92,6 +99,7 @@ __all__ = [
     "round_to_e4m3",
     "mxfp8_quantize",
     "mxfp8_dequantize",
+    "mxfp8_round_rows",
     "e2m1_values",
     "round_to_e2m1",
     "nvfp4_quantize",
@@ -378,25 +386,37 @@ def _weight_values(w) -> np.ndarray:
     return w if w.dtype == np.float64 else bf16_bits_to_f64(w)
 
 
-def swiglu_ffn(x_rows, w_gate_up_bits, w_down_bits) -> np.ndarray:
+def mxfp8_round_rows(v) -> np.ndarray:
+    """v quantised to MXFP8 along its last axis and dequantised: the values an
+    MXFP8 activation operand stands for."""
+    codes, scales = mxfp8_quantize(v)
+    return mxfp8_dequantize(codes, scales)
+
+
+def swiglu_ffn(x_rows, w_gate_up_bits, w_down_bits, act_mxfp8: bool = False) -> np.ndarray:
     """One expert on a block of rows: fp64, with h rounded once to bf16.
 
     x_rows: [m, d] fp64.  w_gate_up: [2I, d] bf16 bits (or fp64 values), rows
     [0, I) = gate and rows [I, 2I) = up.  w_down: [d, I] likewise.  Returns
-    y [m, d] fp64.
+    y [m, d] fp64.  act_mxfp8: x and the bf16 h are quantised to MXFP8 (runs
+    of 32 along d and along I) before their products.
     """
     w_gu = _weight_values(w_gate_up_bits)
     w_d = _weight_values(w_down_bits)
     I = w_gu.shape[0] // 2
+    if act_mxfp8:
+        x_rows = mxfp8_round_rows(x_rows)
     gate = x_rows @ w_gu[:I].T
     up = x_rows @ w_gu[I:].T
     with np.errstate(over="ignore"):
         silu = gate / (1.0 + np.exp(-gate))
     h = round_to_bf16(silu * up)
+    if act_mxfp8:
+        h = mxfp8_round_rows(h)
     return h @ w_d.T
 
 
-def expert_ffn(x_perm, offsets, w_gate_up, w_down) -> np.ndarray:
+def expert_ffn(x_perm, offsets, w_gate_up, w_down, act_mxfp8: bool = False) -> np.ndarray:
     """Grouped expert FFN: rows [offsets[e], offsets[e+1]) go through expert e.
 
     x_perm: [rows, d] fp64 (exact bf16 values).  Returns y [rows, d] fp64.
@@ -408,7 +428,7 @@ def expert_ffn(x_perm, offsets, w_gate_up, w_down) -> np.ndarray:
     for e in range(E):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 > r0:
-            y[r0:r1] = swiglu_ffn(x_perm[r0:r1], w_gate_up[e], w_down[e])
+            y[r0:r1] = swiglu_ffn(x_perm[r0:r1], w_gate_up[e], w_down[e], act_mxfp8)
     return y
 
 
@@ -434,8 +454,9 @@ def combine(y, slot_pos, gates, y_shared=None) -> np.ndarray:
 
 def forward(x_bits, w_router, w_gate_up, w_down, top_k: int, router_bias=None,
             w_gate_up_shared=None, w_down_shared=None,
-            bias_for_selection_only: bool = False) -> dict:
-    """Route -> group -> expert FFN -> combine, every intermediate returned."""
+            bias_for_selection_only: bool = False, act_mxfp8: bool = False) -> dict:
+    """Route -> group -> expert FFN -> combine, every intermediate returned.
+    act_mxfp8: the expert GEMMs' token operands in MXFP8 (see swiglu_ffn)."""
     x_bits = np.asarray(x_bits, dtype=np.uint16)
     T = x_bits.shape[0]
     E = np.asarray(w_router).shape[0]
@@ -443,10 +464,10 @@ def forward(x_bits, w_router, w_gate_up, w_down, top_k: int, router_bias=None,
     counts, offsets, perm, slot_pos = permute(ids, E)
     x = bf16_bits_to_f64(x_bits)
     x_perm = x[perm // top_k]
-    y = expert_ffn(x_perm, offsets, w_gate_up, w_down)
+    y = expert_ffn(x_perm, offsets, w_gate_up, w_down, act_mxfp8)
     y_shared = None
     if w_gate_up_shared is not None:
-        y_shared = swiglu_ffn(x, w_gate_up_shared, w_down_shared)
+        y_shared = swiglu_ffn(x, w_gate_up_shared, w_down_shared, act_mxfp8)
     out = combine(y, slot_pos, gates, y_shared)
     return dict(ids=ids, gates=gates, logits=logits, counts=counts,
                 offsets=offsets, perm=perm, slot_pos=slot_pos, y=y,
@@ -454,7 +475,8 @@ def forward(x_bits, w_router, w_gate_up, w_down, top_k: int, router_bias=None,
 
 
 def forward_tokens(x_bits, tokens, ids, gates, w_gate_up, w_down,
-                   w_gate_up_shared=None, w_down_shared=None) -> np.ndarray:
+                   w_gate_up_shared=None, w_down_shared=None,
+                   act_mxfp8: bool = False) -> np.ndarray:
     """Layer output for selected tokens only, given their routing.
 
     The same per-expert arithmetic as forward(), applied to the selected rows:
@@ -469,8 +491,8 @@ def forward_tokens(x_bits, tokens, ids, gates, w_gate_up, w_down,
     out = np.zeros_like(x)
     for e in np.unique(ids):
         rows, slots = np.nonzero(ids == e)
-        y = swiglu_ffn(x[rows], w_gate_up[e], w_down[e])
+        y = swiglu_ffn(x[rows], w_gate_up[e], w_down[e], act_mxfp8)
         out[rows] += gates[rows, slots][:, None] * y
     if w_gate_up_shared is not None:
-        out += swiglu_ffn(x, w_gate_up_shared, w_down_shared)
+        out += swiglu_ffn(x, w_gate_up_shared, w_down_shared, act_mxfp8)
     return out

@@ -22,6 +22,9 @@ What pins what:
   MXFP8 ........................ E4M3 decode and rounding against torch.float8_e4m3fn; block
                                  scales from numpy frexp; codes against torch's conversion of the
                                  scaled, clamped block; exact round trip of representable values
+  MXFP8 activations ............ one expert, every token routed to it: the layer equals a dense
+                                 FFN whose x and bf16 h are micro-scaled independently (frexp
+                                 scales, torch's E4M3 conversion); quantising twice = once
 """
 
 from __future__ import annotations
@@ -229,6 +232,44 @@ def check_mxfp8(o):
     assert ((top[nz] >= 256) & (top[nz] <= 448)).all()   # the largest maps into the top binade
 
 
+def _mx_round_torch(v):
+    """MXFP8 quantise-dequantise of [m, K] rows in runs of 32 along K, without
+    the oracle: numpy frexp for the block exponent, torch for the E4M3 rounding."""
+    m, K = v.shape
+    blocks = v.reshape(m, K // 32, 32)
+    amax = np.abs(blocks).max(axis=-1)
+    _, expo = np.frexp(amax)
+    xexp = np.where(amax > 0, expo - 1 - 8, -127).astype(np.float64)
+    scaled = np.clip(blocks / 2.0 ** xexp[..., None], -448, 448).astype(np.float32)
+    q = torch.from_numpy(scaled).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return (q * 2.0 ** xexp[..., None]).reshape(m, K)
+
+
+def check_act_mxfp8(o):
+    T, d, I = 32, 64, 64
+    r = _rng(21)
+    x = _bf16_bits_from_f32(r.standard_normal((T, d)) * np.exp(r.uniform(-3, 3, (T, 1))))
+    wr = _bf16_bits_from_f32(r.standard_normal((1, d)))
+    wgu = _bf16_bits_from_f32(r.standard_normal((1, 2 * I, d)) / 8)
+    wd = _bf16_bits_from_f32(r.standard_normal((1, d, I)) / 8)
+    got = o.forward(x, wr, wgu, wd, 1, act_mxfp8=True)["out"]
+    # independent dense form: x and h micro-scaled by _mx_round_torch, h rounded to bf16 by torch
+    xq = _mx_round_torch(_dec(x))
+    g = xq @ _dec(wgu[0][:I]).T
+    u = xq @ _dec(wgu[0][I:]).T
+    with np.errstate(over="ignore"):
+        h = torch.from_numpy(g / (1.0 + np.exp(-g)) * u).to(torch.bfloat16).to(torch.float64).numpy()
+    ref = _mx_round_torch(h) @ _dec(wd[0]).T
+    assert _rel(got, ref) < 1e-12
+    # the quantisation changes the layer (so the check above sees it) ...
+    plain = o.forward(x, wr, wgu, wd, 1)["out"]
+    assert _rel(plain, ref) > 1e-4
+    # ... and values already on the MXFP8 grid go through unchanged
+    once = o.mxfp8_round_rows(_dec(x))
+    assert np.array_equal(once, xq)
+    assert np.array_equal(o.mxfp8_round_rows(once), once)
+
+
 def check_nvfp4(o):
     """E2M1 grid and rounding, NVFP4 scales and codes."""
     vals = o.e2m1_values()
@@ -419,6 +460,7 @@ def check_forward_tokens(o):
 ALL_CHECKS = [
     check_bf16_decode, check_bf16_round, check_logits_one_hot,
     check_topk_brute_force, check_tie_break, check_gates, check_selection_only_bias, check_mxfp8,
+    check_act_mxfp8,
     check_nvfp4,
     check_permute,
     check_swiglu_hand_example, check_single_expert_is_dense_ffn,

@@ -26,7 +26,7 @@ def _fresh_copy():
 
 
 def _m_silu_sign(o):
-    def swiglu_ffn(x_rows, wgu, wd):
+    def swiglu_ffn(x_rows, wgu, wd, act_mxfp8=False):
         wgu = o.bf16_bits_to_f64(wgu); wd = o.bf16_bits_to_f64(wd)
         I = wgu.shape[0] // 2
         g = x_rows @ wgu[:I].T; u = x_rows @ wgu[I:].T
@@ -37,7 +37,7 @@ def _m_silu_sign(o):
 
 
 def _m_gate_up_swapped(o):
-    def swiglu_ffn(x_rows, wgu, wd):
+    def swiglu_ffn(x_rows, wgu, wd, act_mxfp8=False):
         wgu = o.bf16_bits_to_f64(wgu); wd = o.bf16_bits_to_f64(wd)
         I = wgu.shape[0] // 2
         u = x_rows @ wgu[:I].T; g = x_rows @ wgu[I:].T
@@ -48,7 +48,7 @@ def _m_gate_up_swapped(o):
 
 
 def _m_no_h_rounding(o):
-    def swiglu_ffn(x_rows, wgu, wd):
+    def swiglu_ffn(x_rows, wgu, wd, act_mxfp8=False):
         wgu = o.bf16_bits_to_f64(wgu); wd = o.bf16_bits_to_f64(wd)
         I = wgu.shape[0] // 2
         g = x_rows @ wgu[:I].T; u = x_rows @ wgu[I:].T
@@ -59,7 +59,7 @@ def _m_no_h_rounding(o):
 
 
 def _m_down_transposed(o):
-    def swiglu_ffn(x_rows, wgu, wd):
+    def swiglu_ffn(x_rows, wgu, wd, act_mxfp8=False):
         wgu = o.bf16_bits_to_f64(wgu); wd = o.bf16_bits_to_f64(wd)
         I = wgu.shape[0] // 2
         g = x_rows @ wgu[:I].T; u = x_rows @ wgu[I:].T
@@ -136,14 +136,15 @@ def _m_gather_wrong_index(o):
     orig_forward = o.forward
 
     def forward(x_bits, wr, wgu, wd, k, router_bias=None, w_gate_up_shared=None, w_down_shared=None,
-                bias_for_selection_only=False):
+                bias_for_selection_only=False, act_mxfp8=False):
         x_bits = np.asarray(x_bits, dtype=np.uint16)
         ids, gates, logits = o.route(x_bits, wr, k, router_bias, bias_for_selection_only)
         counts, offsets, perm, slot_pos = o.permute(ids, np.asarray(wr).shape[0])
         x = o.bf16_bits_to_f64(x_bits)
         x_perm = x[(perm % k) % x.shape[0]]       # token index taken modulo k
-        y = o.expert_ffn(x_perm, offsets, wgu, wd)
-        ys = o.swiglu_ffn(x, w_gate_up_shared, w_down_shared) if w_gate_up_shared is not None else None
+        y = o.expert_ffn(x_perm, offsets, wgu, wd, act_mxfp8)
+        ys = (o.swiglu_ffn(x, w_gate_up_shared, w_down_shared, act_mxfp8)
+              if w_gate_up_shared is not None else None)
         out = o.combine(y, slot_pos, gates, ys)
         return dict(ids=ids, gates=gates, logits=logits, counts=counts, offsets=offsets,
                     perm=perm, slot_pos=slot_pos, y=y, y_shared=ys, out=out, T=x.shape[0])
@@ -165,7 +166,7 @@ def _m_combine_drops_shared(o):
 
 
 def _m_expert_shift(o):
-    def expert_ffn(x_perm, offsets, wgu, wd):
+    def expert_ffn(x_perm, offsets, wgu, wd, act_mxfp8=False):
         x_perm = np.asarray(x_perm, dtype=np.float64)
         E = len(offsets) - 1
         y = np.zeros_like(x_perm)
@@ -178,7 +179,7 @@ def _m_expert_shift(o):
 
 
 def _m_forward_tokens_no_gate(o):
-    def forward_tokens(x_bits, tokens, ids, gates, wgu, wd, wgus=None, wds=None):
+    def forward_tokens(x_bits, tokens, ids, gates, wgu, wd, wgus=None, wds=None, act_mxfp8=False):
         tokens = np.asarray(tokens)
         x = o.bf16_bits_to_f64(np.asarray(x_bits)[tokens])
         ids = np.asarray(ids)[tokens]
@@ -260,6 +261,38 @@ def _m_nv_block_32(o):
     o.NV_BLOCK = 32
 
 
+def _act_swiglu(o, quant_x, quant_h):
+    """A swiglu_ffn whose activation quantisation steps are the given ones."""
+    def swiglu_ffn(x_rows, wgu, wd, act_mxfp8=False):
+        wgu = o.bf16_bits_to_f64(wgu); wd = o.bf16_bits_to_f64(wd)
+        I = wgu.shape[0] // 2
+        if act_mxfp8:
+            x_rows = quant_x(x_rows)
+        g = x_rows @ wgu[:I].T; u = x_rows @ wgu[I:].T
+        with np.errstate(over="ignore"):
+            h = g / (1.0 + np.exp(-g)) * u
+        h = quant_h(h) if act_mxfp8 else o.round_to_bf16(h)
+        return h @ wd.T
+    return swiglu_ffn
+
+
+def _m_act_h_before_round(o):
+    # h micro-scaled before its bf16 rounding instead of after
+    o.swiglu_ffn = _act_swiglu(o, o.mxfp8_round_rows,
+                               lambda h: o.round_to_bf16(o.mxfp8_round_rows(h)))
+
+
+def _m_act_x_skipped(o):
+    o.swiglu_ffn = _act_swiglu(o, lambda x: x,
+                               lambda h: o.mxfp8_round_rows(o.round_to_bf16(h)))
+
+
+def _m_act_token_axis(o):
+    # x's runs of 32 taken along the tokens instead of along d
+    o.swiglu_ffn = _act_swiglu(o, lambda x: o.mxfp8_round_rows(x.T).T,
+                               lambda h: o.mxfp8_round_rows(o.round_to_bf16(h)))
+
+
 MUTATIONS = [
     _m_silu_sign, _m_gate_up_swapped, _m_no_h_rounding, _m_down_transposed,
     _m_tie_high_index, _m_slots_by_logit, _m_no_renormalise, _m_bias_dropped,
@@ -268,6 +301,7 @@ MUTATIONS = [
     _m_expert_shift, _m_forward_tokens_no_gate, _m_selection_only_ignored,
     _m_selection_only_unbiased_pick, _m_mx_scale_off_by_one, _m_mx_truncates, _m_mx_no_clamp,
     _m_nv_no_tensor_scale, _m_nv_e2m1_truncates, _m_nv_ties_away, _m_nv_block_32,
+    _m_act_h_before_round, _m_act_x_skipped, _m_act_token_axis,
 ]
 
 
@@ -279,6 +313,8 @@ def test_planted_mistake_is_caught(mutate):
     for check in oracle_pins.ALL_CHECKS:
         try:
             check(o)
+        except TypeError as exc:  # a mutant with the wrong signature proves nothing
+            raise AssertionError(f"{mutate.__name__} does not fit {check.__name__}: {exc}")
         except Exception as exc:  # AssertionError, or a shape error the mistake causes
             caught.append((check.__name__, type(exc).__name__))
     assert caught, f"no pin catches {mutate.__name__}"
