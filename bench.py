@@ -7,6 +7,7 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--also NAME,...] [--also-mxfp8 NAME,...]
+                  [--also-mxfp8-act NAME,...]
                   [--also-nvfp4 NAME,...] [--also-single NAME,...]
 
 Default workload: the Qwen3-235B-A22B MoE layer on a 64-token decode batch
@@ -16,6 +17,7 @@ Default workload: the Qwen3-235B-A22B MoE layer on a 64-token decode batch
 The "also" entries measure further workloads at N=1: --also with bf16
 weights, --also-mxfp8 / --also-nvfp4 with the expert weights quantised to
 MXFP8 / NVFP4 once before timing (moe_forward_mxfp8 / moe_forward_nvfp4),
+--also-mxfp8-act with MXFP8 weights and MXFP8 tokens (W8A8, act_mxfp8),
 --also-single with the whole layer as one kernel launch (single_launch).
 A bf16 "also" entry times max(3, K/50) steps (tens of ms, like the burst
 bf16 peak: single GEMMs at full clocks); the prefill entry also times,
@@ -70,7 +72,10 @@ def parse_args():
                     help="workloads also measured at N=1 with MXFP8 expert weights (empty for none)")
     ap.add_argument("--also-nvfp4", default=f"{W.DECODE},{W.PREFILL}",
                     help="workloads also measured at N=1 with NVFP4 expert weights (empty for none)")
-    ap.add_argument("--weights", choices=["bf16", "mxfp8", "nvfp4"], default="bf16",
+    ap.add_argument("--also-mxfp8-act", default=W.DECODE,
+                    help="workloads also measured at N=1 with MXFP8 expert weights and MXFP8 "
+                         "tokens, W8A8 (decode sizes only; empty for none)")
+    ap.add_argument("--weights", choices=["bf16", "mxfp8", "nvfp4", "mxfp8-act"], default="bf16",
                     help="expert weights of the main workload (profiler captures of the "
                          "quantised kernels; e2e is measured for bf16 only)")
     ap.add_argument("--single-launch", action="store_true",
@@ -210,6 +215,13 @@ def kernel_work(name, w, counts):
         return 4 * rows * d * I, int(touched * 2 * I * d * NV_BYTES) + rows * d * 2 + rows * I * 2
     if name == "moe_down_nvfp4":
         return 2 * rows * d * I, int(touched * d * I * NV_BYTES) + rows * I * 2 + rows * d * 2
+    if name == "moe_gate_up_swiglu_mxfp8_a8":  # W8A8: the tokens as MXFP8 codes too
+        return (4 * rows * d * I,
+                int(touched * 2 * I * d * MX_BYTES + rows * d * MX_BYTES) + rows * I * 2)
+    if name == "moe_down_mxfp8_a8":
+        return 2 * rows * d * I, int(touched * d * I * MX_BYTES + rows * I * MX_BYTES) + rows * d * 2
+    if name == "moe_act_mxfp8":  # two launches a layer (x, then h): their mean
+        return 0, int((T * d + rows * I) * (2 + MX_BYTES) / 2)
     if name == "moe_gate_up_swiglu_mxfp8":
         return 4 * rows * d * I, int(touched * 2 * I * d * MX_BYTES) + rows * d * 2 + rows * I * 2
     if name == "moe_down_mxfp8":
@@ -293,14 +305,15 @@ def job_rate(dist, per_rank_rate, world, device):
 # ------------------------------------------------------------------ our arm
 
 def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, peaks,
-            mxfp8=False, nvfp4=False, single_launch=False):
+            mxfp8=False, nvfp4=False, single_launch=False, act_mxfp8=False):
     """mxfp8 / nvfp4: the expert weights are quantised once, outside the
-    timed region, and every step runs moe_forward_mxfp8 / _nvfp4 on them.
+    timed region, and every step runs moe_forward_mxfp8 / _nvfp4 on them
+    (act_mxfp8: MXFP8 tokens too, W8A8).
     single_launch: every step runs the layer as one kernel launch."""
     import torch
     from mixture_experts_layer_20_gb300 import counters as C
     x = W.make_x(w, device="cuda")
-    ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k, w.I_shared)
+    ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k, w.I_shared, act_mxfp8=act_mxfp8)
     out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
     kw = dict(out=out, ws=ws, router_bias=params["router_bias"],
               w_gate_up_shared=params["w_gate_up_shared"], w_down_shared=params["w_down_shared"])
@@ -310,7 +323,8 @@ def measure(moe, W, w, params, steps, warmup, rank, world, dist, sampler_index, 
         mx_d = moe.moe_mxfp8_quantize(params["w_down"])
 
         def step():
-            moe.moe_forward_mxfp8(x, params["w_router"], mx_gu, mx_d, w.top_k, **kw)
+            moe.moe_forward_mxfp8(x, params["w_router"], mx_gu, mx_d, w.top_k, **kw,
+                                  **(dict(act_mxfp8=True) if act_mxfp8 else {}))
     elif nvfp4:
         nv_gu = moe.moe_nvfp4_quantize(params["w_gate_up"])
         nv_d = moe.moe_nvfp4_quantize(params["w_down"])
@@ -632,8 +646,8 @@ def main():
     w = pick_workload(W, args)
     params = W.make_weights(w, device="cuda")
     r = measure(moe, W, w, params, args.steps, args.warmup, rank, world, dist, smi_index, peaks,
-                mxfp8=args.weights == "mxfp8", nvfp4=args.weights == "nvfp4",
-                single_launch=args.single_launch)
+                mxfp8=args.weights in ("mxfp8", "mxfp8-act"), nvfp4=args.weights == "nvfp4",
+                single_launch=args.single_launch, act_mxfp8=args.weights == "mxfp8-act")
     e2e = None
     if args.weights == "bf16":
         e2e = measure_e2e(moe, w, params, r["ws"], r["x"], max(10, min(args.steps, 100)),
@@ -697,6 +711,21 @@ def main():
             if not same:
                 del pa
             torch.cuda.empty_cache()
+        for name in [n for n in args.also_mxfp8_act.split(",") if n]:
+            wa = W.WORKLOADS[name]
+            same = (wa.d, wa.E, wa.I, wa.I_shared, wa.zipf_bias, wa.seed) == \
+                (w.d, w.E, w.I, w.I_shared, w.zipf_bias, w.seed)
+            pa = params if same else W.make_weights(wa, device="cuda")
+            n_q = max(3, args.steps // 10)
+            ra = measure(moe, W, wa, pa, n_q, 3, 0, 1, None, smi_index, peaks, mxfp8=True,
+                         act_mxfp8=True)
+            also.append(also_row(name, "mxfp8 w8a8", ra,
+                                 "sustained" if ra["ms"] * n_q * 1e-3 > 1.0 else "burst"))
+            details.append(detail_line(f"{name} mxfp8 w8a8", ra))
+            del ra
+            if not same:
+                del pa
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -709,7 +738,8 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(r["ms"], 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if args.weights == "bf16" else
-            f"bf16 activations, {args.weights} expert weights",
+            ("mxfp8 tokens and expert weights" if args.weights == "mxfp8-act" else
+             f"bf16 activations, {args.weights} expert weights"),
             "data": "synthetic (seeded Gaussian x and weights)",
             "config": bench_config(w, world),
             "clocks": r["clocks"], "e2e": e2e, "gpu_launches": r["launches"],

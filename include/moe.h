@@ -214,6 +214,17 @@ moe_status_t moe_forward(const moe_bf16* x, const moe_bf16* w_router,
  * reads of y double, and the workspace must hold moe_workspace_size_ex(...,
  * ext) bytes (MOE_ERR_WORKSPACE otherwise).  Not with single_launch
  * (MOE_ERR_UNSUPPORTED).
+ * act_mxfp8 = 1 (moe_forward_mxfp8 only): the expert GEMMs' token operands
+ * are micro-scaled too, W8A8 ('Hosting Qwen on Blackwell', "Quantization":
+ * micro-scaling for the best decode throughput): x before gate_up and h
+ * (after its bf16 rounding) before down are quantised to MXFP8 along the
+ * reduction, in runs of 32 with one E8M0 scale each (the weights' rule), and
+ * the GEMMs multiply the codes with fp8 tensor-core MMAs, each run's fp32
+ * sum scaled by its two scales.  Decode sizes only: at most 8 rows per expert
+ * on average, d and I multiples of 256, no shared expert, not single_launch
+ * (MOE_ERR_UNSUPPORTED otherwise).  The workspace must hold
+ * moe_workspace_size_ex(..., ext) bytes; the codes and scales are left in
+ * its act_x / act_h regions (moe_workspace_layout_ex).
  * Zero-initialise the struct: later fields default to 0. */
 typedef struct {
   const float* router_bias;
@@ -223,11 +234,13 @@ typedef struct {
   int bias_selection_only;
   int single_launch;
   int y_fp32;
+  int act_mxfp8;
 } moe_forward_ext_t;
 
 /* Workspace bytes for moe_forward_ex (and the other calls taking ext) with
- * these options: the shared expert (ext->I_shared) and fp32 y (ext->y_fp32);
- * ext may be NULL (then equal to moe_workspace_size(..., 0)). */
+ * these options: the shared expert (ext->I_shared), fp32 y (ext->y_fp32) and
+ * MXFP8 tokens (ext->act_mxfp8); ext may be NULL (then equal to
+ * moe_workspace_size(..., 0)). */
 size_t moe_workspace_size_ex(int T, int d, int E, int I, int top_k,
                              const moe_forward_ext_t* ext);
 
@@ -334,11 +347,16 @@ moe_status_t moe_graph_launch(moe_graph_t graph, moe_stream_t stream);
 moe_status_t moe_graph_destroy(moe_graph_t graph);
 
 /* Where moe_forward(_ex) keeps its intermediates: byte offsets into `ws`
- * (each 256-byte aligned) for the same shapes. */
+ * (each 256-byte aligned) for the same shapes.  act_x / act_x_scales hold
+ * the MXFP8 tokens x of act_mxfp8 ([T, d] codes, [T, d / 32] E8M0 scales),
+ * act_h / act_h_scales those of h ([T*top_k, I], [T*top_k, I / 32]); their
+ * codes are stored per 256-wide chunk in the order the GEMMs read them (byte
+ * 64 t + 8 r + j of a chunk holds value 32 r + 4 t + (j & 3) + 16 (j >> 2)).
+ * Without act_mxfp8 these regions are empty. */
 typedef struct {
   size_t status, router_logits, topk_ids, topk_gates, expert_counts, expert_offsets, perm,
          slot_pos, chunk_table, x_perm, h, h_shared, y, y_shared, x_stage, out_stage,
-         total;
+         act_x, act_x_scales, act_h, act_h_scales, total;
 } moe_workspace_layout_t;
 
 moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,

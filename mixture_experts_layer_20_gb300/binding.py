@@ -27,13 +27,13 @@ class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "router_logits", "topk_ids", "topk_gates", "expert_counts", "expert_offsets", "perm",
         "slot_pos", "chunk_table", "x_perm", "h", "h_shared", "y", "y_shared", "x_stage",
-        "out_stage", "total")]
+        "out_stage", "act_x", "act_x_scales", "act_h", "act_h_scales", "total")]
 
 
 class ForwardExt(ctypes.Structure):
     _fields_ = [("router_bias", _vp), ("w_gate_up_shared", _vp), ("w_down_shared", _vp),
                 ("I_shared", _i), ("bias_selection_only", _i), ("single_launch", _i),
-                ("y_fp32", _i)]
+                ("y_fp32", _i), ("act_mxfp8", _i)]
 
 
 _SIGS = {
@@ -114,20 +114,20 @@ def _want(t, dtype, name):
 
 # ---------------------------------------------------------------- workspace
 
-def moe_workspace_size(T, d, E, I, top_k, I_shared=0, y_fp32=False) -> int:
-    if not y_fp32:
+def moe_workspace_size(T, d, E, I, top_k, I_shared=0, y_fp32=False, act_mxfp8=False) -> int:
+    if not y_fp32 and not act_mxfp8:
         return int(_lib.moe_workspace_size(T, d, E, I, top_k, I_shared))
-    ext = ForwardExt(None, None, None, I_shared, 0, 0, 1)
+    ext = ForwardExt(None, None, None, I_shared, 0, 0, int(y_fp32), int(act_mxfp8))
     return int(_lib.moe_workspace_size_ex(T, d, E, I, top_k, ctypes.byref(ext)))
 
 
-def moe_workspace_layout(T, d, E, I, top_k, I_shared=0, y_fp32=False) -> dict:
+def moe_workspace_layout(T, d, E, I, top_k, I_shared=0, y_fp32=False, act_mxfp8=False) -> dict:
     lay = WorkspaceLayout()
-    if not y_fp32:
+    if not y_fp32 and not act_mxfp8:
         _check(_lib.moe_workspace_layout(T, d, E, I, top_k, I_shared, ctypes.byref(lay)),
                "moe_workspace_layout")
     else:
-        ext = ForwardExt(None, None, None, I_shared, 0, 0, 1)
+        ext = ForwardExt(None, None, None, I_shared, 0, 0, int(y_fp32), int(act_mxfp8))
         _check(_lib.moe_workspace_layout_ex(T, d, E, I, top_k, ctypes.byref(ext),
                                             ctypes.byref(lay)), "moe_workspace_layout_ex")
     return {n: getattr(lay, n) for n, _ in WorkspaceLayout._fields_}
@@ -137,9 +137,10 @@ def moe_workspace_init(ws: torch.Tensor, stream=None):
     _check(_lib.moe_workspace_init(_p(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
 
 
-def new_workspace(T, d, E, I, top_k, I_shared=0, device="cuda", y_fp32=False) -> torch.Tensor:
-    """A zeroed uint8 device workspace for these shapes (and fp32 y)."""
-    n = max(moe_workspace_size(T, d, E, I, top_k, I_shared, y_fp32), 256)
+def new_workspace(T, d, E, I, top_k, I_shared=0, device="cuda", y_fp32=False,
+                  act_mxfp8=False) -> torch.Tensor:
+    """A zeroed uint8 device workspace for these shapes (and fp32 y, MXFP8 tokens)."""
+    n = max(moe_workspace_size(T, d, E, I, top_k, I_shared, y_fp32, act_mxfp8), 256)
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
@@ -394,10 +395,11 @@ def moe_forward_nvfp4(x, w_router, nv_gate_up, nv_down, top_k, out=None, ws=None
 
 def moe_forward_mxfp8(x, w_router, mx_gate_up, mx_down, top_k, out=None, ws=None,
                       router_bias=None, w_gate_up_shared=None, w_down_shared=None, stream=None,
-                      bias_selection_only=False, y_fp32=False):
+                      bias_selection_only=False, y_fp32=False, act_mxfp8=False):
     """The whole layer with MXFP8 expert weights: mx_gate_up / mx_down are the
     (codes, scales) pairs of moe_mxfp8_quantize for W_gate_up [E,2I,d] and
-    W_down [E,d,I].  Returns out [T, d] bf16."""
+    W_down [E,d,I].  act_mxfp8: the tokens micro-scaled too (W8A8, decode
+    sizes; needs new_workspace(..., act_mxfp8=True)).  Returns out [T, d] bf16."""
     for t, n in ((x, "x"), (w_router, "w_router"), (w_gate_up_shared, "w_gate_up_shared"),
                  (w_down_shared, "w_down_shared")):
         _want(t, torch.bfloat16, n)
@@ -414,11 +416,13 @@ def moe_forward_mxfp8(x, w_router, mx_gate_up, mx_down, top_k, out=None, ws=None
     if out is None:
         out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
     if ws is None:
-        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device, y_fp32=y_fp32)
+        ws = new_workspace(T, d, E, I, top_k, I_s, device=x.device, y_fp32=y_fp32,
+                           act_mxfp8=act_mxfp8)
     ext = ForwardExt(router_bias.data_ptr() if router_bias is not None else None,
                      w_gate_up_shared.data_ptr() if I_s else None,
                      w_down_shared.data_ptr() if I_s else None, I_s,
-                     1 if bias_selection_only else 0, 0, 1 if y_fp32 else 0)
+                     1 if bias_selection_only else 0, 0, 1 if y_fp32 else 0,
+                     1 if act_mxfp8 else 0)
     _check(_lib.moe_forward_mxfp8(_p(x), _p(w_router), _p(cgu), _p(sgu), _p(cd), _p(sd), T, d, E,
                                   I, top_k, _p(out), _p(ws), ws.numel(), _stream(stream),
                                   ctypes.byref(ext)), "moe_forward_mxfp8")
@@ -471,9 +475,10 @@ class ForwardGraph:
             pass
 
 
-def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0, y_fp32=False) -> dict:
+def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0, y_fp32=False,
+                    act_mxfp8=False) -> dict:
     """Typed views of moe_forward's intermediates inside its workspace."""
-    L = moe_workspace_layout(T, d, E, I, top_k, I_shared, y_fp32)
+    L = moe_workspace_layout(T, d, E, I, top_k, I_shared, y_fp32, act_mxfp8)
     n = T * top_k
 
     def view(off, count, dtype, shape):
@@ -490,4 +495,13 @@ def workspace_views(ws: torch.Tensor, T, d, E, I, top_k, I_shared=0, y_fp32=Fals
         "x_perm": view(L["x_perm"], n * d, torch.bfloat16, (n, d)),
         "h": view(L["h"], n * I, torch.bfloat16, (n, I)),
         "y": view(L["y"], n * d, torch.float32 if y_fp32 else torch.float16, (n, d)),
+        # MXFP8 tokens of act_mxfp8 (codes in the GEMMs' order within each 256-wide chunk)
+        "act_x": view(L["act_x"], T * d if act_mxfp8 else 0, torch.uint8,
+                      (T, d) if act_mxfp8 else (0,)),
+        "act_x_scales": view(L["act_x_scales"], T * d // 32 if act_mxfp8 else 0, torch.uint8,
+                             (T, d // 32) if act_mxfp8 else (0,)),
+        "act_h": view(L["act_h"], n * I if act_mxfp8 else 0, torch.uint8,
+                      (n, I) if act_mxfp8 else (0,)),
+        "act_h_scales": view(L["act_h_scales"], n * I // 32 if act_mxfp8 else 0, torch.uint8,
+                             (n, I // 32) if act_mxfp8 else (0,)),
     }

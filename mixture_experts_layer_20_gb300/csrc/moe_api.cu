@@ -89,11 +89,13 @@ moe_status_t check_shapes(int T, int d, int E, int I, int top_k) {
 
 struct Layout {
   size_t status, logits, ids, gates, counts, offsets, perm, slot_pos, chunk, x_perm, h, h_shared,
-      y, y_shared, x_stage, out_stage, total;
+      y, y_shared, x_stage, out_stage, act_x, act_x_scales, act_h, act_h_scales, total;
 };
 
 // y_fp32: the expert outputs y and y_shared kept in fp32 (else fp16).
-Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared, bool y_fp32 = false) {
+// act8: room for the MXFP8 tokens of the W8A8 expert GEMMs (x and h).
+Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared, bool y_fp32 = false,
+                      bool act8 = false) {
   const size_t n = static_cast<size_t>(T) * top_k;
   const size_t nchunks = (n + kPermuteChunk - 1) / kPermuteChunk;
   Layout L{};
@@ -121,6 +123,10 @@ Layout forward_layout(int T, int d, int E, int I, int top_k, int I_shared, bool 
   L.y_shared = take(I_shared ? static_cast<size_t>(T) * d * ybytes : 0);
   L.x_stage = take(static_cast<size_t>(T) * d * 2);
   L.out_stage = take(static_cast<size_t>(T) * d * 2);
+  L.act_x = take(act8 ? static_cast<size_t>(T) * d : 0);
+  L.act_x_scales = take(act8 ? static_cast<size_t>(T) * d / 32 : 0);
+  L.act_h = take(act8 ? n * I : 0);
+  L.act_h_scales = take(act8 ? n * I / 32 : 0);
   L.total = off;
   return L;
 }
@@ -222,14 +228,15 @@ size_t moe_workspace_size_ex(int T, int d, int E, int I, int top_k,
                              const moe_forward_ext_t* ext) {
   const int I_shared = ext ? ext->I_shared : 0;
   if (T < 0 || d <= 0 || E <= 0 || I <= 0 || top_k <= 0 || I_shared < 0) return 0;
-  return forward_layout(T, d, E, I, top_k, I_shared, ext && ext->y_fp32).total;
+  return forward_layout(T, d, E, I, top_k, I_shared, ext && ext->y_fp32, ext && ext->act_mxfp8)
+      .total;
 }
 
 static moe_status_t workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,
-                                     bool y_fp32, moe_workspace_layout_t* out) {
+                                     bool y_fp32, bool act8, moe_workspace_layout_t* out) {
   if (!out || T < 0 || d <= 0 || E <= 0 || I <= 0 || top_k <= 0 || I_shared < 0)
     return fail(MOE_ERR_INVALID_ARG, "bad arguments to moe_workspace_layout");
-  const Layout L = forward_layout(T, d, E, I, top_k, I_shared, y_fp32);
+  const Layout L = forward_layout(T, d, E, I, top_k, I_shared, y_fp32, act8);
   out->status = L.status;
   out->router_logits = L.logits;
   out->topk_ids = L.ids;
@@ -246,18 +253,23 @@ static moe_status_t workspace_layout(int T, int d, int E, int I, int top_k, int 
   out->y_shared = L.y_shared;
   out->x_stage = L.x_stage;
   out->out_stage = L.out_stage;
+  out->act_x = L.act_x;
+  out->act_x_scales = L.act_x_scales;
+  out->act_h = L.act_h;
+  out->act_h_scales = L.act_h_scales;
   out->total = L.total;
   return MOE_OK;
 }
 
 moe_status_t moe_workspace_layout(int T, int d, int E, int I, int top_k, int I_shared,
                                   moe_workspace_layout_t* out) {
-  return workspace_layout(T, d, E, I, top_k, I_shared, false, out);
+  return workspace_layout(T, d, E, I, top_k, I_shared, false, false, out);
 }
 
 moe_status_t moe_workspace_layout_ex(int T, int d, int E, int I, int top_k,
                                      const moe_forward_ext_t* ext, moe_workspace_layout_t* out) {
-  return workspace_layout(T, d, E, I, top_k, ext ? ext->I_shared : 0, ext && ext->y_fp32, out);
+  return workspace_layout(T, d, E, I, top_k, ext ? ext->I_shared : 0, ext && ext->y_fp32,
+                          ext && ext->act_mxfp8, out);
 }
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
@@ -378,6 +390,7 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   const int bias_sel = ext ? ext->bias_selection_only : 0;
   const bool single = ext && ext->single_launch;
   const bool y32 = ext && ext->y_fp32;
+  const bool act8 = ext && ext->act_mxfp8;
   const int I_shared = ext ? ext->I_shared : 0;
   const moe_bf16* wgu_s = ext ? ext->w_gate_up_shared : nullptr;
   const moe_bf16* wd_s = ext ? ext->w_down_shared : nullptr;
@@ -389,7 +402,7 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) ||
       !aligned16(out) || !aligned16(ws) || (I_shared && (!aligned16(wgu_s) || !aligned16(wd_s))))
     return fail(MOE_ERR_INVALID_ARG, "moe_forward: pointers must be 16-byte aligned");
-  const Layout L = forward_layout(T, d, E, I, top_k, I_shared, y32);
+  const Layout L = forward_layout(T, d, E, I, top_k, I_shared, y32, act8);
   if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "moe_forward: workspace too small");
   if (single && y32)
     return fail(MOE_ERR_UNSUPPORTED, "single_launch keeps y in fp16 (y_fp32 unsupported)");
@@ -399,6 +412,11 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
     return fail(MOE_ERR_UNSUPPORTED,
                 "single_launch needs bf16 expert weights, no shared expert, d and I multiples of "
                 "128, T*top_k <= 4096 and at most 16 rows per expert on average");
+  if (act8 && !(mx && mx->fmt == 0 && !I_shared && !single && d % 256 == 0 && I % 256 == 0 &&
+                static_cast<long long>(T) * top_k <= kSmallMRowsPerExpert * static_cast<long long>(E)))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "act_mxfp8 needs MXFP8 expert weights, decode sizes (at most 8 rows per expert "
+                "on average, d and I multiples of 256) and no shared expert");
   if ((st = check_device()) != MOE_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -462,7 +480,13 @@ moe_status_t forward_impl(const moe_bf16* x, const moe_bf16* w_router,
                                  offsets, perm, slot_pos, x_perm, table, status);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   const TokenGather gather{x, perm, top_k, T};
-  if (small_m)
+  if (act8)
+    e = launch_grouped_ffn_smallm_a8(
+        s, x, T, perm, top_k, offsets, rows, d, E, I, mx->codes_gate_up, mx->scales_gate_up,
+        mx->codes_down, mx->scales_down, reinterpret_cast<uint8_t*>(w + L.act_x),
+        reinterpret_cast<uint8_t*>(w + L.act_x_scales), h, reinterpret_cast<uint8_t*>(w + L.act_h),
+        reinterpret_cast<uint8_t*>(w + L.act_h_scales), y, status, y32);
+  else if (small_m)
     e = launch_grouped_ffn_smallm(s, mx->fmt == 0 ? 1 : 2, x, perm, top_k, offsets, rows, d, E, I,
                                   mx->codes_gate_up, mx->scales_gate_up, mx->tscale_gate_up,
                                   mx->codes_down, mx->scales_down, mx->tscale_down, h, y, status,
@@ -548,7 +572,8 @@ moe_status_t moe_forward_host(const moe_bf16* x_host, const moe_bf16* w_router,
   if (T == 0) return MOE_OK;
   if (!x_host || !out_host || !ws) return fail(MOE_ERR_INVALID_ARG, "moe_forward_host: null pointer");
   const int I_shared = ext ? ext->I_shared : 0;
-  const Layout L = forward_layout(T, d, E, I, top_k, I_shared, ext && ext->y_fp32);
+  const Layout L =
+      forward_layout(T, d, E, I, top_k, I_shared, ext && ext->y_fp32, ext && ext->act_mxfp8);
   if (ws_bytes < L.total || !aligned16(ws))
     return fail(MOE_ERR_WORKSPACE, "moe_forward_host: workspace too small");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

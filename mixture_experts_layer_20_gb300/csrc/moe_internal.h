@@ -194,6 +194,17 @@ cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
                                       const float* tscale_down, void* h, void* y,
                                       unsigned* status, bool y_fp32 = false);
 
+// The same with MXFP8 tokens too (W8A8): x [T, d] is quantised into xq / xs
+// ([T, d] codes, [T, d / 32] scales), h into hq / hs ([rows, I], [rows, I / 32])
+// by launch_act_mxfp8; MXFP8 weights only.
+cudaError_t launch_grouped_ffn_smallm_a8(cudaStream_t s, const void* x, int T,
+                                         const int32_t* perm, int div, const int32_t* offsets,
+                                         int rows, int d, int E, int I, const void* w_gate_up,
+                                         const uint8_t* scales_gate_up, const void* w_down,
+                                         const uint8_t* scales_down, uint8_t* xq, uint8_t* xs,
+                                         void* h, uint8_t* hq, uint8_t* hs, void* y,
+                                         unsigned* status, bool y_fp32 = false);
+
 // The whole layer in one cooperative launch, for decode-sized batches with
 // bf16 expert weights and no shared expert (moe_fused.cu).  Requires d and I
 // multiples of 128, E <= 256 and T * k <= kPermuteSmallMax; partial holds
@@ -244,5 +255,12 @@ cudaError_t launch_combine(cudaStream_t s, const void* y, const int32_t* slot_po
 // scales [K / 128][rows][4].
 cudaError_t launch_mxfp8_quantize(cudaStream_t s, const void* w, long long rows, int K,
                                   uint8_t* codes, uint8_t* scales);
+
+// bf16 activations [rows, K] (K a multiple of 256) -> MXFP8 codes [rows, K],
+// each 256-wide chunk in the small-M W8A8 GEMMs' order (byte 64 t + 8 r + j
+// of a chunk: value 32 r + 4 t + (j & 3) + 16 (j >> 2)), and scales
+// [rows][K / 32].
+cudaError_t launch_act_mxfp8(cudaStream_t s, const void* a, long long rows, int K, uint8_t* codes,
+                             uint8_t* scales);
 
 }  // namespace moe

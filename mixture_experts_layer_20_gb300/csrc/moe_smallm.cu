@@ -38,6 +38,14 @@
 // the fp32 sums are multiplied by 2^8 with the tensor scale), so a code costs
 // about two instructions.
 //
+// W8A8 (MXFP8 weights and MXFP8 token rows, an option of the MXFP8 layer):
+// the tokens are quantised like the weights (launch_act_mxfp8: x before
+// gate_up, h before down), and each 32-value run is one mma.sync m16n8k32
+// E4M3 x E4M3 -> fp32 with no accumulator input, whose four sums the lane
+// scales by the runs' weight and token scales (exact powers of two) and adds
+// to its fp32 accumulators in run order.  No code is decoded: the codes go
+// from shared memory (weights) and global memory (tokens) into the MMA.
+//
 // Weights (and their block scales) reach shared memory through a per-warp
 // ring of cp.async copies several chunks ahead, across task boundaries; each
 // lane copies and later reads only its own units, so a lane's own
@@ -134,7 +142,75 @@ cudaError_t sm_ffn(cudaStream_t s, const char* gu_name, const char* dn_name, con
   return sm_launch<FMT, kSmDown>(s, dn_name, q);
 }
 
+// W8A8: x (the T unpermuted tokens) and then h quantised to MXFP8 by
+// launch_act_mxfp8, each GEMM reading the codes with fp8 warp MMAs.
+cudaError_t sm_ffn_a8(cudaStream_t s, const void* x, int T, const int32_t* perm, int div,
+                      const int32_t* offsets, int rows, int d, int E, int I,
+                      const uint8_t* w_gate_up, const uint8_t* s_gate_up, const uint8_t* w_down,
+                      const uint8_t* s_down, uint8_t* xq, uint8_t* xs, void* h, uint8_t* hq,
+                      uint8_t* hs, void* y, unsigned* status, bool y_fp32) {
+  constexpr int F = kSmMx8A8;
+  if (d % sm_chunk_k<F>() || I % sm_chunk_k<F>()) return cudaErrorInvalidValue;
+  cudaError_t e = launch_act_mxfp8(s, x, T, d, xq, xs);
+  if (e != cudaSuccess) return e;
+  SmParams p{};
+  p.w = w_gate_up;
+  p.scales = s_gate_up;
+  p.scale_rows = 2LL * I * E;
+  p.row_bytes = d;
+  p.K = d;
+  p.n_out = I;
+  p.w_rows_per_expert = 2 * I;
+  p.up_offset = I;
+  p.E = E;
+  p.offsets = offsets;
+  p.total_rows = rows;
+  p.bq = xq;
+  p.bs = xs;
+  p.b_rows = T;
+  p.perm = perm;
+  p.div = div;
+  p.out = h;
+  p.ld_out = I;
+  p.status = status;
+  e = sm_launch<F, kSmGateUp>(s, "moe_gate_up_swiglu_mxfp8_a8_smallm", p);
+  if (e == cudaSuccess) e = launch_act_mxfp8(s, h, rows, I, hq, hs);
+  if (e != cudaSuccess) return e;
+  SmParams q = p;
+  q.w = w_down;
+  q.scales = s_down;
+  q.scale_rows = static_cast<long long>(E) * d;
+  q.row_bytes = I;
+  q.K = I;
+  q.n_out = d;
+  q.w_rows_per_expert = d;
+  q.up_offset = 0;
+  q.bq = hq;
+  q.bs = hs;
+  q.b_rows = rows;
+  q.perm = nullptr;
+  q.div = 1;
+  q.out = y;
+  q.ld_out = d;
+  q.y_fp32 = y_fp32 ? 1 : 0;
+  return sm_launch<F, kSmDown>(s, "moe_down_mxfp8_a8_smallm", q);
+}
+
 }  // namespace
+
+cudaError_t launch_grouped_ffn_smallm_a8(cudaStream_t s, const void* x, int T,
+                                         const int32_t* perm, int div, const int32_t* offsets,
+                                         int rows, int d, int E, int I, const void* w_gate_up,
+                                         const uint8_t* scales_gate_up, const void* w_down,
+                                         const uint8_t* scales_down, uint8_t* xq, uint8_t* xs,
+                                         void* h, uint8_t* hq, uint8_t* hs, void* y,
+                                         unsigned* status, bool y_fp32) {
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
+  return sm_ffn_a8(s, x, T, perm, div, offsets, rows, d, E, I,
+                   static_cast<const uint8_t*>(w_gate_up), scales_gate_up,
+                   static_cast<const uint8_t*>(w_down), scales_down, xq, xs, h, hq, hs, y, status,
+                   y_fp32);
+}
 
 cudaError_t launch_grouped_ffn_smallm(cudaStream_t s, int fmt, const void* a,
                                       const int32_t* perm, int div, const int32_t* offsets,

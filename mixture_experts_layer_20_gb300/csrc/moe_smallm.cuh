@@ -14,7 +14,8 @@
 
 namespace moe {
 
-enum SmFmt : int { kSmMx8 = 1, kSmNv4 = 2 };
+// kSmMx8A8: MXFP8 weights and MXFP8 token rows (W8A8, fp8 warp MMAs)
+enum SmFmt : int { kSmMx8 = 1, kSmNv4 = 2, kSmMx8A8 = 3 };
 enum SmKind : int { kSmGateUp = 1, kSmDown = 2 };
 
 constexpr int kSmWarps = 8;               // warps per CTA
@@ -33,6 +34,14 @@ template <> struct SmF<kSmMx8> {
 template <> struct SmF<kSmNv4> {
   static constexpr int V = 32, U = 2, NS = 4, SB = 16;
   static constexpr int kBytesX2 = 1;
+};
+// W8A8: the same weight stages as kSmMx8 (a lane's unit i: bytes 16 tig ..
+// + 15 of the chunk's 64-byte span i, of rows g and g + 8), stored at a
+// swizzled unit slot so that ldmatrix reads the MMA fragments without bank
+// conflicts (one fp8 MMA per 32-value run).
+template <> struct SmF<kSmMx8A8> {
+  static constexpr int V = 16, U = 4, NS = 3, SB = 8;
+  static constexpr int kBytesX2 = 2;
 };
 template <int FMT>
 __host__ __device__ constexpr int sm_chunk_k() {
@@ -73,6 +82,9 @@ struct SmParams {
   int ld_out;
   int y_fp32;                // down: y in fp32 (else fp16, saturated at the fp16 range)
   unsigned* status;
+  // W8A8: token rows as MXFP8 (launch_act_mxfp8's layout) instead of b
+  const uint8_t* bq;         // codes [b_rows, K]
+  const uint8_t* bs;         // scales [b_rows, K / 32]
 };
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
@@ -106,6 +118,28 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A B with A 16 x 32 E4M3 (row-major fragment), B 32 x 8 E4M3
+// (column-major fragment), D 16 x 8 fp32 (no accumulator input).
+__device__ __forceinline__ void mma_16832_e4m3(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Four 8 x 8 matrices of 16-bit elements (here 8 rows of 16 codes each) from
+// shared memory: lanes 8 m .. 8 m + 7 give the row addresses of matrix m;
+// register m of lane (g, tig) gets bytes 4 tig .. + 3 of row g of matrix m.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
@@ -149,7 +183,7 @@ __device__ __forceinline__ SmTask sm_task(const SmParams& p, const int* s_act, c
   }
   t.w0 = p.w + r0 * p.row_bytes + 16 * tig;
   t.w1 = p.w + r1 * p.row_bytes + 16 * tig;
-  if constexpr (FMT == kSmMx8) {
+  if constexpr (FMT == kSmMx8 || FMT == kSmMx8A8) {
     t.s0 = p.scales + r0 * 4;
     t.s1 = p.scales + r1 * 4;
   } else {
@@ -168,13 +202,15 @@ __device__ __forceinline__ void sm_fetch(const SmParams& p, const SmTask& t, int
   using F = SmF<FMT>;
   constexpr int kChunkBytes = sm_chunk_k<FMT>() * F::kBytesX2 / 2;  // = 64 U
   const long long off = static_cast<long long>(c) * kChunkBytes;
+  // W8A8: the unit of lane (g, tig) goes to slot 4 g + (tig ^ ((g >> 1) & 3))
+  const int u_slot = FMT == kSmMx8A8 ? (lane & ~3) | ((lane & 3) ^ ((lane >> 3) & 3)) : lane;
 #pragma unroll
   for (int i = 0; i < F::U; ++i) {
-    cp_async_16(slot + (i * 32 + lane) * 16, t.w0 + off + 64 * i);
-    cp_async_16(slot + ((F::U + i) * 32 + lane) * 16, t.w1 + off + 64 * i);
+    cp_async_16(slot + (i * 32 + u_slot) * 16, t.w0 + off + 64 * i);
+    cp_async_16(slot + ((F::U + i) * 32 + u_slot) * 16, t.w1 + off + 64 * i);
   }
   const uint32_t s = slot + 2 * F::U * 32 * 16 + lane * sm_scale_slot<FMT>();
-  if constexpr (FMT == kSmMx8) {
+  if constexpr (FMT == kSmMx8 || FMT == kSmMx8A8) {
     // a 256-wide chunk spans two 128-wide scale stages: one word per row each
     const long long st = 2LL * c * p.scale_rows * 4;
     const long long st2 = st + p.scale_rows * 4;
@@ -278,23 +314,103 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
         FMT == kSmNv4 ? (p.tscale ? __ldg(p.tscale + t.e) : 1.0f) * 256.0f : 1.0f;
 #pragma unroll 1
     for (int pass = 0; pass < t.npass; ++pass) {
-      // this lane's token: n = 8 pass + g (none past the expert's rows)
-      const __nv_bfloat16* brow = nullptr;
-      {
-        const int n = pass * kSmTok + g;
-        if (n < t.m) {
-          const int pos = t.row_off + n;
-          const long long src = p.perm ? ld_in<COHERENT>(p.perm + pos) / p.div : pos;
-          if (src >= 0 && src < p.b_rows) brow = p.b + src * p.K;
-          else atomicOr(p.status, kStatusDeviceCheck);  // a bad permutation: read zeros
-        }
-      }
+      // Source row of the expert's token n (-1 past the expert's rows, or for a
+      // bad permutation entry, which is recorded and read as zeros).
+      auto src_row = [&](int n) -> long long {
+        if (n >= t.m) return -1;
+        const int pos = t.row_off + n;
+        const long long src = p.perm ? ld_in<COHERENT>(p.perm + pos) / p.div : pos;
+        if (src >= 0 && src < p.b_rows) return src;
+        atomicOr(p.status, kStatusDeviceCheck);
+        return -1;
+      };
       // kAcc accumulators, taken in turn by a unit's MMAs, break the MMA
       // dependency chain; they are added in a fixed order at the end
       constexpr int kAcc = F::V / 4 < 4 ? F::V / 4 : 4;
       float acc[kAcc][4];
 #pragma unroll
       for (int q = 0; q < kAcc; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
+
+      if constexpr (FMT == kSmMx8A8) {
+        // W8A8.  B operand: token n = 8 pass + g (its MXFP8 codes); the
+        // accumulator columns are tokens 8 pass + 2 tig and + 1, whose run
+        // scales multiply the partial sums.  One MMA per 32-value run r of a
+        // chunk, k-position = value index within the run: ldmatrix brings the
+        // weight fragments (rows g / g + 8, values 4 tig + j / 16 + 4 tig + j)
+        // from the units of the lanes that copied them, and the token codes
+        // are stored so that a lane's 8 bytes of run r are those values.
+        // This lane's row address for ldmatrix: matrix mm = lane / 8 (rows g
+        // or g + 8, first or second 16 codes of the run), row jj = lane % 8.
+        const int mm = lane >> 3, jj = lane & 7;
+        const int ld_unit = (mm & 1) * F::U;          // units of rows g + 8 follow those of g
+        const int ld_half = mm >> 1;                  // 16-code half of the run
+        const long long sb = src_row(pass * kSmTok + g);
+        const uint8_t* bqrow = sb >= 0 ? p.bq + sb * p.K : nullptr;
+        const uint8_t* bsr[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const long long sr = src_row(pass * kSmTok + 2 * tig + hh);
+          bsr[hh] = sr >= 0 ? p.bs + sr * (p.K / 32) : nullptr;
+        }
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          __syncwarp();  // every lane has read the slot that fetch_next refills
+          uint4 bv[F::U];
+#pragma unroll
+          for (int i = 0; i < F::U; ++i)
+            bv[i] = bqrow ? ld_in<kBCoherent>(reinterpret_cast<const uint4*>(bqrow + c * KC + 64 * tig + 16 * i))
+                          : make_uint4(0u, 0u, 0u, 0u);
+          uint2 sx[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            sx[hh] = bsr[hh] ? ld_in<kBCoherent>(reinterpret_cast<const uint2*>(bsr[hh] + c * 8))
+                             : make_uint2(0u, 0u);
+          fetch_next();
+          cp_async_wait<F::NS - 1>();
+          __syncwarp();  // the other lanes' units of this slot have landed
+          const uint32_t cur = st;
+          st += sm_stage_bytes<FMT>();
+          if (st == ring + F::NS * sm_stage_bytes<FMT>()) st = ring;
+          // weight run scales: x / y row g runs 0-3 / 4-7, z / w row g + 8
+          const uint4 sc = lds128(cur + 2 * F::U * 32 * 16 + lane * sm_scale_slot<FMT>());
+          // the chunk's eight MMAs first (independent), then their scaling,
+          // so that no MMA waits for the one before it
+          float d[2 * F::U][4];
+#pragma unroll
+          for (int i = 0; i < F::U; ++i) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              // run 2 i + hh: bytes 32 hh + 16 ld_half of span i, copied by
+              // lane (jj, 2 hh + ld_half) into its swizzled slot
+              const int tsrc = 2 * hh + ld_half;
+              const uint32_t addr =
+                  cur + ((ld_unit + i) * 32 + 4 * jj + (tsrc ^ ((jj >> 1) & 3))) * 16;
+              uint32_t a0, a1, a2, a3;
+              ldmatrix_x4(addr, a0, a1, a2, a3);
+              mma_16832_e4m3(d[2 * i + hh], a0, a1, a2, a3, word_of(bv[i], 2 * hh),
+                             word_of(bv[i], 2 * hh + 1));
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < 2 * F::U; ++r) {
+            const int sh = 8 * (r & 3);
+            const float w0 = e8m0_to_float(((r < 4 ? sc.x : sc.y) >> sh) & 0xffu);
+            const float w1 = e8m0_to_float(((r < 4 ? sc.z : sc.w) >> sh) & 0xffu);
+            const float x0 = e8m0_to_float(((r < 4 ? sx[0].x : sx[0].y) >> sh) & 0xffu);
+            const float x1 = e8m0_to_float(((r < 4 ? sx[1].x : sx[1].y) >> sh) & 0xffu);
+            acc[0][0] = fmaf(d[r][0], w0 * x0, acc[0][0]);
+            acc[0][1] = fmaf(d[r][1], w0 * x1, acc[0][1]);
+            acc[0][2] = fmaf(d[r][2], w1 * x0, acc[0][2]);
+            acc[0][3] = fmaf(d[r][3], w1 * x1, acc[0][3]);
+          }
+        }
+      } else {
+      // this lane's token: n = 8 pass + g (none past the expert's rows)
+      const __nv_bfloat16* brow = nullptr;
+      {
+        const long long src = src_row(pass * kSmTok + g);
+        if (src >= 0) brow = p.b + src * p.K;
+      }
 
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
@@ -393,6 +509,7 @@ __device__ __forceinline__ void sm_phase(const SmParams& p, uint8_t* sm_raw) {
         if (FMT == kSmMx8 && slow) chunk_body(std::true_type{});
         else chunk_body(std::false_type{});
       }
+      }  // not W8A8
 
       // epilogue: acc = {(row g, token 2 tig), (g, 2 tig + 1), (g + 8, 2 tig), (g + 8, 2 tig + 1)}
 #pragma unroll

@@ -21,18 +21,19 @@ import oracle
 def _expert_y(args):
     """y rows of one expert: the oracle's SwiGLU FFN on the oracle's own
     quantise-dequantise round trip of the expert's bf16 weights (fmt "mxfp8",
-    "nvfp4") or on the bf16 weights themselves (fmt None)."""
+    "nvfp4"; "mxfp8_a8": MXFP8 weights and tokens) or on the bf16 weights
+    themselves (fmt None)."""
     fmt, x_rows, gu_bits, d_bits = args
 
     def weights(bits):
         if fmt is None:
             return bits
         vals = oracle.bf16_bits_to_f64(bits)
-        if fmt == "mxfp8":
+        if fmt in ("mxfp8", "mxfp8_a8"):
             return oracle.f64_to_bf16_bits(oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(vals)))
         return oracle.nvfp4_dequantize(*oracle.nvfp4_quantize(vals.astype(np.float32)))
 
-    return oracle.swiglu_ffn(x_rows, weights(gu_bits), weights(d_bits))
+    return oracle.swiglu_ffn(x_rows, weights(gu_bits), weights(d_bits), act_mxfp8=fmt == "mxfp8_a8")
 
 
 def layer_out(x_bits, ids, gates, E, expert_bits, fmt=None, processes=None):

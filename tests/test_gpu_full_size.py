@@ -71,19 +71,21 @@ def test_full_size_whole_layer(moe, name):
           f"max_rel={max_rel:.3e} mean_rel={mean_rel:.3e}")
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp8_a8"])
 def test_full_size_decode_quantised_weights(moe, fmt):
-    """The decode workload with MXFP8 / NVFP4 expert weights, as the benchmark
-    runs it: routing for every token, and every token's output (all 64 x 4096
-    values but near-ties) against the oracle on its own quantisation of the
-    experts' weights."""
+    """The decode workload with MXFP8 / NVFP4 expert weights (mxfp8_a8: MXFP8
+    tokens too), as the benchmark runs it: routing for every token, and every
+    token's output (all 64 x 4096 values but near-ties) against the oracle on
+    its own quantisation of the experts' weights (and tokens)."""
     w = W.WORKLOADS[W.DECODE]
     p = W.make_weights(w, device="cuda")
     x = W.make_x(w, device="cuda")
-    ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k)
-    if fmt == "mxfp8":
+    a8 = fmt == "mxfp8_a8"
+    ws = moe.new_workspace(w.T, w.d, w.E, w.I, w.top_k, act_mxfp8=a8)
+    if fmt in ("mxfp8", "mxfp8_a8"):
         out = moe.moe_forward_mxfp8(x, p["w_router"], moe.moe_mxfp8_quantize(p["w_gate_up"]),
-                                    moe.moe_mxfp8_quantize(p["w_down"]), w.top_k, ws=ws)
+                                    moe.moe_mxfp8_quantize(p["w_down"]), w.top_k, ws=ws,
+                                    act_mxfp8=a8)
     else:
         out = moe.moe_forward_nvfp4(x, p["w_router"], moe.moe_nvfp4_quantize(p["w_gate_up"]),
                                     moe.moe_nvfp4_quantize(p["w_down"]), w.top_k, ws=ws)

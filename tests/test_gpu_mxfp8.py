@@ -1,6 +1,7 @@
 """MXFP8 weights on the GPU against the oracle: quantisation codes and scales
 bit for bit, and the whole layer against the oracle's layer with the weights
-it quantised and dequantised itself."""
+it quantised and dequantised itself; with act_mxfp8 (W8A8) the tokens' codes
+and scales bit for bit too, and the layer against the oracle's W8A8 layer."""
 
 import numpy as np
 import pytest
@@ -157,3 +158,73 @@ def test_forward_mxfp8_fp32_y(moe, T, d, E, k, I, Is):
     assert differ.size == 0
     assert_layer_close(f64(v["y"]), ref["y"], "y")
     assert_layer_close(f64(out), ref["out"], "out")
+
+
+# ---------------------------------------------------------------- W8A8 (act_mxfp8)
+
+def _unpermute_act(codes):
+    """Token codes [rows, K] in the GEMMs' order (byte 64 t + 8 r + j of a
+    256-wide chunk holds value 32 r + 4 t + (j & 3) + 16 (j >> 2)) -> value order."""
+    rows, K = codes.shape
+    # [.., t, r, jh, jl] -> values [.., r, jh, t, jl]
+    return codes.reshape(rows, K // 256, 4, 8, 2, 4).transpose(0, 1, 3, 4, 2, 5).reshape(rows, K)
+
+
+def _forward_a8(moe, T, d, E, k, I, zipf, seed):
+    w = W.Workload("mxa8", T, d, E, k, I, zipf_bias=zipf, seed=seed)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    ws = moe.new_workspace(T, d, E, I, k, act_mxfp8=True)
+    out = moe.moe_forward_mxfp8(x, p["w_router"], moe.moe_mxfp8_quantize(p["w_gate_up"]),
+                                moe.moe_mxfp8_quantize(p["w_down"]), k, ws=ws,
+                                router_bias=p["router_bias"], act_mxfp8=True)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    return w, p, x, out, moe.workspace_views(ws, T, d, E, I, k, act_mxfp8=True)
+
+
+A8_CASES = [
+    # T, d, E, k, I, zipf: at most 8 rows per expert on average (the small-M kernels)
+    (32, 512, 32, 8, 256, False),
+    (60, 768, 64, 8, 512, True),      # biased router: hot experts take several passes of 8
+    (17, 1024, 16, 4, 512, False),
+    (1, 256, 8, 2, 256, False),
+]
+
+
+@pytest.mark.parametrize("T,d,E,k,I,zipf", A8_CASES)
+def test_forward_mxfp8_act(moe, T, d, E, k, I, zipf):
+    """W8A8: the tokens x and h quantised bit for bit like the oracle, and the
+    layer against the oracle's layer with MXFP8 weights and tokens."""
+    w, p, x, out, v = _forward_a8(moe, T, d, E, k, I, zipf, seed=T + 5 * d)
+    xc, xs = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(W.to_bits(x)))
+    assert np.array_equal(_unpermute_act(v["act_x"].cpu().numpy()), xc)
+    assert np.array_equal(v["act_x_scales"].cpu().numpy(), xs)
+    hc, hs = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(W.to_bits(v["h"])))
+    assert np.array_equal(_unpermute_act(v["act_h"].cpu().numpy()), hc)
+    assert np.array_equal(v["act_h_scales"].cpu().numpy(), hs)
+    ref = oracle.forward(
+        W.to_bits(x), W.to_bits(p["w_router"]), _dequantised_bits(p["w_gate_up"]),
+        _dequantised_bits(p["w_down"]), k,
+        router_bias=None if p["router_bias"] is None else p["router_bias"].cpu().numpy(),
+        act_mxfp8=True)
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ref["ids"], ref["gates"], ref["logits"], k)
+    assert differ.size == 0
+    assert_layer_close(f64(v["y"]), ref["y"], "y")
+    assert_layer_close(f64(out), ref["out"], "out")
+
+
+def test_forward_mxfp8_act_unsupported(moe):
+    """W8A8 outside decode sizes, or with a shared expert, is refused on the
+    host before anything runs."""
+    w = W.Workload("mxa8u", 64, 512, 8, 4, 256, I_shared=128, seed=9)   # 32 rows per expert
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    q_gu = moe.moe_mxfp8_quantize(p["w_gate_up"])
+    q_d = moe.moe_mxfp8_quantize(p["w_down"])
+    with pytest.raises(RuntimeError, match="act_mxfp8"):
+        moe.moe_forward_mxfp8(x, p["w_router"], q_gu, q_d, 4, act_mxfp8=True)
+    with pytest.raises(RuntimeError, match="act_mxfp8"):
+        moe.moe_forward_mxfp8(x[:8], p["w_router"], q_gu, q_d, 4, act_mxfp8=True,
+                              w_gate_up_shared=p["w_gate_up_shared"],
+                              w_down_shared=p["w_down_shared"])
