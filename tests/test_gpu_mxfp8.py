@@ -228,3 +228,29 @@ def test_forward_mxfp8_act_unsupported(moe):
         moe.moe_forward_mxfp8(x[:8], p["w_router"], q_gu, q_d, 4, act_mxfp8=True,
                               w_gate_up_shared=p["w_gate_up_shared"],
                               w_down_shared=p["w_down_shared"])
+
+
+def test_forward_mxfp8_act_extreme_scales(moe):
+    """Tokens scaled by 2^-70 (scale bytes below 64, h underflowing to bf16
+    subnormals and zeros) still match the oracle's W8A8 layer; the other
+    tokens share experts with them."""
+    T, d, E, k, I = 32, 512, 16, 4, 256
+    w = W.Workload("mxa8x", T, d, E, k, I, seed=123)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    x[::3] = (x[::3].float() * 2.0 ** -70).to(torch.bfloat16)
+    ws = moe.new_workspace(T, d, E, I, k, act_mxfp8=True)
+    out = moe.moe_forward_mxfp8(x, p["w_router"], moe.moe_mxfp8_quantize(p["w_gate_up"]),
+                                moe.moe_mxfp8_quantize(p["w_down"]), k, ws=ws, act_mxfp8=True)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, T, d, E, I, k, act_mxfp8=True)
+    assert int(v["act_x_scales"].min()) < 64
+    xc, xs = oracle.mxfp8_quantize(oracle.bf16_bits_to_f64(W.to_bits(x)))
+    assert np.array_equal(_unpermute_act(v["act_x"].cpu().numpy()), xc)
+    assert np.array_equal(v["act_x_scales"].cpu().numpy(), xs)
+    ref = oracle.forward(W.to_bits(x), W.to_bits(p["w_router"]), _dequantised_bits(p["w_gate_up"]),
+                         _dequantised_bits(p["w_down"]), k, act_mxfp8=True)
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ref["ids"], ref["gates"], ref["logits"], k)
+    keep = np.setdiff1d(np.arange(T), differ)
+    assert_layer_close(f64(out)[keep], ref["out"][keep], "out")
