@@ -260,7 +260,8 @@ def also_row(name, weights, r, peak_kind):
     roof, layer = r["roofline"], r["layer"]
     return [name, weights, int(round(r["tokens_per_s"])), round(r["ms"], 4), c.get("sm_mhz"),
             ",".join(c.get("reasons", [])), round(layer["tc_peak_frac"], 3),
-            round(layer["hbm_frac"], 3), roof["kernel"].removeprefix("moe_"), roof["bound"],
+            round(layer["hbm_frac"], 3),
+            roof["kernel"].removeprefix("moe_").replace("_swiglu", ""), roof["bound"],
             round(roof["frac"], 3),
             "sust" if peak_kind == "sustained" else "burst"]
 
@@ -269,7 +270,7 @@ def bench_config(w, world):
     """The workload's config, the same for both arms."""
     return {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "top_k": w.top_k, "I": w.I,
             "I_shared": w.I_shared, "parallelism": f"replicas x{world}",
-            "l2": "inputs > L2: each step streams the touched expert weights from HBM"}
+            "l2": "inputs > L2 (touched expert weights streamed from HBM each step)"}
 
 
 def detail_line(label, r):
