@@ -8,9 +8,27 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+_REPORT = []  # lines of the run's parity summary
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+@pytest.fixture
+def report(request):
+    """Append a line to the run's parity summary, which the terminal report
+    prints after the results (also under -q, where captured output of passing
+    tests is not shown)."""
+    return _REPORT.append
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    if _REPORT:
+        terminalreporter.section("parity against the oracle")
+        for line in _REPORT:
+            terminalreporter.write_line(line)
 
 
 def pytest_collection_modifyitems(config, items):

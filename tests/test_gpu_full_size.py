@@ -26,7 +26,7 @@ def moe():
 
 
 @pytest.mark.parametrize("name", [W.DECODE, W.PREFILL, W.SKEWED, W.DEEPSEEK])
-def test_full_size_whole_layer(moe, name):
+def test_full_size_whole_layer(moe, name, report):
     w = W.WORKLOADS[name]
     p = W.make_weights(w, device="cuda")
     x = W.make_x(w, device="cuda")
@@ -40,7 +40,7 @@ def test_full_size_whole_layer(moe, name):
     ids_ref, gates_ref, logits = oracle.route(W.to_bits(x), W.to_bits(p["w_router"]), w.top_k, bias)
     ids = v["topk_ids"].cpu().numpy()
     differ = compare_routing(ids, v["topk_gates"].cpu().numpy(), ids_ref, gates_ref, logits, w.top_k)
-    print(f"{name}: {differ.size} near-tie tokens routed differently: {differ.tolist()}")
+    report(f"{name}: {differ.size} near-tie tokens routed differently: {differ.tolist()}")
 
     counts = v["expert_counts"].cpu().numpy()
     assert counts.sum() == w.T * w.top_k
@@ -67,12 +67,12 @@ def test_full_size_whole_layer(moe, name):
     got = f64(out[torch.as_tensor(tokens, device="cuda")])
     assert got.shape == (w.T - differ.size, w.d)
     max_rel, mean_rel = assert_layer_close(got, ref, name)
-    print(f"{name}: whole layer, {tokens.size} of {w.T} tokens x {w.d} columns: "
+    report(f"{name}: whole layer, {tokens.size} of {w.T} tokens x {w.d} columns: "
           f"max_rel={max_rel:.3e} mean_rel={mean_rel:.3e}")
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4", "mxfp8_a8"])
-def test_full_size_decode_quantised_weights(moe, fmt):
+def test_full_size_decode_quantised_weights(moe, fmt, report):
     """The decode workload with MXFP8 / NVFP4 expert weights (mxfp8_a8: MXFP8
     tokens too), as the benchmark runs it: routing for every token, and every
     token's output (all 64 x 4096 values but near-ties) against the oracle on
@@ -102,5 +102,5 @@ def test_full_size_decode_quantised_weights(moe, fmt):
     got = f64(out[torch.as_tensor(tokens, device="cuda")])
     assert got.shape == (w.T - differ.size, w.d)
     max_rel, mean_rel = assert_layer_close(got, ref, f"decode {fmt}")
-    print(f"decode {fmt}: whole layer, {tokens.size} of {w.T} tokens: "
+    report(f"decode {fmt}: whole layer, {tokens.size} of {w.T} tokens: "
           f"max_rel={max_rel:.3e} mean_rel={mean_rel:.3e}")
