@@ -18,14 +18,13 @@ from tests.gpu_util import ExpertsStreamed, assert_layer_close, compare_routing,
 pytestmark = pytest.mark.gpu
 
 
-
 @pytest.fixture(scope="module")
 def moe():
     from mixture_experts_layer_20_gb300 import binding
     return binding
 
 
-@pytest.mark.parametrize("name", [W.DECODE, W.PREFILL, W.SKEWED, W.DEEPSEEK])
+@pytest.mark.parametrize("name", [W.TINY, W.DECODE, W.PREFILL, W.SKEWED, W.DEEPSEEK])
 def test_full_size_whole_layer(moe, name, report):
     w = W.WORKLOADS[name]
     p = W.make_weights(w, device="cuda")

@@ -254,3 +254,30 @@ def test_forward_mxfp8_act_extreme_scales(moe):
                              ref["ids"], ref["gates"], ref["logits"], k)
     keep = np.setdiff1d(np.arange(T), differ)
     assert_layer_close(f64(out)[keep], ref["out"][keep], "out")
+
+
+def test_forward_mxfp8_act_fp32_y(moe):
+    """W8A8 with y kept in fp32 (y_fp32): the fp32 expert outputs and the layer
+    against the oracle's W8A8 layer, and out equal to the fp16-y run's within
+    the layer tolerance (only y's storage differs)."""
+    T, d, E, k, I = 32, 512, 32, 8, 256
+    w = W.Workload("mxa8y", T, d, E, k, I, seed=77)
+    p = W.make_weights(w, device="cuda")
+    x = W.make_x(w, device="cuda")
+    q_gu = moe.moe_mxfp8_quantize(p["w_gate_up"])
+    q_d = moe.moe_mxfp8_quantize(p["w_down"])
+    ws = moe.new_workspace(T, d, E, I, k, y_fp32=True, act_mxfp8=True)
+    out = moe.moe_forward_mxfp8(x, p["w_router"], q_gu, q_d, k, ws=ws, y_fp32=True,
+                                act_mxfp8=True)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    v = moe.workspace_views(ws, T, d, E, I, k, y_fp32=True, act_mxfp8=True)
+    assert v["y"].dtype == torch.float32
+    ref = oracle.forward(W.to_bits(x), W.to_bits(p["w_router"]), _dequantised_bits(p["w_gate_up"]),
+                         _dequantised_bits(p["w_down"]), k, act_mxfp8=True)
+    differ = compare_routing(v["topk_ids"].cpu().numpy(), v["topk_gates"].cpu().numpy(),
+                             ref["ids"], ref["gates"], ref["logits"], k)
+    assert differ.size == 0
+    assert_layer_close(f64(v["y"]), ref["y"], "y")
+    assert_layer_close(f64(out), ref["out"], "out")
+    out16 = moe.moe_forward_mxfp8(x, p["w_router"], q_gu, q_d, k, act_mxfp8=True)
+    assert_layer_close(f64(out16), f64(out), "fp16 y against fp32 y")
